@@ -1,0 +1,423 @@
+"""Pins for the fp64 oracle: each check rests on something other than the oracle itself.
+
+* indexer - special cases that reduce to a matrix product (numpy), the identity
+  ReLU(x) - ReLU(-x) = x, exactness on dyadic inputs, mask structure;
+* top-k - hand-derived fixtures (tests/golden/topk_ties.txt), exhaustive subset
+  search on tiny rows, numpy lexsort, invariants;
+* attention - dense masked attention through torch's scaled_dot_product_attention
+  in fp64 (index mask built from the selected lists), closed forms (first token,
+  constant keys), permutation invariance;
+* backward - torch.autograd in fp64 through the same dense routine, central
+  finite differences of the oracle forward, and closed-form sums.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from helpers import bf16_bits_to_f64, f64_to_bf16_bits
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------- fixtures
+
+def _dyadic_inputs(B, S, Hi, Di, seed, lo=-8, hi=8, nonneg=False, seg_docs=0):
+    if nonneg:
+        lo = 0
+    q = synth.dyadic_bf16((B, S, Hi, Di), seed, 1, lo, hi, 3)
+    k = synth.dyadic_bf16((B, S, Di), seed, 2, lo, hi, 3)
+    w = synth.dyadic_f32((B, S, Hi), seed, 3, 0 if nonneg else -4, 4, 4)
+    seg = synth.segments(B, S, seg_docs, seed) if seg_docs else None
+    return q, k, w, seg
+
+
+def _negate_bf16(u16):
+    return (u16 ^ np.uint16(0x8000)).astype(np.uint16)
+
+
+# ------------------------------------------------------------------ indexer
+
+def test_indexer_single_head_unit_weight_is_relu_of_matmul():
+    """Hi = 1, w = 1: I[t, s] = ReLU(q[t] . k[s]) - one matrix product."""
+    B, S, Di = 2, 37, 24
+    q, k, _, _ = _dyadic_inputs(B, S, 1, Di, seed=11)
+    w = np.ones((B, S, 1), dtype=np.float32)
+    got = oracle.index_scores(q, k, w, None)
+    qf, kf = bf16_bits_to_f64(q)[:, :, 0, :], bf16_bits_to_f64(k)
+    for b in range(B):
+        ref = np.maximum(qf[b] @ kf[b].T, 0.0)
+        for t in range(S):
+            np.testing.assert_array_equal(got[b * S + t, : t + 1], ref[t, : t + 1])
+
+
+def test_indexer_nonnegative_inputs_collapse_heads():
+    """q, k, w >= 0 make every ReLU the identity, so I[t,:] = (w[t] @ q[t]) @ k^T."""
+    B, S, Hi, Di = 2, 29, 5, 16
+    q, k, w, _ = _dyadic_inputs(B, S, Hi, Di, seed=12, nonneg=True)
+    got = oracle.index_scores(q, k, w, None)
+    qf, kf = bf16_bits_to_f64(q), bf16_bits_to_f64(k)
+    for b in range(B):
+        for t in range(S):
+            wq = w[b, t].astype(np.float64) @ qf[b, t]          # [Di]
+            ref = kf[b, : t + 1] @ wq
+            np.testing.assert_array_equal(got[b * S + t, : t + 1], ref)
+
+
+def test_indexer_relu_split_identity():
+    """ReLU(x) - ReLU(-x) = x: I(q, k) - I(q, -k) = sum_h w[t,h] q[t,h] . k[s] for any signs."""
+    B, S, Hi, Di = 1, 41, 7, 32
+    q, k, w, _ = _dyadic_inputs(B, S, Hi, Di, seed=13)
+    plus = oracle.index_scores(q, k, w, None)
+    minus = oracle.index_scores(q, _negate_bf16(k), w, None)
+    qf, kf = bf16_bits_to_f64(q), bf16_bits_to_f64(k)
+    for t in range(S):
+        wq = w[0, t].astype(np.float64) @ qf[0, t]
+        np.testing.assert_array_equal(plus[t, : t + 1] - minus[t, : t + 1], kf[0, : t + 1] @ wq)
+    # all dot products <= 0  =>  every score is exactly zero
+    qn, kn, wn, _ = _dyadic_inputs(B, S, Hi, Di, seed=14, nonneg=True)
+    zero = oracle.index_scores(qn, _negate_bf16(kn), w, None)
+    for t in range(S):
+        assert np.all(zero[t, : t + 1] == 0.0)
+
+
+def test_indexer_mask_structure_and_segments():
+    """NaN above the diagonal; -inf exactly where the document differs; finite elsewhere."""
+    B, S, Hi, Di = 2, 53, 4, 16
+    q, k, w, seg = _dyadic_inputs(B, S, Hi, Di, seed=15, seg_docs=3)
+    got = oracle.index_scores(q, k, w, seg)
+    plain = oracle.index_scores(q, k, w, None)
+    for b in range(B):
+        for t in range(S):
+            row = got[b * S + t]
+            assert np.all(np.isnan(row[t + 1:]))
+            same = seg[b, : t + 1] == seg[b, t]
+            assert np.all(np.isneginf(row[: t + 1][~same]))
+            np.testing.assert_array_equal(row[: t + 1][same], plain[b * S + t, : t + 1][same])
+            assert same[t]
+
+
+def test_indexer_dyadic_workload_is_exact_in_fp32():
+    """On the dyadic workloads every score is an fp32 value (the GPU must match bit for bit)."""
+    wl = synth.WORKLOADS["packed_s489"]
+    inp = synth.indexer_inputs(wl)
+    rows = synth.sample_rows(wl, 24)
+    got = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], inp["seg"], rows=rows)
+    finite = np.isfinite(got)
+    assert np.all(got[finite].astype(np.float32).astype(np.float64) == got[finite])
+    # granularity 2^-10 (q, k in 1/8 steps, w in 1/16 steps)
+    assert np.all(np.mod(got[finite] * 1024.0, 1.0) == 0.0)
+
+
+def test_indexer_weight_homogeneity_and_linearity():
+    """I is linear in w: I(2 w) = 2 I(w); I(w1 + w2) = I(w1) + I(w2)."""
+    B, S, Hi, Di = 1, 23, 6, 16
+    q, k, w, _ = _dyadic_inputs(B, S, Hi, Di, seed=16)
+    w2 = synth.dyadic_f32((B, S, Hi), 99, 3, -4, 4, 4)
+    a = oracle.index_scores(q, k, w, None)
+    b2 = oracle.index_scores(q, k, w2, None)
+    ab = oracle.index_scores(q, k, (w + w2).astype(np.float32), None)
+    d = oracle.index_scores(q, k, (2 * w).astype(np.float32), None)
+    for t in range(S):
+        np.testing.assert_array_equal(d[t, : t + 1], 2 * a[t, : t + 1])
+        np.testing.assert_array_equal(ab[t, : t + 1], a[t, : t + 1] + b2[t, : t + 1])
+
+
+# ------------------------------------------------------------------- top-k
+
+def _parse_golden():
+    cases = []
+    with open(os.path.join(GOLDEN, "topk_ties.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, seg, scores, expect = [p.strip() for p in line.split("|")]
+            cases.append((int(k), None if seg == "-" else [int(x) for x in seg.split()],
+                          [float(x) for x in scores.split()], [int(x) for x in expect.split()]))
+    return cases
+
+
+@pytest.mark.parametrize("case", _parse_golden())
+def test_topk_golden_fixtures(case):
+    k, seg, scores, expect = case
+    S = len(scores)
+    t = S - 1
+    sc = np.full((1, S), np.nan)
+    sc[0, : t + 1] = scores
+    seg_a = None if seg is None else np.array([seg], dtype=np.int32)
+    idx, cnt = oracle.topk(sc, seg_a, S, k, rows=np.array([t]))
+    assert idx[0].tolist() == expect
+    assert cnt[0] == sum(1 for x in expect if x >= 0)
+
+
+def _brute_force_topk(scores, valid, k):
+    """The unique subset T, |T| = min(k, n), such that every s in T beats every u not in T."""
+    cand = [s for s in range(len(scores)) if valid[s]]
+    m = min(k, len(cand))
+
+    def beats(s, u):
+        return scores[s] > scores[u] or (scores[s] == scores[u] and s < u)
+
+    found = []
+    for T in itertools.combinations(cand, m):
+        rest = [u for u in cand if u not in T]
+        if all(beats(s, u) for s in T for u in rest):
+            found.append(list(T))
+    assert len(found) == 1
+    return found[0] + [-1] * (k - m)
+
+
+def test_topk_exhaustive_subset_search_tiny_rows():
+    rng = np.random.default_rng(5)
+    S = 9
+    for trial in range(60):
+        k = int(rng.integers(1, 6))
+        vals = rng.choice([-1.0, -0.0, 0.0, 0.5, 0.5, 2.0], size=S)   # many ties, both zeros
+        seg = np.sort(rng.integers(0, 3, size=S)).astype(np.int32)[None] if trial % 2 else None
+        sc = np.tile(vals, (S, 1))
+        rows = np.arange(S)
+        idx, _ = oracle.topk(sc, seg, S, k, rows=rows)
+        for t in range(S):
+            valid = [s <= t and (seg is None or seg[0, s] == seg[0, t]) for s in range(S)]
+            assert idx[t].tolist() == _brute_force_topk(list(vals), valid, k)
+
+
+def test_topk_matches_numpy_lexsort():
+    """Library route: np.lexsort on (s, -score) gives the same selection."""
+    wl = synth.WORKLOADS["tiny_s128"]
+    inp = synth.indexer_inputs(wl)
+    sc = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], None)
+    idx, cnt = oracle.topk(sc, None, wl.S, wl.topk)
+    for t in range(wl.S):
+        s_idx = np.arange(t + 1)
+        order = np.lexsort((s_idx, -sc[t, : t + 1]))
+        m = min(wl.topk, t + 1)
+        exp = np.sort(order[:m]).tolist() + [-1] * (wl.topk - m)
+        assert idx[t].tolist() == exp
+        assert cnt[t] == m
+
+
+@pytest.mark.parametrize("name", ["tiny_s128", "packed_s489"])
+def test_topk_invariants_on_workloads(name):
+    wl = synth.WORKLOADS[name]
+    inp = synth.indexer_inputs(wl)
+    rows = synth.sample_rows(wl, 40)
+    sc = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], inp["seg"], rows=rows)
+    idx, cnt = oracle.topk(sc, inp["seg"], wl.S, wl.topk, rows=rows, B=wl.B)
+    seg = inp["seg"]
+    for r, row in enumerate(rows):
+        b, t = divmod(int(row), wl.S)
+        valid = np.array([seg is None or seg[b, s] == seg[b, t] for s in range(t + 1)])
+        n = int(valid.sum())
+        m = min(wl.topk, n)
+        sel = idx[r, :m]
+        assert cnt[r] == m
+        assert np.all(idx[r, m:] == -1)
+        assert np.all(np.diff(sel) > 0)
+        assert np.all(sel <= t) and np.all(valid[sel])
+        chosen = np.zeros(t + 1, bool)
+        chosen[sel] = True
+        rest = valid & ~chosen
+        if rest.any():
+            lo = sc[r, : t + 1][chosen].min()
+            hi = sc[r, : t + 1][rest].max()
+            assert lo >= hi
+            # ties at the threshold went to the lower indices
+            tie_sel = np.nonzero(chosen & (sc[r, : t + 1] == lo))[0]
+            tie_rest = np.nonzero(rest & (sc[r, : t + 1] == lo))[0]
+            if tie_rest.size:
+                assert tie_sel.max() < tie_rest.min()
+        if wl.topk >= n:
+            assert chosen[valid].all()
+
+
+# --------------------------------------------------------------- attention
+
+def _attn_case(B, S, H, Hkv, Dqk, Dv, seed, k, seg_docs=0):
+    Q = synth.normal_bf16((B, S, H, Dqk), seed, 4)
+    K = synth.normal_bf16((B, S, Hkv, Dqk), seed, 5)
+    V = synth.normal_bf16((B, S, Hkv, Dv), seed, 6)
+    dO = synth.normal_bf16((B, S, H, Dv), seed, 7)
+    seg = synth.segments(B, S, seg_docs, seed) if seg_docs else None
+    # a selection from the oracle's own top-k over oracle index scores
+    Hi, Di = 3, 16
+    q_idx = synth.dyadic_bf16((B, S, Hi, Di), seed, 1, -8, 8, 3)
+    k_idx = synth.dyadic_bf16((B, S, Di), seed, 2, -8, 8, 3)
+    w = synth.dyadic_f32((B, S, Hi), seed, 3, -4, 4, 4)
+    sc = oracle.index_scores(q_idx, k_idx, w, seg)
+    idx, _ = oracle.topk(sc, seg, S, k, B=B)
+    return Q, K, V, dO, idx.reshape(B, S, k), seg
+
+
+def _dense_mask(idx, S):
+    """Boolean [B, S, S] mask: causal AND selected (the index mask of the pages)."""
+    B, _, k = idx.shape
+    m = np.zeros((B, S, S), dtype=bool)
+    for b in range(B):
+        for t in range(S):
+            for s in idx[b, t]:
+                if 0 <= s <= t:
+                    m[b, t, s] = True
+    return m
+
+
+def _torch_dense(Q, K, V, mask, scale, H, Hkv, requires_grad=False):
+    q = torch.from_numpy(bf16_bits_to_f64(Q)).permute(0, 2, 1, 3).contiguous()
+    k = torch.from_numpy(bf16_bits_to_f64(K)).permute(0, 2, 1, 3).contiguous()
+    v = torch.from_numpy(bf16_bits_to_f64(V)).permute(0, 2, 1, 3).contiguous()
+    for x in (q, k, v):
+        x.requires_grad_(requires_grad)
+    kk = k.repeat_interleave(H // Hkv, dim=1)
+    vv = v.repeat_interleave(H // Hkv, dim=1)
+    am = torch.from_numpy(mask)[:, None, :, :]
+    o = torch.nn.functional.scaled_dot_product_attention(q, kk, vv, attn_mask=am, scale=scale)
+    return q, k, v, o
+
+
+@pytest.mark.parametrize("Hkv", [1, 4])
+@pytest.mark.parametrize("seg_docs", [0, 3])
+def test_attn_fwd_matches_dense_sdpa(Hkv, seg_docs):
+    B, S, H, Dqk, Dv, k = 2, 40, 4, 24, 16, 7
+    Q, K, V, _, idx, seg = _attn_case(B, S, H, Hkv, Dqk, Dv, seed=21, k=k, seg_docs=seg_docs)
+    scale = 1 / np.sqrt(Dqk)
+    O, lse = oracle.attn_fwd(Q, K, V, idx, scale)
+    _, _, _, o = _torch_dense(Q, K, V, _dense_mask(idx, S), scale, H, Hkv)
+    ref = o.permute(0, 2, 1, 3).reshape(B * S, H, Dv).numpy()
+    np.testing.assert_allclose(O, ref, rtol=1e-12, atol=1e-12)
+    # LSE: softmax weights recovered from it sum to one (closed form of log-sum-exp)
+    assert np.all(np.isfinite(lse))
+
+
+def test_attn_fwd_k_at_least_s_is_dense_causal_attention():
+    """k >= S selects every causal key: the result is plain causal softmax attention."""
+    B, S, H, Dqk, Dv = 1, 33, 3, 16, 8
+    Q, K, V, _, idx, _ = _attn_case(B, S, H, 1, Dqk, Dv, seed=22, k=S + 3)
+    assert np.all((idx[0] >= 0).sum(-1) == np.arange(1, S + 1))
+    scale = 0.37
+    O, lse = oracle.attn_fwd(Q, K, V, idx, scale)
+    q = torch.from_numpy(bf16_bits_to_f64(Q)).permute(0, 2, 1, 3)
+    k = torch.from_numpy(bf16_bits_to_f64(K)).permute(0, 2, 1, 3).expand(B, H, S, Dqk)
+    v = torch.from_numpy(bf16_bits_to_f64(V)).permute(0, 2, 1, 3).expand(B, H, S, Dv)
+    o = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True, scale=scale)
+    np.testing.assert_allclose(O, o.permute(0, 2, 1, 3).reshape(S, H, Dv).numpy(), rtol=1e-12,
+                               atol=1e-12)
+    logits = torch.einsum("bhtd,bhsd->bhts", q, k) * scale
+    logits = logits.masked_fill(~torch.ones(S, S, dtype=torch.bool).tril(), float("-inf"))
+    np.testing.assert_allclose(lse, torch.logsumexp(logits, -1)[0].T.numpy(), rtol=1e-12)
+
+
+def test_attn_fwd_closed_forms():
+    B, S, H, Dqk, Dv, k = 1, 20, 2, 16, 8, 5
+    Q, K, V, _, idx, _ = _attn_case(B, S, H, 1, Dqk, Dv, seed=23, k=k)
+    scale = 0.25
+    O, lse = oracle.attn_fwd(Q, K, V, idx, scale)
+    Vf, Qf, Kf = bf16_bits_to_f64(V), bf16_bits_to_f64(Q), bf16_bits_to_f64(K)
+    # first token: one key, so O = V[0] and LSE = scale * q . k
+    np.testing.assert_array_equal(O[0], np.tile(Vf[0, 0, 0], (H, 1)))
+    np.testing.assert_allclose(lse[0], scale * Qf[0, 0] @ Kf[0, 0, 0], rtol=1e-14)
+    # all-zero keys: uniform weights, O = mean of the selected values, LSE = log m
+    Kz = np.zeros_like(K)
+    Oz, lz = oracle.attn_fwd(Q, Kz, V, idx, scale)
+    for t in range(S):
+        sel = idx[0, t][idx[0, t] >= 0]
+        np.testing.assert_allclose(Oz[t], np.tile(Vf[0, sel, 0].mean(0), (H, 1)), rtol=1e-13)
+        np.testing.assert_allclose(lz[t], np.log(len(sel)), rtol=1e-14)
+    # order of the selected list does not matter (it is a mask)
+    perm = idx.copy()
+    rng = np.random.default_rng(0)
+    for t in range(S):
+        rng.shuffle(perm[0, t])
+    Op, lp = oracle.attn_fwd(Q, K, V, perm, scale)
+    np.testing.assert_allclose(Op, O, rtol=1e-13, atol=1e-15)
+    # keys above the diagonal in the list are masked out by causality
+    bad = idx.copy()
+    bad[0, 3, -1] = 10
+    Ob, _ = oracle.attn_fwd(Q, K, V, bad, scale)
+    np.testing.assert_array_equal(Ob[3], O[3])
+
+
+def test_attn_empty_selection():
+    B, S, H, D = 1, 4, 2, 16
+    Q = synth.normal_bf16((B, S, H, D), 1, 4)
+    K = synth.normal_bf16((B, S, 1, D), 1, 5)
+    V = synth.normal_bf16((B, S, 1, D), 1, 6)
+    idx = np.full((B, S, 3), -1, dtype=np.int32)
+    O, lse = oracle.attn_fwd(Q, K, V, idx, 0.25)
+    assert np.all(O == 0) and np.all(np.isneginf(lse))
+
+
+# ----------------------------------------------------------------- backward
+
+@pytest.mark.parametrize("Hkv", [1, 2])
+@pytest.mark.parametrize("seg_docs", [0, 3])
+def test_attn_bwd_matches_torch_autograd(Hkv, seg_docs):
+    B, S, H, Dqk, Dv, k = 2, 30, 4, 16, 8, 6
+    Q, K, V, dO, idx, seg = _attn_case(B, S, H, Hkv, Dqk, Dv, seed=31, k=k, seg_docs=seg_docs)
+    scale = 1 / np.sqrt(Dqk)
+    dQ, dK, dV = oracle.attn_bwd(Q, K, V, idx, dO, scale)
+    q, kt, vt, o = _torch_dense(Q, K, V, _dense_mask(idx, S), scale, H, Hkv, requires_grad=True)
+    g = torch.from_numpy(bf16_bits_to_f64(dO)).permute(0, 2, 1, 3)
+    (o * g).sum().backward()
+    np.testing.assert_allclose(dQ, q.grad.permute(0, 2, 1, 3).reshape(B * S, H, Dqk).numpy(),
+                               rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dK, kt.grad.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(dV, vt.grad.permute(0, 2, 1, 3).numpy(), rtol=1e-10, atol=1e-12)
+
+
+def test_attn_bwd_finite_differences():
+    """Central differences of L = <dO, O> with a step of 2^-6 on exactly representable entries."""
+    B, S, H, Dqk, Dv, k = 1, 12, 2, 16, 8, 4
+    Q, K, V, dO, idx, _ = _attn_case(B, S, H, 1, Dqk, Dv, seed=32, k=k)
+    # move the probed entries to 1.0 so that 1 +- 2^-6 are bf16 values
+    probes = [("Q", (0, 9, 1, 3)), ("Q", (0, 4, 0, 0)), ("K", (0, 2, 0, 5)), ("K", (0, 7, 0, 1)),
+              ("V", (0, 3, 0, 2)), ("V", (0, 8, 0, 7))]
+    arrs = {"Q": Q.copy(), "K": K.copy(), "V": V.copy()}
+    for name, ix in probes:
+        arrs[name][ix] = f64_to_bf16_bits(np.array([1.0]))[0]
+    scale = 0.3
+    dQ, dK, dV = oracle.attn_bwd(arrs["Q"], arrs["K"], arrs["V"], idx, dO, scale)
+    grads = {"Q": dQ.reshape(B, S, H, Dqk), "K": dK, "V": dV}
+    dOf = bf16_bits_to_f64(dO).reshape(B * S, H, Dv)
+    eps = 2.0 ** -6
+
+    def loss(a):
+        O, _ = oracle.attn_fwd(a["Q"], a["K"], a["V"], idx, scale)
+        return float((O * dOf).sum())
+
+    for name, ix in probes:
+        vals = []
+        for sgn in (+1, -1):
+            a = {n: x.copy() for n, x in arrs.items()}
+            a[name][ix] = f64_to_bf16_bits(np.array([1.0 + sgn * eps]))[0]
+            vals.append(loss(a))
+        fd = (vals[0] - vals[1]) / (2 * eps)
+        an = grads[name][ix]
+        assert abs(fd - an) <= 2e-3 * max(1.0, abs(an)), (name, ix, fd, an)
+
+
+def test_attn_bwd_closed_form_sums():
+    B, S, H, Dqk, Dv, k = 2, 25, 3, 16, 8, 5
+    Q, K, V, dO, idx, _ = _attn_case(B, S, H, 1, Dqk, Dv, seed=33, k=k)
+    scale = 0.2
+    dQ, dK, dV = oracle.attn_bwd(Q, K, V, idx, dO, scale)
+    # softmax weights sum to one: sum over keys of dV equals sum over queries and heads of dO
+    dOf = bf16_bits_to_f64(dO)
+    np.testing.assert_allclose(dV.sum(axis=(1, 2)), dOf.sum(axis=(1, 2)), rtol=1e-12, atol=1e-12)
+    # the rows of dS sum to zero: with every key equal to one vector c, dQ = 0
+    Kc = np.tile(K[:, :1], (1, S, 1, 1))
+    dQc, dKc, _ = oracle.attn_bwd(Q, Kc, V, idx, dO, scale)
+    assert np.max(np.abs(dQc)) < 1e-12
+    # ... and dK summed over keys is zero as well (sum_j dS_j = 0 for every query)
+    np.testing.assert_allclose(dK.sum(axis=1), 0.0, atol=1e-11)
+    # a subset of rows contributes a part: partial sums over a row split add up
+    rows_a = np.arange(0, B * S, 2)
+    rows_b = np.arange(1, B * S, 2)
+    _, dKa, dVa = oracle.attn_bwd(Q, K, V, idx, dO, scale, rows=rows_a)
+    _, dKb, dVb = oracle.attn_bwd(Q, K, V, idx, dO, scale, rows=rows_b)
+    np.testing.assert_allclose(dKa + dKb, dK, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(dVa + dVb, dV, rtol=1e-12, atol=1e-13)
