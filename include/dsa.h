@@ -1,0 +1,173 @@
+/*
+ * dsa.h - C ABI of libdsa.so: the DeepSeek Sparse Attention (DSA) layer hot
+ * path on one NVIDIA GB300 (sm_103a).
+ *
+ * The path has three stages ("DeepSeek3.2: Onboard sparse attention",
+ * Background): a lightning indexer that scores every causal (query, key)
+ * pair, a per-query top-k that turns the scores into an index set, and
+ * attention restricted to that set, forward and backward ("Support Ring
+ * Attention with DeepSeek DSA Sparse Indexer", Forward Flow / Backward Flow).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - All pointers are DEVICE pointers owned by the caller, 16-byte aligned,
+ *    to contiguous row-major tensors of the shapes given below. The library
+ *    never allocates or frees device memory.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Every call
+ *    only enqueues work on it and returns; nothing synchronises except
+ *    dsa_get_last_device_error().
+ *  - Every call returns a dsa_status. Arguments are validated on the host
+ *    before anything is launched; an unsupported shape returns
+ *    DSA_ERR_UNSUPPORTED and nothing runs (there is no fallback path).
+ *  - Faults found on the device (an index outside [-1, S), a bounded wait that
+ *    ran out) do not trap: the kernel records a code in a device error word,
+ *    skips the bad access and finishes. Read it with
+ *    dsa_get_last_device_error().
+ *  - "Valid" pairs: key s is valid for query t when s <= t (the causal mask
+ *    q_pos >= kv_pos, diagonal included; "Support Ring Attention with
+ *    DeepSeek DSA Sparse Indexer", Forward Flow step 3) and, when segment ids
+ *    are given, seg[b,s] == seg[b,t] (packed documents; same page, Tests:
+ *    indexer mask with segment ids).
+ *  - bf16 arguments are IEEE bfloat16 bit patterns; results are rounded to
+ *    nearest even from fp32.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer */
+  DSA_ERR_UNSUPPORTED = 2, /* well-formed but outside what the kernels implement */
+  DSA_ERR_WORKSPACE = 3,   /* workspace pointer null or smaller than required */
+  DSA_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
+  DSA_ERR_TIMEOUT = 5,     /* a bounded device-side wait ran out */
+  DSA_ERR_DEVICE = 6       /* the device reported bad input (see the code) */
+} dsa_status;
+
+typedef enum { DSA_BF16 = 0, DSA_F32 = 1 } dsa_dtype;
+
+/* Device error codes returned by dsa_get_last_device_error(). 0 = none. The
+ * low byte is the kind, the next byte the stage that reported it. */
+#define DSA_DEVERR_TIMEOUT 0x01   /* a bounded mbarrier wait ran out */
+#define DSA_DEVERR_BAD_INDEX 0x02 /* an index outside [-1, S) was skipped */
+#define DSA_DEVERR_MISALIGNED 0x03 /* shared memory not aligned as the kernel needs */
+#define DSA_STAGE_INDEXER 0x100
+#define DSA_STAGE_TOPK 0x200
+#define DSA_STAGE_FWD 0x300
+#define DSA_STAGE_BWD 0x400
+
+/* Human-readable name of a status. Never NULL. */
+const char* dsa_status_string(int status);
+
+/* Library version, e.g. 100 for 0.1.0. */
+int dsa_version(void);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word of the
+ * current device. *code receives the first code recorded since the last read
+ * (0 if none). Returns DSA_OK, or DSA_ERR_CUDA if the synchronisation failed.
+ */
+int dsa_get_last_device_error(void* stream, int32_t* code);
+
+/*
+ * dsa_index_scores - lightning-indexer scores.
+ *
+ * Defines ("DeepSeek3.2: Onboard sparse attention", Background: a per-head
+ * q.k product gives the index score; "Implement QK attention head chunking
+ * for CSA", Description: per-head products reduced over heads):
+ *
+ *     I[b,t,s] = sum_h w[b,t,h] * max(0, sum_d q_idx[b,t,h,d] * k_idx[b,s,d])
+ *
+ * for valid (t, s); -inf where s <= t but the document differs. Entries with
+ * s > t are not written. Per-head products are never stored.
+ *
+ *   q_idx   bf16 [B, S, Hi, Di]
+ *   k_idx   bf16 [B, S, Di]
+ *   w       [B, S, Hi], fp32 (w_dtype = DSA_F32) or bf16 (DSA_BF16)
+ *   seg     int32 [B, S] or NULL (NULL: one document per row)
+ *   scores  fp32 [B, S, ld_scores], ld_scores >= S and a multiple of 4
+ *
+ * Supported: Hi in {1, 2, 4, ..., 128}, Di in {32, 64, 128}. Accumulation is
+ * fp32 on the tensor cores; with inputs whose partial sums are all exact in
+ * fp32 (e.g. small dyadic values) the result is exact.
+ */
+int dsa_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
+                     const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
+                     int64_t ld_scores, void* stream);
+
+/*
+ * dsa_topk - per-query top-k of the index scores ("DeepSeek3.2: Onboard
+ * sparse attention", Background: non-parametric top-k token selection).
+ *
+ * For each (b, t) select m(t) = min(k, n(t)) valid keys (n(t) = number of
+ * valid keys) with the largest score. Equal scores go to the lower key index;
+ * -0.0 equals +0.0. Scores must not be NaN.
+ *
+ *   scores  fp32 [B, S, ld_scores]; only valid entries (s <= t) are read
+ *   seg     int32 [B, S] or NULL
+ *   idx     int32 [B, S, k] out: the selected keys in ascending order,
+ *           slots m(t)..k-1 set to -1
+ *   count   int32 [B, S] out, or NULL: m(t)
+ *   ws      workspace of dsa_topk_workspace_size() bytes (may be NULL if 0)
+ */
+size_t dsa_topk_workspace_size(int B, int S, int k);
+int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* seg, int B, int S, int k,
+             int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dsa_sparse_attn_fwd - attention over the selected keys ("Support Ring
+ * Attention with DeepSeek DSA Sparse Indexer", Forward Flow step 5):
+ *
+ *     l_j = scale * Q[b,t,h] . K[b,s_j]      for the listed s_j with s_j <= t
+ *     O[b,t,h] = sum_j softmax(l)_j V[b,s_j],   lse[b,t,h] = log sum_j exp(l_j)
+ *
+ * The selected set of query t is shared by all H heads. Entries of idx equal
+ * to -1 and entries above the diagonal are ignored; a row with no key gets
+ * O = 0 and lse = -inf. The entries of a row must be distinct.
+ *
+ *   Q    bf16 [B, S, H, Dqk]     K  bf16 [B, S, Hkv, Dqk]    V  bf16 [B, S, Hkv, Dv]
+ *   idx  int32 [B, S, k]         O  bf16 [B, S, H, Dv] out   lse fp32 [B, S, H] out
+ *
+ * Supported: Hkv = 1 (one K/V row shared by every head), 1 <= H <= 128,
+ * (Dqk, Dv) in {(32, 32), (64, 64), (128, 128), (192, 128)}.
+ */
+int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
+                        int S, int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O,
+                        float* lse, void* stream);
+
+/*
+ * dsa_sparse_attn_bwd - gradients of the sparse attention ("Support Ring
+ * Attention with DeepSeek DSA Sparse Indexer", Backward Flow step 6:
+ * dQ = dP.K, dK = dP^T.Q, dV = P^T.dO over the same mask, "dP" being the
+ * gradient of the logits):
+ *
+ *     P_j recomputed from lse;  Delta = sum_c dO[c] O[c];  dS_j = P_j (dO.V[s_j] - Delta)
+ *     dQ[t,h] = scale sum_j dS_j K[s_j];  dK[s] = scale sum dS Q;  dV[s] = sum P dO
+ *
+ *   Q, K, V, idx as for the forward; O, lse the forward's outputs;
+ *   dO bf16 [B, S, H, Dv];  dQ bf16 [B, S, H, Dqk] out;
+ *   dK bf16 [B, S, Hkv, Dqk] out;  dV bf16 [B, S, Hkv, Dv] out;
+ *   ws  workspace of dsa_sparse_attn_bwd_workspace_size() bytes (fp32 dK/dV
+ *       accumulators; overwritten).
+ *
+ * Supported shapes as for the forward. dK/dV are summed with fp32 atomics, so
+ * their rounding order is not fixed from run to run.
+ */
+size_t dsa_sparse_attn_bwd_workspace_size(int B, int S, int H, int Hkv, int Dqk, int Dv);
+int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
+                        const void* O, const float* lse, const void* dO, int B, int S, int H,
+                        int Hkv, int Dqk, int Dv, int k, float scale, void* dQ, void* dK, void* dV,
+                        void* ws, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,197 @@
+"""DeepSeek Sparse Attention (DSA) layer hot path for one GB300 (sm_103a).
+
+A thin ctypes binding over ``libdsa.so`` (the C ABI in ``include/dsa.h``).
+Every function here only checks tensors and marshals pointers; all the work
+runs in the library's CUDA kernels. PyTorch provides device memory and
+streams. If the library has not been built the import fails: there is no
+fallback path.
+
+Entry points (same names as the C ABI):
+
+* ``dsa_index_scores`` - lightning-indexer scores I[b,t,s] (causal / document mask)
+* ``dsa_topk``         - per-query top-k key indices, ascending, -1 padded
+* ``dsa_sparse_attn_fwd`` - attention over the selected keys -> (O, lse)
+* ``dsa_sparse_attn_bwd`` - its gradients -> (dQ, dK, dV)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdsa.so")
+
+DSA_BF16, DSA_F32 = 0, 1
+STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
+          4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_DEVICE"}
+
+# every symbol include/dsa.h declares
+EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa_index_scores",
+           "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd",
+           "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd")
+
+
+class DsaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"{LIB_PATH} is missing: build it with "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, ci, i64, sz, cf = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t,
+                           ctypes.c_float)
+    lib.dsa_status_string.argtypes = [ci]
+    lib.dsa_status_string.restype = ctypes.c_char_p
+    lib.dsa_version.restype = ci
+    lib.dsa_get_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
+    lib.dsa_index_scores.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, vp, i64, vp]
+    lib.dsa_topk_workspace_size.argtypes = [ci, ci, ci]
+    lib.dsa_topk_workspace_size.restype = sz
+    lib.dsa_topk.argtypes = [vp, i64, vp, ci, ci, ci, vp, vp, vp, sz, vp]
+    lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp]
+    lib.dsa_sparse_attn_bwd_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
+    lib.dsa_sparse_attn_bwd_workspace_size.restype = sz
+    lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
+                                        vp, vp, vp, vp, sz, vp]
+    for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_topk",
+                 "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd"):
+        getattr(lib, name).restype = ci
+    return lib
+
+
+lib = _load()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise DsaError(rc, where)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def dsa_get_last_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    code = ctypes.c_int32(0)
+    _check(lib.dsa_get_last_device_error(_stream(stream), ctypes.byref(code)),
+           "dsa_get_last_device_error")
+    return int(code.value)
+
+
+def dsa_index_scores(q_idx, k_idx, w, seg=None, scores=None, ld: int | None = None, stream=None):
+    """q_idx [B,S,Hi,Di] bf16, k_idx [B,S,Di] bf16, w [B,S,Hi] fp32/bf16, seg [B,S] int32.
+
+    Returns scores fp32 [B,S,ld] (ld >= S, multiple of 4); only s <= t is written.
+    """
+    B, S, Hi, Di = q_idx.shape
+    if ld is None:
+        ld = (S + 3) // 4 * 4
+    if scores is None:
+        scores = torch.empty((B, S, ld), dtype=torch.float32, device=q_idx.device)
+    ld = scores.shape[-1]
+    w_dtype = DSA_F32 if w.dtype == torch.float32 else DSA_BF16
+    rc = lib.dsa_index_scores(_dev(q_idx, "q_idx", torch.bfloat16), _dev(k_idx, "k_idx", torch.bfloat16),
+                              _dev(w, "w"), w_dtype,
+                              None if seg is None else _dev(seg, "seg", torch.int32),
+                              B, S, Hi, Di, _dev(scores, "scores", torch.float32), ld,
+                              _stream(stream))
+    _check(rc, "dsa_index_scores")
+    return scores
+
+
+def dsa_topk(scores, k: int, seg=None, S: int | None = None, idx=None, count=None, stream=None):
+    """scores fp32 [B,S,ld] -> (idx int32 [B,S,k] ascending / -1 padded, count int32 [B,S])."""
+    B, S_, ld = scores.shape
+    S = S_ if S is None else S
+    if idx is None:
+        idx = torch.empty((B, S, k), dtype=torch.int32, device=scores.device)
+    if count is None:
+        count = torch.empty((B, S), dtype=torch.int32, device=scores.device)
+    rc = lib.dsa_topk(_dev(scores, "scores", torch.float32), ld,
+                      None if seg is None else _dev(seg, "seg", torch.int32), B, S, k,
+                      _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32), None, 0,
+                      _stream(stream))
+    _check(rc, "dsa_topk")
+    return idx, count
+
+
+def dsa_sparse_attn_fwd(Q, K, V, idx, scale: float, O=None, lse=None, stream=None):
+    """Q [B,S,H,Dqk], K [B,S,Hkv,Dqk], V [B,S,Hkv,Dv] bf16, idx [B,S,k] -> (O bf16, lse fp32)."""
+    B, S, H, Dqk = Q.shape
+    Hkv, Dv = V.shape[2], V.shape[3]
+    k = idx.shape[2]
+    if O is None:
+        O = torch.empty((B, S, H, Dv), dtype=torch.bfloat16, device=Q.device)
+    if lse is None:
+        lse = torch.empty((B, S, H), dtype=torch.float32, device=Q.device)
+    rc = lib.dsa_sparse_attn_fwd(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
+                                 _dev(V, "V", torch.bfloat16), _dev(idx, "idx", torch.int32),
+                                 B, S, H, Hkv, Dqk, Dv, k, float(scale),
+                                 _dev(O, "O", torch.bfloat16), _dev(lse, "lse", torch.float32),
+                                 _stream(stream))
+    _check(rc, "dsa_sparse_attn_fwd")
+    return O, lse
+
+
+def bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv) -> int:
+    return int(lib.dsa_sparse_attn_bwd_workspace_size(B, S, H, Hkv, Dqk, Dv))
+
+
+def dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, scale: float, dQ=None, dK=None, dV=None,
+                        ws=None, stream=None):
+    """Gradients of the sparse attention -> (dQ [B,S,H,Dqk], dK [B,S,Hkv,Dqk], dV [B,S,Hkv,Dv])."""
+    B, S, H, Dqk = Q.shape
+    Hkv, Dv = V.shape[2], V.shape[3]
+    k = idx.shape[2]
+    dev = Q.device
+    if dQ is None:
+        dQ = torch.empty_like(Q)
+    if dK is None:
+        dK = torch.empty((B, S, Hkv, Dqk), dtype=torch.bfloat16, device=dev)
+    if dV is None:
+        dV = torch.empty((B, S, Hkv, Dv), dtype=torch.bfloat16, device=dev)
+    need = bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv)
+    if ws is None:
+        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    rc = lib.dsa_sparse_attn_bwd(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
+                                 _dev(V, "V", torch.bfloat16), _dev(idx, "idx", torch.int32),
+                                 _dev(O, "O", torch.bfloat16), _dev(lse, "lse", torch.float32),
+                                 _dev(dO, "dO", torch.bfloat16), B, S, H, Hkv, Dqk, Dv, k,
+                                 float(scale), _dev(dQ, "dQ", torch.bfloat16),
+                                 _dev(dK, "dK", torch.bfloat16), _dev(dV, "dV", torch.bfloat16),
+                                 _dev(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "dsa_sparse_attn_bwd")
+    return dQ, dK, dV
+
+
+def dsa_layer(q_idx, k_idx, w, Q, K, V, topk: int, scale: float, seg=None, dO=None, stream=None):
+    """The whole hot path: scores -> top-k -> sparse attention forward (and backward if dO)."""
+    scores = dsa_index_scores(q_idx, k_idx, w, seg, stream=stream)
+    idx, count = dsa_topk(scores, topk, seg, stream=stream)
+    O, lse = dsa_sparse_attn_fwd(Q, K, V, idx, scale, stream=stream)
+    out = {"scores": scores, "idx": idx, "count": count, "O": O, "lse": lse}
+    if dO is not None:
+        out["dQ"], out["dK"], out["dV"] = dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, scale,
+                                                               stream=stream)
+    return out

@@ -1,0 +1,152 @@
+// The C ABI of libdsa.so: argument validation, then the kernel launchers.
+// See include/dsa.h for the contract of every entry point.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/dsa.h"
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+
+// The library's device error word (one per device that loads the library).
+__device__ int g_device_error = 0;
+
+int* device_error_word() {
+  constexpr int kMaxDevices = 64;
+  static int* addr[kMaxDevices] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
+}
+
+}  // namespace dsa
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+bool attn_common_ok(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
+                    int H, int Hkv, int Dqk, int Dv, int k) {
+  if (!Q || !K || !V || !idx) return false;
+  if (B < 1 || S < 1 || H < 1 || Hkv < 1 || k < 1 || Dqk < 1 || Dv < 1) return false;
+  if (Dqk % 16 != 0 || Dv % 16 != 0) return false;
+  if (H % Hkv != 0) return false;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(idx)) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dsa_status_string(int status) {
+  switch (status) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED: return "DSA_ERR_UNSUPPORTED";
+    case DSA_ERR_WORKSPACE: return "DSA_ERR_WORKSPACE";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_TIMEOUT: return "DSA_ERR_TIMEOUT";
+    case DSA_ERR_DEVICE: return "DSA_ERR_DEVICE";
+    default: return "DSA_ERR_UNKNOWN";
+  }
+}
+
+int dsa_version(void) { return 100; }
+
+int dsa_get_last_device_error(void* stream, int32_t* code) {
+  if (!code) return DSA_ERR_INVALID_ARG;
+  *code = 0;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return DSA_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, dsa::g_device_error, sizeof(int)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(dsa::g_device_error, &zero, sizeof(int)) != cudaSuccess)
+      return DSA_ERR_CUDA;
+  }
+  *code = v;
+  return DSA_OK;
+}
+
+int dsa_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
+                     const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
+                     int64_t ld_scores, void* stream) {
+  if (!q_idx || !k_idx || !w || !scores) return DSA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || Hi < 1 || Di < 1) return DSA_ERR_INVALID_ARG;
+  if (w_dtype != DSA_F32 && w_dtype != DSA_BF16) return DSA_ERR_INVALID_ARG;
+  if (ld_scores < S || ld_scores % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(scores) ||
+      (seg && !aligned16(seg)))
+    return DSA_ERR_INVALID_ARG;
+  if (Di % 8 != 0) return DSA_ERR_INVALID_ARG;
+  if (!dsa::indexer_dims_supported(Hi, Di)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * S * Hi >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_index_scores(q_idx, k_idx, w, w_dtype == DSA_BF16, seg, B, S, Hi, Di,
+                                  scores, ld_scores, as_stream(stream));
+}
+
+size_t dsa_topk_workspace_size(int B, int S, int k) {
+  (void)B;
+  (void)S;
+  (void)k;
+  return 0;
+}
+
+int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* seg, int B, int S, int k,
+             int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!scores || !idx) return DSA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || k < 1) return DSA_ERR_INVALID_ARG;
+  if (ld_scores < S || ld_scores % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(scores) || !aligned16(idx) || (seg && !aligned16(seg)) ||
+      (count && !aligned16(count)))
+    return DSA_ERR_INVALID_ARG;
+  if (static_cast<long long>(B) * S >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_topk(scores, ld_scores, seg, B, S, k, idx, count, as_stream(stream));
+}
+
+int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
+                        int S, int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O,
+                        float* lse, void* stream) {
+  if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
+  if (!O || !lse || !aligned16(O) || !aligned16(lse)) return DSA_ERR_INVALID_ARG;
+  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_attn_fwd(Q, K, V, idx, B, S, H, Dqk, Dv, k, scale, O, lse,
+                              as_stream(stream));
+}
+
+size_t dsa_sparse_attn_bwd_workspace_size(int B, int S, int H, int Hkv, int Dqk, int Dv) {
+  (void)H;
+  if (B < 1 || S < 1 || Hkv < 1 || Dqk < 1 || Dv < 1) return 0;
+  return static_cast<size_t>(B) * S * Hkv * (Dqk + Dv) * sizeof(float);
+}
+
+int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
+                        const void* O, const float* lse, const void* dO, int B, int S, int H,
+                        int Hkv, int Dqk, int Dv, int k, float scale, void* dQ, void* dK, void* dV,
+                        void* ws, size_t ws_bytes, void* stream) {
+  if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
+  if (!O || !lse || !dO || !dQ || !dK || !dV) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(O) || !aligned16(lse) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
+      !aligned16(dV))
+    return DSA_ERR_INVALID_ARG;
+  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  const size_t need = dsa_sparse_attn_bwd_workspace_size(B, S, H, Hkv, Dqk, Dv);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+  return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
+                              static_cast<float*>(ws), as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,99 @@
+// Pieces shared by the sparse-attention forward and backward kernels: the
+// parameter block, the per-query index-row staging and the K/V row gather.
+#pragma once
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+
+struct AttnParams {
+  const uint16_t *Q, *K, *V, *O_in, *dO;
+  const int32_t* idx;
+  const float* lse_in;
+  int B, S, H, k;
+  float scale, scale_log2;
+  uint16_t* O;
+  float* lse;
+  uint16_t* dQ;
+  float* ws;   // fp32 [B*S, Dqk + Dv] dK / dV accumulators
+  int* err;    // device error word
+};
+
+inline AttnParams make_attn_params(const void* Q, const void* K, const void* V,
+                                   const int32_t* idx, int B, int S, int H, int k, float scale) {
+  AttnParams p = {};
+  p.Q = static_cast<const uint16_t*>(Q);
+  p.K = static_cast<const uint16_t*>(K);
+  p.V = static_cast<const uint16_t*>(V);
+  p.idx = idx;
+  p.B = B;
+  p.S = S;
+  p.H = H;
+  p.k = k;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.err = device_error_word();
+  return p;
+}
+
+// Shared-memory layout of the forward kernel: Q rows, two K/V chunk buffers
+// (rows padded by 16 bytes so ldmatrix row addresses hit distinct banks), a
+// small header and the query's index row.
+template <int DQK, int DV, int NK, int NW>
+struct AttnLayout {
+  static constexpr int KP = DQK + 8;   // element pitch of Q / K rows
+  static constexpr int VP = DV + 8;    // element pitch of V rows
+  static constexpr size_t kQ = 0;
+  static constexpr size_t kK = kQ + static_cast<size_t>(NW) * 16 * KP * 2;
+  static constexpr size_t kV = kK + 2ull * NK * KP * 2;
+  static constexpr size_t kMeta = kV + 2ull * NK * VP * 2;
+  static constexpr size_t kIdx = kMeta + 16;
+  static size_t bytes(int k) { return kIdx + ((static_cast<size_t>(k) + 3) & ~3ull) * 4; }
+};
+
+// Stage the index row of query (row, t) in shared memory. Entries outside
+// [-1, S) are reported and dropped; entries above the diagonal are dropped
+// (causal mask). Returns kend = 1 + the last position holding a key (0: none).
+__device__ __forceinline__ int load_index_row(const AttnParams& p, long long row, int t,
+                                              int* idx_s, int* meta, int stage) {
+  if (threadIdx.x == 0) meta[0] = 0;
+  __syncthreads();
+  int last = 0;
+  for (int j = threadIdx.x; j < p.k; j += blockDim.x) {
+    int s = __ldg(p.idx + row * p.k + j);
+    if (s < -1 || s >= p.S) {
+      report_error(p.err, stage | DSA_DEVERR_BAD_INDEX);
+      s = -1;
+    }
+    if (s > t) s = -1;
+    idx_s[j] = s;
+    if (s >= 0) last = j + 1;
+  }
+  if (last) atomicMax(&meta[0], last);
+  __syncthreads();
+  return meta[0];
+}
+
+// Gather the K and V rows of chunk c (positions c*NK .. c*NK+NK-1 of the index
+// row) with 16-byte cp.async; rows without a key are zero-filled.
+template <int DQK, int DV, int NK, int NT>
+__device__ __forceinline__ void gather_kv(const AttnParams& p, int b, int c, int kend,
+                                          const int* idx_s, uint16_t* Kdst, uint16_t* Vdst) {
+  constexpr int PK = DQK / 8, PV = DV / 8, PER = PK + PV;
+  constexpr int KP = DQK + 8, VP = DV + 8;
+  for (int i = threadIdx.x; i < NK * PER; i += NT) {
+    const int r = i / PER, pc = i - r * PER;
+    const int j = c * NK + r;
+    const int s = j < kend ? idx_s[j] : -1;
+    const bool ok = s >= 0;
+    const long long kv = static_cast<long long>(b) * p.S + (ok ? s : 0);
+    if (pc < PK)
+      cp_async_16(smem_u32(Kdst + r * KP + pc * 8), p.K + kv * DQK + pc * 8, ok ? 16u : 0u);
+    else
+      cp_async_16(smem_u32(Vdst + r * VP + (pc - PK) * 8), p.V + kv * DV + (pc - PK) * 8,
+                  ok ? 16u : 0u);
+  }
+}
+
+}  // namespace dsa

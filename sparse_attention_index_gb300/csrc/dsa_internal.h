@@ -1,0 +1,33 @@
+// Launchers behind the C ABI. Each validates nothing (dsa_api.cu does) and
+// returns a dsa_status after enqueueing its kernels on `stream`.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dsa {
+
+// Device address of the library's error word on the current device.
+int* device_error_word();
+
+int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                        const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
+                        int64_t ld, cudaStream_t stream);
+
+int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
+                int32_t* idx, int32_t* count, cudaStream_t stream);
+
+int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
+                    int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
+                    cudaStream_t stream);
+
+int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
+                    const void* O, const float* lse, const void* dO, int B, int S, int H, int Dqk,
+                    int Dv, int k, float scale, void* dQ, void* dK, void* dV, float* ws_dkv,
+                    cudaStream_t stream);
+
+bool attn_dims_supported(int Dqk, int Dv);
+bool indexer_dims_supported(int Hi, int Di);
+
+}  // namespace dsa

@@ -1,0 +1,430 @@
+// Lightning-indexer scores on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+//   I[b,t,s] = sum_h w[b,t,h] * max(0, q_idx[b,t,h,:] . k_idx[b,s,:])     (valid s <= t)
+//
+// ("DeepSeek3.2: Onboard sparse attention", Background: the indexer's per-head
+// q.k product; "Implement QK attention head chunking for CSA", Description:
+// per-head products reduced over heads. The per-head [S, S] products that the
+// pages materialise and chunk never exist here: they live in TMEM for one tile
+// and are reduced in registers.)
+//
+// Tiling. One UMMA tile is D[128 keys, 256 cols] = K_blk[128, Di] x Q_grp[256, Di]^T,
+// where the 256 columns are G = 256/Hi consecutive queries x Hi heads (the rows of
+// q_idx are already laid out that way). Each TMEM lane is one key, so the
+// epilogue's sum over heads is a reduction inside one thread, and the scores of
+// 32 consecutive keys of one query row leave as one coalesced 128-byte store.
+//
+// Persistent, warp-specialised CTA (one per SM):
+//   warp 0     TMA producer: Q group tile (2 slots) and key tiles (3-stage ring)
+//   warp 1     TMEM allocator and single-thread UMMA issuer (2 accumulators of 256 cols)
+//   warps 2-9  epilogue: tcgen05.ld, ReLU, x w, sum over heads, mask, store
+// Work item = (batch, query group); key blocks 0..t_max/128 of the item stream
+// through the ring. Items are handed out heaviest first, strided over CTAs.
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kKeysPerTile = 128;  // UMMA M (TMEM lanes)
+constexpr int kColsPerTile = 256;  // UMMA N
+constexpr int kKStages = 3;
+constexpr int kQSlots = 2;
+constexpr int kAccBufs = 2;
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + kEpiWarps * 32;
+constexpr int kErr = DSA_STAGE_INDEXER | DSA_DEVERR_TIMEOUT;
+
+struct IndexerParams {
+  int B, S, Di;
+  int G;          // queries per tile (256 / Hi)
+  int n_groups;   // ceil(S / G)
+  int n_items;    // B * n_groups
+  int atom;       // K elements per swizzled row segment (16, 32 or 64)
+  int n_atoms;    // Di / atom
+  uint32_t layout;
+  uint32_t q_slot_bytes, k_stage_bytes;
+  const void* w;
+  int w_bf16;
+  const int32_t* seg;
+  float* scores;
+  long long ld;
+  int* err;
+};
+
+struct SmemTail {
+  float w_s[kQSlots][kColsPerTile];  // head weights of the item, one slot per Q slot
+  uint64_t q_full[kQSlots], q_empty[kQSlots];
+  uint64_t w_full[kQSlots], w_empty[kQSlots];
+  uint64_t k_full[kKStages], k_empty[kKStages];
+  uint64_t acc_full[kAccBufs], acc_empty[kAccBufs];
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__device__ __forceinline__ void item_coords(const IndexerParams& p, int item, int& b, int& t0,
+                                            int& nkb) {
+  // heaviest items (largest t) first
+  const int gi = item / p.B;
+  b = item - gi * p.B;
+  const int g = p.n_groups - 1 - gi;
+  t0 = g * p.G;
+  int t_last = t0 + p.G - 1;
+  if (t_last > p.S - 1) t_last = p.S - 1;
+  nkb = t_last / kKeysPerTile + 1;
+}
+
+// Drain wait used only at exit: ignores the abort flag, still bounded.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      report_error(err, kErr);
+      return;
+    }
+  }
+}
+
+template <int HI>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tm_q,
+                   const __grid_constant__ CUtensorMap tm_k, const IndexerParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  // The swizzled tiles need 1024-byte alignment. The dynamic window starts
+  // 1024-aligned when the kernel has no static shared memory; refuse to run
+  // (and say so) rather than feed misaligned tiles to TMA / UMMA.
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) report_error(p.err, DSA_STAGE_INDEXER | DSA_DEVERR_MISALIGNED);
+    return;
+  }
+  uint8_t* q_smem = smem;
+  uint8_t* k_smem = q_smem + kQSlots * p.q_slot_bytes;
+  SmemTail* tail = reinterpret_cast<SmemTail*>(k_smem + kKStages * p.k_stage_bytes);
+  volatile int* abort_flag = &tail->abort_flag;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kQSlots; ++i) {
+      mbar_init(&tail->q_full[i], 1);
+      mbar_init(&tail->q_empty[i], 1);
+      mbar_init(&tail->w_full[i], 32);
+      mbar_init(&tail->w_empty[i], kEpiWarps);
+    }
+    for (int i = 0; i < kKStages; ++i) {
+      mbar_init(&tail->k_full[i], 1);
+      mbar_init(&tail->k_empty[i], 1);
+    }
+    for (int i = 0; i < kAccBufs; ++i) {
+      mbar_init(&tail->acc_full[i], 1);
+      mbar_init(&tail->acc_empty[i], kEpiWarps);
+    }
+    mbar_init(&tail->drain, 1);
+    tail->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tail->tmem_base, kAccBufs * kColsPerTile);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tail->tmem_base;
+
+  const uint32_t atom_bytes = static_cast<uint32_t>(p.atom) * 2u;
+  const uint32_t sbo = 8u * atom_bytes;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    // All 32 lanes stage the head weights of each item; lane 0 issues the TMA copies.
+    int ks = 0, qs = 0;
+    uint32_t k_par = 1, q_par = 1;
+    uint32_t k_issued[kKStages] = {0, 0, 0}, q_issued[kQSlots] = {0, 0};
+    uint32_t k_last_par[kKStages] = {0, 0, 0}, q_last_par[kQSlots] = {0, 0};
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      int b, t0, nkb;
+      item_coords(p, item, b, t0, nkb);
+      int okw = 1;
+      if (lane == 0) okw = mbar_wait(&tail->w_empty[qs], q_par, abort_flag, p.err, kErr) ? 1 : 0;
+      if (__shfl_sync(0xffffffffu, okw, 0) == 0) break;
+      for (int c = lane; c < kColsPerTile; c += 32) {
+        const int tq = t0 + c / HI;
+        float wv = 0.f;
+        if (tq < p.S) {
+          const long long off = (static_cast<long long>(b) * p.S + tq) * HI + (c % HI);
+          wv = p.w_bf16 ? bf16_bits_to_float(static_cast<const uint16_t*>(p.w)[off])
+                        : static_cast<const float*>(p.w)[off];
+        }
+        tail->w_s[qs][c] = wv;
+      }
+      mbar_arrive(&tail->w_full[qs]);
+      if (lane == 0) {
+        if (!mbar_wait(&tail->q_empty[qs], q_par, abort_flag, p.err, kErr)) ok = false;
+        if (ok) {
+          mbar_arrive_expect_tx(&tail->q_full[qs], p.q_slot_bytes);
+          const int qrow = (b * p.S + t0) * HI;
+          for (int a = 0; a < p.n_atoms; ++a)
+            tma_load_2d(q_smem + qs * p.q_slot_bytes + a * kColsPerTile * atom_bytes, &tm_q,
+                        &tail->q_full[qs], a * p.atom, qrow);
+          q_issued[qs] = 1;
+          q_last_par[qs] = q_par ^ 1u;
+        }
+        for (int j = 0; ok && j < nkb; ++j) {
+          if (!mbar_wait(&tail->k_empty[ks], k_par, abort_flag, p.err, kErr)) { ok = false; break; }
+          mbar_arrive_expect_tx(&tail->k_full[ks], p.k_stage_bytes);
+          const int krow = b * p.S + j * kKeysPerTile;
+          for (int a = 0; a < p.n_atoms; ++a)
+            tma_load_2d(k_smem + ks * p.k_stage_bytes + a * kKeysPerTile * atom_bytes, &tm_k,
+                        &tail->k_full[ks], a * p.atom, krow);
+          k_issued[ks] = 1;
+          k_last_par[ks] = k_par ^ 1u;
+          if (++ks == kKStages) { ks = 0; k_par ^= 1u; }
+        }
+      }
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (++qs == kQSlots) { qs = 0; q_par ^= 1u; }
+    }
+    // Let every copy this warp started land before the CTA exits.
+    if (lane == 0) {
+      for (int i = 0; i < kQSlots; ++i)
+        if (q_issued[i]) drain_wait(&tail->q_full[i], q_last_par[i], p.err);
+      for (int i = 0; i < kKStages; ++i)
+        if (k_issued[i]) drain_wait(&tail->k_full[i], k_last_par[i], p.err);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ UMMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = umma_idesc_bf16(kKeysPerTile, kColsPerTile);
+      const int ksteps_per_atom = p.atom / 16;
+      int ks = 0, qs = 0, as = 0;
+      uint32_t k_par = 0, q_par = 0, a_par = 1;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        int b, t0, nkb;
+        item_coords(p, item, b, t0, nkb);
+        if (!mbar_wait(&tail->q_full[qs], q_par, abort_flag, p.err, kErr)) { ok = false; break; }
+        const uint32_t q_addr = smem_u32(q_smem + qs * p.q_slot_bytes);
+        for (int j = 0; j < nkb; ++j) {
+          if (!mbar_wait(&tail->k_full[ks], k_par, abort_flag, p.err, kErr)) { ok = false; break; }
+          if (!mbar_wait(&tail->acc_empty[as], a_par, abort_flag, p.err, kErr)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t k_addr = smem_u32(k_smem + ks * p.k_stage_bytes);
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * kColsPerTile);
+          for (int a = 0; a < p.n_atoms; ++a) {
+            for (int kk = 0; kk < ksteps_per_atom; ++kk) {
+              const uint32_t off = static_cast<uint32_t>(kk) * 32u;
+              const uint64_t adesc =
+                  umma_sdesc(k_addr + a * kKeysPerTile * atom_bytes + off, sbo, p.layout);
+              const uint64_t bdesc =
+                  umma_sdesc(q_addr + a * kColsPerTile * atom_bytes + off, sbo, p.layout);
+              umma_bf16(d_tmem, adesc, bdesc, idesc, (a | kk) != 0 ? 1u : 0u);
+            }
+          }
+          umma_commit(&tail->k_empty[ks]);
+          umma_commit(&tail->acc_full[as]);
+          if (++ks == kKStages) { ks = 0; k_par ^= 1u; }
+          if (++as == kAccBufs) { as = 0; a_par ^= 1u; }
+        }
+        if (!ok) break;
+        umma_commit(&tail->q_empty[qs]);
+        if (++qs == kQSlots) { qs = 0; q_par ^= 1u; }
+      }
+      // Every UMMA issued above has completed once this arrives.
+      umma_commit(&tail->drain);
+      drain_wait(&tail->drain, 0, p.err);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int e = warp - 2;              // 0..7
+    const int quarter = warp & 3;        // TMEM lane quarter this warp may access
+    const int half = e >> 2;             // which 128 of the 256 columns
+    constexpr int QPC = HI >= 32 ? 1 : 32 / HI;  // queries per 32-column chunk
+    constexpr int CPQ = HI >= 32 ? HI / 32 : 1;  // chunks per query
+    int as = 0, ws = 0;
+    uint32_t a_par = 0, w_par = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      int b, t0, nkb;
+      item_coords(p, item, b, t0, nkb);
+      // head weights of this query group: column c = (query c / HI, head c % HI)
+      if (!__all_sync(0xffffffffu, mbar_wait(&tail->w_full[ws], w_par, abort_flag, p.err, kErr))) break;
+      const float* w_item = tail->w_s[ws];
+
+      for (int j = 0; j < nkb; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&tail->acc_full[as], a_par, abort_flag, p.err, kErr))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const int s = j * kKeysPerTile + quarter * 32 + lane;
+        const int seg_s = (p.seg != nullptr && s < p.S) ? __ldg(p.seg + b * p.S + s) : 0;
+        const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                static_cast<uint32_t>(as * kColsPerTile + half * 128);
+#pragma unroll 1
+        for (int cq = 0; cq < 4; cq += CPQ) {
+          float acc[QPC];
+#pragma unroll
+          for (int i = 0; i < QPC; ++i) acc[i] = 0.f;
+#pragma unroll
+          for (int c2 = 0; c2 < CPQ; ++c2) {
+            const int ch = cq + c2;   // chunk within this half
+            uint32_t v[32];
+            tmem_ld_x32(t_base + ch * 32, v);
+            tmem_ld_wait();
+            const float* wrow = w_item + half * 128 + ch * 32;
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj)
+              acc[jj / (32 / QPC)] =
+                  fmaf(wrow[jj], fmaxf(__uint_as_float(v[jj]), 0.f), acc[jj / (32 / QPC)]);
+          }
+#pragma unroll
+          for (int i = 0; i < QPC; ++i) {
+            const int qi = (half * 128 + cq * 32) / HI + i;
+            const int t = t0 + qi;
+            if (t < p.S && s <= t) {
+              float val = acc[i];
+              if (p.seg != nullptr && seg_s != __ldg(p.seg + b * p.S + t)) val = -INFINITY;
+              p.scores[(static_cast<long long>(b) * p.S + t) * p.ld + s] = val;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tail->acc_empty[as]);
+        if (++as == kAccBufs) { as = 0; a_par ^= 1u; }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tail->w_empty[ws]);
+      if (++ws == kQSlots) { ws = 0; w_par ^= 1u; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, kAccBufs * kColsPerTile);
+}
+
+// ----------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int cols, int box_cols,
+              int box_rows, CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = get_encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HI>
+int launch_hi(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& p,
+              size_t smem_bytes, cudaStream_t stream) {
+  auto kern = indexer_kernel<HI>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem_bytes)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int grid = p.n_items < sms ? p.n_items : sms;
+  if (grid < 1) grid = 1;
+  kern<<<grid, kThreads, smem_bytes, stream>>>(mq, mk, p);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace
+
+bool indexer_dims_supported(int Hi, int Di) {
+  const bool hi_ok = Hi >= 1 && Hi <= 128 && (Hi & (Hi - 1)) == 0;
+  const bool di_ok = Di == 32 || Di == 64 || Di == 128;
+  return hi_ok && di_ok;
+}
+
+int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                        const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
+                        int64_t ld, cudaStream_t stream) {
+  IndexerParams p;
+  p.B = B;
+  p.S = S;
+  p.Di = Di;
+  p.G = kColsPerTile / Hi;
+  p.n_groups = (S + p.G - 1) / p.G;
+  p.n_items = B * p.n_groups;
+  p.atom = Di >= 64 ? 64 : Di;
+  p.n_atoms = Di / p.atom;
+  CUtensorMapSwizzle swz;
+  if (p.atom == 64) {
+    p.layout = kLayoutSw128;
+    swz = CU_TENSOR_MAP_SWIZZLE_128B;
+  } else if (p.atom == 32) {
+    p.layout = kLayoutSw64;
+    swz = CU_TENSOR_MAP_SWIZZLE_64B;
+  } else {
+    p.layout = kLayoutSw32;
+    swz = CU_TENSOR_MAP_SWIZZLE_32B;
+  }
+  p.q_slot_bytes = static_cast<uint32_t>(kColsPerTile) * Di * 2;
+  p.k_stage_bytes = static_cast<uint32_t>(kKeysPerTile) * Di * 2;
+  p.w = w;
+  p.w_bf16 = w_is_bf16;
+  p.seg = seg;
+  p.scores = scores;
+  p.ld = ld;
+  p.err = device_error_word();
+
+  CUtensorMap mq, mk;
+  if (!make_map(&mq, q_idx, static_cast<uint64_t>(B) * S * Hi, Di, p.atom, kColsPerTile, swz))
+    return DSA_ERR_CUDA;
+  if (!make_map(&mk, k_idx, static_cast<uint64_t>(B) * S, Di, p.atom, kKeysPerTile, swz))
+    return DSA_ERR_CUDA;
+
+  const size_t smem_bytes = kQSlots * static_cast<size_t>(p.q_slot_bytes) +
+                            kKStages * static_cast<size_t>(p.k_stage_bytes) + sizeof(SmemTail);
+  switch (Hi) {
+    case 1: return launch_hi<1>(mq, mk, p, smem_bytes, stream);
+    case 2: return launch_hi<2>(mq, mk, p, smem_bytes, stream);
+    case 4: return launch_hi<4>(mq, mk, p, smem_bytes, stream);
+    case 8: return launch_hi<8>(mq, mk, p, smem_bytes, stream);
+    case 16: return launch_hi<16>(mq, mk, p, smem_bytes, stream);
+    case 32: return launch_hi<32>(mq, mk, p, smem_bytes, stream);
+    case 64: return launch_hi<64>(mq, mk, p, smem_bytes, stream);
+    case 128: return launch_hi<128>(mq, mk, p, smem_bytes, stream);
+    default: return DSA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace dsa

@@ -1,0 +1,88 @@
+"""The C ABI loads without a GPU, exports every declared symbol, and rejects bad
+arguments on the host before anything is launched (no device is touched)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import sparse_attention_index_gb300 as m
+    return m
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text))
+
+
+def test_every_declared_symbol_is_exported(dsa):
+    declared = _declared()
+    assert declared == set(dsa.EXPORTS)
+    for name in declared:
+        assert hasattr(dsa.lib, name), name
+
+
+def test_status_strings_and_version(dsa):
+    assert dsa.lib.dsa_status_string(0) == b"DSA_OK"
+    assert dsa.lib.dsa_status_string(2) == b"DSA_ERR_UNSUPPORTED"
+    assert dsa.lib.dsa_status_string(99) == b"DSA_ERR_UNKNOWN"
+    assert dsa.lib.dsa_version() == 100
+
+
+def test_workspace_sizes(dsa):
+    assert dsa.lib.dsa_sparse_attn_bwd_workspace_size(1, 16384, 128, 1, 192, 128) == \
+        16384 * 320 * 4
+    assert dsa.lib.dsa_sparse_attn_bwd_workspace_size(0, 1, 1, 1, 1, 1) == 0
+    assert dsa.lib.dsa_topk_workspace_size(1, 16384, 2048) == 0
+
+
+# Fake (never dereferenced) 16-byte-aligned addresses: every call below fails
+# validation on the host and returns before any CUDA call.
+P = ctypes.c_void_p(1 << 20)
+MIS = ctypes.c_void_p((1 << 20) + 4)
+
+
+def test_index_scores_validation(dsa):
+    f = dsa.lib.dsa_index_scores
+    assert f(None, P, P, 1, None, 1, 128, 64, 128, P, 128, None) == 1        # null q_idx
+    assert f(P, P, P, 1, None, 1, 128, 64, 128, P, 100, None) == 1           # ld < S
+    assert f(P, P, P, 1, None, 1, 128, 64, 128, P, 130, None) == 1           # ld % 4
+    assert f(P, P, P, 7, None, 1, 128, 64, 128, P, 128, None) == 1           # bad w dtype
+    assert f(MIS, P, P, 1, None, 1, 128, 64, 128, P, 128, None) == 1         # misaligned
+    assert f(P, P, P, 1, None, 0, 128, 64, 128, P, 128, None) == 1           # B = 0
+    assert f(P, P, P, 1, None, 1, 128, 48, 128, P, 128, None) == 2           # Hi not 2^n
+    assert f(P, P, P, 1, None, 1, 128, 64, 96, P, 128, None) == 2            # Di unsupported
+    assert f(P, P, P, 1, None, 1, 128, 256, 128, P, 128, None) == 2          # Hi > 128
+
+
+def test_topk_validation(dsa):
+    f = dsa.lib.dsa_topk
+    assert f(None, 128, None, 1, 128, 4, P, None, None, 0, None) == 1
+    assert f(P, 127, None, 1, 128, 4, P, None, None, 0, None) == 1
+    assert f(P, 128, None, 1, 128, 0, P, None, None, 0, None) == 1
+    assert f(P, 128, MIS, 1, 128, 4, P, None, None, 0, None) == 1
+
+
+def test_attention_validation(dsa):
+    fwd = dsa.lib.dsa_sparse_attn_fwd
+    # B, S, H, Hkv, Dqk, Dv, k
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 192, 128, 8, 0.1, None, P, None) == 1   # null O
+    assert fwd(P, P, P, P, 1, 64, 16, 3, 192, 128, 8, 0.1, P, P, None) == 1      # H % Hkv
+    assert fwd(P, P, P, P, 1, 64, 16, 16, 192, 128, 8, 0.1, P, P, None) == 2     # Hkv = H
+    assert fwd(P, P, P, P, 1, 64, 256, 1, 192, 128, 8, 0.1, P, P, None) == 2     # H > 128
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 96, 128, 8, 0.1, P, P, None) == 2       # dims
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 100, 128, 8, 0.1, P, P, None) == 1      # Dqk % 16
+    bwd = dsa.lib.dsa_sparse_attn_bwd
+    need = dsa.lib.dsa_sparse_attn_bwd_workspace_size(1, 64, 16, 1, 192, 128)
+    args = [P] * 7 + [1, 64, 16, 1, 192, 128, 8, 0.1] + [P, P, P]
+    assert bwd(*args, None, need, None) == 3                                      # no ws
+    assert bwd(*args, P, need - 4, None) == 3                                     # small ws
+    assert bwd(*([P] * 6 + [None] + args[7:]), P, need, None) == 1                # null dO

@@ -1,0 +1,255 @@
+"""GPU parity: every kernel against the fp64 oracle on the same seeded inputs.
+
+Index scores and top-k index sets must match bit for bit (dyadic indexer
+inputs make every fp32 sum exact). Attention outputs, LSE and gradients must
+satisfy max|err| <= 2e-2 * max|ref| per tensor.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import TOL, bf16_dev, dev, host_f64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def _dsa():
+    import sparse_attention_index_gb300 as dsa
+    return dsa
+
+
+def _indexer_case(B, S, Hi, Di, seed, ndocs=0, w_kind="dyadic"):
+    q = synth.dyadic_bf16((B, S, Hi, Di), seed, synth.STREAM_Q_IDX, -8, 8, 3)
+    k = synth.dyadic_bf16((B, S, Di), seed, synth.STREAM_K_IDX, -8, 8, 3)
+    if w_kind == "dyadic":
+        w = synth.dyadic_f32((B, S, Hi), seed, synth.STREAM_W, -1, 1, 4)
+    else:
+        w = synth.signed_nonzero_f32((B, S, Hi), seed, synth.STREAM_W, 8, 3)
+    seg = synth.segments(B, S, ndocs, seed) if ndocs else None
+    return {"q_idx": q, "k_idx": k, "w": w, "seg": seg}
+
+
+def _check_scores(gpu_scores, ref, rows, S):
+    """Exact equality on s <= t (values; -0 == +0), -inf in the same places."""
+    for r, row in enumerate(rows):
+        b, t = divmod(int(row), S)
+        g = gpu_scores[b, t, : t + 1]
+        o = ref[r, : t + 1]
+        assert np.array_equal(np.isneginf(g), np.isneginf(o)), (b, t)
+        fin = np.isfinite(o)
+        bad = np.nonzero(g[fin] != o[fin])[0]
+        assert bad.size == 0, (b, t, bad[:5], g[fin][bad[:5]], o[fin][bad[:5]])
+
+
+def _run_scores(inp, w_bf16=False):
+    dsa = _dsa()
+    w = dev(inp["w"])
+    if w_bf16:
+        w = w.to(torch.bfloat16)
+    seg = None if inp["seg"] is None else dev(inp["seg"])
+    sc = dsa.dsa_index_scores(bf16_dev(inp["q_idx"]), bf16_dev(inp["k_idx"]), w, seg)
+    assert dsa.dsa_get_last_device_error() == 0
+    return sc
+
+
+# ------------------------------------------------------------------ indexer
+
+INDEXER_CASES = [
+    # B, S, Hi, Di, ndocs, w_kind
+    (1, 128, 4, 32, 0, "signed_nonzero"),
+    (2, 700, 64, 128, 0, "dyadic"),
+    (1, 489, 64, 128, 3, "dyadic"),
+    (1, 300, 1, 64, 0, "dyadic"),
+    (1, 300, 8, 64, 2, "dyadic"),
+    (1, 333, 16, 64, 0, "dyadic"),
+    (1, 257, 32, 32, 0, "dyadic"),
+    (2, 190, 128, 128, 0, "dyadic"),
+]
+
+
+@pytest.mark.parametrize("case", INDEXER_CASES)
+def test_index_scores_exact(case):
+    B, S, Hi, Di, ndocs, w_kind = case
+    inp = _indexer_case(B, S, Hi, Di, seed=100 + S, ndocs=ndocs, w_kind=w_kind)
+    sc = host_f64(_run_scores(inp))
+    ref = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], inp["seg"])
+    _check_scores(sc, ref, np.arange(B * S), S)
+
+
+def test_index_scores_bf16_weights():
+    inp = _indexer_case(1, 260, 64, 128, seed=7)
+    sc = host_f64(_run_scores(inp, w_bf16=True))
+    ref = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], None)
+    _check_scores(sc, ref, np.arange(260), 260)
+
+
+def test_index_scores_leading_dimension():
+    dsa = _dsa()
+    inp = _indexer_case(1, 150, 64, 128, seed=8)
+    scores = torch.full((1, 150, 160), 7.0, device="cuda")
+    dsa.dsa_index_scores(bf16_dev(inp["q_idx"]), bf16_dev(inp["k_idx"]), dev(inp["w"]), None,
+                         scores=scores)
+    ref = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], None)
+    _check_scores(host_f64(scores), ref, np.arange(150), 150)
+    assert torch.all(scores[..., 150:] == 7.0)   # padding columns untouched
+
+
+# ------------------------------------------------------------------- top-k
+
+def _check_topk(idx_gpu, cnt_gpu, scores_f64, seg, S, k, rows):
+    ref_idx, ref_cnt = oracle.topk(scores_f64, seg, S, k, rows=rows, B=idx_gpu.shape[0])
+    flat_idx = idx_gpu.reshape(-1, k)[rows]
+    flat_cnt = cnt_gpu.reshape(-1)[rows]
+    for r in range(len(rows)):
+        assert np.array_equal(flat_idx[r], ref_idx[r]), (int(rows[r]), flat_idx[r][:8],
+                                                         ref_idx[r][:8])
+    assert np.array_equal(flat_cnt, ref_cnt)
+
+
+@pytest.mark.parametrize("case", INDEXER_CASES[:4])
+@pytest.mark.parametrize("k", [1, 4, 37, 300])
+def test_topk_on_gpu_scores_exact(case, k):
+    dsa = _dsa()
+    B, S, Hi, Di, ndocs, w_kind = case
+    inp = _indexer_case(B, S, Hi, Di, seed=200 + S, ndocs=ndocs, w_kind=w_kind)
+    sc = _run_scores(inp)
+    seg = None if inp["seg"] is None else dev(inp["seg"])
+    idx, cnt = dsa.dsa_topk(sc, k, seg)
+    rows = np.arange(B * S)
+    sc64 = host_f64(sc[:, :, :S]).reshape(B * S, S)
+    _check_topk(idx.cpu().numpy(), cnt.cpu().numpy(), sc64, inp["seg"], S, k, rows)
+
+
+@pytest.mark.parametrize("ndocs", [0, 3])
+@pytest.mark.parametrize("k", [1, 2, 64, 999, 2000])
+def test_topk_heavy_ties(ndocs, k):
+    """Scores from a 7-value set with both zeros: ties decide most of the selection."""
+    dsa = _dsa()
+    B, S = 2, 1000
+    rng = np.random.default_rng(ndocs * 100 + k)
+    vals = np.array([-2.0, -0.5, -0.0, 0.0, 0.25, 0.25, 1.0], dtype=np.float32)
+    sc = vals[rng.integers(0, len(vals), size=(B, S, S))]
+    seg = synth.segments(B, S, ndocs, 9) if ndocs else None
+    sct = dev(sc)
+    idx, cnt = dsa.dsa_topk(sct, k, None if seg is None else dev(seg))
+    _check_topk(idx.cpu().numpy(), cnt.cpu().numpy(), sc.reshape(B * S, S).astype(np.float64),
+                seg, S, k, np.arange(B * S))
+
+
+def test_topk_rows_longer_than_the_shared_stage():
+    dsa = _dsa()
+    S, k = 17000, 100
+    rng = np.random.default_rng(3)
+    sc = rng.standard_normal((1, S, S), dtype=np.float32)
+    sc[0, -1, ::7] = 3.5   # ties at the top of the last row
+    idx, cnt = dsa.dsa_topk(dev(sc), k)
+    rows = np.array([0, 50, 16383, 16384, 16385, 16999], dtype=np.int64)
+    _check_topk(idx.cpu().numpy(), cnt.cpu().numpy(), sc[0][rows].astype(np.float64), None, S,
+                k, rows)
+
+
+def test_topk_golden_fixtures_on_gpu():
+    from test_oracle_pins import _parse_golden
+    dsa = _dsa()
+    for k, seg, scores, expect in _parse_golden():
+        S = len(scores)
+        sc = np.zeros((1, S, (S + 3) // 4 * 4), dtype=np.float32)
+        sc[0, S - 1, :S] = scores
+        segt = None if seg is None else dev(np.array([seg], dtype=np.int32))
+        idx, cnt = dsa.dsa_topk(dev(sc), k, segt, S=S)
+        assert idx[0, S - 1].cpu().tolist() == expect
+
+
+# --------------------------------------------------------------- attention
+
+ATTN_CASES = [
+    # B, S, H, Dqk, Dv, k, ndocs
+    (1, 128, 2, 32, 32, 4, 0),
+    (1, 489, 16, 192, 128, 512, 3),
+    (1, 300, 128, 192, 128, 64, 0),
+    (2, 200, 16, 192, 128, 100, 0),
+    (1, 150, 64, 128, 128, 40, 0),
+    (1, 130, 32, 64, 64, 33, 2),
+    (1, 100, 8, 192, 128, 7, 0),
+    (1, 96, 128, 192, 128, 200, 0),
+]
+
+
+def _attn_case(B, S, H, Dqk, Dv, k, ndocs, seed):
+    Q = synth.normal_bf16((B, S, H, Dqk), seed, synth.STREAM_Q)
+    K = synth.normal_bf16((B, S, 1, Dqk), seed, synth.STREAM_K)
+    V = synth.normal_bf16((B, S, 1, Dv), seed, synth.STREAM_V)
+    dO = synth.normal_bf16((B, S, H, Dv), seed, synth.STREAM_DO)
+    ind = _indexer_case(B, S, 4, 32, seed, ndocs=ndocs)
+    sc = oracle.index_scores(ind["q_idx"], ind["k_idx"], ind["w"], ind["seg"])
+    idx, _ = oracle.topk(sc, ind["seg"], S, k, B=B)
+    return Q, K, V, dO, idx.reshape(B, S, k)
+
+
+@pytest.mark.parametrize("case", ATTN_CASES)
+def test_sparse_attn_fwd_bwd(case):
+    dsa = _dsa()
+    B, S, H, Dqk, Dv, k, ndocs = case
+    Q, K, V, dO, idx = _attn_case(*case, seed=300 + S + H)
+    scale = 1.0 / np.sqrt(Dqk)
+    Qd, Kd, Vd, dOd, idxd = bf16_dev(Q), bf16_dev(K), bf16_dev(V), bf16_dev(dO), dev(idx)
+    O, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, idxd, scale)
+    dQ, dK, dV = dsa.dsa_sparse_attn_bwd(Qd, Kd, Vd, idxd, O, lse, dOd, scale)
+    assert dsa.dsa_get_last_device_error() == 0
+    O_ref, lse_ref = oracle.attn_fwd(Q, K, V, idx, scale)
+    assert rel_err(host_f64(O).reshape(O_ref.shape), O_ref) <= TOL
+    assert rel_err(host_f64(lse).reshape(lse_ref.shape), lse_ref) <= TOL
+    dQ_ref, dK_ref, dV_ref = oracle.attn_bwd(Q, K, V, idx, dO, scale)
+    assert rel_err(host_f64(dQ).reshape(dQ_ref.shape), dQ_ref) <= TOL
+    assert rel_err(host_f64(dK), dK_ref) <= TOL
+    assert rel_err(host_f64(dV), dV_ref) <= TOL
+
+
+def test_sparse_attn_user_index_lists():
+    """-1 anywhere, entries above the diagonal, empty rows, unsorted lists."""
+    dsa = _dsa()
+    B, S, H, Dqk, Dv, k = 1, 80, 16, 192, 128, 70
+    Q, K, V, dO, _ = _attn_case(B, S, H, Dqk, Dv, 8, 0, seed=5)
+    rng = np.random.default_rng(11)
+    idx = np.full((B, S, k), -1, dtype=np.int32)
+    for t in range(S):
+        if t % 9 == 4:
+            continue                                    # empty row
+        pick = rng.choice(S, size=min(S, k), replace=False).astype(np.int32)
+        pick[rng.random(pick.size) < 0.2] = -1          # holes
+        idx[0, t] = pick                                # some above the diagonal
+    scale = 0.1
+    Qd, Kd, Vd, dOd, idxd = bf16_dev(Q), bf16_dev(K), bf16_dev(V), bf16_dev(dO), dev(idx)
+    O, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, idxd, scale)
+    dQ, dK, dV = dsa.dsa_sparse_attn_bwd(Qd, Kd, Vd, idxd, O, lse, dOd, scale)
+    assert dsa.dsa_get_last_device_error() == 0
+    O_ref, lse_ref = oracle.attn_fwd(Q, K, V, idx, scale)
+    assert rel_err(host_f64(O).reshape(O_ref.shape), O_ref) <= TOL
+    lg = host_f64(lse).reshape(lse_ref.shape)
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    assert rel_err(lg[fin], lse_ref[fin]) <= TOL
+    dQ_ref, dK_ref, dV_ref = oracle.attn_bwd(Q, K, V, idx, dO, scale)
+    assert rel_err(host_f64(dQ).reshape(dQ_ref.shape), dQ_ref) <= TOL
+    assert rel_err(host_f64(dK), dK_ref) <= TOL
+    assert rel_err(host_f64(dV), dV_ref) <= TOL
+
+
+def test_bad_index_is_reported_not_faulted():
+    dsa = _dsa()
+    B, S, H, D, k = 1, 40, 16, 64, 8
+    Q, K, V, dO, idx = _attn_case(B, S, H, D, D, k, 0, seed=6)
+    idx = idx.copy()
+    idx[0, 30, 0] = S + 5      # out of range: skipped and reported
+    Qd, Kd, Vd = bf16_dev(Q), bf16_dev(K), bf16_dev(V)
+    dsa.dsa_get_last_device_error()
+    O, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, dev(idx), 0.125)
+    code = dsa.dsa_get_last_device_error()
+    assert code == (0x300 | 0x02)
+    assert dsa.dsa_get_last_device_error() == 0   # cleared by the read
+    idx_ok = idx.copy()
+    idx_ok[0, 30, 0] = -1
+    O_ref, _ = oracle.attn_fwd(Q, K, V, idx_ok, 0.125)
+    assert rel_err(host_f64(O).reshape(O_ref.shape), O_ref) <= TOL
