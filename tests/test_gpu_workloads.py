@@ -1,0 +1,95 @@
+"""Full-size workloads, run exactly as bench.py launches them, checked on samples.
+
+At these sizes the oracle cannot recompute everything, so the checks are:
+* index scores and top-k sets: bit-exact on sampled query rows
+  (t = 0, k-1, k, S-1 and uniform draws, per batch row);
+* attention output / LSE and dQ: within 2e-2 * max|ref| on the sampled rows;
+* dK / dV: exact reference for the last keys of every batch row (key s only
+  receives gradient from queries t >= s, so the oracle over the last rows
+  gives those keys completely);
+* sum over keys of dV equals the sum over queries and heads of dO (softmax
+  weights sum to one), at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import TOL, bf16_dev, dev, host_f64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+TAIL = 48
+
+
+def _run(wl):
+    import sparse_attention_index_gb300 as dsa
+    ind = synth.indexer_inputs(wl)
+    att = synth.attention_inputs(wl)
+    seg = None if ind["seg"] is None else dev(ind["seg"])
+    out = dsa.dsa_layer(bf16_dev(ind["q_idx"]), bf16_dev(ind["k_idx"]), dev(ind["w"]),
+                        bf16_dev(att["Q"]), bf16_dev(att["K"]), bf16_dev(att["V"]), wl.topk,
+                        wl.scale, seg=seg, dO=bf16_dev(att["dO"]) if wl.backward else None)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_last_device_error() == 0
+    return ind, att, out
+
+
+def _check(wl, n_uniform):
+    ind, att, out = _run(wl)
+    rows = synth.sample_rows(wl, n_uniform)
+    S, k = wl.S, wl.topk
+    b_idx, t_idx = rows // S, rows % S
+
+    # index scores, bit-exact on the sampled rows
+    ref_sc = oracle.index_scores(ind["q_idx"], ind["k_idx"], ind["w"], ind["seg"], rows=rows)
+    gsc = out["scores"][torch.as_tensor(b_idx), torch.as_tensor(t_idx), :S].double().cpu().numpy()
+    for r in range(rows.size):
+        t = t_idx[r]
+        g, o = gsc[r, : t + 1], ref_sc[r, : t + 1]
+        assert np.array_equal(np.isneginf(g), np.isneginf(o))
+        fin = np.isfinite(o)
+        assert np.array_equal(g[fin], o[fin]), (int(rows[r]),)
+
+    # top-k sets, bit-exact
+    ref_idx, ref_cnt = oracle.topk(ref_sc, ind["seg"], S, k, rows=rows, B=wl.B)
+    idx = out["idx"].cpu().numpy()
+    assert np.array_equal(idx.reshape(-1, k)[rows], ref_idx)
+    assert np.array_equal(out["count"].cpu().numpy().reshape(-1)[rows], ref_cnt)
+
+    # attention forward on the sampled rows (GPU selection == oracle selection there)
+    O_ref, lse_ref = oracle.attn_fwd(att["Q"], att["K"], att["V"], idx, wl.scale, rows=rows)
+    O = out["O"].reshape(wl.B * S, wl.H, wl.Dv)[torch.as_tensor(rows)]
+    lse = out["lse"].reshape(wl.B * S, wl.H)[torch.as_tensor(rows)]
+    assert rel_err(host_f64(O), O_ref) <= TOL
+    assert rel_err(host_f64(lse), lse_ref) <= TOL
+
+    if not wl.backward:
+        return
+    dQ_ref, _, _ = oracle.attn_bwd(att["Q"], att["K"], att["V"], idx, att["dO"], wl.scale,
+                                   rows=rows)
+    dQ = out["dQ"].reshape(wl.B * S, wl.H, wl.Dqk)[torch.as_tensor(rows)]
+    assert rel_err(host_f64(dQ), dQ_ref) <= TOL
+    tail_rows = np.concatenate([b * S + np.arange(S - TAIL, S) for b in range(wl.B)])
+    _, dK_ref, dV_ref = oracle.attn_bwd(att["Q"], att["K"], att["V"], idx, att["dO"], wl.scale,
+                                        rows=tail_rows)
+    dK = host_f64(out["dK"][:, S - TAIL:])
+    dV = host_f64(out["dV"][:, S - TAIL:])
+    assert rel_err(dK, dK_ref[:, S - TAIL:]) <= TOL
+    assert rel_err(dV, dV_ref[:, S - TAIL:]) <= TOL
+    # sum_s dV[s] = sum_{t,h} dO[t,h]
+    dv_sum = out["dV"].double().sum(dim=(1, 2)).cpu().numpy()
+    do_sum = bf16_dev(att["dO"]).double().sum(dim=(1, 2)).cpu().numpy()
+    assert rel_err(dv_sum, do_sum) <= TOL
+
+
+@pytest.mark.parametrize("name", ["tiny_s128", "packed_s489", "small2b_s4096", "packed_s4096",
+                                  "v32_671b_s16k"])
+def test_workload(name):
+    _check(synth.WORKLOADS[name], n_uniform=12)
+
+
+@pytest.mark.slow
+def test_long_context_workload():
+    _check(synth.WORKLOADS["long_s128k"], n_uniform=6)
