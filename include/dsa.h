@@ -166,6 +166,37 @@ int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32
                         int Hkv, int Dqk, int Dv, int k, float scale, void* dQ, void* dK, void* dV,
                         void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * dsa_sparse_attn_bwd_noalloc - dsa_sparse_attn_bwd for callers that cannot
+ * allocate device memory. The pages have no counterpart: this is a
+ * deployment variant of the same backward pass, not part of the method.
+ *
+ * Callers that are handed their input and output buffers by a host program
+ * and cannot obtain more device memory (a plugin inside a runtime that owns
+ * every allocation through its own pool, or code that must not call
+ * cudaMalloc while it runs because an allocation there can fail or stall the
+ * device) cannot pass the fp32 workspace of dsa_sparse_attn_bwd. This entry
+ * point takes the same tensors without it and keeps the dK/dV accumulator in
+ * a fixed array inside the library: DSA_NOALLOC_BWD_MAX_FLOATS floats
+ * (32 MiB), held on every GPU that loads the library until the process exits.
+ *
+ *  - Limit: B * S * Hkv * (Dqk + Dv) must not exceed DSA_NOALLOC_BWD_MAX_FLOATS
+ *    (e.g. 26214 tokens at Dqk + Dv = 320); larger calls return
+ *    DSA_ERR_WORKSPACE and launch nothing.
+ *  - Nothing is allocated or freed. The first call on a device looks up the
+ *    array's device address (cudaGetSymbolAddress) with that device current;
+ *    make that first call before any stream capture.
+ *  - Every call shares the one array and zeroes the part it uses before
+ *    accumulating, so calls whose work overlaps on the GPU (two streams, or
+ *    two host threads) race and corrupt each other's dK/dV. Serialise them.
+ *  - Arguments, supported shapes and results are those of dsa_sparse_attn_bwd.
+ */
+#define DSA_NOALLOC_BWD_MAX_FLOATS 8388608
+int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const void* V, const int32_t* idx,
+                                const void* O, const float* lse, const void* dO, int B, int S,
+                                int H, int Hkv, int Dqk, int Dv, int k, float scale, void* dQ,
+                                void* dK, void* dV, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -30,7 +30,8 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 # every symbol include/dsa.h declares
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa_index_scores",
            "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd",
-           "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd")
+           "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
+           "dsa_sparse_attn_bwd_noalloc")
 
 
 class DsaError(RuntimeError):
@@ -59,8 +60,10 @@ def _load() -> ctypes.CDLL:
     lib.dsa_sparse_attn_bwd_workspace_size.restype = sz
     lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
                                         vp, vp, vp, vp, sz, vp]
+    lib.dsa_sparse_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci,
+                                                ci, ci, cf, vp, vp, vp, vp]
     for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_topk",
-                 "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd"):
+                 "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_sparse_attn_bwd_noalloc"):
         getattr(lib, name).restype = ci
     return lib
 
@@ -182,6 +185,30 @@ def dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, scale: float, dQ=None, dK=None
                                  _dev(dK, "dK", torch.bfloat16), _dev(dV, "dV", torch.bfloat16),
                                  _dev(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
     _check(rc, "dsa_sparse_attn_bwd")
+    return dQ, dK, dV
+
+
+def dsa_sparse_attn_bwd_noalloc(Q, K, V, idx, O, lse, dO, scale: float, dQ=None, dK=None,
+                                dV=None, stream=None):
+    """dsa_sparse_attn_bwd without a caller workspace: the library's fixed
+    accumulator is used (see include/dsa.h for its size limit)."""
+    B, S, H, Dqk = Q.shape
+    Hkv, Dv = V.shape[2], V.shape[3]
+    k = idx.shape[2]
+    dev = Q.device
+    if dQ is None:
+        dQ = torch.empty_like(Q)
+    if dK is None:
+        dK = torch.empty((B, S, Hkv, Dqk), dtype=torch.bfloat16, device=dev)
+    if dV is None:
+        dV = torch.empty((B, S, Hkv, Dv), dtype=torch.bfloat16, device=dev)
+    rc = lib.dsa_sparse_attn_bwd_noalloc(
+        _dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16), _dev(V, "V", torch.bfloat16),
+        _dev(idx, "idx", torch.int32), _dev(O, "O", torch.bfloat16),
+        _dev(lse, "lse", torch.float32), _dev(dO, "dO", torch.bfloat16), B, S, H, Hkv, Dqk, Dv, k,
+        float(scale), _dev(dQ, "dQ", torch.bfloat16), _dev(dK, "dK", torch.bfloat16),
+        _dev(dV, "dV", torch.bfloat16), _stream(stream))
+    _check(rc, "dsa_sparse_attn_bwd_noalloc")
     return dQ, dK, dV
 
 
