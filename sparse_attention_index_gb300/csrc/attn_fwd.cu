@@ -190,7 +190,8 @@ int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* 
   p.O = static_cast<uint16_t*>(O);
   p.lse = lse;
   const long long rows = static_cast<long long>(B) * S;
-  if (rows > 0x7fffffffLL || H > 128) return DSA_ERR_UNSUPPORTED;
+  if (rows * H > 0x7fffffffLL || H > 128) return DSA_ERR_UNSUPPORTED;
+  if (attn_fwd_tc_supported(H, Dqk, Dv, scale)) return launch_attn_fwd_tc(p, Dqk, Dv, stream);
   if (Dqk == 192 && Dv == 128) return launch_fwd_dims<192, 128>(p, rows, stream);
   if (Dqk == 128 && Dv == 128) return launch_fwd_dims<128, 128>(p, rows, stream);
   if (Dqk == 64 && Dv == 64) return launch_fwd_dims<64, 64>(p, rows, stream);

@@ -37,6 +37,10 @@ inline AttnParams make_attn_params(const void* Q, const void* K, const void* V,
   return p;
 }
 
+// tcgen05 forward (attn_fwd_tc.cu): used for 64 < H <= 128 heads and a positive scale.
+bool attn_fwd_tc_supported(int H, int Dqk, int Dv, float scale);
+int launch_attn_fwd_tc(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream);
+
 // Shared-memory layout of the forward kernel: Q rows, two K/V chunk buffers
 // (rows padded by 16 bytes so ldmatrix row addresses hit distinct banks), a
 // small header and the query's index row.

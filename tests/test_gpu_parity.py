@@ -174,6 +174,10 @@ ATTN_CASES = [
     (1, 130, 32, 64, 64, 33, 2),
     (1, 100, 8, 192, 128, 7, 0),
     (1, 96, 128, 192, 128, 200, 0),
+    (1, 260, 128, 128, 128, 150, 0),
+    (1, 200, 96, 192, 128, 97, 2),
+    (2, 150, 128, 192, 128, 300, 0),
+    (1, 700, 128, 192, 128, 512, 3),
 ]
 
 
@@ -207,10 +211,11 @@ def test_sparse_attn_fwd_bwd(case):
     assert rel_err(host_f64(dV), dV_ref) <= TOL
 
 
-def test_sparse_attn_user_index_lists():
+@pytest.mark.parametrize("H", [16, 128])
+def test_sparse_attn_user_index_lists(H):
     """-1 anywhere, entries above the diagonal, empty rows, unsorted lists."""
     dsa = _dsa()
-    B, S, H, Dqk, Dv, k = 1, 80, 16, 192, 128, 70
+    B, S, Dqk, Dv, k = 1, 80, 192, 128, 70
     Q, K, V, dO, _ = _attn_case(B, S, H, Dqk, Dv, 8, 0, seed=5)
     rng = np.random.default_rng(11)
     idx = np.full((B, S, k), -1, dtype=np.int32)
