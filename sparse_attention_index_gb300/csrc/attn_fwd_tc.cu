@@ -17,12 +17,13 @@
 // which bf16 and fp32 hold as well as with a fresh max, and the final O / l is
 // unchanged.
 //
-// Persistent CTA (one per SM), warp-specialised, 256 threads:
-//   warps 0-2  gather: per chunk of NK = 96 selected keys, 16-byte cp.async of the K
-//              and V rows into 128B-swizzled tiles (3 stages); the copy hardware
-//              signals each stage when its rows have landed
-//   warp  3    TMEM owner and single-thread UMMA issuer
-//   warps 4-7  softmax / output: Q row -> TMEM, softmax, P -> TMEM, final O and LSE
+// Persistent CTA (one per SM), warp-specialised, 384 threads:
+//   warps 0-3   softmax / output: Q row -> TMEM, softmax, P -> TMEM, final O and LSE
+//   warp  4     TMEM owner and single-thread UMMA issuer
+//   warps 5-11  gather: per chunk of NK = 96 selected keys, 16-byte cp.async of the K
+//               and V rows into 128B-swizzled tiles (3 stages), four keys per group so
+//               that every copy instruction uses all 32 lanes; the copy hardware
+//               signals each stage when its rows have landed
 // TMEM: [Q: Dqk/2 cols][S/P: 3 buffers x NK cols][O: Dv cols] = 512 columns.
 // Query rows are handed out longest first, strided over CTAs.
 
@@ -33,8 +34,10 @@ namespace {
 
 constexpr int kNK = 96;              // keys per chunk (UMMA N of S; K of PV)
 constexpr int kStages = 3;           // K/V stages == S/P buffers
-constexpr int kGatherThreads = kNK;  // one gather thread owns one key slot (3 warps)
-constexpr int kThreads = 256;
+constexpr int kGatherWarp0 = 5;
+constexpr int kGatherWarps = 7;
+constexpr int kGatherThreads = 32 * kGatherWarps;
+constexpr int kThreads = 384;
 constexpr int kErrTc = DSA_STAGE_FWD | DSA_DEVERR_TIMEOUT;
 constexpr float kRescaleLog2 = 8.f;  // refresh the running max when it grows by > 2^8
 
@@ -61,6 +64,7 @@ struct ChunkHeader {
 
 struct TcTail {
   ChunkHeader hdr[kStages];
+  int key[kStages][kNK];   // key index per slot of each stage (-1: none)
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t s_full[kStages], s_empty[kStages], p_full[kStages];
   uint64_t q_tmem_full, o_free;
@@ -68,7 +72,7 @@ struct TcTail {
   uint32_t tmem_base;
   int abort_flag;
   int okb[2];
-  int red[4];
+  int red[kGatherWarps];
 };
 
 __device__ __forceinline__ void bar_gather() {
@@ -80,7 +84,7 @@ __device__ __forceinline__ void bar_gather() {
 // one sample after it (two slots, so a fast thread 0 cannot overwrite a verdict
 // a slow thread has yet to read).
 __device__ __forceinline__ bool bar_gather_ok(int* okb, int& nb, volatile int* abort_flag) {
-  if (threadIdx.x == 0) okb[nb & 1] = (*abort_flag == 0);
+  if (threadIdx.x == 32 * kGatherWarp0) okb[nb & 1] = (*abort_flag == 0);
   bar_gather();
   const bool ok = reinterpret_cast<volatile int*>(okb)[nb & 1] != 0;
   ++nb;
@@ -125,6 +129,12 @@ __device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
       : "memory");
 }
 
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnParams p) {
   using L = TcFwdLayout<DQK, DV>;
@@ -153,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
     tail->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 3) {
+  if (warp == 4) {
     tmem_alloc(&tail->tmem_base, 512);
     tmem_relinquish();
   }
@@ -162,12 +172,32 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
   tc_fence_after();
   const uint32_t tmem = tail->tmem_base;
 
-  if (warp < 3) {
+  if (warp >= kGatherWarp0) {
     // ================================================================ gather
     // Every gather thread takes part in each step, so the named barriers always
     // see all of them; a timed-out wait sets the abort flag, which all read after
-    // the next barrier. Thread r owns key slot r of every chunk.
-    const int r = threadIdx.x;
+    // the next barrier. Gather thread gt < NK owns key slot gt of every chunk.
+    const int gt = threadIdx.x - 32 * kGatherWarp0;
+    const int gw = warp - kGatherWarp0;
+    constexpr int PK = DQK / 8, PV = DV / 8;     // 16-byte pieces of a K / V row
+    constexpr int KI = PK / 8, VI = PV / 8;      // copy instructions per group of 4 keys
+    // this lane's (key in group, piece) for each instruction of a group
+    int k_kig[KI], k_off[KI], v_kig[VI], v_off[VI];
+    uint32_t k_dst[KI], v_dst[VI];
+#pragma unroll
+    for (int i = 0; i < KI; ++i) {
+      const int q = i * 32 + lane, pc = q % PK;
+      k_kig[i] = q / PK;
+      k_off[i] = pc * 8;
+      k_dst[i] = (pc >> 3) * L::kAtom + ((pc & 7) << 4);
+    }
+#pragma unroll
+    for (int i = 0; i < VI; ++i) {
+      const int q = i * 32 + lane, pv = q % PV;
+      v_kig[i] = q / PV;
+      v_off[i] = pv * 8;
+      v_dst[i] = (L::KA + (pv >> 3)) * L::kAtom + ((pv & 7) << 4);
+    }
     int g = 0, nb = 0;
     for (int i = blockIdx.x; i < nrows; i += gridDim.x) {
       const long long row = row_of(i, nrows);
@@ -176,61 +206,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
       const int32_t* irow = p.idx + row * p.k;
       // kend: one past the last slot holding a causal key (independent loads)
       int last = 0;
-#pragma unroll 4
-      for (int j = r; j < p.k; j += kGatherThreads) {
+#pragma unroll 10
+      for (int j = gt; j < p.k; j += kGatherThreads) {
         const int s = __ldg(irow + j);
         if (s >= 0 && s <= t && s < p.S) last = j + 1;
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-      if (lane == 0) tail->red[warp] = last;
+      if (lane == 0) tail->red[gw] = last;
       if (!bar_gather_ok(tail->okb, nb, abort_flag)) break;
-      const int kend = max(max(tail->red[0], tail->red[1]), tail->red[2]);
+      int kend = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kGatherWarps; ++w2) kend = max(kend, tail->red[w2]);
       const int nch = kend > 0 ? (kend + kNK - 1) / kNK : 1;
-      int s_next = load_key(p, irow, r, kend, t);
+      int s_next = gt < kNK ? load_key(p, irow, gt, kend, t) : -1;
       bool stop = false;
       for (int c = 0; c < nch; ++c, ++g) {
         const int st = g % kStages;
         const int s = s_next;
-        if (c + 1 < nch) s_next = load_key(p, irow, (c + 1) * kNK + r, kend, t);
+        if (gt < kNK && c + 1 < nch) s_next = load_key(p, irow, (c + 1) * kNK + gt, kend, t);
         mbar_wait(&tail->kv_empty[st], ((g / kStages) & 1) ^ 1u, abort_flag, p.err, kErrTc);
         ChunkHeader& h = tail->hdr[st];
-        const uint32_t bal = __ballot_sync(0xffffffffu, s >= 0);
-        if (lane == 0) h.valid[warp] = bal;
-        if (r == 0) {
+        if (gt < kNK) {
+          tail->key[st][gt] = s;
+          const uint32_t bal = __ballot_sync(0xffffffffu, s >= 0);
+          if (lane == 0) h.valid[gw] = bal;
+        }
+        if (gt == 0) {
           h.row = static_cast<int>(row);
           h.first = c == 0;
           h.last = c == nch - 1;
         }
         if (!bar_gather_ok(tail->okb, nb, abort_flag)) { stop = true; break; }
         mbar_arrive(&tail->kv_full[st]);   // releases this thread's header writes
-        // this warp copies the rows of its own 32 key slots, lanes over 16-byte pieces
-        uint8_t* stage = smem + st * L::kStage;
-        for (int kk = 0; kk < 32; ++kk) {
-          const int key = warp * 32 + kk;
-          const int ks = __shfl_sync(0xffffffffu, s, kk);
-          const bool valid = ks >= 0;
-          const long long kv = static_cast<long long>(b) * p.S + (valid ? ks : 0);
+        const uint32_t stage = smem_u32(smem + st * L::kStage);
+        const long long rowbase = static_cast<long long>(b) * p.S;
+        for (int grp = gw; grp < kNK / 4; grp += kGatherWarps) {
+          const int4 kq = *reinterpret_cast<const int4*>(&tail->key[st][grp * 4]);
+          const int keys[4] = {kq.x, kq.y, kq.z, kq.w};
 #pragma unroll
-          for (int pc0 = 0; pc0 < L::PIECES; pc0 += 32) {
-            const int pc = pc0 + lane;
-            if (pc < L::PIECES) {
-              const uint16_t* src;
-              uint32_t atom, cc;
-              if (pc < DQK / 8) {
-                src = p.K + kv * DQK + pc * 8;
-                atom = pc >> 3;
-                cc = pc & 7;
-              } else {
-                const int pv = pc - DQK / 8;
-                src = p.V + kv * DV + pv * 8;
-                atom = L::KA + (pv >> 3);
-                cc = pv & 7;
-              }
-              const uint32_t dst = smem_u32(stage + atom * L::kAtom + key * 128) +
-                                   ((cc ^ static_cast<uint32_t>(key & 7)) << 4);
-              cp_async_16(dst, src, valid ? 16u : 0u);
-            }
+          for (int ii = 0; ii < KI; ++ii) {
+            const int kig = k_kig[ii], key = grp * 4 + kig;
+            const int ks = kig == 0 ? keys[0] : (kig == 1 ? keys[1] : (kig == 2 ? keys[2] : keys[3]));
+            const long long kv = rowbase + (ks >= 0 ? ks : 0);
+            const uint32_t dst = stage + key * 128 + (k_dst[ii] ^ ((key & 7) << 4));
+            cp_async_16(dst, p.K + kv * DQK + k_off[ii], ks >= 0 ? 16u : 0u);
+          }
+#pragma unroll
+          for (int ii = 0; ii < VI; ++ii) {
+            const int kig = v_kig[ii], key = grp * 4 + kig;
+            const int ks = kig == 0 ? keys[0] : (kig == 1 ? keys[1] : (kig == 2 ? keys[2] : keys[3]));
+            const long long kv = rowbase + (ks >= 0 ? ks : 0);
+            const uint32_t dst = stage + key * 128 + (v_dst[ii] ^ ((key & 7) << 4));
+            cp_async_16(dst, p.V + kv * DV + v_off[ii], ks >= 0 ? 16u : 0u);
           }
         }
         // second arrival, made by the copy hardware once this thread's copies have landed
@@ -239,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
       if (stop) break;
     }
     cp_async_wait<0>();
-  } else if (warp == 3) {
+  } else if (warp == 4) {
     // ================================================================ UMMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16_mn(128, kNK, false);
@@ -325,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
     }
   } else {
     // ================================================================ softmax / output
-    const int quarter = warp & 3;
+    const int quarter = warp;                              // warps 0-3: TMEM lane quarters
     const int hrow = quarter * 32 + lane;                  // head of this thread
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.scale_log2;
@@ -441,8 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            float e0 = exp2f(fmaf(__uint_as_float(sv[j]), c2, -base));
-            float e1 = exp2f(fmaf(__uint_as_float(sv[j + 1]), c2, -base));
+            float e0 = ex2(fmaf(__uint_as_float(sv[j]), c2, -base));
+            float e1 = ex2(fmaf(__uint_as_float(sv[j + 1]), c2, -base));
             if (!all_valid) {
               e0 = ((vm >> j) & 1u) ? e0 : 0.f;
               e1 = ((vm >> (j + 1)) & 1u) ? e1 : 0.f;
@@ -501,7 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 3) tmem_dealloc(tmem, 512);
+  if (warp == 4) tmem_dealloc(tmem, 512);
 }
 
 template <int DQK, int DV>
