@@ -311,12 +311,13 @@ int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* 
   p.dQ = static_cast<uint16_t*>(dQ);
   p.ws = ws_dkv;
   const long long rows = static_cast<long long>(B) * S;
-  if (rows > 0x7fffffffLL || H > 128) return DSA_ERR_UNSUPPORTED;
+  if (rows * H > 0x7fffffffLL || H > 128) return DSA_ERR_UNSUPPORTED;
   if (cudaMemsetAsync(ws_dkv, 0, static_cast<size_t>(rows) * (Dqk + Dv) * sizeof(float),
                       stream) != cudaSuccess)
     return DSA_ERR_CUDA;
   int rc;
-  if (Dqk == 192 && Dv == 128) rc = launch_bwd_dims<192, 128>(p, rows, stream);
+  if (attn_bwd_tc_supported(H, Dqk, Dv, scale)) rc = launch_attn_bwd_tc(p, stream);
+  else if (Dqk == 192 && Dv == 128) rc = launch_bwd_dims<192, 128>(p, rows, stream);
   else if (Dqk == 128 && Dv == 128) rc = launch_bwd_dims<128, 128>(p, rows, stream);
   else if (Dqk == 64 && Dv == 64) rc = launch_bwd_dims<64, 64>(p, rows, stream);
   else if (Dqk == 32 && Dv == 32) rc = launch_bwd_dims<32, 32>(p, rows, stream);

@@ -1,0 +1,593 @@
+// Sparse attention backward on the 5th-generation tensor cores, for 64 < H <= 128 heads.
+//
+// ("Support Ring Attention with DeepSeek DSA Sparse Indexer", Backward Flow
+// step 6: dQ = dP K, dK = dP^T Q, dV = P^T dO over the same mask, "dP" read as
+// the gradient of the logits.)
+//
+// Per query row t (all heads; the row's selected keys in chunks of NK = 64):
+//
+//   S   = Q . K_c^T            M = heads, N = keys   A = Q   (smem, K-major)   B = K_c (K-major)
+//   dP  = dO . V_c^T           M = heads, N = keys   A = dO  (smem, K-major)   B = V_c (K-major)
+//   P   = exp2(S*scale*log2e - lse*log2e), dS = P (dP - Delta)      softmax warps -> bf16 tiles
+//   dQ += dS . K_c             M = heads, N = Dqk    A = dS  (smem, K-major)   B = K_c (MN-major)
+//   dK_c^T = Q^T . dS          M = dims,  N = keys   A = Q   (smem, MN-major)  B = dS  (MN-major)
+//   dV_c^T = dO^T . P          M = dims,  N = keys   A = dO  (smem, MN-major)  B = P   (MN-major)
+//
+// The same shared tiles serve as K-major and MN-major operands. dK/dV are
+// produced transposed (a TMEM lane per dimension), so the fp32 reductions
+// that add them into the [B*S, Dqk+Dv] accumulator are row-contiguous: a warp
+// covers 32 consecutive floats of one key row per instruction. dQ stays in
+// TMEM for the whole row. Delta = sum_c dO O is formed at the start of each row.
+//
+// Persistent CTA (one per SM), 384 threads:
+//   warps 0-3   softmax: Delta, P and dS tiles, final dQ (one head per thread)
+//   warps 4-7   drain: dK^T / dV^T from TMEM -> fp32 reductions (one dim per thread)
+//   warp  8     TMEM owner and single-thread UMMA issuer
+//   warps 9-11  gather: K/V rows of each chunk (cp.async, 2 stages)
+// The MMA thread also loads each row's Q / dO tiles (TMA) once the previous row's
+// MMAs have released them.
+// TMEM: dQ [0,192) S [192,256) dP [256,320) dK^T lo [320,384) hi [384,448) dV^T [448,512).
+
+#include "dsa_attn_common.cuh"
+
+namespace dsa {
+namespace {
+
+constexpr int NK = 64;               // keys per chunk
+constexpr int kStages = 2;           // K/V gather stages
+constexpr int kKeyRing = 4;          // key lists of chunks in flight
+constexpr int kGatherWarp0 = 9;
+constexpr int kGatherWarps = 3;
+constexpr int kGatherThreads = 32 * kGatherWarps;
+constexpr int kThreads = 384;
+constexpr int kErrB = DSA_STAGE_BWD | DSA_DEVERR_TIMEOUT;
+
+// Dqk = 192, Dv = 128
+constexpr int DQK = 192, DV = 128;
+constexpr uint32_t kQAtom = 128 * 128;           // [128 head rows x 64 dims]
+constexpr uint32_t kQOff = 0;                    // 3 atoms
+constexpr uint32_t kDOOff = 3 * kQAtom;          // 2 atoms, right after Q
+constexpr uint32_t kKVAtom = NK * 128;           // [64 key rows x 64 dims]
+constexpr uint32_t kKVStage = 5 * kKVAtom;       // K: 3 atoms, V: 2 atoms
+constexpr uint32_t kKVOff = kDOOff + 2 * kQAtom;
+constexpr uint32_t kPOff = kKVOff + kStages * kKVStage;   // [128 heads x 64 keys]
+constexpr uint32_t kDSOff = kPOff + kQAtom;
+constexpr uint32_t kTailOff = kDSOff + kQAtom;
+constexpr uint32_t kColDQ = 0, kColS = 192, kColDP = 256, kColDKlo = 320, kColDKhi = 384,
+                   kColDV = 448;
+
+struct BwdTail {
+  int key[kKeyRing][NK];       // key index per slot (-1: none)
+  int row[kKeyRing];
+  int flags[kKeyRing];         // bit 0: first chunk of row, bit 1: last
+  uint32_t valid[kKeyRing][2];
+  uint64_t keys_full[kKeyRing];   // the key list / flags of a ring slot are written
+  uint64_t kv_full[kStages], kv_empty[kStages];
+  uint64_t qdo_full, qdo_free;
+  uint64_t sdp_full, pds_full, pds_free;
+  uint64_t dkv_full, dkv_free;
+  uint64_t dq_full, dq_free;
+  uint64_t drain;
+  uint32_t tmem_base;
+  int abort_flag;
+  int okb[2];
+  int red[kGatherWarps];
+};
+
+__device__ __forceinline__ void bar_gather() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kGatherThreads) : "memory");
+}
+
+__device__ __forceinline__ bool bar_gather_ok(int* okb, int& nb, volatile int* abort_flag) {
+  if (threadIdx.x == 32 * kGatherWarp0) okb[nb & 1] = (*abort_flag == 0);
+  bar_gather();
+  const bool ok = reinterpret_cast<volatile int*>(okb)[nb & 1] != 0;
+  ++nb;
+  return ok;
+}
+
+__device__ __forceinline__ long long brow_of(int i, int nrows) {
+  return static_cast<long long>(nrows) - 1 - i;
+}
+
+__device__ __forceinline__ void drain_wait_b(uint64_t* bar, uint32_t parity, int* err) {
+  const uint32_t a = smem_u32(bar);
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(a, parity)) {
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      report_error(err, kErrB);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ int load_key_b(const AttnParams& p, const int32_t* irow, int j,
+                                          int kend, int t) {
+  if (j >= kend) return -1;
+  int s = __ldg(irow + j);
+  if (s < -1 || s >= p.S) {
+    report_error(p.err, DSA_STAGE_BWD | DSA_DEVERR_BAD_INDEX);
+    s = -1;
+  }
+  return s > t ? -1 : s;
+}
+
+__device__ __forceinline__ float ex2b(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void umma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                        uint32_t acc) {
+  umma_bf16(d, a, b, idesc, acc);
+}
+
+// instruction descriptor with both major bits
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn ? (1u << 15) : 0u) |
+         (b_mn ? (1u << 16) : 0u) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                       const __grid_constant__ CUtensorMap tm_do, const AttnParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if ((smem_u32(smem) & 1023u) != 0) {
+    if (threadIdx.x == 0) report_error(p.err, DSA_STAGE_BWD | DSA_DEVERR_MISALIGNED);
+    return;
+  }
+  BwdTail* tail = reinterpret_cast<BwdTail*>(smem + kTailOff);
+  volatile int* abort_flag = &tail->abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nrows = p.B * p.S;
+  const int H = p.H;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&tail->kv_full[i], 2 * kGatherThreads);
+      mbar_init(&tail->kv_empty[i], 1);
+    }
+    for (int i = 0; i < kKeyRing; ++i) mbar_init(&tail->keys_full[i], kGatherThreads);
+    mbar_init(&tail->qdo_full, 1);
+    mbar_init(&tail->qdo_free, 1);
+    mbar_init(&tail->sdp_full, 1);
+    mbar_init(&tail->pds_full, 128);
+    mbar_init(&tail->pds_free, 1);
+    mbar_init(&tail->dkv_full, 1);
+    mbar_init(&tail->dkv_free, 128);
+    mbar_init(&tail->dq_full, 1);
+    mbar_init(&tail->dq_free, 128);
+    mbar_init(&tail->drain, 1);
+    tail->abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_do);
+  }
+  if (warp == 8) {
+    tmem_alloc(&tail->tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tail->tmem_base;
+
+  if (warp >= kGatherWarp0) {
+    // ================================================================ gather
+    const int gt = threadIdx.x - 32 * kGatherWarp0;   // 0..95; gt < NK owns key slot gt
+    const int gw = warp - kGatherWarp0;
+    constexpr int PK = DQK / 8, PV = DV / 8;          // 24 + 16 pieces of 16 bytes
+    constexpr int KI = PK / 8, VI = PV / 8;           // instructions per group of 4 keys
+    int k_kig[KI], k_off[KI], v_kig[VI], v_off[VI];
+    uint32_t k_dst[KI], v_dst[VI];
+#pragma unroll
+    for (int i = 0; i < KI; ++i) {
+      const int q = i * 32 + lane, pc = q % PK;
+      k_kig[i] = q / PK;
+      k_off[i] = pc * 8;
+      k_dst[i] = (pc >> 3) * kKVAtom + ((pc & 7) << 4);
+    }
+#pragma unroll
+    for (int i = 0; i < VI; ++i) {
+      const int q = i * 32 + lane, pv = q % PV;
+      v_kig[i] = q / PV;
+      v_off[i] = pv * 8;
+      v_dst[i] = (3 + (pv >> 3)) * kKVAtom + ((pv & 7) << 4);
+    }
+    int g = 0, nb = 0;
+    for (int i = blockIdx.x; i < nrows; i += gridDim.x) {
+      const long long row = brow_of(i, nrows);
+      const int b = static_cast<int>(row / p.S);
+      const int t = static_cast<int>(row - static_cast<long long>(b) * p.S);
+      const int32_t* irow = p.idx + row * p.k;
+      int last = 0;
+#pragma unroll 8
+      for (int j = gt; j < p.k; j += kGatherThreads) {
+        const int s = __ldg(irow + j);
+        if (s >= 0 && s <= t && s < p.S) last = j + 1;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+      if (lane == 0) tail->red[gw] = last;
+      if (!bar_gather_ok(tail->okb, nb, abort_flag)) break;
+      const int kend = max(max(tail->red[0], tail->red[1]), tail->red[2]);
+      const int nch = kend > 0 ? (kend + NK - 1) / NK : 1;
+      int s_next = gt < NK ? load_key_b(p, irow, gt, kend, t) : -1;
+      bool stop = false;
+      for (int c = 0; c < nch; ++c, ++g) {
+        const int st = g % kStages, kr = g % kKeyRing;
+        const int s = s_next;
+        if (gt < NK && c + 1 < nch) s_next = load_key_b(p, irow, (c + 1) * NK + gt, kend, t);
+        mbar_wait(&tail->kv_empty[st], ((g / kStages) & 1) ^ 1u, abort_flag, p.err, kErrB);
+        if (gt < NK) {
+          tail->key[kr][gt] = s;
+          const uint32_t bal = __ballot_sync(0xffffffffu, s >= 0);
+          if (lane == 0) tail->valid[kr][gw] = bal;
+        }
+        if (gt == 0) {
+          tail->row[kr] = static_cast<int>(row);
+          tail->flags[kr] = (c == 0 ? 1 : 0) | (c == nch - 1 ? 2 : 0);
+        }
+        if (!bar_gather_ok(tail->okb, nb, abort_flag)) { stop = true; break; }
+        mbar_arrive(&tail->keys_full[kr]);   // releases this thread's list writes
+        mbar_arrive(&tail->kv_full[st]);
+        const uint32_t stage = smem_u32(smem + kKVOff + st * kKVStage);
+        const long long rowbase = static_cast<long long>(b) * p.S;
+        for (int grp = gw; grp < NK / 4; grp += kGatherWarps) {
+          const int4 kq = *reinterpret_cast<const int4*>(&tail->key[kr][grp * 4]);
+          const int keys[4] = {kq.x, kq.y, kq.z, kq.w};
+#pragma unroll
+          for (int ii = 0; ii < KI; ++ii) {
+            const int kig = k_kig[ii], key = grp * 4 + kig;
+            const int ks = kig == 0 ? keys[0] : (kig == 1 ? keys[1] : (kig == 2 ? keys[2] : keys[3]));
+            const long long kv = rowbase + (ks >= 0 ? ks : 0);
+            cp_async_16(stage + key * 128 + (k_dst[ii] ^ ((key & 7) << 4)),
+                        p.K + kv * DQK + k_off[ii], ks >= 0 ? 16u : 0u);
+          }
+#pragma unroll
+          for (int ii = 0; ii < VI; ++ii) {
+            const int kig = v_kig[ii], key = grp * 4 + kig;
+            const int ks = kig == 0 ? keys[0] : (kig == 1 ? keys[1] : (kig == 2 ? keys[2] : keys[3]));
+            const long long kv = rowbase + (ks >= 0 ? ks : 0);
+            cp_async_16(stage + key * 128 + (v_dst[ii] ^ ((key & 7) << 4)),
+                        p.V + kv * DV + v_off[ii], ks >= 0 ? 16u : 0u);
+          }
+        }
+        cp_async_mbar_arrive(&tail->kv_full[st]);
+      }
+      if (stop) break;
+    }
+    cp_async_wait<0>();
+  } else if (warp == 8) {
+    // ================================================================ UMMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_sdp = idesc_bf16(128, NK, false, false);
+      constexpr uint32_t id_dq = idesc_bf16(128, DQK, false, true);
+      constexpr uint32_t id_dkv = idesc_bf16(128, NK, true, true);
+      const uint32_t q_s = smem_u32(smem + kQOff), do_s = smem_u32(smem + kDOOff);
+      const uint32_t p_s = smem_u32(smem + kPOff), ds_s = smem_u32(smem + kDSOff);
+      int g = 0, nrow = 0;
+      int pend = -1, pend_flags = 0, pend_row = 0;
+      bool ok = true;
+      // dQ, dK^T, dV^T of chunk pg (its P / dS tiles are ready); prow = its row ordinal
+      auto issue_grads = [&](int pg, int flags, int prow) -> bool {
+        const int st = pg % kStages;
+        if (!mbar_wait(&tail->pds_full, pg & 1, abort_flag, p.err, kErrB)) return false;
+        if ((flags & 1) &&   // first chunk of a row: the previous row's dQ was read out
+            !mbar_wait(&tail->dq_free, (prow & 1) ^ 1u, abort_flag, p.err, kErrB))
+          return false;
+        tc_fence_after();
+        const uint32_t kst = smem_u32(smem + kKVOff + st * kKVStage);
+#pragma unroll
+        for (int kk = 0; kk < NK / 16; ++kk) {
+          umma_ss(tmem + kColDQ, umma_sdesc(ds_s + kk * 32, 1024, kLayoutSw128),
+                  umma_sdesc_lbo(kst + kk * 2048, kKVAtom, 1024, kLayoutSw128), id_dq,
+                  ((flags & 1) && kk == 0) ? 0u : 1u);
+        }
+        if (flags & 2) umma_commit(&tail->dq_full);
+        // the previous chunk's dK/dV have been drained out of TMEM
+        if (!mbar_wait(&tail->dkv_free, (pg & 1) ^ 1u, abort_flag, p.err, kErrB)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < 128 / 16; ++kk) {
+          const uint64_t bds = umma_sdesc_lbo(ds_s + kk * 2048, kQAtom, 1024, kLayoutSw128);
+          umma_ss(tmem + kColDKlo, umma_sdesc_lbo(q_s + kk * 2048, kQAtom, 1024, kLayoutSw128),
+                  bds, id_dkv, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + kColDKhi,
+                  umma_sdesc_lbo(q_s + 2 * kQAtom + kk * 2048, kQAtom, 1024, kLayoutSw128), bds,
+                  id_dkv, kk > 0 ? 1u : 0u);
+          umma_ss(tmem + kColDV, umma_sdesc_lbo(do_s + kk * 2048, kQAtom, 1024, kLayoutSw128),
+                  umma_sdesc_lbo(p_s + kk * 2048, kQAtom, 1024, kLayoutSw128), id_dkv,
+                  kk > 0 ? 1u : 0u);
+        }
+        umma_commit(&tail->dkv_full);
+        umma_commit(&tail->kv_empty[st]);
+        umma_commit(&tail->pds_free);
+        if (flags & 2) umma_commit(&tail->qdo_free);
+        return true;
+      };
+      for (int i = blockIdx.x; ok && i < nrows; i += gridDim.x, ++nrow) {
+        bool last = false;
+        while (ok && !last) {
+          const int st = g % kStages, kr = g % kKeyRing;
+          if (!mbar_wait(&tail->kv_full[st], (g / kStages) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
+          const int flags = tail->flags[kr];
+          last = (flags & 2) != 0;
+          if (flags & 1) {
+            // a new row: finish the previous row first; once its MMAs are done its
+            // Q / dO tiles can be replaced by this row's (TMA)
+            if (pend >= 0) {
+              if (!issue_grads(pend, pend_flags, pend_row)) { ok = false; break; }
+              pend = -1;
+            }
+            if (nrow > 0 &&
+                !mbar_wait(&tail->qdo_free, (nrow - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
+            mbar_arrive_expect_tx(&tail->qdo_full, 5 * kQAtom);
+            const int qrow = tail->row[kr] * H;
+#pragma unroll
+            for (int a = 0; a < 3; ++a)
+              tma_load_2d(smem + kQOff + a * kQAtom, &tm_q, &tail->qdo_full, a * 64, qrow);
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+              tma_load_2d(smem + kDOOff + a * kQAtom, &tm_do, &tail->qdo_full, a * 64, qrow);
+            if (!mbar_wait(&tail->qdo_full, nrow & 1, abort_flag, p.err, kErrB)) {
+              drain_wait_b(&tail->qdo_full, nrow & 1, p.err);   // let the copy land before exit
+              ok = false;
+              break;
+            }
+          }
+          // S / dP of this chunk need the softmax warps to have read the previous ones
+          if (g > 0 && !mbar_wait(&tail->pds_full, (g - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
+          fence_proxy_async_smem();
+          tc_fence_after();
+          const uint32_t kst = smem_u32(smem + kKVOff + st * kKVStage);
+#pragma unroll
+          for (int kk = 0; kk < DQK / 16; ++kk)
+            umma_ss(tmem + kColS, umma_sdesc(q_s + (kk >> 2) * kQAtom + (kk & 3) * 32, 1024, kLayoutSw128),
+                    umma_sdesc(kst + (kk >> 2) * kKVAtom + (kk & 3) * 32, 1024, kLayoutSw128), id_sdp,
+                    kk > 0 ? 1u : 0u);
+#pragma unroll
+          for (int kk = 0; kk < DV / 16; ++kk)
+            umma_ss(tmem + kColDP, umma_sdesc(do_s + (kk >> 2) * kQAtom + (kk & 3) * 32, 1024, kLayoutSw128),
+                    umma_sdesc(kst + (3 + (kk >> 2)) * kKVAtom + (kk & 3) * 32, 1024, kLayoutSw128),
+                    id_sdp, kk > 0 ? 1u : 0u);
+          umma_commit(&tail->sdp_full);
+          if (pend >= 0 && !issue_grads(pend, pend_flags, pend_row)) { ok = false; break; }
+          pend = g;
+          pend_flags = flags;
+          pend_row = nrow;
+          ++g;
+        }
+      }
+      if (ok && pend >= 0) issue_grads(pend, pend_flags, pend_row);
+      umma_commit(&tail->drain);
+      drain_wait_b(&tail->drain, 0, p.err);
+    }
+  } else if (warp < 4) {
+    // ================================================================ softmax
+    const int hrow = warp * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const float c2 = p.scale_log2;
+    uint8_t* prow = smem + kPOff + hrow * 128;
+    uint8_t* dsrow = smem + kDSOff + hrow * 128;
+    const uint32_t sw = static_cast<uint32_t>(hrow & 7);
+    int g = 0, nrow = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < nrows; i += gridDim.x, ++nrow) {
+      const long long row = brow_of(i, nrows);
+      const bool hv = hrow < H;
+      // Delta = sum_c dO[c] O[c] and lse of this head (fp32)
+      float delta = 0.f, lse2 = 0.f;
+      if (hv) {
+        const uint4* o4 = reinterpret_cast<const uint4*>(p.O_in + (row * H + hrow) * DV);
+        const uint4* d4 = reinterpret_cast<const uint4*>(p.dO + (row * H + hrow) * DV);
+#pragma unroll 4
+        for (int j = 0; j < DV / 8; ++j) {
+          const uint4 a = __ldg(o4 + j), d = __ldg(d4 + j);
+          const uint32_t av[4] = {a.x, a.y, a.z, a.w}, dv[4] = {d.x, d.y, d.z, d.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            delta = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(dv[e] << 16), delta);
+            delta = fmaf(__uint_as_float(av[e] & 0xffff0000u), __uint_as_float(dv[e] & 0xffff0000u),
+                         delta);
+          }
+        }
+        lse2 = p.lse_in[row * H + hrow] * 1.4426950408889634f;
+      }
+      bool last = false;
+      while (!last) {
+        const int kr = g % kKeyRing;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tail->sdp_full, g & 1, abort_flag, p.err, kErrB))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // acquire the gather threads' list writes (the slot is not rewritten before
+        // this chunk's P / dS have been consumed)
+        if (!__all_sync(0xffffffffu, mbar_wait(&tail->keys_full[kr], (g / kKeyRing) & 1,
+                                                abort_flag, p.err, kErrB))) {
+          ok = false;
+          break;
+        }
+        last = (tail->flags[kr] & 2) != 0;
+        const uint32_t vm0 = tail->valid[kr][0], vm1 = tail->valid[kr][1];
+        uint32_t sv[64], dv[64];
+        tmem_ld_x32(tmem + lane_off + kColS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld_x32(tmem + lane_off + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld_x32(tmem + lane_off + kColDP, *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
+        tmem_ld_x32(tmem + lane_off + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
+        tmem_ld_wait();
+        // the previous chunk's P / dS tiles have been consumed by the tensor cores
+        if (g > 0 && !__all_sync(0xffffffffu, mbar_wait(&tail->pds_free, (g - 1) & 1, abort_flag,
+                                                         p.err, kErrB))) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint32_t pw[4], dw[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int j = cc * 8 + e * 2;
+            const uint32_t vm = j < 32 ? vm0 : vm1;
+            const bool v0 = hv && ((vm >> (j & 31)) & 1u), v1 = hv && ((vm >> ((j + 1) & 31)) & 1u);
+            const float p0 = v0 ? ex2b(fmaf(__uint_as_float(sv[j]), c2, -lse2)) : 0.f;
+            const float p1 = v1 ? ex2b(fmaf(__uint_as_float(sv[j + 1]), c2, -lse2)) : 0.f;
+            const float d0 = p0 * (__uint_as_float(dv[j]) - delta);
+            const float d1 = p1 * (__uint_as_float(dv[j + 1]) - delta);
+            pw[e] = pack_bf16(p0, p1);
+            dw[e] = pack_bf16(d0, d1);
+          }
+          const uint32_t off = (static_cast<uint32_t>(cc) ^ sw) << 4;
+          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+          *reinterpret_cast<uint4*>(dsrow + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&tail->pds_full);
+        ++g;
+      }
+      if (!ok) break;
+      // dQ of this row: scale * (sum over chunks of dS . K)
+      if (!__all_sync(0xffffffffu, mbar_wait(&tail->dq_full, nrow & 1, abort_flag, p.err, kErrB))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint4* qrow = reinterpret_cast<uint4*>(p.dQ + (row * H + hrow) * DQK);
+#pragma unroll
+      for (int d0 = 0; d0 < DQK; d0 += 32) {
+        uint32_t v[32];
+        tmem_ld_x32(tmem + lane_off + kColDQ + d0, v);
+        tmem_ld_wait();
+        if (hv) {
+#pragma unroll
+          for (int d = 0; d < 32; d += 8) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(v[d]) * p.scale, __uint_as_float(v[d + 1]) * p.scale);
+            w.y = pack_bf16(__uint_as_float(v[d + 2]) * p.scale, __uint_as_float(v[d + 3]) * p.scale);
+            w.z = pack_bf16(__uint_as_float(v[d + 4]) * p.scale, __uint_as_float(v[d + 5]) * p.scale);
+            w.w = pack_bf16(__uint_as_float(v[d + 6]) * p.scale, __uint_as_float(v[d + 7]) * p.scale);
+            qrow[(d0 + d) / 8] = w;
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tail->dq_free);
+    }
+  } else {
+    // ================================================================ drain
+    // warp 4+q owns TMEM lanes 32q..32q+31: dims 32q.. of dK^T lo / dV^T and
+    // dims 128+32q.. of dK^T hi (q < 2). Per key of the chunk one instruction adds
+    // 32 consecutive floats of that key's accumulator row.
+    const int q = warp & 3;
+    const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    int g = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < nrows; i += gridDim.x) {
+      bool last = false;
+      while (!last) {
+        const int kr = g % kKeyRing;
+        if (!__all_sync(0xffffffffu, mbar_wait(&tail->dkv_full, g & 1, abort_flag, p.err, kErrB))) {
+          ok = false;
+          break;
+        }
+        // the slot is not rewritten before this chunk has been drained
+        if (!__all_sync(0xffffffffu, mbar_wait(&tail->keys_full[kr], (g / kKeyRing) & 1,
+                                                abort_flag, p.err, kErrB))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        last = (tail->flags[kr] & 2) != 0;
+        const int row = tail->row[kr];
+        const int b = row / p.S;
+        float* ws = p.ws + static_cast<long long>(b) * p.S * (DQK + DV);
+        const int* keys = tail->key[kr];
+        // regions: dK^T lo (dims 0-127), dK^T hi (dims 128-191, quarters 0-1), dV^T
+#pragma unroll 1
+        for (int reg = 0; reg < 3; ++reg) {
+          if (reg == 1 && q >= 2) continue;
+          const uint32_t col = reg == 0 ? kColDKlo : (reg == 1 ? kColDKhi : kColDV);
+          const int dim = (reg == 0 ? 0 : (reg == 1 ? 128 : DQK)) + q * 32 + lane;
+#pragma unroll
+          for (int j0 = 0; j0 < NK; j0 += 32) {
+            uint32_t v[32];
+            tmem_ld_x32(tmem + lane_off + col + j0, v);
+            tmem_ld_wait();
+            const float sc = reg == 2 ? 1.f : p.scale;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int key = keys[j0 + j];
+              if (key >= 0)
+                atomicAdd(ws + static_cast<long long>(key) * (DQK + DV) + dim,
+                          __uint_as_float(v[j]) * sc);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tail->dkv_free);
+        ++g;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 8) tmem_dealloc(tmem, 512);
+}
+
+typedef CUresult (*EncodeTiledFnBwd)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                     const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                     const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                     CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+bool make_row_map(CUtensorMap* map, const void* base, long long rows, int cols) {
+  static EncodeTiledFnBwd fn = nullptr;
+  if (fn == nullptr) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return false;
+    fn = reinterpret_cast<EncodeTiledFnBwd>(ptr);
+  }
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool attn_bwd_tc_supported(int H, int Dqk, int Dv, float scale) {
+  return H > 64 && H <= 128 && scale > 0.f && Dqk == 192 && Dv == 128;
+}
+
+// ws must be zeroed by the caller's stream before this runs.
+int launch_attn_bwd_tc(const AttnParams& p, cudaStream_t stream) {
+  const long long qrows = static_cast<long long>(p.B) * p.S * p.H;
+  CUtensorMap mq, mdo;
+  if (!make_row_map(&mq, p.Q, qrows, DQK) || !make_row_map(&mdo, p.dO, qrows, DV))
+    return DSA_ERR_CUDA;
+  const size_t smem = kTailOff + sizeof(BwdTail);
+  if (cudaFuncSetAttribute(attn_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long rows = static_cast<long long>(p.B) * p.S;
+  const int grid = static_cast<int>(rows < sms ? rows : sms);
+  attn_bwd_tc_kernel<<<grid, kThreads, smem, stream>>>(mq, mdo, p);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+}  // namespace dsa

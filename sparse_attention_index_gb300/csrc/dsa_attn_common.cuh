@@ -41,6 +41,11 @@ inline AttnParams make_attn_params(const void* Q, const void* K, const void* V,
 bool attn_fwd_tc_supported(int H, int Dqk, int Dv, float scale);
 int launch_attn_fwd_tc(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream);
 
+// tcgen05 backward (attn_bwd_tc.cu): 64 < H <= 128, Dqk = 192, Dv = 128, positive scale.
+// The fp32 dK/dV accumulator p.ws must already be zero on the stream.
+bool attn_bwd_tc_supported(int H, int Dqk, int Dv, float scale);
+int launch_attn_bwd_tc(const AttnParams& p, cudaStream_t stream);
+
 // Shared-memory layout of the forward kernel: Q rows, two K/V chunk buffers
 // (rows padded by 16 bytes so ldmatrix row addresses hit distinct banks), a
 // small header and the query's index row.
