@@ -52,7 +52,10 @@ constexpr uint32_t kKVStage = 5 * kKVAtom;       // K: 3 atoms, V: 2 atoms
 constexpr uint32_t kKVOff = kDOOff + 2 * kQAtom;
 constexpr uint32_t kPOff = kKVOff + kStages * kKVStage;   // [128 heads x 64 keys]
 constexpr uint32_t kDSOff = kPOff + kQAtom;
-constexpr uint32_t kTailOff = kDSOff + kQAtom;
+constexpr uint32_t kDrainOff = kDSOff + kQAtom;              // per drain warp: [32 keys x 36]
+constexpr int kDrainPitch = 36;                                // floats; rows stay 16-byte aligned
+constexpr uint32_t kDrainTile = 32 * kDrainPitch * 4;
+constexpr uint32_t kTailOff = kDrainOff + 4 * kDrainTile;
 constexpr uint32_t kColDQ = 0, kColS = 192, kColDP = 256, kColDKlo = 320, kColDKhi = 384,
                    kColDV = 448;
 
@@ -506,25 +509,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = row / p.S;
         float* ws = p.ws + static_cast<long long>(b) * p.S * (DQK + DV);
         const int* keys = tail->key[kr];
-        // regions: dK^T lo (dims 0-127), dK^T hi (dims 128-191, quarters 0-1), dV^T
+        // regions: dK^T lo (dims 0-127), dK^T hi (dims 128-191, quarters 0-1), dV^T.
+        // Each 32-dim x 32-key block goes through a shared tile so that a thread
+        // holds 4 consecutive dims of one key: one 16-byte reduction per thread,
+        // 4 key rows x 128 contiguous bytes per warp instruction.
+        float* tile = reinterpret_cast<float*>(smem + kDrainOff + q * kDrainTile);
+        const int rr = lane >> 3, c4 = (lane & 7) * 4;
 #pragma unroll 1
         for (int reg = 0; reg < 3; ++reg) {
           if (reg == 1 && q >= 2) continue;
           const uint32_t col = reg == 0 ? kColDKlo : (reg == 1 ? kColDKhi : kColDV);
-          const int dim = (reg == 0 ? 0 : (reg == 1 ? 128 : DQK)) + q * 32 + lane;
-#pragma unroll
+          const int dim0 = (reg == 0 ? 0 : (reg == 1 ? 128 : DQK)) + q * 32;
+          const float sc = reg == 2 ? 1.f : p.scale;
+#pragma unroll 1
           for (int j0 = 0; j0 < NK; j0 += 32) {
             uint32_t v[32];
             tmem_ld_x32(tmem + lane_off + col + j0, v);
             tmem_ld_wait();
-            const float sc = reg == 2 ? 1.f : p.scale;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const int key = keys[j0 + j];
-              if (key >= 0)
-                atomicAdd(ws + static_cast<long long>(key) * (DQK + DV) + dim,
-                          __uint_as_float(v[j]) * sc);
+            for (int j = 0; j < 32; ++j) tile[j * kDrainPitch + lane] = __uint_as_float(v[j]) * sc;
+            __syncwarp();
+#pragma unroll
+            for (int i4 = 0; i4 < 8; ++i4) {
+              const int r = rr + 4 * i4;
+              const int key = keys[j0 + r];
+              if (key >= 0) {
+                const float4 x = *reinterpret_cast<const float4*>(tile + r * kDrainPitch + c4);
+                atomicAdd(reinterpret_cast<float4*>(ws + static_cast<long long>(key) * (DQK + DV) +
+                                                    dim0 + c4),
+                          x);
+              }
             }
+            __syncwarp();
           }
         }
         tc_fence_before();
