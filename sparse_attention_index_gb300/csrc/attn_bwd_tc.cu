@@ -19,11 +19,13 @@
 // covers 32 consecutive floats of one key row per instruction. dQ stays in
 // TMEM for the whole row. Delta = sum_c dO O is formed at the start of each row.
 //
-// Persistent CTA (one per SM), 384 threads:
+// Persistent CTA (one per SM), 512 threads:
 //   warps 0-3   softmax: Delta, P and dS tiles, final dQ (one head per thread)
-//   warps 4-7   drain: dK^T / dV^T from TMEM -> fp32 reductions (one dim per thread)
-//   warp  8     TMEM owner and single-thread UMMA issuer
-//   warps 9-11  gather: K/V rows of each chunk (cp.async, 2 stages)
+//   warps 4-11  drain: dK^T / dV^T from TMEM -> fp32 reductions (one dim per thread;
+//               two warps per TMEM lane quarter, one per half of the chunk's keys)
+//   warp  12    TMEM owner and single-thread UMMA issuer
+//   warps 13-15 gather: K/V rows of each chunk (cp.async, 2 stages; a stage is
+//               released as soon as the chunk's dQ product has read it)
 // The MMA thread also loads each row's Q / dO tiles (TMA) once the previous row's
 // MMAs have released them.
 // TMEM: dQ [0,192) S [192,256) dP [256,320) dK^T lo [320,384) hi [384,448) dV^T [448,512).
@@ -36,10 +38,12 @@ namespace {
 constexpr int NK = 64;               // keys per chunk
 constexpr int kStages = 2;           // K/V gather stages
 constexpr int kKeyRing = 4;          // key lists of chunks in flight
-constexpr int kGatherWarp0 = 9;
+constexpr int kDrainWarps = 8;
+constexpr int kMmaWarp = 12;
+constexpr int kGatherWarp0 = 13;
 constexpr int kGatherWarps = 3;
 constexpr int kGatherThreads = 32 * kGatherWarps;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr int kErrB = DSA_STAGE_BWD | DSA_DEVERR_TIMEOUT;
 
 // Dqk = 192, Dv = 128
@@ -52,10 +56,10 @@ constexpr uint32_t kKVStage = 5 * kKVAtom;       // K: 3 atoms, V: 2 atoms
 constexpr uint32_t kKVOff = kDOOff + 2 * kQAtom;
 constexpr uint32_t kPOff = kKVOff + kStages * kKVStage;   // [128 heads x 64 keys]
 constexpr uint32_t kDSOff = kPOff + kQAtom;
-constexpr uint32_t kDrainOff = kDSOff + kQAtom;              // per drain warp: [32 keys x 36]
+constexpr uint32_t kDrainOff = kDSOff + kQAtom;              // per drain warp: [16 keys x 36]
 constexpr int kDrainPitch = 36;                                // floats; rows stay 16-byte aligned
-constexpr uint32_t kDrainTile = 32 * kDrainPitch * 4;
-constexpr uint32_t kTailOff = kDrainOff + 4 * kDrainTile;
+constexpr uint32_t kDrainTile = 16 * kDrainPitch * 4;
+constexpr uint32_t kTailOff = kDrainOff + kDrainWarps * kDrainTile;
 constexpr uint32_t kColDQ = 0, kColS = 192, kColDP = 256, kColDKlo = 320, kColDKhi = 384,
                    kColDV = 448;
 
@@ -67,8 +71,8 @@ struct BwdTail {
   uint64_t keys_full[kKeyRing];   // the key list / flags of a ring slot are written
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t qdo_full, qdo_free;
-  uint64_t sdp_full, pds_full, pds_free;
-  uint64_t dkv_full, dkv_free;
+  uint64_t sdp_full, sdp_free, pds_full, pds_free;
+  uint64_t dkv_full[3], dkv_free[3];   // per region: dV^T, dK^T lo, dK^T hi
   uint64_t dq_full, dq_free;
   uint64_t drain;
   uint32_t tmem_base;
@@ -156,10 +160,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&tail->qdo_full, 1);
     mbar_init(&tail->qdo_free, 1);
     mbar_init(&tail->sdp_full, 1);
+    mbar_init(&tail->sdp_free, 128);
     mbar_init(&tail->pds_full, 128);
     mbar_init(&tail->pds_free, 1);
-    mbar_init(&tail->dkv_full, 1);
-    mbar_init(&tail->dkv_free, 128);
+    for (int r = 0; r < 3; ++r) {
+      mbar_init(&tail->dkv_full[r], 1);
+      mbar_init(&tail->dkv_free[r], 32 * kDrainWarps);
+    }
     mbar_init(&tail->dq_full, 1);
     mbar_init(&tail->dq_free, 128);
     mbar_init(&tail->drain, 1);
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_do);
   }
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tmem_alloc(&tail->tmem_base, 512);
     tmem_relinquish();
   }
@@ -263,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (stop) break;
     }
     cp_async_wait<0>();
-  } else if (warp == 8) {
+  } else if (warp == kMmaWarp) {
     // ================================================================ UMMA issuer
     if (lane == 0) {
       constexpr uint32_t id_sdp = idesc_bf16(128, NK, false, false);
@@ -290,23 +297,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                   ((flags & 1) && kk == 0) ? 0u : 1u);
         }
         if (flags & 2) umma_commit(&tail->dq_full);
-        // the previous chunk's dK/dV have been drained out of TMEM
-        if (!mbar_wait(&tail->dkv_free, (pg & 1) ^ 1u, abort_flag, p.err, kErrB)) return false;
-        tc_fence_after();
+        umma_commit(&tail->kv_empty[st]);   // K / V of this stage are no longer read
+        // dV^T, dK^T lo, dK^T hi of this chunk, each once the drain warps have emptied
+        // that region of the previous chunk (so draining and MMAs overlap by region)
+#pragma unroll 1
+        for (int reg = 0; reg < 3; ++reg) {
+          if (!mbar_wait(&tail->dkv_free[reg], (pg & 1) ^ 1u, abort_flag, p.err, kErrB)) return false;
+          tc_fence_after();
+          const uint32_t dcol = reg == 0 ? kColDV : (reg == 1 ? kColDKlo : kColDKhi);
+          const uint32_t abase = reg == 0 ? do_s : (reg == 1 ? q_s : q_s + 2 * kQAtom);
+          const uint32_t bbase = reg == 0 ? p_s : ds_s;
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk) {
-          const uint64_t bds = umma_sdesc_lbo(ds_s + kk * 2048, kQAtom, 1024, kLayoutSw128);
-          umma_ss(tmem + kColDKlo, umma_sdesc_lbo(q_s + kk * 2048, kQAtom, 1024, kLayoutSw128),
-                  bds, id_dkv, kk > 0 ? 1u : 0u);
-          umma_ss(tmem + kColDKhi,
-                  umma_sdesc_lbo(q_s + 2 * kQAtom + kk * 2048, kQAtom, 1024, kLayoutSw128), bds,
-                  id_dkv, kk > 0 ? 1u : 0u);
-          umma_ss(tmem + kColDV, umma_sdesc_lbo(do_s + kk * 2048, kQAtom, 1024, kLayoutSw128),
-                  umma_sdesc_lbo(p_s + kk * 2048, kQAtom, 1024, kLayoutSw128), id_dkv,
-                  kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < 128 / 16; ++kk)
+            umma_ss(tmem + dcol, umma_sdesc_lbo(abase + kk * 2048, kQAtom, 1024, kLayoutSw128),
+                    umma_sdesc_lbo(bbase + kk * 2048, kQAtom, 1024, kLayoutSw128), id_dkv,
+                    kk > 0 ? 1u : 0u);
+          umma_commit(&tail->dkv_full[reg]);
         }
-        umma_commit(&tail->dkv_full);
-        umma_commit(&tail->kv_empty[st]);
         umma_commit(&tail->pds_free);
         if (flags & 2) umma_commit(&tail->qdo_free);
         return true;
@@ -342,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           // S / dP of this chunk need the softmax warps to have read the previous ones
-          if (g > 0 && !mbar_wait(&tail->pds_full, (g - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
+          if (g > 0 && !mbar_wait(&tail->sdp_free, (g - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
           fence_proxy_async_smem();
           tc_fence_after();
           const uint32_t kst = smem_u32(smem + kKVOff + st * kKVStage);
@@ -416,12 +423,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         last = (tail->flags[kr] & 2) != 0;
         const uint32_t vm0 = tail->valid[kr][0], vm1 = tail->valid[kr][1];
-        uint32_t sv[64], dv[64];
-        tmem_ld_x32(tmem + lane_off + kColS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld_x32(tmem + lane_off + kColS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-        tmem_ld_x32(tmem + lane_off + kColDP, *reinterpret_cast<uint32_t(*)[32]>(&dv[0]));
-        tmem_ld_x32(tmem + lane_off + kColDP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dv[32]));
-        tmem_ld_wait();
+        // P and dS of this chunk, packed to bf16 pairs in registers (8 keys at a time)
+        uint32_t pw[32], dw[32];
+#pragma unroll
+        for (int qk = 0; qk < 8; ++qk) {
+          uint32_t sv[8], dv[8];
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+              : "=r"(sv[0]), "=r"(sv[1]), "=r"(sv[2]), "=r"(sv[3]), "=r"(sv[4]), "=r"(sv[5]),
+                "=r"(sv[6]), "=r"(sv[7])
+              : "r"(tmem + lane_off + kColS + qk * 8)
+              : "memory");
+          asm volatile(
+              "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+              : "=r"(dv[0]), "=r"(dv[1]), "=r"(dv[2]), "=r"(dv[3]), "=r"(dv[4]), "=r"(dv[5]),
+                "=r"(dv[6]), "=r"(dv[7])
+              : "r"(tmem + lane_off + kColDP + qk * 8)
+              : "memory");
+          tmem_ld_wait();
+          const uint32_t vm = (qk < 4 ? vm0 : vm1) >> ((qk & 3) * 8);
+#pragma unroll
+          for (int j = 0; j < 8; j += 2) {
+            const bool v0 = hv && ((vm >> j) & 1u), v1 = hv && ((vm >> (j + 1)) & 1u);
+            const float p0 = v0 ? ex2b(fmaf(__uint_as_float(sv[j]), c2, -lse2)) : 0.f;
+            const float p1 = v1 ? ex2b(fmaf(__uint_as_float(sv[j + 1]), c2, -lse2)) : 0.f;
+            pw[qk * 4 + j / 2] = pack_bf16(p0, p1);
+            dw[qk * 4 + j / 2] = pack_bf16(p0 * (__uint_as_float(dv[j]) - delta),
+                                           p1 * (__uint_as_float(dv[j + 1]) - delta));
+          }
+        }
+        // S / dP are in registers: the next chunk's S / dP may overwrite them
+        tc_fence_before();
+        mbar_arrive(&tail->sdp_free);
         // the previous chunk's P / dS tiles have been consumed by the tensor cores
         if (g > 0 && !__all_sync(0xffffffffu, mbar_wait(&tail->pds_free, (g - 1) & 1, abort_flag,
                                                          p.err, kErrB))) {
@@ -430,22 +463,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          uint32_t pw[4], dw[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int j = cc * 8 + e * 2;
-            const uint32_t vm = j < 32 ? vm0 : vm1;
-            const bool v0 = hv && ((vm >> (j & 31)) & 1u), v1 = hv && ((vm >> ((j + 1) & 31)) & 1u);
-            const float p0 = v0 ? ex2b(fmaf(__uint_as_float(sv[j]), c2, -lse2)) : 0.f;
-            const float p1 = v1 ? ex2b(fmaf(__uint_as_float(sv[j + 1]), c2, -lse2)) : 0.f;
-            const float d0 = p0 * (__uint_as_float(dv[j]) - delta);
-            const float d1 = p1 * (__uint_as_float(dv[j + 1]) - delta);
-            pw[e] = pack_bf16(p0, p1);
-            dw[e] = pack_bf16(d0, d1);
-          }
           const uint32_t off = (static_cast<uint32_t>(cc) ^ sw) << 4;
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-          *reinterpret_cast<uint4*>(dsrow + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+          *reinterpret_cast<uint4*>(prow + off) =
+              make_uint4(pw[cc * 4], pw[cc * 4 + 1], pw[cc * 4 + 2], pw[cc * 4 + 3]);
+          *reinterpret_cast<uint4*>(dsrow + off) =
+              make_uint4(dw[cc * 4], dw[cc * 4 + 1], dw[cc * 4 + 2], dw[cc * 4 + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -482,69 +504,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================================================ drain
-    // warp 4+q owns TMEM lanes 32q..32q+31: dims 32q.. of dK^T lo / dV^T and
-    // dims 128+32q.. of dK^T hi (q < 2). Per key of the chunk one instruction adds
-    // 32 consecutive floats of that key's accumulator row.
-    const int q = warp & 3;
+    // warp 4 + q + 4h owns TMEM lanes 32q..32q+31 (dims 32q.. of dK^T lo / dV^T and
+    // 128+32q.. of dK^T hi for q < 2) and keys 32h..32h+31 of each chunk.
+    const int dw_ = warp - 4;
+    const int q = dw_ & 3, hk = dw_ >> 2;
     const uint32_t lane_off = static_cast<uint32_t>(q * 32) << 16;
+    float* tile = reinterpret_cast<float*>(smem + kDrainOff + dw_ * kDrainTile);
+    const int rr = lane >> 3, c4 = (lane & 7) * 4;
     int g = 0;
     bool ok = true;
     for (int i = blockIdx.x; ok && i < nrows; i += gridDim.x) {
       bool last = false;
       while (!last) {
         const int kr = g % kKeyRing;
-        if (!__all_sync(0xffffffffu, mbar_wait(&tail->dkv_full, g & 1, abort_flag, p.err, kErrB))) {
-          ok = false;
-          break;
-        }
         // the slot is not rewritten before this chunk has been drained
         if (!__all_sync(0xffffffffu, mbar_wait(&tail->keys_full[kr], (g / kKeyRing) & 1,
                                                 abort_flag, p.err, kErrB))) {
           ok = false;
           break;
         }
-        tc_fence_after();
         last = (tail->flags[kr] & 2) != 0;
         const int row = tail->row[kr];
         const int b = row / p.S;
         float* ws = p.ws + static_cast<long long>(b) * p.S * (DQK + DV);
         const int* keys = tail->key[kr];
-        // regions: dK^T lo (dims 0-127), dK^T hi (dims 128-191, quarters 0-1), dV^T.
-        // Each 32-dim x 32-key block goes through a shared tile so that a thread
-        // holds 4 consecutive dims of one key: one 16-byte reduction per thread,
-        // 4 key rows x 128 contiguous bytes per warp instruction.
-        float* tile = reinterpret_cast<float*>(smem + kDrainOff + q * kDrainTile);
-        const int rr = lane >> 3, c4 = (lane & 7) * 4;
+        // regions in the order the tensor cores produce them: dV^T, dK^T lo, dK^T hi
+        // (dims 128-191: quarters 0-1). Each 32-dim x 16-key block goes through a
+        // shared tile so that a thread holds 4 consecutive dims of one key: one
+        // 16-byte reduction per thread, 4 key rows x 128 contiguous bytes per warp
+        // instruction.
 #pragma unroll 1
         for (int reg = 0; reg < 3; ++reg) {
-          if (reg == 1 && q >= 2) continue;
-          const uint32_t col = reg == 0 ? kColDKlo : (reg == 1 ? kColDKhi : kColDV);
-          const int dim0 = (reg == 0 ? 0 : (reg == 1 ? 128 : DQK)) + q * 32;
-          const float sc = reg == 2 ? 1.f : p.scale;
-#pragma unroll 1
-          for (int j0 = 0; j0 < NK; j0 += 32) {
-            uint32_t v[32];
-            tmem_ld_x32(tmem + lane_off + col + j0, v);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) tile[j * kDrainPitch + lane] = __uint_as_float(v[j]) * sc;
-            __syncwarp();
-#pragma unroll
-            for (int i4 = 0; i4 < 8; ++i4) {
-              const int r = rr + 4 * i4;
-              const int key = keys[j0 + r];
-              if (key >= 0) {
-                const float4 x = *reinterpret_cast<const float4*>(tile + r * kDrainPitch + c4);
-                atomicAdd(reinterpret_cast<float4*>(ws + static_cast<long long>(key) * (DQK + DV) +
-                                                    dim0 + c4),
-                          x);
-              }
-            }
-            __syncwarp();
+          if (!__all_sync(0xffffffffu,
+                          mbar_wait(&tail->dkv_full[reg], g & 1, abort_flag, p.err, kErrB))) {
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          if (!(reg == 2 && q >= 2)) {
+            const uint32_t col = reg == 0 ? kColDV : (reg == 1 ? kColDKlo : kColDKhi);
+            const int dim0 = (reg == 0 ? DQK : (reg == 1 ? 0 : 128)) + q * 32;
+            const float sc = reg == 0 ? 1.f : p.scale;
+#pragma unroll 1
+            for (int j0 = hk * 32; j0 < hk * 32 + 32; j0 += 16) {
+              uint32_t v[16];
+              asm volatile(
+                  "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+                  "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+                  : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
+                    "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
+                    "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+                  : "r"(tmem + lane_off + col + j0)
+                  : "memory");
+              tmem_ld_wait();
+#pragma unroll
+              for (int j = 0; j < 16; ++j) tile[j * kDrainPitch + lane] = __uint_as_float(v[j]) * sc;
+              __syncwarp();
+#pragma unroll
+              for (int i4 = 0; i4 < 4; ++i4) {
+                const int r = rr + 4 * i4;
+                const int key = keys[j0 + r];
+                if (key >= 0) {
+                  const float4 x = *reinterpret_cast<const float4*>(tile + r * kDrainPitch + c4);
+                  atomicAdd(reinterpret_cast<float4*>(ws + static_cast<long long>(key) * (DQK + DV) +
+                                                      dim0 + c4),
+                            x);
+                }
+              }
+              __syncwarp();
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(&tail->dkv_free[reg]);
         }
-        tc_fence_before();
-        mbar_arrive(&tail->dkv_free);
+        if (!ok) break;
         ++g;
       }
     }
@@ -553,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 8) tmem_dealloc(tmem, 512);
+  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
 }
 
 typedef CUresult (*EncodeTiledFnBwd)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
