@@ -7,15 +7,15 @@
 // One CTA per query row (b, t). The valid keys are s in [0, t] with, when
 // segment ids are given, seg[s] == seg[t]; n = their number.
 //   n <= k : every valid key is selected (ordered compaction, no score read).
-//   n >  k : the scores are mapped to order-preserving 32-bit keys (-0 -> +0),
-//            staged in shared memory when the row fits, and the k-th largest
-//            key T is found digit by digit (4 x 8 bits, warp-aggregated
-//            shared-memory histograms via __match_any_sync). A final ordered
-//            pass selects every key > T and the lowest-index `need` keys == T,
-//            writing positions from one block-wide scan, so the output is
-//            ascending. Slots m..k-1 get -1.
-// Rows longer than the shared-memory stage are re-read from global memory
-// (L2) on every digit pass.
+//   n >  k : the scores are mapped to order-preserving 32-bit keys (-0 -> +0)
+//            and the k-th largest key T is found digit by digit with
+//            warp-aggregated (__match_any_sync) shared-memory histograms. Rows
+//            that fit in shared memory are staged there while the first 11-bit
+//            histogram is built; at most two more passes (11, 10 bits) run on
+//            the staged keys. Longer rows take 4 x 8-bit passes over global
+//            memory (L2). A final ordered pass selects every key > T and the
+//            lowest-index `need` keys == T; each warp owns a contiguous segment,
+//            so one barrier orders the output. Slots m..k-1 get -1.
 
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
@@ -38,8 +38,9 @@ struct TopkParams {
 };
 
 struct TopkSmem {
-  uint32_t hist[256];
+  uint32_t hist[2048];
   int warp_tot[kWarps];
+  int wgt[kWarps], weq[kWarps];
   int bcast[4];
 };
 
@@ -79,6 +80,80 @@ __device__ __forceinline__ int block_scan(int v, int& total, TopkSmem* sm) {
   return x + before;
 }
 
+// Ordered selection: for s in [0, len), flags(s) gives (gt, eq). Every gt element
+// and the first `need` eq elements (in s order) are written to out[] in ascending s;
+// an element's slot is (#gt before it) + min(#eq before it, need). Each warp owns one
+// contiguous, 32-aligned segment; one block barrier orders the warps.
+template <class Flags>
+__device__ __forceinline__ void ordered_select(int len, Flags flags, int need, int32_t* out,
+                                               int kmax, TopkSmem* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg_len = ((len + kThreads - 1) / kThreads) * 32;
+  const int s_begin = warp * seg_len, s_end = min(len, s_begin + seg_len);
+  int cg = 0, ce = 0;
+  for (int s = s_begin + lane; s < s_end; s += 32) {
+    const int2 f = flags(s);
+    cg += f.x;
+    ce += f.y;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cg += __shfl_xor_sync(0xffffffffu, cg, o);
+    ce += __shfl_xor_sync(0xffffffffu, ce, o);
+  }
+  if (lane == 0) {
+    sm->wgt[warp] = cg;
+    sm->weq[warp] = ce;
+  }
+  __syncthreads();
+  int gt_base = 0, eq_base = 0;
+  for (int w = 0; w < warp; ++w) {
+    gt_base += sm->wgt[w];
+    eq_base += sm->weq[w];
+  }
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int s0 = s_begin; s0 < s_end; s0 += 32) {
+    const int s = s0 + lane;
+    const int2 f = s < s_end ? flags(s) : make_int2(0, 0);
+    const uint32_t bg = __ballot_sync(0xffffffffu, f.x), be = __ballot_sync(0xffffffffu, f.y);
+    const int eq_before = eq_base + __popc(be & lt);
+    const int pos = gt_base + __popc(bg & lt) + min(eq_before, need);
+    if ((f.x || (f.y && eq_before < need)) && pos < kmax) out[pos] = s;
+    gt_base += __popc(bg);
+    eq_base += __popc(be);
+  }
+}
+
+// Over nb histogram bins taken from the top: the bin holding the `need`-th largest
+// key, the number of keys in higher bins and in that bin (broadcast through sm).
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, TopkSmem* sm,
+                                         int& bin, int& above, int& in_bin) {
+  const int per = nb / kThreads;   // 4 or 2 bins per thread, highest bins to thread 0
+  const int tid = threadIdx.x;
+  int c[4] = {0, 0, 0, 0};
+  int sum = 0;
+  for (int i = 0; i < per; ++i) {
+    c[i] = static_cast<int>(hist[nb - 1 - (tid * per + i)]);
+    sum += c[i];
+  }
+  int tot;
+  const int incl = block_scan(sum, tot, sm);
+  int run = incl - sum;
+  for (int i = 0; i < per; ++i) {
+    if (run < need && run + c[i] >= need) {
+      sm->bcast[0] = nb - 1 - (tid * per + i);
+      sm->bcast[1] = run;
+      sm->bcast[2] = c[i];
+    }
+    run += c[i];
+  }
+  __syncthreads();
+  bin = sm->bcast[0];
+  above = sm->bcast[1];
+  in_bin = sm->bcast[2];
+  __syncthreads();
+}
+
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   TopkSmem* sm = reinterpret_cast<TopkSmem*>(smem_raw);
@@ -108,15 +183,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 
   if (n <= p.k) {
     // every valid key is selected, in ascending order
-    int base = 0;
-    for (int s0 = 0; s0 < len; s0 += kThreads) {
-      const int s = s0 + tid;
-      const int v = (s < len) && (!seg_row || seg_row[s] == seg_t);
-      int tot;
-      const int incl = block_scan(v, tot, sm);
-      if (v) out[base + incl - 1] = s;
-      base += tot;
-    }
+    ordered_select(
+        len, [&](int s) { return make_int2(!seg_row || seg_row[s] == seg_t, 0); }, 0, out, p.k,
+        sm);
     for (int j = n + tid; j < p.k; j += kThreads) out[j] = -1;
     if (p.count && tid == 0) p.count[row] = n;
     return;
@@ -124,15 +193,84 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 
   const bool staged = len <= p.stage_cap;
   if (staged) {
-    for (int s = tid; s < len; s += kThreads) {
-      const bool v = !seg_row || seg_row[s] == seg_t;
-      keys[s] = v ? order_key(__ldg(srow + s)) : 0u;
+    // ---- rows held in shared memory: 11 + 11 + 10 bit radix select, the first
+    // histogram built while the row is loaded
+    // raw scores -> shared memory with 16-byte asynchronous copies (rows are
+    // 16-byte aligned: ld is a multiple of 4)
+    const int nvec = len >> 2;
+    for (int c = tid; c < nvec; c += kThreads)
+      cp_async_16(smem_u32(keys + 4 * c), srow + 4 * c, 16u);
+    cp_async_commit();
+    for (int s = 4 * nvec + tid; s < len; s += kThreads)
+      keys[s] = __float_as_uint(__ldg(srow + s));
+    for (int i = tid; i < 2048; i += kThreads) sm->hist[i] = 0u;
+    cp_async_wait<0>();
+    __syncthreads();
+    // order keys in place (invalid -> 0) and the first 11-bit histogram,
+    // four consecutive keys per thread
+    const int nq = (len + 3) >> 2;
+    for (int c0 = 0; c0 < nq; c0 += kThreads) {
+      const int c = c0 + tid;
+      uint32_t kq[4] = {0u, 0u, 0u, 0u};
+      if (c < nq) {
+        const uint4 raw = reinterpret_cast<const uint4*>(keys)[c];
+        const uint32_t rv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int si = 4 * c + e;
+          const bool v = si < len && (!seg_row || seg_row[si] == seg_t);
+          kq[e] = v ? order_key(__uint_as_float(rv[e])) : 0u;
+        }
+        reinterpret_cast<uint4*>(keys)[c] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool part = kq[e] != 0u;
+        const uint32_t bin = kq[e] >> 21;
+        const uint32_t peers = __match_any_sync(0xffffffffu, part ? bin : 0xFFFFFFFFu);
+        if (part && lane == __ffs(peers) - 1) atomicAdd(&sm->hist[bin], __popc(peers));
+      }
     }
+    __syncthreads();
+    int bin, above, in_bin;
+    find_bin(sm->hist, 2048, p.k, sm, bin, above, in_bin);
+    uint32_t prefix = static_cast<uint32_t>(bin) << 21, mask = 0xFFE00000u;
+    int need = p.k - above;
+    const int shifts[2] = {10, 0};
+    const int nbins[2] = {2048, 1024};
+#pragma unroll 1
+    for (int lvl = 0; lvl < 2 && in_bin != need; ++lvl) {
+      const int shift = shifts[lvl], nb = nbins[lvl];
+      for (int i = tid; i < nb; i += kThreads) sm->hist[i] = 0u;
+      __syncthreads();
+      for (int s0 = 0; s0 < len; s0 += kThreads) {
+        const int s = s0 + tid;
+        const uint32_t key = s < len ? keys[s] : 0u;
+        const bool part = key != 0u && (key & mask) == prefix;
+        const uint32_t b2 = (key >> shift) & static_cast<uint32_t>(nb - 1);
+        const uint32_t peers = __match_any_sync(0xffffffffu, part ? b2 : 0xFFFFFFFFu);
+        if (part && lane == __ffs(peers) - 1) atomicAdd(&sm->hist[b2], __popc(peers));
+      }
+      __syncthreads();
+      find_bin(sm->hist, nb, need, sm, bin, above, in_bin);
+      prefix |= static_cast<uint32_t>(bin) << shift;
+      mask |= static_cast<uint32_t>(nb - 1) << shift;
+      need -= above;
+    }
+    const uint32_t fmask = mask, fprefix = prefix;
+    ordered_select(
+        len,
+        [&](int s) {
+          const uint32_t key = keys[s];
+          const uint32_t km = key & fmask;
+          return make_int2(key != 0u && km > fprefix, key != 0u && km == fprefix);
+        },
+        need, out, p.k, sm);
+    if (p.count && tid == 0) p.count[row] = p.k;
+    return;
   }
-  __syncthreads();
-
+  // ---- rows longer than the shared stage: 4 x 8-bit passes re-reading the row (L2)
   auto key_at = [&](int s) -> uint32_t {
-    if (staged) return keys[s];
     const bool v = !seg_row || seg_row[s] == seg_t;
     return v ? order_key(__ldg(srow + s)) : 0u;
   };
@@ -207,6 +345,7 @@ int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int 
   p.idx = idx;
   p.count = count;
   p.stage_cap = S < kStageMax ? S : kStageMax;
+  p.stage_cap = (p.stage_cap + 3) & ~3;   // whole uint4 groups
   const size_t smem = sizeof(TopkSmem) + static_cast<size_t>(p.stage_cap) * 4;
   if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
