@@ -85,8 +85,9 @@ def load_peaks():
 
 
 def kernel_source_hash(stage: str) -> str:
-    files = {"indexer": ["indexer.cu"], "topk": ["topk.cu"], "attn_fwd": ["attn_fwd.cu"],
-             "attn_bwd": ["attn_bwd.cu"]}[stage]
+    files = {"indexer": ["indexer.cu"], "topk": ["topk.cu"],
+             "attn_fwd": ["attn_fwd.cu", "attn_fwd_tc.cu"],
+             "attn_bwd": ["attn_bwd.cu", "attn_bwd_tc.cu"]}[stage]
     h = hashlib.sha256()
     for f in files + ["dsa_common.cuh", "dsa_attn_common.cuh"]:
         with open(os.path.join(ROOT, "sparse_attention_index_gb300", "csrc", f), "rb") as fh:

@@ -9,13 +9,17 @@
 //   n <= k : every valid key is selected (ordered compaction, no score read).
 //   n >  k : the scores are mapped to order-preserving 32-bit keys (-0 -> +0)
 //            and the k-th largest key T is found digit by digit with
-//            warp-aggregated (__match_any_sync) shared-memory histograms. Rows
-//            that fit in shared memory are staged there while the first 11-bit
-//            histogram is built; at most two more passes (11, 10 bits) run on
-//            the staged keys. Longer rows take 4 x 8-bit passes over global
-//            memory (L2). A final ordered pass selects every key > T and the
-//            lowest-index `need` keys == T; each warp owns a contiguous segment,
-//            so one barrier orders the output. Slots m..k-1 get -1.
+//            shared-memory histograms. Rows that fit in shared memory are staged
+//            there (16-byte asynchronous copies) and the first 11-bit histogram is
+//            built while the keys are converted; at most two more levels (11, 10
+//            bits) run on the staged keys, four keys per thread, and stop as soon
+//            as the selected bin holds exactly the keys still needed. The final
+//            ordered pass selects every key > T and the lowest-index `need` keys
+//            == T: each warp owns a contiguous segment, a count sweep gives the
+//            segment offsets and a write sweep places the keys, through a shared
+//            staging row for coalesced stores. Longer rows take 4 x 8-bit passes
+//            over global memory (L2) with warp-aggregated (__match_any_sync)
+//            histograms. Slots m..k-1 get -1.
 
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
@@ -154,6 +158,85 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need,
   __syncthreads();
 }
 
+// Final ordered selection over the staged keys (uint4 groups of four consecutive
+// keys): every key with (key & mask) > prefix and the first `need` keys with
+// (key & mask) == prefix, written to out[] in ascending key index. Each warp owns
+// a contiguous segment of groups; a count sweep gives the segment offsets, a
+// write sweep places each key at (#gt before it) + min(#eq before it, need).
+__device__ __forceinline__ void select_staged(const uint4* keys4, int nq, uint32_t mask,
+                                              uint32_t prefix, int need, int32_t* out,
+                                              int kmax, TopkSmem* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int segq = ((nq + kWarps * 32 - 1) / (kWarps * 32)) * 32;
+  const int q_begin = warp * segq, q_end = min(nq, q_begin + segq);
+  int cg = 0, ce = 0;
+  for (int q = q_begin + lane; q < q_end; q += 32) {
+    const uint4 kv = keys4[q];
+    const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t km = kk[e] & mask;
+      cg += (kk[e] != 0u && km > prefix);
+      ce += (kk[e] != 0u && km == prefix);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cg += __shfl_xor_sync(0xffffffffu, cg, o);
+    ce += __shfl_xor_sync(0xffffffffu, ce, o);
+  }
+  if (lane == 0) {
+    sm->wgt[warp] = cg;
+    sm->weq[warp] = ce;
+  }
+  __syncthreads();
+  int gt_base = 0, eq_base = 0;
+  for (int w = 0; w < warp; ++w) {
+    gt_base += sm->wgt[w];
+    eq_base += sm->weq[w];
+  }
+  for (int q0 = q_begin; q0 < q_end; q0 += 32) {
+    const int q = q0 + lane;
+    uint32_t kk[4] = {0u, 0u, 0u, 0u};
+    if (q < q_end) {
+      const uint4 kv = keys4[q];
+      kk[0] = kv.x;
+      kk[1] = kv.y;
+      kk[2] = kv.z;
+      kk[3] = kv.w;
+    }
+    int fg[4], fe[4], ng = 0, ne = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t km = kk[e] & mask;
+      fg[e] = kk[e] != 0u && km > prefix;
+      fe[e] = kk[e] != 0u && km == prefix;
+      ng += fg[e];
+      ne += fe[e];
+    }
+    // warp inclusive scan of (gt count | eq count << 16)
+    const int own = ng | (ne << 16);
+    int incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - own;
+    int g_before = gt_base + (excl & 0xFFFF), e_before = eq_base + (excl >> 16);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int pos = g_before + min(e_before, need);
+      if ((fg[e] || (fe[e] && e_before < need)) && pos < kmax) out[pos] = 4 * q + e;
+      g_before += fg[e];
+      e_before += fe[e];
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
+    gt_base += tot & 0xFFFF;
+    eq_base += tot >> 16;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   TopkSmem* sm = reinterpret_cast<TopkSmem*>(smem_raw);
@@ -206,30 +289,24 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     for (int i = tid; i < 2048; i += kThreads) sm->hist[i] = 0u;
     cp_async_wait<0>();
     __syncthreads();
-    // order keys in place (invalid -> 0) and the first 11-bit histogram,
-    // four consecutive keys per thread
+    // order keys in place (invalid -> 0; the tail of the last uint4 -> 0) and
+    // the first 11-bit histogram, four consecutive keys per thread
     const int nq = (len + 3) >> 2;
-    for (int c0 = 0; c0 < nq; c0 += kThreads) {
-      const int c = c0 + tid;
-      uint32_t kq[4] = {0u, 0u, 0u, 0u};
-      if (c < nq) {
-        const uint4 raw = reinterpret_cast<const uint4*>(keys)[c];
-        const uint32_t rv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int si = 4 * c + e;
-          const bool v = si < len && (!seg_row || seg_row[si] == seg_t);
-          kq[e] = v ? order_key(__uint_as_float(rv[e])) : 0u;
-        }
-        reinterpret_cast<uint4*>(keys)[c] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
-      }
+    uint4* keys4 = reinterpret_cast<uint4*>(keys);
+    for (int c = tid; c < nq; c += kThreads) {
+      const uint4 raw = keys4[c];
+      const uint32_t rv[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t kq[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const bool part = kq[e] != 0u;
-        const uint32_t bin = kq[e] >> 21;
-        const uint32_t peers = __match_any_sync(0xffffffffu, part ? bin : 0xFFFFFFFFu);
-        if (part && lane == __ffs(peers) - 1) atomicAdd(&sm->hist[bin], __popc(peers));
+        const int si = 4 * c + e;
+        const bool v = si < len && (!seg_row || seg_row[si] == seg_t);
+        kq[e] = v ? order_key(__uint_as_float(rv[e])) : 0u;
       }
+      keys4[c] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (kq[e] != 0u) atomicAdd(&sm->hist[kq[e] >> 21], 1u);
     }
     __syncthreads();
     int bin, above, in_bin;
@@ -243,13 +320,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       const int shift = shifts[lvl], nb = nbins[lvl];
       for (int i = tid; i < nb; i += kThreads) sm->hist[i] = 0u;
       __syncthreads();
-      for (int s0 = 0; s0 < len; s0 += kThreads) {
-        const int s = s0 + tid;
-        const uint32_t key = s < len ? keys[s] : 0u;
-        const bool part = key != 0u && (key & mask) == prefix;
-        const uint32_t b2 = (key >> shift) & static_cast<uint32_t>(nb - 1);
-        const uint32_t peers = __match_any_sync(0xffffffffu, part ? b2 : 0xFFFFFFFFu);
-        if (part && lane == __ffs(peers) - 1) atomicAdd(&sm->hist[b2], __popc(peers));
+      for (int c = tid; c < nq; c += kThreads) {
+        const uint4 kv = keys4[c];
+        const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (kk[e] != 0u && (kk[e] & mask) == prefix)
+            atomicAdd(&sm->hist[(kk[e] >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
       }
       __syncthreads();
       find_bin(sm->hist, nb, need, sm, bin, above, in_bin);
@@ -257,15 +334,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       mask |= static_cast<uint32_t>(nb - 1) << shift;
       need -= above;
     }
-    const uint32_t fmask = mask, fprefix = prefix;
-    ordered_select(
-        len,
-        [&](int s) {
-          const uint32_t key = keys[s];
-          const uint32_t km = key & fmask;
-          return make_int2(key != 0u && km > fprefix, key != 0u && km == fprefix);
-        },
-        need, out, p.k, sm);
+    // output row staged in the (now free) histogram when it fits
+    int32_t* ostage = p.k <= 2048 ? reinterpret_cast<int32_t*>(sm->hist) : out;
+    select_staged(keys4, nq, mask, prefix, need, ostage, p.k, sm);
+    if (ostage != out) {
+      __syncthreads();
+      for (int j = tid; j < p.k; j += kThreads) out[j] = ostage[j];
+    }
     if (p.count && tid == 0) p.count[row] = p.k;
     return;
   }

@@ -166,6 +166,10 @@ WORKLOADS = {
         "v32_671b_s16k", seed=2, B=1, S=16384, Hi=64, Di=128, topk=2048, H=128, Dqk=192, Dv=128,
         backward=True,
         description="DS-v3.2-671B layer shape: 64 idx heads x 128, top-2048, 128 heads, fwd+bwd"),
+    "v32_671b_s4096": Workload(
+        "v32_671b_s4096", seed=2, B=1, S=4096, Hi=64, Di=128, topk=2048, H=128, Dqk=192, Dv=128,
+        backward=True,
+        description="DS-v3.2-671B layer shape cut to S=4096 (profiling size), fwd+bwd"),
     "long_s128k": Workload(
         "long_s128k", seed=3, B=1, S=131072, Hi=64, Di=128, topk=2048, H=128, Dqk=192, Dv=128,
         backward=False,
