@@ -10,16 +10,21 @@
 //   n >  k : the scores are mapped to order-preserving 32-bit keys (-0 -> +0)
 //            and the k-th largest key T is found digit by digit with
 //            shared-memory histograms. Rows that fit in shared memory are staged
-//            there (16-byte asynchronous copies) and the first 11-bit histogram is
-//            built while the keys are converted; at most two more levels (11, 10
-//            bits) run on the staged keys, four keys per thread, and stop as soon
-//            as the selected bin holds exactly the keys still needed. The final
-//            ordered pass selects every key > T and the lowest-index `need` keys
-//            == T: each warp owns a contiguous segment, a count sweep gives the
-//            segment offsets and a write sweep places the keys, through a shared
-//            staging row for coalesced stores. Longer rows take 4 x 8-bit passes
-//            over global memory (L2) with warp-aggregated (__match_any_sync)
-//            histograms. Slots m..k-1 get -1.
+//            there (16-byte asynchronous copies). The first level bins key >> 17
+//            (64 bins per octave) over 32 octaves of the sign where a 512-score
+//            sample puts the k-th largest score, with one bin each for the keys
+//            below and above that window; it is built while the keys are
+//            converted. When at most kCandCap keys share the threshold bin, one
+//            sweep writes the bitmap of the keys above it and the list of the keys
+//            in it; the remaining digits are resolved on the list, whose selected
+//            keys join the bitmaps, and one bitmap word per thread emits the
+//            selection in ascending order (through a shared staging row for
+//            coalesced stores). Otherwise 11 + 11 + 10 bit levels run over all
+//            staged keys and an ordered sweep per warp segment writes the result.
+//            Longer rows take 4 x 8-bit passes over global memory (L2) with
+//            warp-aggregated (__match_any_sync) histograms. Every selection takes
+//            the keys > T and the lowest-index `need` keys == T. Slots m..k-1
+//            get -1.
 
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
@@ -30,6 +35,8 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kStageMax = 16384;   // keys staged in shared memory per row
+constexpr int kCandCap = 1024;     // threshold-bin keys resolved as a list
+static_assert(kStageMax <= 32 * kThreads, "one bitmap word per thread");
 
 struct TopkParams {
   const float* scores;
@@ -46,6 +53,7 @@ struct TopkSmem {
   int warp_tot[kWarps];
   int wgt[kWarps], weq[kWarps];
   int bcast[4];
+  uint32_t ubc[4];
 };
 
 // Larger float -> larger key; -0.0 and +0.0 map to the same key; key 0 is never
@@ -132,12 +140,14 @@ __device__ __forceinline__ void ordered_select(int len, Flags flags, int need, i
 // key, the number of keys in higher bins and in that bin (broadcast through sm).
 __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, TopkSmem* sm,
                                          int& bin, int& above, int& in_bin) {
-  const int per = nb / kThreads;   // 4 or 2 bins per thread, highest bins to thread 0
+  // up to 4 bins per thread (nb <= 4 * kThreads), the highest bins to thread 0
+  const int per = nb > kThreads ? nb / kThreads : 1;
   const int tid = threadIdx.x;
   int c[4] = {0, 0, 0, 0};
   int sum = 0;
   for (int i = 0; i < per; ++i) {
-    c[i] = static_cast<int>(hist[nb - 1 - (tid * per + i)]);
+    const int j = tid * per + i;
+    c[i] = j < nb ? static_cast<int>(hist[nb - 1 - j]) : 0;
     sum += c[i];
   }
   int tot;
@@ -237,6 +247,185 @@ __device__ __forceinline__ void select_staged(const uint4* keys4, int nq, uint32
   }
 }
 
+// First-level bins: h = key >> 17 (sign, exponent and six mantissa bits) over a
+// window of 2046 values of h (32 octaves of one sign); bin 0 takes the keys below
+// the window and bin 2047 the keys above it. The keys of a window bin share one
+// 15-bit prefix.
+struct LevelOne {
+  uint32_t base;   // h of bin 1
+  __device__ __forceinline__ uint32_t bucket(uint32_t key) const {
+    const uint32_t h = key >> 17;
+    return h < base ? 0u : min(h - base + 1u, 2047u);
+  }
+  __device__ __forceinline__ bool interior(uint32_t bin) const {
+    return bin >= 1u && bin <= 2046u;
+  }
+  __device__ __forceinline__ uint32_t prefix(uint32_t bin) const {
+    return (base + bin - 1u) << 17;
+  }
+  // From the largest positive score bits, the largest negative-score magnitude
+  // bits and whether the k-th largest score is expected to be >= 0: the window
+  // ends two octaves above the positive maximum, or starts two octaves beyond the
+  // negative one.
+  static __device__ __forceinline__ LevelOne make(uint32_t apos, uint32_t aneg,
+                                                  bool positive_side) {
+    LevelOne w;
+    if (positive_side) {
+      const uint32_t whi = min(0x4000u + (apos >> 17) + 128u, 0x7FFFu);
+      w.base = whi - 2045u;
+    } else {
+      const uint32_t ha = (0x7FFFFFFFu - aneg) >> 17;
+      w.base = ha > 128u ? ha - 128u : 0u;
+    }
+    return w;
+  }
+};
+
+// Selection when the first level leaves at most kCandCap keys in the threshold bin
+// ((key & 0xFFFE0000) == prefix): one sweep over the staged keys writes the
+// bitmap of the keys above the bin and the list of the keys in it; the remaining
+// digits are resolved on that list alone; the selected list keys are added to the
+// bitmaps (above T / equal to T) and one word per thread emits the selection in
+// ascending order, the first `need` keys equal to T included. The histogram area
+// holds the bitmaps, the list and the small histogram, and then the output row.
+__device__ __forceinline__ void select_candidates(const uint32_t* keys, const uint4* keys4,
+                                                  int len, int nq, const LevelOne& w1,
+                                                  uint32_t bin1, int need, int in_bin,
+                                                  int32_t* out, int kmax, TopkSmem* sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  uint32_t* gtw = sm->hist;                                     // [512] above T
+  uint32_t* eqw = sm->hist + 512;                               // [512] equal to T
+  uint16_t* cand = reinterpret_cast<uint16_t*>(sm->hist + 1024);   // [kCandCap]
+  uint32_t* h2 = sm->hist + 1536;                               // [512]
+  const bool inner = w1.interior(bin1);
+  uint32_t mask = inner ? 0xFFFE0000u : 0u;
+  uint32_t prefix = inner ? w1.prefix(bin1) : 0u;
+  const int nwords = (len + 31) >> 5;
+  const int ncand = in_bin;
+  for (int i = tid; i < 512; i += kThreads) eqw[i] = 0u;
+  if (tid == 0) sm->ubc[3] = 0u;
+  __syncthreads();
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int c0 = 0; c0 < nq; c0 += kThreads) {
+    const int c = c0 + tid;
+    uint32_t kk[4] = {0u, 0u, 0u, 0u};
+    if (c < nq) {
+      const uint4 kv = keys4[c];
+      kk[0] = kv.x;
+      kk[1] = kv.y;
+      kk[2] = kv.z;
+      kk[3] = kv.w;
+    }
+    uint32_t nib = 0u;
+    bool cd[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t b1 = w1.bucket(kk[e]);
+      nib |= static_cast<uint32_t>(kk[e] != 0u && b1 > bin1) << e;
+      cd[e] = kk[e] != 0u && b1 == bin1;
+    }
+    // lanes 8j..8j+7 hold the 32 keys of one bitmap word
+    uint32_t wv = nib << (4 * (lane & 7));
+    wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+    wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+    wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
+    if ((lane & 7) == 0 && c < nq) gtw[c >> 3] = wv;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t bal = __ballot_sync(0xffffffffu, cd[e]);
+      if (bal) {
+        const int leader = __ffs(bal) - 1;
+        uint32_t base = 0u;
+        if (lane == leader) base = atomicAdd(&sm->ubc[3], static_cast<uint32_t>(__popc(bal)));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        const uint32_t r = base + __popc(bal & lt);
+        if (cd[e] && r < kCandCap) cand[r] = static_cast<uint16_t>(4 * c + e);
+      }
+    }
+  }
+  __syncthreads();
+  // remaining digits on the list: bits 16..8 and 7..0 of an interior bin,
+  // four bytes otherwise
+  const int nlev = inner ? 2 : 4;
+  int cur = in_bin;
+#pragma unroll 1
+  for (int lvl = 0; lvl < nlev && cur != need; ++lvl) {
+    const int shift = inner ? 8 - 8 * lvl : 24 - 8 * lvl;
+    const int nb = inner && lvl == 0 ? 512 : 256;
+    const uint32_t low = (1u << shift) - 1u;
+    for (int i = tid; i < nb; i += kThreads) h2[i] = 0u;
+    if (tid == 0) {
+      sm->ubc[1] = 0u;
+      sm->ubc[2] = 0xFFFFFFFFu;
+    }
+    __syncthreads();
+    uint32_t lo_or = 0u, lo_and = 0xFFFFFFFFu;
+    for (int j = tid; j < ncand; j += kThreads) {
+      const uint32_t key = keys[cand[j]];
+      if ((key & mask) == prefix) {
+        atomicAdd(&h2[(key >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+        lo_or |= key & low;
+        lo_and &= key & low;
+      }
+    }
+    lo_or = __reduce_or_sync(0xffffffffu, lo_or);
+    lo_and = __reduce_and_sync(0xffffffffu, lo_and);
+    if (lane == 0) {
+      atomicOr(&sm->ubc[1], lo_or);
+      atomicAnd(&sm->ubc[2], lo_and);
+    }
+    __syncthreads();
+    const uint32_t all_or = sm->ubc[1], all_and = sm->ubc[2];
+    int bin, above;
+    find_bin(h2, nb, need, sm, bin, above, cur);
+    prefix |= static_cast<uint32_t>(bin) << shift;
+    mask |= static_cast<uint32_t>(nb - 1) << shift;
+    need -= above;
+    if (all_or == (all_and & low)) {
+      prefix |= all_or;
+      mask |= low;
+      break;
+    }
+  }
+  // list keys above T / equal to T into the bitmaps
+  for (int j = tid; j < ncand; j += kThreads) {
+    const int sj = cand[j];
+    const uint32_t km = keys[sj] & mask;
+    if (km > prefix) atomicOr(&gtw[sj >> 5], 1u << (sj & 31));
+    else if (km == prefix) atomicOr(&eqw[sj >> 5], 1u << (sj & 31));
+  }
+  __syncthreads();
+  // one word per thread: offsets by a block scan of (above count | equal count << 16)
+  uint32_t g = 0u, q = 0u;
+  if (tid < nwords) {
+    g = gtw[tid];
+    q = eqw[tid];
+  }
+  const int own = __popc(g) | (__popc(q) << 16);
+  int tot;
+  const int excl = block_scan(own, tot, sm) - own;   // every word is read before this returns
+  int gb = excl & 0xFFFF, eb = excl >> 16;
+  int32_t* ost = kmax <= 2048 ? reinterpret_cast<int32_t*>(sm->hist) : out;
+  uint32_t bits = g | q;
+  while (bits) {
+    const int b = __ffs(bits) - 1;
+    bits &= bits - 1u;
+    const int sj = tid * 32 + b;
+    if ((g >> b) & 1u) {
+      const int pos = gb + min(eb, need);
+      if (pos < kmax) ost[pos] = sj;
+      ++gb;
+    } else {
+      if (eb < need && gb + eb < kmax) ost[gb + eb] = sj;
+      ++eb;
+    }
+  }
+  if (ost != out) {
+    __syncthreads();
+    for (int j = tid; j < kmax; j += kThreads) out[j] = ost[j];
+  }
+}
+
 __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   TopkSmem* sm = reinterpret_cast<TopkSmem*>(smem_raw);
@@ -287,12 +476,66 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     for (int s = 4 * nvec + tid; s < len; s += kThreads)
       keys[s] = __float_as_uint(__ldg(srow + s));
     for (int i = tid; i < 2048; i += kThreads) sm->hist[i] = 0u;
+    if (tid == 0) {
+      sm->ubc[0] = 0u;
+      sm->ubc[1] = 0u;
+      sm->ubc[2] = 0u;
+      sm->ubc[3] = 0u;
+    }
     cp_async_wait<0>();
     __syncthreads();
-    // order keys in place (invalid -> 0; the tail of the last uint4 -> 0) and
-    // the first 11-bit histogram, four consecutive keys per thread
     const int nq = (len + 3) >> 2;
     uint4* keys4 = reinterpret_cast<uint4*>(keys);
+    // first-level window from up to 512 evenly spread valid scores (from the
+    // whole row when none of them is valid): the largest positive score, the
+    // largest negative magnitude and the share of scores >= 0
+    uint32_t npos, nval;
+    {
+      const int si = static_cast<int>((static_cast<long long>(tid) * len) / kThreads);
+      const bool v = !seg_row || seg_row[si] == seg_t;
+      const uint32_t u = keys[si];
+      const bool pos = v && ((u & 0x80000000u) == 0u || u == 0x80000000u);
+      const uint32_t ap = __reduce_max_sync(0xffffffffu, pos ? (u & 0x7FFFFFFFu) : 0u);
+      const uint32_t an = __reduce_max_sync(0xffffffffu, v && !pos ? (u & 0x7FFFFFFFu) : 0u);
+      if (lane == 0) {
+        atomicMax(&sm->ubc[0], ap);
+        atomicMax(&sm->ubc[1], an);
+      }
+      npos = static_cast<uint32_t>(__syncthreads_count(pos));
+      nval = static_cast<uint32_t>(__syncthreads_count(v));
+    }
+    if (nval == 0u) {
+      uint32_t ap = 0u, an = 0u, cp = 0u, cv = 0u;
+      for (int si = tid; si < len; si += kThreads) {
+        if (seg_row[si] != seg_t) continue;
+        const uint32_t u = keys[si];
+        const bool pos = (u & 0x80000000u) == 0u || u == 0x80000000u;
+        if (pos) ap = max(ap, u & 0x7FFFFFFFu);
+        else an = max(an, u & 0x7FFFFFFFu);
+        cp += pos;
+        ++cv;
+      }
+      ap = __reduce_max_sync(0xffffffffu, ap);
+      an = __reduce_max_sync(0xffffffffu, an);
+      cp = __reduce_add_sync(0xffffffffu, cp);
+      cv = __reduce_add_sync(0xffffffffu, cv);
+      if (lane == 0) {
+        atomicMax(&sm->ubc[0], ap);
+        atomicMax(&sm->ubc[1], an);
+        atomicAdd(&sm->ubc[2], cp);
+        atomicAdd(&sm->ubc[3], cv);
+      }
+      __syncthreads();
+      npos = sm->ubc[2];
+      nval = sm->ubc[3];
+    }
+    // the k-th largest score is expected >= 0 when at least k of the n valid
+    // scores are expected >= 0
+    const bool positive_side =
+        static_cast<unsigned long long>(npos) * n >= static_cast<unsigned long long>(nval) * p.k;
+    const LevelOne w1 = LevelOne::make(sm->ubc[0], sm->ubc[1], positive_side);
+    // order keys in place (invalid -> 0; the tail of the last uint4 -> 0) and the
+    // first-level histogram, four consecutive keys per thread
     for (int c = tid; c < nq; c += kThreads) {
       const uint4 raw = keys4[c];
       const uint32_t rv[4] = {raw.x, raw.y, raw.z, raw.w};
@@ -306,33 +549,65 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
       keys4[c] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
 #pragma unroll
       for (int e = 0; e < 4; ++e)
-        if (kq[e] != 0u) atomicAdd(&sm->hist[kq[e] >> 21], 1u);
+        if (kq[e] != 0u) atomicAdd(&sm->hist[w1.bucket(kq[e])], 1u);
     }
     __syncthreads();
     int bin, above, in_bin;
     find_bin(sm->hist, 2048, p.k, sm, bin, above, in_bin);
-    uint32_t prefix = static_cast<uint32_t>(bin) << 21, mask = 0xFFE00000u;
-    int need = p.k - above;
-    const int shifts[2] = {10, 0};
-    const int nbins[2] = {2048, 1024};
+    if (in_bin <= kCandCap) {
+      select_candidates(keys, keys4, len, nq, w1, static_cast<uint32_t>(bin), p.k - above,
+                        in_bin, out, p.k, sm);
+      if (p.count && tid == 0) p.count[row] = p.k;
+      return;
+    }
+    // many keys share the threshold bin: 11 + 11 + 10 bit levels over all staged
+    // keys
+    uint32_t prefix = 0u, mask = 0u;
+    int need = p.k;
+    in_bin = -1;
+    const int shifts[3] = {21, 10, 0};
+    const int nbins[3] = {2048, 2048, 1024};
+    const int nlev = 3;
 #pragma unroll 1
-    for (int lvl = 0; lvl < 2 && in_bin != need; ++lvl) {
+    for (int lvl = 0; lvl < nlev && in_bin != need; ++lvl) {
       const int shift = shifts[lvl], nb = nbins[lvl];
+      const uint32_t low = (1u << shift) - 1u;
       for (int i = tid; i < nb; i += kThreads) sm->hist[i] = 0u;
+      if (tid == 0) {
+        sm->ubc[1] = 0u;            // OR of the bits below this level
+        sm->ubc[2] = 0xFFFFFFFFu;   // AND of the bits below this level
+      }
       __syncthreads();
+      uint32_t lo_or = 0u, lo_and = 0xFFFFFFFFu;
       for (int c = tid; c < nq; c += kThreads) {
         const uint4 kv = keys4[c];
         const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          if (kk[e] != 0u && (kk[e] & mask) == prefix)
+          if (kk[e] != 0u && (kk[e] & mask) == prefix) {
             atomicAdd(&sm->hist[(kk[e] >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+            lo_or |= kk[e] & low;
+            lo_and &= kk[e] & low;
+          }
+      }
+      lo_or = __reduce_or_sync(0xffffffffu, lo_or);
+      lo_and = __reduce_and_sync(0xffffffffu, lo_and);
+      if (lane == 0) {
+        atomicOr(&sm->ubc[1], lo_or);
+        atomicAnd(&sm->ubc[2], lo_and);
       }
       __syncthreads();
+      const uint32_t all_or = sm->ubc[1], all_and = sm->ubc[2];
       find_bin(sm->hist, nb, need, sm, bin, above, in_bin);
       prefix |= static_cast<uint32_t>(bin) << shift;
       mask |= static_cast<uint32_t>(nb - 1) << shift;
       need -= above;
+      if (all_or == (all_and & low)) {
+        // every key still in play has the same lower bits: the key is resolved
+        prefix |= all_or;
+        mask |= low;
+        break;
+      }
     }
     // output row staged in the (now free) histogram when it fits
     int32_t* ostage = p.k <= 2048 ? reinterpret_cast<int32_t*>(sm->hist) : out;

@@ -138,6 +138,29 @@ def test_topk_heavy_ties(ndocs, k):
                 seg, S, k, np.arange(B * S))
 
 
+@pytest.mark.parametrize("kind", ["ulps", "wide"])
+@pytest.mark.parametrize("k", [3, 100, 700])
+def test_topk_close_and_wide_keys(kind, k):
+    """Keys a few ulps apart (every radix digit decides) and keys over ~120 octaves
+    (the k-th largest far below the row maximum)."""
+    dsa = _dsa()
+    B, S = 1, 900
+    rng = np.random.default_rng(k + (0 if kind == "ulps" else 1))
+    if kind == "ulps":
+        base = np.float32(1.0 + 2.0 ** -10)
+        sc = base + rng.integers(-300, 300, size=(B, S, S)).astype(np.float32) * np.float32(2 ** -23)
+        sc[..., ::5] *= -1
+    else:
+        mant = rng.uniform(1.0, 2.0, size=(B, S, S))
+        sc = (np.sign(rng.standard_normal((B, S, S))) * mant *
+              np.exp2(rng.integers(-60, 61, size=(B, S, S)))).astype(np.float32)
+        sc[0, :, 0] = 1e30   # one huge key per row
+    idx, cnt = dsa.dsa_topk(dev(sc.astype(np.float32)), k)
+    _check_topk(idx.cpu().numpy(), cnt.cpu().numpy(),
+                sc.astype(np.float32).reshape(B * S, S).astype(np.float64), None, S, k,
+                np.arange(B * S))
+
+
 def test_topk_rows_longer_than_the_shared_stage():
     dsa = _dsa()
     S, k = 17000, 100
