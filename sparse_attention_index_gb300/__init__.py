@@ -24,6 +24,9 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libdsa.so")
 
 DSA_BF16, DSA_F32 = 0, 1
+# device error codes (dsa_get_last_device_error): kind | stage
+DSA_DEVERR_TIMEOUT, DSA_DEVERR_BAD_INDEX, DSA_DEVERR_MISALIGNED = 0x01, 0x02, 0x03
+DSA_STAGE_INDEXER, DSA_STAGE_TOPK, DSA_STAGE_FWD, DSA_STAGE_BWD = 0x100, 0x200, 0x300, 0x400
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
           4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_DEVICE"}
 

@@ -27,6 +27,8 @@
 // TMEM: [Q: Dqk/2 cols][S/P: 3 buffers x NK cols][O: Dv cols] = 512 columns.
 // Query rows are handed out longest first, strided over CTAs.
 
+#include <cstdlib>
+
 #include "dsa_attn_common.cuh"
 
 namespace dsa {
@@ -238,7 +240,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
           h.last = c == nch - 1;
         }
         if (!bar_gather_ok(tail->okb, nb, abort_flag)) { stop = true; break; }
-        mbar_arrive(&tail->kv_full[st]);   // releases this thread's header writes
+        // releases this thread's header writes (the failure-detection test drops the
+        // first one of CTA 0, so that the issuer's bounded wait runs out)
+        if (!(p.test_drop_arrive && blockIdx.x == 0 && g == 0 && gt == 0))
+          mbar_arrive(&tail->kv_full[st]);
         const uint32_t stage = smem_u32(smem + st * L::kStage);
         const long long rowbase = static_cast<long long>(b) * p.S;
         for (int grp = gw; grp < kNK / 4; grp += kGatherWarps) {
@@ -545,7 +550,13 @@ int launch_tc(const AttnParams& p, cudaStream_t stream) {
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const long long rows = static_cast<long long>(p.B) * p.S;
   const int grid = static_cast<int>(rows < sms ? rows : sms);
-  kern<<<grid, kThreads, smem, stream>>>(p);
+  // Failure-detection test: with DSA_TEST_DROP_ARRIVE set in the environment
+  // when the library first launches this kernel, one producer arrive is skipped
+  // and the call ends through the bounded-wait timeout path.
+  static const int drop = std::getenv("DSA_TEST_DROP_ARRIVE") != nullptr ? 1 : 0;
+  AttnParams q = p;
+  q.test_drop_arrive = drop;
+  kern<<<grid, kThreads, smem, stream>>>(q);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

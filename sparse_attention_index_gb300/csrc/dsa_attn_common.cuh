@@ -18,6 +18,7 @@ struct AttnParams {
   uint16_t* dQ;
   float* ws;   // fp32 [B*S, Dqk + Dv] dK / dV accumulators
   int* err;    // device error word
+  int test_drop_arrive;   // failure-detection test only: see attn_fwd_tc.cu
 };
 
 inline AttnParams make_attn_params(const void* Q, const void* K, const void* V,
