@@ -43,6 +43,7 @@ constexpr int kMmaWarp = 12;
 constexpr int kGatherWarp0 = 13;
 constexpr int kGatherWarps = 3;
 constexpr int kGatherThreads = 32 * kGatherWarps;
+constexpr int kPrefetch = 22;        // index-list entries per gather thread held ahead
 constexpr int kThreads = 512;
 constexpr int kErrB = DSA_STAGE_BWD | DSA_DEVERR_TIMEOUT;
 
@@ -206,6 +207,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       v_off[i] = pv * 8;
       v_dst[i] = (3 + (pv >> 3)) * kKVAtom + ((pv & 7) << 4);
     }
+    // kend of a row (one past its last slot holding a causal key) needs the whole
+    // index list; for k <= kPrefetch * kGatherThreads the next row's list is loaded
+    // into registers while the current row is gathered
+    const bool prefetch = p.k <= kPrefetch * kGatherThreads;
+    int pre[kPrefetch];
+    auto load_list = [&](long long row) {
+      const int32_t* ir = p.idx + row * p.k;
+#pragma unroll
+      for (int u = 0; u < kPrefetch; ++u) {
+        const int j = gt + u * kGatherThreads;
+        pre[u] = j < p.k ? __ldg(ir + j) : -1;
+      }
+    };
+    if (prefetch && static_cast<int>(blockIdx.x) < nrows) load_list(brow_of(blockIdx.x, nrows));
     int g = 0, nb = 0;
     for (int i = blockIdx.x; i < nrows; i += gridDim.x) {
       const long long row = brow_of(i, nrows);
@@ -213,10 +228,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = static_cast<int>(row - static_cast<long long>(b) * p.S);
       const int32_t* irow = p.idx + row * p.k;
       int last = 0;
+      if (prefetch) {
+#pragma unroll
+        for (int u = 0; u < kPrefetch; ++u) {
+          const int s = pre[u];
+          if (s >= 0 && s <= t && s < p.S) last = gt + u * kGatherThreads + 1;
+        }
+        if (i + static_cast<int>(gridDim.x) < nrows) load_list(brow_of(i + gridDim.x, nrows));
+      } else {
 #pragma unroll 8
-      for (int j = gt; j < p.k; j += kGatherThreads) {
-        const int s = __ldg(irow + j);
-        if (s >= 0 && s <= t && s < p.S) last = j + 1;
+        for (int j = gt; j < p.k; j += kGatherThreads) {
+          const int s = __ldg(irow + j);
+          if (s >= 0 && s <= t && s < p.S) last = j + 1;
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));

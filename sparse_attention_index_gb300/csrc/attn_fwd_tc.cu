@@ -39,6 +39,7 @@ constexpr int kStages = 3;           // K/V stages == S/P buffers
 constexpr int kGatherWarp0 = 5;
 constexpr int kGatherWarps = 7;
 constexpr int kGatherThreads = 32 * kGatherWarps;
+constexpr int kPrefetch = 10;         // index-list entries per gather thread held ahead
 constexpr int kThreads = 384;
 constexpr int kErrTc = DSA_STAGE_FWD | DSA_DEVERR_TIMEOUT;
 constexpr float kRescaleLog2 = 8.f;  // refresh the running max when it grows by > 2^8
@@ -200,18 +201,40 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
       v_off[i] = pv * 8;
       v_dst[i] = (L::KA + (pv >> 3)) * L::kAtom + ((pv & 7) << 4);
     }
+    // kend of a row (one past its last slot holding a causal key) needs the whole
+    // index list; for k <= kPrefetch * kGatherThreads the next row's list is loaded
+    // into registers while the current row is gathered
+    const bool prefetch = p.k <= kPrefetch * kGatherThreads;
+    int pre[kPrefetch];
+    auto load_list = [&](long long row) {
+      const int32_t* ir = p.idx + row * p.k;
+#pragma unroll
+      for (int u = 0; u < kPrefetch; ++u) {
+        const int j = gt + u * kGatherThreads;
+        pre[u] = j < p.k ? __ldg(ir + j) : -1;
+      }
+    };
+    if (prefetch && static_cast<int>(blockIdx.x) < nrows) load_list(row_of(blockIdx.x, nrows));
     int g = 0, nb = 0;
     for (int i = blockIdx.x; i < nrows; i += gridDim.x) {
       const long long row = row_of(i, nrows);
       const int b = static_cast<int>(row / p.S);
       const int t = static_cast<int>(row - static_cast<long long>(b) * p.S);
       const int32_t* irow = p.idx + row * p.k;
-      // kend: one past the last slot holding a causal key (independent loads)
       int last = 0;
+      if (prefetch) {
+#pragma unroll
+        for (int u = 0; u < kPrefetch; ++u) {
+          const int s = pre[u];
+          if (s >= 0 && s <= t && s < p.S) last = gt + u * kGatherThreads + 1;
+        }
+        if (i + static_cast<int>(gridDim.x) < nrows) load_list(row_of(i + gridDim.x, nrows));
+      } else {
 #pragma unroll 10
-      for (int j = gt; j < p.k; j += kGatherThreads) {
-        const int s = __ldg(irow + j);
-        if (s >= 0 && s <= t && s < p.S) last = j + 1;
+        for (int j = gt; j < p.k; j += kGatherThreads) {
+          const int s = __ldg(irow + j);
+          if (s >= 0 && s <= t && s < p.S) last = j + 1;
+        }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
@@ -328,8 +351,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
             umma_commit(&tail->kv_empty[pb]);
             umma_commit(&tail->s_empty[pb]);
           }
-          pend = g;
-          pend_first = first;
+          if (last) {
+            // the row's last chunk: its PV right away, so that the row's O is
+            // complete before the next row's first chunk arrives
+            const int pb = sb;
+            if (!mbar_wait(&tail->p_full[pb], use_par, abort_flag, p.err, kErrTc)) { ok = false; break; }
+            if (first) {
+              if (!mbar_wait(&tail->o_free, of_par, abort_flag, p.err, kErrTc)) { ok = false; break; }
+              of_par ^= 1u;
+            }
+            tc_fence_after();
+            const uint32_t vbase = smem_u32(smem + pb * L::kStage + L::KA * L::kAtom);
+#pragma unroll
+            for (int ks = 0; ks < kNK / 16; ++ks) {
+              const uint64_t bdesc =
+                  umma_sdesc_lbo(vbase + ks * 2048, L::kAtom, 1024, kLayoutSw128);
+              umma_bf16_ts(tmem + L::kColO, tmem + L::kColS + pb * kNK + ks * 8, bdesc, idesc_pv,
+                           (first && ks == 0) ? 0u : 1u);
+            }
+            umma_commit(&tail->kv_empty[pb]);
+            umma_commit(&tail->s_empty[pb]);
+            pend = -1;
+          } else {
+            pend = g;
+            pend_first = first;
+          }
           ++g;
         }
       }
@@ -440,8 +486,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
         }
         if (first) {
           m = mx;
-        } else if (mx > m && (m == -INFINITY || (mx - m) * c2 > kRescaleLog2)) {
-          // refresh the running max: rescale O (every earlier PV product is done) and l
+        } else if (__any_sync(0xffffffffu,
+                              mx > m && (m == -INFINITY || (mx - m) * c2 > kRescaleLog2))) {
+          // refresh the running max of every head of the warp (a no-op where it has
+          // not grown): rescale O (every earlier PV product is done) and l
           const int pg = g - 1;
           if (!__all_sync(0xffffffffu,
                           mbar_wait(&tail->s_empty[pg % kStages], (pg / kStages) & 1, abort_flag,
@@ -450,7 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
             break;
           }
           tc_fence_after();
-          const float f = m == -INFINITY ? 0.f : exp2f((m - mx) * c2);
+          const float mnew = fmaxf(m, mx);
+          const float f = m == -INFINITY ? 0.f : exp2f((m - mnew) * c2);
 #pragma unroll
           for (int d0 = 0; d0 < DV; d0 += 16) {
             uint32_t ov[16];
@@ -462,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
           }
           tmem_st_wait();
           l *= f;
-          m = mx;
+          m = mnew;
         }
         // P = exp2(S*c2 - m*c2) over valid keys -> bf16 pairs in the buffer's first NK/2 cols
         const float base = m == -INFINITY ? 0.f : m * c2;
