@@ -302,6 +302,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t id_dkv = idesc_bf16(128, NK, true, true);
       const uint32_t q_s = smem_u32(smem + kQOff), do_s = smem_u32(smem + kDOOff);
       const uint32_t p_s = smem_u32(smem + kPOff), ds_s = smem_u32(smem + kDSOff);
+      const uint32_t kv0 = smem_u32(smem + kKVOff);
+      // base descriptors, built once; every MMA below advances one by a constant
+      const uint64_t q_k = umma_sdesc(q_s, 1024, kLayoutSw128);      // K-major operands
+      const uint64_t do_k = umma_sdesc(do_s, 1024, kLayoutSw128);
+      const uint64_t ds_k = umma_sdesc(ds_s, 1024, kLayoutSw128);
+      const uint64_t kv_k = umma_sdesc(kv0, 1024, kLayoutSw128);
+      const uint64_t kv_mn = umma_sdesc_lbo(kv0, kKVAtom, 1024, kLayoutSw128);   // MN-major
+      const uint64_t q_mn = umma_sdesc_lbo(q_s, kQAtom, 1024, kLayoutSw128);
+      const uint64_t do_mn = umma_sdesc_lbo(do_s, kQAtom, 1024, kLayoutSw128);
+      const uint64_t p_mn = umma_sdesc_lbo(p_s, kQAtom, 1024, kLayoutSw128);
+      const uint64_t ds_mn = umma_sdesc_lbo(ds_s, kQAtom, 1024, kLayoutSw128);
       int g = 0, nrow = 0;
       int pend = -1, pend_flags = 0, pend_row = 0;
       bool ok = true;
@@ -313,12 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             !mbar_wait(&tail->dq_free, (prow & 1) ^ 1u, abort_flag, p.err, kErrB))
           return false;
         tc_fence_after();
-        const uint32_t kst = smem_u32(smem + kKVOff + st * kKVStage);
+        const uint64_t kst_mn = umma_desc_adv(kv_mn, st * kKVStage);
 #pragma unroll
         for (int kk = 0; kk < NK / 16; ++kk) {
-          umma_ss(tmem + kColDQ, umma_sdesc(ds_s + kk * 32, 1024, kLayoutSw128),
-                  umma_sdesc_lbo(kst + kk * 2048, kKVAtom, 1024, kLayoutSw128), id_dq,
-                  ((flags & 1) && kk == 0) ? 0u : 1u);
+          umma_ss(tmem + kColDQ, umma_desc_adv(ds_k, kk * 32), umma_desc_adv(kst_mn, kk * 2048),
+                  id_dq, ((flags & 1) && kk == 0) ? 0u : 1u);
         }
         if (flags & 2) umma_commit(&tail->dq_full);
         umma_commit(&tail->kv_empty[st]);   // K / V of this stage are no longer read
@@ -329,12 +339,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&tail->dkv_free[reg], (pg & 1) ^ 1u, abort_flag, p.err, kErrB)) return false;
           tc_fence_after();
           const uint32_t dcol = reg == 0 ? kColDV : (reg == 1 ? kColDKlo : kColDKhi);
-          const uint32_t abase = reg == 0 ? do_s : (reg == 1 ? q_s : q_s + 2 * kQAtom);
-          const uint32_t bbase = reg == 0 ? p_s : ds_s;
+          const uint64_t ad = reg == 0 ? do_mn : (reg == 1 ? q_mn : umma_desc_adv(q_mn, 2 * kQAtom));
+          const uint64_t bd = reg == 0 ? p_mn : ds_mn;
 #pragma unroll
           for (int kk = 0; kk < 128 / 16; ++kk)
-            umma_ss(tmem + dcol, umma_sdesc_lbo(abase + kk * 2048, kQAtom, 1024, kLayoutSw128),
-                    umma_sdesc_lbo(bbase + kk * 2048, kQAtom, 1024, kLayoutSw128), id_dkv,
+            umma_ss(tmem + dcol, umma_desc_adv(ad, kk * 2048), umma_desc_adv(bd, kk * 2048), id_dkv,
                     kk > 0 ? 1u : 0u);
           umma_commit(&tail->dkv_full[reg]);
         }
@@ -376,17 +385,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (g > 0 && !mbar_wait(&tail->sdp_free, (g - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
           fence_proxy_async_smem();
           tc_fence_after();
-          const uint32_t kst = smem_u32(smem + kKVOff + st * kKVStage);
+          const uint64_t kst_k = umma_desc_adv(kv_k, st * kKVStage);
 #pragma unroll
           for (int kk = 0; kk < DQK / 16; ++kk)
-            umma_ss(tmem + kColS, umma_sdesc(q_s + (kk >> 2) * kQAtom + (kk & 3) * 32, 1024, kLayoutSw128),
-                    umma_sdesc(kst + (kk >> 2) * kKVAtom + (kk & 3) * 32, 1024, kLayoutSw128), id_sdp,
+            umma_ss(tmem + kColS, umma_desc_adv(q_k, (kk >> 2) * kQAtom + (kk & 3) * 32),
+                    umma_desc_adv(kst_k, (kk >> 2) * kKVAtom + (kk & 3) * 32), id_sdp,
                     kk > 0 ? 1u : 0u);
 #pragma unroll
           for (int kk = 0; kk < DV / 16; ++kk)
-            umma_ss(tmem + kColDP, umma_sdesc(do_s + (kk >> 2) * kQAtom + (kk & 3) * 32, 1024, kLayoutSw128),
-                    umma_sdesc(kst + (3 + (kk >> 2)) * kKVAtom + (kk & 3) * 32, 1024, kLayoutSw128),
-                    id_sdp, kk > 0 ? 1u : 0u);
+            umma_ss(tmem + kColDP, umma_desc_adv(do_k, (kk >> 2) * kQAtom + (kk & 3) * 32),
+                    umma_desc_adv(kst_k, (3 + (kk >> 2)) * kKVAtom + (kk & 3) * 32), id_sdp,
+                    kk > 0 ? 1u : 0u);
           umma_commit(&tail->sdp_full);
           if (pend >= 0 && !issue_grads(pend, pend_flags, pend_row)) { ok = false; break; }
           pend = g;

@@ -225,6 +225,15 @@ __device__ __forceinline__ uint64_t umma_sdesc(uint32_t saddr, uint32_t sbo_byte
   return d;
 }
 
+// The descriptor of the operand `byte_off` bytes further on. The start-address
+// field holds the shared-memory address >> 4 in its low 14 bits and shared-memory
+// addresses stay below 256 KB, so the offset never carries out of the field. Issuing
+// threads build base descriptors once and advance them by constants: the MMA issue
+// rate of a single thread is bounded by its scalar work per instruction.
+__device__ __forceinline__ uint64_t umma_desc_adv(uint64_t desc, uint32_t byte_off) {
+  return desc + static_cast<uint64_t>(byte_off >> 4);
+}
+
 // Layout codes of the descriptor's swizzle field.
 constexpr uint32_t kLayoutSw128 = 2, kLayoutSw64 = 4, kLayoutSw32 = 6;
 
