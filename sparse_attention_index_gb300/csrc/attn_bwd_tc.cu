@@ -313,6 +313,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t do_mn = umma_sdesc_lbo(do_s, kQAtom, 1024, kLayoutSw128);
       const uint64_t p_mn = umma_sdesc_lbo(p_s, kQAtom, 1024, kLayoutSw128);
       const uint64_t ds_mn = umma_sdesc_lbo(ds_s, kQAtom, 1024, kLayoutSw128);
+      const uint64_t q_hi_mn = umma_desc_adv(q_mn, 2 * kQAtom);
       int g = 0, nrow = 0;
       int pend = -1, pend_flags = 0, pend_row = 0;
       bool ok = true;
@@ -333,13 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (flags & 2) umma_commit(&tail->dq_full);
         umma_commit(&tail->kv_empty[st]);   // K / V of this stage are no longer read
         // dV^T, dK^T lo, dK^T hi of this chunk, each once the drain warps have emptied
-        // that region of the previous chunk (so draining and MMAs overlap by region)
-#pragma unroll 1
+        // that region of the previous chunk (so draining and MMAs overlap by region);
+        // unrolled, so that each MMA is a constant advance of a base descriptor
+#pragma unroll
         for (int reg = 0; reg < 3; ++reg) {
           if (!mbar_wait(&tail->dkv_free[reg], (pg & 1) ^ 1u, abort_flag, p.err, kErrB)) return false;
           tc_fence_after();
           const uint32_t dcol = reg == 0 ? kColDV : (reg == 1 ? kColDKlo : kColDKhi);
-          const uint64_t ad = reg == 0 ? do_mn : (reg == 1 ? q_mn : umma_desc_adv(q_mn, 2 * kQAtom));
+          const uint64_t ad = reg == 0 ? do_mn : (reg == 1 ? q_mn : q_hi_mn);
           const uint64_t bd = reg == 0 ? p_mn : ds_mn;
 #pragma unroll
           for (int kk = 0; kk < 128 / 16; ++kk)
