@@ -431,10 +431,12 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   TopkSmem* sm = reinterpret_cast<TopkSmem*>(smem_raw);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkSmem));
 
-  // long rows first
-  const long long row = static_cast<long long>(gridDim.x) - 1 - blockIdx.x;
-  const int b = static_cast<int>(row / p.S);
-  const int t = static_cast<int>(row - static_cast<long long>(b) * p.S);
+  // rows t < stage_cap of every batch row, long rows first
+  const int sc = min(p.S, p.stage_cap);
+  const long long i = static_cast<long long>(gridDim.x) - 1 - blockIdx.x;
+  const int b = static_cast<int>(i / sc);
+  const int t = static_cast<int>(i - static_cast<long long>(b) * sc);
+  const long long row = static_cast<long long>(b) * p.S + t;
   const int len = t + 1;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -463,8 +465,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     return;
   }
 
-  const bool staged = len <= p.stage_cap;
-  if (staged) {
+  {
     // ---- rows held in shared memory: 11 + 11 + 10 bit radix select, the first
     // histogram built while the row is loaded
     // raw scores -> shared memory with 16-byte asynchronous copies (rows are
@@ -619,68 +620,462 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
     if (p.count && tid == 0) p.count[row] = p.k;
     return;
   }
-  // ---- rows longer than the shared stage: 4 x 8-bit passes re-reading the row (L2)
-  auto key_at = [&](int s) -> uint32_t {
-    const bool v = !seg_row || seg_row[s] == seg_t;
-    return v ? order_key(__ldg(srow + s)) : 0u;
-  };
+  // rows longer than the shared stage are handled by topk_long_kernel
+}
 
-  // ---- radix select: the k-th largest key, 8 bits at a time
-  uint32_t prefix = 0u, mask = 0u;
-  int need = p.k;
-#pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    if (tid < 256) sm->hist[tid] = 0u;
-    __syncthreads();
-    for (int s0 = 0; s0 < len; s0 += kThreads) {
-      const int s = s0 + tid;
-      const uint32_t key = s < len ? key_at(s) : 0u;
-      const bool part = key != 0u && (key & mask) == prefix;
-      const uint32_t bin = (key >> shift) & 255u;
-      const uint32_t peers = __match_any_sync(0xffffffffu, part ? bin : 0xFFFFFFFFu);
-      if (part && lane == __ffs(peers) - 1) atomicAdd(&sm->hist[bin], __popc(peers));
+// ------------------------------------------------------------------ long rows
+// Rows longer than the shared stage (t >= kStageMax): one persistent CTA of 1024
+// threads per SM, so that the rows in flight (152 x at most 512 KB at S = 131072)
+// stay in L2 between passes. Every pass reads the row from global memory in
+// 16-byte groups of four keys: the first from DRAM (first-level histogram), the
+// following ones from L2. The selection is the same as for staged rows: a window
+// histogram, then either a candidate list with bitmaps (rows of at most
+// kLongWords * 32 keys and at most kLongCand keys in the threshold bin) or further
+// levels over the row with an ordered sweep.
+namespace lr {
+
+constexpr int NT = 1024;
+constexpr int NW = NT / 32;
+constexpr int kLongWords = 4096;   // bitmap words: rows up to 131072 keys
+constexpr int kLongCand = 4096;
+constexpr int kWpt = kLongWords / NT;   // bitmap words per thread
+
+struct Smem {
+  uint32_t hist[2048];
+  uint32_t gtw[kLongWords];   // keys above T
+  uint32_t eqw[kLongWords];   // keys equal to T
+  uint32_t cand[kLongCand];   // threshold-bin key indices; then the output row
+  int warp_tot[NW];
+  int wgt[NW], weq[NW];
+  int bcast[4];
+  uint32_t ubc[8];
+};
+
+// keys of one row read from global memory (tail of the last group and other
+// documents' keys read as 0; the row stride is a multiple of 4 and at least S)
+struct RowKeys {
+  const float* srow;
+  const int32_t* seg_row;
+  int len, seg_t;
+  __device__ __forceinline__ uint4 load4(int c) const {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(srow) + c);
+    const float fv[4] = {f.x, f.y, f.z, f.w};
+    uint32_t kq[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int si = 4 * c + e;
+      const bool v = si < len && (!seg_row || __ldg(seg_row + si) == seg_t);
+      kq[e] = v ? order_key(fv[e]) : 0u;
     }
-    __syncthreads();
-    // bins in descending order: thread i owns bin 255 - i
-    int cnt = tid < 256 ? static_cast<int>(sm->hist[255 - tid]) : 0;
-    int tot;
-    const int incl = block_scan(cnt, tot, sm);
-    if (tid < 256 && incl >= need && incl - cnt < need) {
-      sm->bcast[0] = 255 - tid;      // selected bin
-      sm->bcast[1] = incl - cnt;     // keys in higher bins
-      sm->bcast[2] = cnt;
-    }
-    __syncthreads();
-    const uint32_t sel = static_cast<uint32_t>(sm->bcast[0]);
-    need -= sm->bcast[1];
-    const int in_bin = sm->bcast[2];
-    __syncthreads();
-    prefix |= sel << shift;
-    mask |= 255u << shift;
-    if (in_bin == need) break;   // every key with this prefix is taken
+    return make_uint4(kq[0], kq[1], kq[2], kq[3]);
   }
+  __device__ __forceinline__ uint32_t key(int s) const { return order_key(__ldg(srow + s)); }
+};
 
-  // ---- ordered selection: key > T, or key == T among the first `need` of them
+__device__ __forceinline__ int block_scan(int v, int& total, Smem* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm->warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NW ? sm->warp_tot[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < NW) sm->warp_tot[lane] = w;
+  }
+  __syncthreads();
+  const int before = warp > 0 ? sm->warp_tot[warp - 1] : 0;
+  total = sm->warp_tot[NW - 1];
+  __syncthreads();
+  return x + before;
+}
+
+// the bin of the need-th largest key among nb bins (nb <= 2 * NT), keys above it
+// and in it
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, Smem* sm,
+                                         int& bin, int& above, int& in_bin) {
+  const int per = nb > NT ? nb / NT : 1;
+  const int tid = threadIdx.x;
+  int c[2];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int j = tid * per + i;
+    c[i] = i < per && j < nb ? static_cast<int>(hist[nb - 1 - j]) : 0;
+    sum += c[i];
+  }
+  int tot;
+  const int incl = block_scan(sum, tot, sm);
+  int run = incl - sum;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    if (i < per && run < need && run + c[i] >= need) {
+      sm->bcast[0] = nb - 1 - (tid * per + i);
+      sm->bcast[1] = run;
+      sm->bcast[2] = c[i];
+    }
+    run += c[i];
+  }
+  __syncthreads();
+  bin = sm->bcast[0];
+  above = sm->bcast[1];
+  in_bin = sm->bcast[2];
+  __syncthreads();
+}
+
+// digits below a known prefix over the keys visit(fn) presents (see the staged
+// path: histogram levels, early stop when the bin holds exactly the keys needed
+// or every key in play has the same lower bits)
+template <class Visit>
+__device__ __forceinline__ void resolve_levels(Visit visit, uint32_t* hist, int nlev,
+                                               const int* shifts, const int* nbins,
+                                               uint32_t& prefix, uint32_t& mask, int& need,
+                                               int in_bin, Smem* sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+#pragma unroll 1
+  for (int lvl = 0; lvl < nlev && in_bin != need; ++lvl) {
+    const int shift = shifts[lvl], nb = nbins[lvl];
+    const uint32_t low = (1u << shift) - 1u;
+    for (int i = tid; i < nb; i += NT) hist[i] = 0u;
+    if (tid == 0) {
+      sm->ubc[4] = 0u;
+      sm->ubc[5] = 0xFFFFFFFFu;
+    }
+    __syncthreads();
+    uint32_t lo_or = 0u, lo_and = 0xFFFFFFFFu;
+    const uint32_t pf = prefix, mk = mask;
+    visit([&](uint32_t key) {
+      if (key != 0u && (key & mk) == pf) {
+        atomicAdd(&hist[(key >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+        lo_or |= key & low;
+        lo_and &= key & low;
+      }
+    });
+    lo_or = __reduce_or_sync(0xffffffffu, lo_or);
+    lo_and = __reduce_and_sync(0xffffffffu, lo_and);
+    if (lane == 0) {
+      atomicOr(&sm->ubc[4], lo_or);
+      atomicAnd(&sm->ubc[5], lo_and);
+    }
+    __syncthreads();
+    const uint32_t all_or = sm->ubc[4], all_and = sm->ubc[5];
+    int bin, above;
+    find_bin(hist, nb, need, sm, bin, above, in_bin);
+    prefix |= static_cast<uint32_t>(bin) << shift;
+    mask |= static_cast<uint32_t>(nb - 1) << shift;
+    need -= above;
+    if (all_or == (all_and & low)) {
+      prefix |= all_or;
+      mask |= low;
+      break;
+    }
+  }
+}
+
+// ordered selection over the row by per-warp segments (count sweep, write sweep)
+__device__ __forceinline__ void select_sweep(const RowKeys& rk, int nq, uint32_t mask,
+                                             uint32_t prefix, int need, int32_t* out, int kmax,
+                                             Smem* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int segq = ((nq + NW * 32 - 1) / (NW * 32)) * 32;
+  const int q_begin = warp * segq, q_end = min(nq, q_begin + segq);
+  int cg = 0, ce = 0;
+  for (int q = q_begin + lane; q < q_end; q += 32) {
+    const uint4 kv = rk.load4(q);
+    const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t km = kk[e] & mask;
+      cg += (kk[e] != 0u && km > prefix);
+      ce += (kk[e] != 0u && km == prefix);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    cg += __shfl_xor_sync(0xffffffffu, cg, o);
+    ce += __shfl_xor_sync(0xffffffffu, ce, o);
+  }
+  if (lane == 0) {
+    sm->wgt[warp] = cg;
+    sm->weq[warp] = ce;
+  }
+  __syncthreads();
   int gt_base = 0, eq_base = 0;
-  for (int s0 = 0; s0 < len; s0 += kThreads) {
-    const int s = s0 + tid;
-    const uint32_t key = s < len ? key_at(s) : 0u;
-    const uint32_t km = key & mask;
-    const int gt = key != 0u && km > prefix;
-    const int eq = key != 0u && km == prefix;
-    int tot;
-    const int incl = block_scan(gt | (eq << 16), tot, sm);
-    const int gt_before = gt_base + ((incl & 0xFFFF) - gt);
-    const int eq_before = eq_base + ((incl >> 16) - eq);
-    const int pos = gt_before + min(eq_before, need);
-    if ((gt || (eq && eq_before < need)) && pos < p.k) out[pos] = s;
+  for (int w = 0; w < warp; ++w) {
+    gt_base += sm->wgt[w];
+    eq_base += sm->weq[w];
+  }
+  for (int q0 = q_begin; q0 < q_end; q0 += 32) {
+    const int q = q0 + lane;
+    uint32_t kk[4] = {0u, 0u, 0u, 0u};
+    if (q < q_end) {
+      const uint4 kv = rk.load4(q);
+      kk[0] = kv.x;
+      kk[1] = kv.y;
+      kk[2] = kv.z;
+      kk[3] = kv.w;
+    }
+    int fg[4], fe[4], ng = 0, ne = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t km = kk[e] & mask;
+      fg[e] = kk[e] != 0u && km > prefix;
+      fe[e] = kk[e] != 0u && km == prefix;
+      ng += fg[e];
+      ne += fe[e];
+    }
+    const int own = ng | (ne << 16);
+    int incl = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const int excl = incl - own;
+    int g_before = gt_base + (excl & 0xFFFF), e_before = eq_base + (excl >> 16);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int pos = g_before + min(e_before, need);
+      if ((fg[e] || (fe[e] && e_before < need)) && pos < kmax) out[pos] = 4 * q + e;
+      g_before += fg[e];
+      e_before += fe[e];
+    }
+    const int tot = __shfl_sync(0xffffffffu, incl, 31);
     gt_base += tot & 0xFFFF;
     eq_base += tot >> 16;
   }
-  if (p.count && tid == 0) p.count[row] = p.k;   // n > k: exactly k selected, no padding
+  __syncthreads();   // wgt / weq are reused by the next row
 }
 
+__device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, const TopkParams& p,
+                                           int32_t* out, long long row, Smem* sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int len = t + 1;
+  const int nq = (len + 3) >> 2;
+  if (n <= p.k) {
+    // every valid key is selected: an ordered sweep taking every valid key as
+    // "equal" (mask 0) with need = k >= n
+    select_sweep(rk, nq, 0u, 0u, p.k, out, p.k, sm);
+    for (int j = n + tid; j < p.k; j += NT) out[j] = -1;
+    if (p.count && tid == 0) p.count[row] = n;
+    return;
+  }
+  for (int i = tid; i < 2048; i += NT) sm->hist[i] = 0u;
+  if (tid < 4) sm->ubc[tid] = 0u;
+  // the first group of each thread (the row's first 4096 keys) places the window
+  const uint4 first = tid < nq ? rk.load4(tid) : make_uint4(0u, 0u, 0u, 0u);
+  {
+    const uint32_t fk[4] = {first.x, first.y, first.z, first.w};
+    uint32_t ap = 0u, an = 0u, cp = 0u, cv = 0u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (fk[e] == 0u) continue;
+      const bool pos = fk[e] >= 0x80000000u;
+      if (pos) ap = max(ap, fk[e] & 0x7FFFFFFFu);
+      else an = max(an, ~fk[e] & 0x7FFFFFFFu);
+      cp += pos;
+      ++cv;
+    }
+    ap = __reduce_max_sync(0xffffffffu, ap);
+    an = __reduce_max_sync(0xffffffffu, an);
+    cp = __reduce_add_sync(0xffffffffu, cp);
+    cv = __reduce_add_sync(0xffffffffu, cv);
+    __syncthreads();
+    if (lane == 0) {
+      atomicMax(&sm->ubc[0], ap);
+      atomicMax(&sm->ubc[1], an);
+      atomicAdd(&sm->ubc[2], cp);
+      atomicAdd(&sm->ubc[3], cv);
+    }
+    __syncthreads();
+  }
+  const uint32_t npos = sm->ubc[2], nval = sm->ubc[3];
+  const bool positive_side = nval == 0u || static_cast<unsigned long long>(npos) * n >=
+                                               static_cast<unsigned long long>(nval) * p.k;
+  const LevelOne w1 = LevelOne::make(sm->ubc[0], sm->ubc[1], positive_side);
+  // first-level histogram over the row (four groups in flight per thread)
+  {
+    int c = tid;
+    if (c < nq) {
+      const uint32_t kk[4] = {first.x, first.y, first.z, first.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (kk[e] != 0u) atomicAdd(&sm->hist[w1.bucket(kk[e])], 1u);
+    }
+    for (c += NT; c < nq; c += 4 * NT) {
+      uint4 kv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        kv[u] = c + u * NT < nq ? rk.load4(c + u * NT) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (kk[e] != 0u) atomicAdd(&sm->hist[w1.bucket(kk[e])], 1u);
+      }
+    }
+  }
+  __syncthreads();
+  int bin, above, in_bin;
+  find_bin(sm->hist, 2048, p.k, sm, bin, above, in_bin);
+  const bool inner = w1.interior(static_cast<uint32_t>(bin));
+  const int nwords = (4 * nq + 31) >> 5;
+  if (nwords <= kLongWords && in_bin <= kLongCand) {
+    // ---- candidate list and bitmaps
+    uint32_t mask = inner ? 0xFFFE0000u : 0u;
+    uint32_t prefix = inner ? w1.prefix(static_cast<uint32_t>(bin)) : 0u;
+    int need = p.k - above;
+    for (int i = tid; i < nwords; i += NT) sm->eqw[i] = 0u;
+    if (tid == 0) sm->ubc[6] = 0u;
+    __syncthreads();
+    const uint32_t lt = (1u << lane) - 1u;
+    const uint32_t b1 = static_cast<uint32_t>(bin);
+    for (int c0 = 0; c0 < nq; c0 += NT) {
+      const int c = c0 + tid;
+      const uint4 kv = c < nq ? rk.load4(c) : make_uint4(0u, 0u, 0u, 0u);
+      const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
+      uint32_t nib = 0u;
+      bool cd[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t bk = w1.bucket(kk[e]);
+        nib |= static_cast<uint32_t>(kk[e] != 0u && bk > b1) << e;
+        cd[e] = kk[e] != 0u && bk == b1;
+      }
+      uint32_t wv = nib << (4 * (lane & 7));
+      wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+      wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+      wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
+      if ((lane & 7) == 0 && c < nq) sm->gtw[c >> 3] = wv;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t bal = __ballot_sync(0xffffffffu, cd[e]);
+        if (bal) {
+          const int leader = __ffs(bal) - 1;
+          uint32_t base = 0u;
+          if (lane == leader) base = atomicAdd(&sm->ubc[6], static_cast<uint32_t>(__popc(bal)));
+          base = __shfl_sync(0xffffffffu, base, leader);
+          const uint32_t r = base + __popc(bal & lt);
+          if (cd[e] && r < kLongCand) sm->cand[r] = static_cast<uint32_t>(4 * c + e);
+        }
+      }
+    }
+    __syncthreads();
+    const int ncand = min(in_bin, kLongCand);
+    const int shifts_in[2] = {8, 0}, nbins_in[2] = {512, 256};
+    const int shifts_out[4] = {24, 16, 8, 0}, nbins_out[4] = {256, 256, 256, 256};
+    resolve_levels(
+        [&](auto fn) {
+          for (int j = tid; j < ncand; j += NT) fn(rk.key(static_cast<int>(sm->cand[j])));
+        },
+        sm->hist, inner ? 2 : 4, inner ? shifts_in : shifts_out, inner ? nbins_in : nbins_out,
+        prefix, mask, need, in_bin, sm);
+    for (int j = tid; j < ncand; j += NT) {
+      const int sj = static_cast<int>(sm->cand[j]);
+      const uint32_t km = rk.key(sj) & mask;
+      if (km > prefix) atomicOr(&sm->gtw[sj >> 5], 1u << (sj & 31));
+      else if (km == prefix) atomicOr(&sm->eqw[sj >> 5], 1u << (sj & 31));
+    }
+    __syncthreads();
+    uint32_t g[kWpt], q[kWpt];
+    int own = 0;
+#pragma unroll
+    for (int i = 0; i < kWpt; ++i) {
+      const int wd = tid * kWpt + i;
+      g[i] = wd < nwords ? sm->gtw[wd] : 0u;
+      q[i] = wd < nwords ? sm->eqw[wd] : 0u;
+      own += __popc(g[i]) | (__popc(q[i]) << 16);
+    }
+    int tot;
+    const int excl = block_scan(own, tot, sm) - own;   // every word is read before this returns
+    int gb = excl & 0xFFFF, eb = excl >> 16;
+    int32_t* ost = p.k <= kLongCand ? reinterpret_cast<int32_t*>(sm->cand) : out;
+#pragma unroll
+    for (int i = 0; i < kWpt; ++i) {
+      uint32_t bits = g[i] | q[i];
+      while (bits) {
+        const int bb = __ffs(bits) - 1;
+        bits &= bits - 1u;
+        const int sj = (tid * kWpt + i) * 32 + bb;
+        if ((g[i] >> bb) & 1u) {
+          const int pos = gb + min(eb, need);
+          if (pos < p.k) ost[pos] = sj;
+          ++gb;
+        } else {
+          if (eb < need && gb + eb < p.k) ost[gb + eb] = sj;
+          ++eb;
+        }
+      }
+    }
+    __syncthreads();
+    if (ost != out)
+      for (int j = tid; j < p.k; j += NT) out[j] = ost[j];
+  } else {
+    // ---- further levels over the whole row
+    uint32_t prefix = 0u, mask = 0u;
+    int need = p.k;
+    if (inner) {
+      prefix = w1.prefix(static_cast<uint32_t>(bin));
+      mask = 0xFFFE0000u;
+      need = p.k - above;
+    } else {
+      in_bin = -1;
+    }
+    const int shifts_in[2] = {6, 0}, nbins_in[2] = {2048, 64};
+    const int shifts_out[3] = {21, 10, 0}, nbins_out[3] = {2048, 2048, 1024};
+    resolve_levels(
+        [&](auto fn) {
+          for (int c = tid; c < nq; c += NT) {
+            const uint4 kv = rk.load4(c);
+            fn(kv.x);
+            fn(kv.y);
+            fn(kv.z);
+            fn(kv.w);
+          }
+        },
+        sm->hist, inner ? 2 : 3, inner ? shifts_in : shifts_out, inner ? nbins_in : nbins_out,
+        prefix, mask, need, in_bin, sm);
+    select_sweep(rk, nq, mask, prefix, need, out, p.k, sm);
+  }
+  if (p.count && tid == 0) p.count[row] = p.k;
+  __syncthreads();   // the shared state is reused by the next row
+}
+
+}  // namespace lr
+
+// rows t >= t0 of every batch row; persistent, longest rows first
+__global__ void __launch_bounds__(lr::NT, 1) topk_long_kernel(const TopkParams p, int t0) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  lr::Smem* sm = reinterpret_cast<lr::Smem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const long long nlong = static_cast<long long>(p.B) * (p.S - t0);
+  for (long long j = blockIdx.x; j < nlong; j += gridDim.x) {
+    const int b = static_cast<int>(j % p.B);
+    const int t = p.S - 1 - static_cast<int>(j / p.B);
+    const long long row = static_cast<long long>(b) * p.S + t;
+    const int32_t* seg_row = p.seg ? p.seg + static_cast<long long>(b) * p.S : nullptr;
+    const int seg_t = seg_row ? seg_row[t] : 0;
+    int n = t + 1;
+    if (seg_row) {
+      int c = 0;
+      for (int s = tid; s <= t; s += lr::NT) c += (seg_row[s] == seg_t);
+      int tot;
+      lr::block_scan(c, tot, sm);
+      n = tot;
+    }
+    const lr::RowKeys rk{p.scores + row * p.ld, seg_row, t + 1, seg_t};
+    lr::select_row(rk, t, n, p, p.idx + row * p.k, row, sm);
+  }
+}
 }  // namespace
 
 int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
@@ -702,8 +1097,25 @@ int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int 
     return DSA_ERR_CUDA;
   const long long rows = static_cast<long long>(B) * S;
   if (rows > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
-  topk_kernel<<<static_cast<unsigned>(rows), kThreads, smem, stream>>>(p);
-  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+  // rows t < stage_cap: one CTA per row with the row staged in shared memory
+  const long long nshort = static_cast<long long>(B) * (S < p.stage_cap ? S : p.stage_cap);
+  topk_kernel<<<static_cast<unsigned>(nshort), kThreads, smem, stream>>>(p);
+  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  if (S > kStageMax) {
+    // longer rows: persistent CTAs, one per SM
+    const size_t lsmem = sizeof(lr::Smem);
+    if (cudaFuncSetAttribute(topk_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(lsmem)) != cudaSuccess)
+      return DSA_ERR_CUDA;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long nlong = static_cast<long long>(B) * (S - kStageMax);
+    const int grid = static_cast<int>(nlong < sms ? nlong : sms);
+    topk_long_kernel<<<grid, lr::NT, lsmem, stream>>>(p, kStageMax);
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
 }
 
 }  // namespace dsa
