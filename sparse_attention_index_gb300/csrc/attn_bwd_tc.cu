@@ -1,4 +1,4 @@
-// Sparse attention backward on the 5th-generation tensor cores, for 64 < H <= 128 heads.
+// Sparse attention backward on the 5th-generation tensor cores, for H <= 128 heads.
 //
 // ("Support Ring Attention with DeepSeek DSA Sparse Indexer", Backward Flow
 // step 6: dQ = dP K, dK = dP^T Q, dV = P^T dO over the same mask, "dP" read as
@@ -651,8 +651,10 @@ bool make_row_map(CUtensorMap* map, const void* base, long long rows, int cols) 
 
 }  // namespace
 
+// Any H <= 128: P and dS of the TMEM lanes >= H are zero, so those lanes add
+// nothing to dK / dV, and their dQ is not stored.
 bool attn_bwd_tc_supported(int H, int Dqk, int Dv, float scale) {
-  return H > 64 && H <= 128 && scale > 0.f && Dqk == 192 && Dv == 128;
+  return H >= 1 && H <= 128 && scale > 0.f && Dqk == 192 && Dv == 128;
 }
 
 // ws must be zeroed by the caller's stream before this runs.

@@ -1,4 +1,4 @@
-// Sparse attention forward on the 5th-generation tensor cores, for 64 < H <= 128 heads.
+// Sparse attention forward on the 5th-generation tensor cores, for H <= 128 heads.
 //
 // ("Support Ring Attention with DeepSeek DSA Sparse Indexer", Forward Flow
 // step 5: logits = where(mask, Q K^T * scale, -inf), softmax, P V; the mask is
@@ -611,8 +611,12 @@ int launch_tc(const AttnParams& p, cudaStream_t stream) {
 
 }  // namespace
 
+// Any H <= 128: the heads fill TMEM lanes 0..H-1 and the lanes above compute on
+// the following query rows' Q (or zeros) and store nothing. With few heads most of
+// the M = 128 tile is idle, but the kernel is bound by its per-chunk pipeline and
+// the K/V gather rather than by the tensor cores.
 bool attn_fwd_tc_supported(int H, int Dqk, int Dv, float scale) {
-  return H > 64 && H <= 128 && scale > 0.f &&
+  return H >= 1 && H <= 128 && scale > 0.f &&
          ((Dqk == 192 && Dv == 128) || (Dqk == 128 && Dv == 128));
 }
 

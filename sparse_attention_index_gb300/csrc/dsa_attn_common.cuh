@@ -38,11 +38,12 @@ inline AttnParams make_attn_params(const void* Q, const void* K, const void* V,
   return p;
 }
 
-// tcgen05 forward (attn_fwd_tc.cu): used for 64 < H <= 128 heads and a positive scale.
+// tcgen05 forward (attn_fwd_tc.cu): used for H <= 128 heads, (Dqk, Dv) = (192, 128) or
+// (128, 128), and a positive scale.
 bool attn_fwd_tc_supported(int H, int Dqk, int Dv, float scale);
 int launch_attn_fwd_tc(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream);
 
-// tcgen05 backward (attn_bwd_tc.cu): 64 < H <= 128, Dqk = 192, Dv = 128, positive scale.
+// tcgen05 backward (attn_bwd_tc.cu): H <= 128, Dqk = 192, Dv = 128, positive scale.
 // The fp32 dK/dV accumulator p.ws must already be zero on the stream.
 bool attn_bwd_tc_supported(int H, int Dqk, int Dv, float scale);
 int launch_attn_bwd_tc(const AttnParams& p, cudaStream_t stream);
