@@ -91,6 +91,16 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
+// acc += a * b on both halves with one paired fp32 FMA (each half rounds as fmaf)
+__device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
+  unsigned long long d, x, y;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(acc.x), "f"(acc.y));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(x), "l"(y));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(d));
+}
+
 template <int HI>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -271,33 +281,49 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int seg_s = (p.seg != nullptr && s < p.S) ? __ldg(p.seg + b * p.S + s) : 0;
         const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                 static_cast<uint32_t>(as * kColsPerTile + half * 128);
-#pragma unroll 1
-        for (int cq = 0; cq < 4; cq += CPQ) {
-          float acc[QPC];
+        // this warp's 128 columns as two pairs of 32-column chunks, two TMEM loads
+        // per wait; heads h, h+1 of a query go through one paired fp32 FMA (even and
+        // odd heads summed apart, then added)
+        float2 acc2[QPC];
 #pragma unroll
-          for (int i = 0; i < QPC; ++i) acc[i] = 0.f;
+        for (int i = 0; i < QPC; ++i) acc2[i] = make_float2(0.f, 0.f);
+        auto chunk = [&](int ch, const uint32_t (&v)[32]) {
+          const float* wrow = w_item + half * 128 + ch * 32;
 #pragma unroll
-          for (int c2 = 0; c2 < CPQ; ++c2) {
-            const int ch = cq + c2;   // chunk within this half
-            uint32_t v[32];
-            tmem_ld_x32(t_base + ch * 32, v);
-            tmem_ld_wait();
-            const float* wrow = w_item + half * 128 + ch * 32;
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj)
-              acc[jj / (32 / QPC)] =
-                  fmaf(wrow[jj], fmaxf(__uint_as_float(v[jj]), 0.f), acc[jj / (32 / QPC)]);
-          }
-#pragma unroll
-          for (int i = 0; i < QPC; ++i) {
-            const int qi = (half * 128 + cq * 32) / HI + i;
-            const int t = t0 + qi;
-            if (t < p.S && s <= t) {
-              float val = acc[i];
-              if (p.seg != nullptr && seg_s != __ldg(p.seg + b * p.S + t)) val = -INFINITY;
-              p.scores[(static_cast<long long>(b) * p.S + t) * p.ld + s] = val;
+          for (int jj = 0; jj < 32; jj += 2) {
+            const float2 w2 = *reinterpret_cast<const float2*>(wrow + jj);
+            const float2 r2 = make_float2(fmaxf(__uint_as_float(v[jj]), 0.f),
+                                          fmaxf(__uint_as_float(v[jj + 1]), 0.f));
+            if (HI >= 2) {
+              ffma2(acc2[jj / (32 / QPC)], r2, w2);
+            } else {   // one head per query: every column is its own query
+              acc2[jj].x = fmaf(w2.x, r2.x, acc2[jj].x);
+              acc2[jj + 1].x = fmaf(w2.y, r2.y, acc2[jj + 1].x);
             }
           }
+          if ((ch + 1) % CPQ == 0) {
+            const int cq = ch + 1 - CPQ;
+#pragma unroll
+            for (int i = 0; i < QPC; ++i) {
+              const int qi = (half * 128 + cq * 32) / HI + i;
+              const int t = t0 + qi;
+              if (t < p.S && s <= t) {
+                float val = acc2[i].x + acc2[i].y;
+                if (p.seg != nullptr && seg_s != __ldg(p.seg + b * p.S + t)) val = -INFINITY;
+                p.scores[(static_cast<long long>(b) * p.S + t) * p.ld + s] = val;
+              }
+              acc2[i] = make_float2(0.f, 0.f);
+            }
+          }
+        };
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+          uint32_t va[32], vb[32];
+          tmem_ld_x32(t_base + (2 * pr) * 32, va);
+          tmem_ld_x32(t_base + (2 * pr + 1) * 32, vb);
+          tmem_ld_wait();
+          chunk(2 * pr, va);
+          chunk(2 * pr + 1, vb);
         }
         tc_fence_before();
         __syncwarp();
