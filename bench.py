@@ -285,42 +285,26 @@ def run_ours(args, wl, rank, world, local_rank):
             h_in["seg"] = pin(ind["seg"])
         if wl.backward:
             h_in["dO"] = pin(att["dO"])
-        d_in = {n: torch.empty(t.shape, dtype=t.dtype, device=device) for n, t in h_in.items()}
-        outs = {"idx": idx, "count": count, "O": O, "lse": lse}
-        if wl.backward:
-            outs.update({"dQ": dQ, "dK": dK, "dV": dV})
-        h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in outs.items()}
+        # the public host-to-host API: copies in, the four stages and copies out on
+        # three streams, overlapped (sparse_attention_index_gb300.HostPipeline)
+        pipe = dsa.HostPipeline(B, S, wl.Hi, wl.Di, wl.H, wl.Dqk, wl.Dv, k, wl.scale,
+                                backward=wl.backward, segments=seg is not None, device=device)
+        h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in pipe.out.items()}
         h2d = sum(t.numel() * t.element_size() for t in h_in.values())
         d2h = sum(t.numel() * t.element_size() for t in h_out.values())
-        bf = lambda n: d_in[n].view(torch.bfloat16)  # noqa: E731
-
-        def e2e_step():
-            for n, t in h_in.items():
-                d_in[n].copy_(t, non_blocking=True)
-            sg = d_in.get("seg")
-            dsa.dsa_index_scores(bf("q_idx"), bf("k_idx"), d_in["w"], sg, scores=scores,
-                                 stream=stream)
-            dsa.dsa_topk(scores, k, sg, idx=idx, count=count, stream=stream)
-            dsa.dsa_sparse_attn_fwd(bf("Q"), bf("K"), bf("V"), idx, wl.scale, O=O, lse=lse,
-                                    stream=stream)
-            if wl.backward:
-                dsa.dsa_sparse_attn_bwd(bf("Q"), bf("K"), bf("V"), idx, O, lse, bf("dO"),
-                                        wl.scale, dQ=dQ, dK=dK, dV=dV, ws=ws, stream=stream)
-            for n, t in outs.items():
-                h_out[n].copy_(t, non_blocking=True)
-
-        with torch.cuda.stream(stream):
-            for _ in range(max(1, min(args.warmup, 3))):
-                e2e_step()
-            torch.cuda.synchronize(device)
-            n_e2e = max(1, min(args.steps, 10))
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            barrier(world)
-            e0.record(stream)
-            for _ in range(n_e2e):
-                e2e_step()
-            e1.record(stream)
-            torch.cuda.synchronize(device)
+        for _ in range(max(1, min(args.warmup, 3))):
+            pipe.step(h_in, h_out)
+        torch.cuda.synchronize(device)
+        n_e2e = max(1, min(args.steps, 10))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        e0.record(pipe.s_in)   # every stream's work of the timed steps follows this
+        for _ in range(n_e2e):
+            pipe.step(h_in, h_out)
+        e1.record(pipe.s_out)  # the last copy-out follows every kernel of the last step
+        torch.cuda.synchronize(device)
+        if dsa.dsa_get_last_device_error(stream) != 0:
+            raise RuntimeError("device error during the end-to-end steps")
         e2e_ms = reduce_max(e0.elapsed_time(e1) / n_e2e, world)
         e2e = {"value": world * B * S / (e2e_ms / 1e3), "unit": "tokens/s",
                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

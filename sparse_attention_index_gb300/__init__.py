@@ -215,6 +215,131 @@ def dsa_sparse_attn_bwd_noalloc(Q, K, V, idx, O, lse, dO, scale: float, dQ=None,
     return dQ, dK, dV
 
 
+class HostPipeline:
+    """Whole-layer steps from pinned host tensors to pinned host tensors.
+
+    Host->device copies, the four stages and device->host copies run on three streams
+    ordered by events, so that the copies overlap the kernels: the indexer starts as
+    soon as its own (small) inputs have landed while Q, K, V, dO are still on their way,
+    and the index lists and O leave while the backward runs. Consecutive steps overlap
+    too: a step's indexer inputs load once the previous step's indexer has read them,
+    and Q, K, V, dO are double-buffered, so the next step's load into the other set
+    runs during this step's attention. Device buffers are allocated once; every stage
+    runs in the library's kernels.
+    """
+
+    def __init__(self, B, S, Hi, Di, H, Dqk, Dv, topk, scale, backward=True, segments=False,
+                 device=None):
+        dev = torch.device("cuda") if device is None else torch.device(device)
+        self.dev, self.topk, self.scale, self.backward = dev, topk, scale, backward
+        e = lambda *shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
+        self.d = {"q_idx": e(B, S, Hi, Di), "k_idx": e(B, S, Di), "w": e(B, S, Hi, dt=torch.float32)}
+        if segments:
+            self.d["seg"] = e(B, S, dt=torch.int32)
+        self.big = []
+        for _ in range(2):
+            sets = {"Q": e(B, S, H, Dqk), "K": e(B, S, 1, Dqk), "V": e(B, S, 1, Dv)}
+            if backward:
+                sets["dO"] = e(B, S, H, Dv)
+            self.big.append(sets)
+        self.n = 0
+        ld = (S + 3) // 4 * 4
+        self.scores = e(B, S, ld, dt=torch.float32)
+        self.out = {"idx": e(B, S, topk, dt=torch.int32), "count": e(B, S, dt=torch.int32),
+                    "O": e(B, S, H, Dv), "lse": e(B, S, H, dt=torch.float32)}
+        if backward:
+            self.out.update({"dQ": e(B, S, H, Dqk), "dK": e(B, S, 1, Dqk), "dV": e(B, S, 1, Dv)})
+            self.ws = e(bwd_workspace_bytes(B, S, H, 1, Dqk, Dv), dt=torch.uint8)
+        self.s_in, self.s_c, self.s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        # events of earlier steps that the next one must respect
+        self.ev_idx_read = None
+        self.ev_attn_read = [None, None]   # per Q/K/V/dO set: its last reader is done
+        self.ev_out1 = self.ev_out2 = self.ev_out3 = None
+        self._ev = ev
+
+    def _wait(self, stream, event):
+        if event is not None:
+            stream.wait_event(event)
+
+    @staticmethod
+    def _bits(dst, src):
+        """dst viewed with src's dtype when only the element type name differs
+        (bf16 data held as 16-bit integers on the host): a bit copy."""
+        return dst if dst.dtype == src.dtype else dst.view(src.dtype)
+
+    def step(self, h_in: dict, h_out: dict):
+        """Enqueue one step: h_in / h_out hold pinned host tensors named like the
+        device buffers (inputs q_idx, k_idx, w, [seg], Q, K, V, [dO]; outputs idx,
+        count, O, lse, [dQ, dK, dV]). Returns the event that completes the step."""
+        d, o, ev = self.d, self.out, self._ev
+        par = self.n & 1
+        bd = self.big[par]
+        small = [n for n in ("q_idx", "k_idx", "w", "seg") if n in d]
+        big = [n for n in ("Q", "K", "V", "dO") if n in bd]
+        # host -> device
+        with torch.cuda.stream(self.s_in):
+            self._wait(self.s_in, self.ev_idx_read)
+            for n in small:
+                self._bits(d[n], h_in[n]).copy_(h_in[n], non_blocking=True)
+            in1 = ev()
+            in1.record(self.s_in)
+            self._wait(self.s_in, self.ev_attn_read[par])
+            for n in big:
+                self._bits(bd[n], h_in[n]).copy_(h_in[n], non_blocking=True)
+            in2 = ev()
+            in2.record(self.s_in)
+        # the layer
+        sc = self.s_c
+        sc.wait_event(in1)
+        self._wait(sc, self.ev_out1)
+        dsa_index_scores(d["q_idx"], d["k_idx"], d["w"], d.get("seg"), scores=self.scores,
+                         stream=sc)
+        idx_read = ev()
+        idx_read.record(sc)
+        dsa_topk(self.scores, self.topk, d.get("seg"), idx=o["idx"], count=o["count"], stream=sc)
+        topk_done = ev()
+        topk_done.record(sc)
+        sc.wait_event(in2)
+        self._wait(sc, self.ev_out2)
+        dsa_sparse_attn_fwd(bd["Q"], bd["K"], bd["V"], o["idx"], self.scale, O=o["O"],
+                            lse=o["lse"], stream=sc)
+        fwd_done = ev()
+        fwd_done.record(sc)
+        bwd_done = fwd_done
+        if self.backward:
+            self._wait(sc, self.ev_out3)
+            dsa_sparse_attn_bwd(bd["Q"], bd["K"], bd["V"], o["idx"], o["O"], o["lse"], bd["dO"],
+                                self.scale, dQ=o["dQ"], dK=o["dK"], dV=o["dV"], ws=self.ws,
+                                stream=sc)
+            bwd_done = ev()
+            bwd_done.record(sc)
+        # device -> host
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(topk_done)
+            for n in ("idx", "count"):
+                h_out[n].copy_(self._bits(o[n], h_out[n]), non_blocking=True)
+            out1 = ev()
+            out1.record(self.s_out)
+            self.s_out.wait_event(fwd_done)
+            for n in ("O", "lse"):
+                h_out[n].copy_(self._bits(o[n], h_out[n]), non_blocking=True)
+            out2 = ev()
+            out2.record(self.s_out)
+            out3 = out2
+            if self.backward:
+                self.s_out.wait_event(bwd_done)
+                for n in ("dQ", "dK", "dV"):
+                    h_out[n].copy_(self._bits(o[n], h_out[n]), non_blocking=True)
+                out3 = ev()
+                out3.record(self.s_out)
+        self.ev_idx_read = idx_read
+        self.ev_attn_read[par] = bwd_done
+        self.ev_out1, self.ev_out2, self.ev_out3 = out1, out2, out3
+        self.n += 1
+        return out3
+
+
 def dsa_layer(q_idx, k_idx, w, Q, K, V, topk: int, scale: float, seg=None, dO=None, stream=None):
     """The whole hot path: scores -> top-k -> sparse attention forward (and backward if dO)."""
     scores = dsa_index_scores(q_idx, k_idx, w, seg, stream=stream)

@@ -1,0 +1,48 @@
+"""HostPipeline: host -> device copies, the four stages and device -> host copies on
+three streams. Its host outputs must equal the device-resident path's results (the
+same kernels: bit-exact, except dK / dV, whose fp32 atomic order is unspecified),
+also over consecutive overlapped steps."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_util import TOL, bf16_dev, dev, host_f64, rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name", ["packed_s489", "small2b_s4096"])
+def test_host_pipeline_matches_device_path(name):
+    import sparse_attention_index_gb300 as dsa
+    wl = synth.WORKLOADS[name]
+    if name == "small2b_s4096":
+        wl = wl.replace(B=1, S=1500)
+    ind = synth.indexer_inputs(wl)
+    att = synth.attention_inputs(wl)
+    seg = None if ind["seg"] is None else dev(ind["seg"])
+    ref = dsa.dsa_layer(bf16_dev(ind["q_idx"]), bf16_dev(ind["k_idx"]), dev(ind["w"]),
+                        bf16_dev(att["Q"]), bf16_dev(att["K"]), bf16_dev(att["V"]), wl.topk,
+                        wl.scale, seg=seg, dO=bf16_dev(att["dO"]) if wl.backward else None)
+    torch.cuda.synchronize()
+
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_in = {n: pin(ind[n]) for n in ("q_idx", "k_idx", "w")}
+    h_in.update({n: pin(att[n]) for n in ("Q", "K", "V")})
+    if seg is not None:
+        h_in["seg"] = pin(ind["seg"])
+    if wl.backward:
+        h_in["dO"] = pin(att["dO"])
+    pipe = dsa.HostPipeline(wl.B, wl.S, wl.Hi, wl.Di, wl.H, wl.Dqk, wl.Dv, wl.topk, wl.scale,
+                            backward=wl.backward, segments=seg is not None)
+    h_out = {n: torch.zeros(t.shape, dtype=t.dtype).pin_memory() for n, t in pipe.out.items()}
+    for _ in range(3):   # overlapped consecutive steps over the same inputs
+        pipe.step(h_in, h_out)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_last_device_error() == 0
+
+    for n in ("idx", "count", "O", "lse") + (("dQ",) if wl.backward else ()):
+        assert torch.equal(h_out[n], ref[n].cpu()), n
+    if wl.backward:
+        for n in ("dK", "dV"):
+            assert rel_err(host_f64(h_out[n]), host_f64(ref[n])) <= TOL, n
