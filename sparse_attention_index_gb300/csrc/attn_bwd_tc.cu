@@ -23,11 +23,11 @@
 //   warps 0-3   softmax: Delta, P and dS tiles, final dQ (one head per thread)
 //   warps 4-11  drain: dK^T / dV^T from TMEM -> fp32 reductions (one dim per thread;
 //               two warps per TMEM lane quarter, one per half of the chunk's keys)
-//   warp  12    TMEM owner and single-thread UMMA issuer
-//   warps 13-15 gather: K/V rows of each chunk (cp.async, 2 stages; a stage is
+//   warp  12    TMEM owner; issues S and dP, and loads each row's Q / dO tiles (TMA)
+//               once the previous row's gradient MMAs have released them
+//   warp  13    issues dQ, dK^T and dV^T
+//   warps 14-15 gather: K/V rows of each chunk (cp.async, 2 stages; a stage is
 //               released as soon as the chunk's dQ product has read it)
-// The MMA thread also loads each row's Q / dO tiles (TMA) once the previous row's
-// MMAs have released them.
 // TMEM: dQ [0,192) S [192,256) dP [256,320) dK^T lo [320,384) hi [384,448) dV^T [448,512).
 
 #include "dsa_attn_common.cuh"
@@ -39,11 +39,13 @@ constexpr int NK = 64;               // keys per chunk
 constexpr int kStages = 2;           // K/V gather stages
 constexpr int kKeyRing = 4;          // key lists of chunks in flight
 constexpr int kDrainWarps = 8;
-constexpr int kMmaWarp = 12;
-constexpr int kGatherWarp0 = 13;
-constexpr int kGatherWarps = 3;
+constexpr int kMmaWarp = 12;        // TMEM owner, Q / dO loads, S and dP MMAs
+constexpr int kGradWarp = 13;        // dQ, dK^T, dV^T MMAs
+constexpr int kGatherWarp0 = 14;
+constexpr int kGatherWarps = 2;
 constexpr int kGatherThreads = 32 * kGatherWarps;
-constexpr int kPrefetch = 22;        // index-list entries per gather thread held ahead
+static_assert(kGatherThreads >= 64, "a gather thread per key slot");
+constexpr int kPrefetch = 32;        // index-list entries per gather thread held ahead
 constexpr int kThreads = 512;
 constexpr int kErrB = DSA_STAGE_BWD | DSA_DEVERR_TIMEOUT;
 
@@ -75,7 +77,7 @@ struct BwdTail {
   uint64_t sdp_full, sdp_free, pds_full, pds_free;
   uint64_t dkv_full[3], dkv_free[3];   // per region: dV^T, dK^T lo, dK^T hi
   uint64_t dq_full, dq_free;
-  uint64_t drain;
+  uint64_t drain, drain_g;
   uint32_t tmem_base;
   int abort_flag;
   int okb[2];
@@ -171,6 +173,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&tail->dq_full, 1);
     mbar_init(&tail->dq_free, 128);
     mbar_init(&tail->drain, 1);
+    mbar_init(&tail->drain_g, 1);
     tail->abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -246,7 +249,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
       if (lane == 0) tail->red[gw] = last;
       if (!bar_gather_ok(tail->okb, nb, abort_flag)) break;
-      const int kend = max(max(tail->red[0], tail->red[1]), tail->red[2]);
+      int kend = 0;
+#pragma unroll
+      for (int w2 = 0; w2 < kGatherWarps; ++w2) kend = max(kend, tail->red[w2]);
       const int nch = kend > 0 ? (kend + NK - 1) / NK : 1;
       int s_next = gt < NK ? load_key_b(p, irow, gt, kend, t) : -1;
       bool stop = false;
@@ -294,8 +299,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (stop) break;
     }
     cp_async_wait<0>();
-  } else if (warp == kMmaWarp) {
-    // ================================================================ UMMA issuer
+  } else if (warp == kMmaWarp || warp == kGradWarp) {
+    // ================================================================ UMMA issuers
+    // Two issuing threads keep the tensor pipe fed while either waits: warp 12 issues
+    // S / dP (and loads each row's Q / dO), warp 13 the gradients. A commit tracks the
+    // committing thread's own MMAs; the gradient MMAs of a chunk start only after its
+    // dS exists, so the S / dP MMAs that read the same K / V stage are complete then.
     if (lane == 0) {
       constexpr uint32_t id_sdp = idesc_bf16(128, NK, false, false);
       constexpr uint32_t id_dq = idesc_bf16(128, DQK, false, true);
@@ -315,7 +324,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t ds_mn = umma_sdesc_lbo(ds_s, kQAtom, 1024, kLayoutSw128);
       const uint64_t q_hi_mn = umma_desc_adv(q_mn, 2 * kQAtom);
       int g = 0, nrow = 0;
-      int pend = -1, pend_flags = 0, pend_row = 0;
       bool ok = true;
       // dQ, dK^T, dV^T of chunk pg (its P / dS tiles are ready); prow = its row ordinal
       auto issue_grads = [&](int pg, int flags, int prow) -> bool {
@@ -353,62 +361,73 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (flags & 2) umma_commit(&tail->qdo_free);
         return true;
       };
-      for (int i = blockIdx.x; ok && i < nrows; i += gridDim.x, ++nrow) {
-        bool last = false;
-        while (ok && !last) {
-          const int st = g % kStages, kr = g % kKeyRing;
-          if (!mbar_wait(&tail->kv_full[st], (g / kStages) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
-          const int flags = tail->flags[kr];
-          last = (flags & 2) != 0;
-          if (flags & 1) {
-            // a new row: finish the previous row first; once its MMAs are done its
-            // Q / dO tiles can be replaced by this row's (TMA)
-            if (pend >= 0) {
-              if (!issue_grads(pend, pend_flags, pend_row)) { ok = false; break; }
-              pend = -1;
-            }
-            if (nrow > 0 &&
-                !mbar_wait(&tail->qdo_free, (nrow - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
-            mbar_arrive_expect_tx(&tail->qdo_full, 5 * kQAtom);
-            const int qrow = tail->row[kr] * H;
-#pragma unroll
-            for (int a = 0; a < 3; ++a)
-              tma_load_2d(smem + kQOff + a * kQAtom, &tm_q, &tail->qdo_full, a * 64, qrow);
-#pragma unroll
-            for (int a = 0; a < 2; ++a)
-              tma_load_2d(smem + kDOOff + a * kQAtom, &tm_do, &tail->qdo_full, a * 64, qrow);
-            if (!mbar_wait(&tail->qdo_full, nrow & 1, abort_flag, p.err, kErrB)) {
-              drain_wait_b(&tail->qdo_full, nrow & 1, p.err);   // let the copy land before exit
+      if (warp == kGradWarp) {
+        // chunks in order, their flags from the key ring
+        for (int i = blockIdx.x; ok && i < nrows; i += gridDim.x, ++nrow) {
+          bool last = false;
+          while (ok && !last) {
+            const int kr = g % kKeyRing;
+            if (!mbar_wait(&tail->keys_full[kr], (g / kKeyRing) & 1, abort_flag, p.err, kErrB)) {
               ok = false;
               break;
             }
+            const int flags = tail->flags[kr];
+            last = (flags & 2) != 0;
+            if (!issue_grads(g, flags, nrow)) { ok = false; break; }
+            ++g;
           }
-          // S / dP of this chunk need the softmax warps to have read the previous ones
-          if (g > 0 && !mbar_wait(&tail->sdp_free, (g - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
-          fence_proxy_async_smem();
-          tc_fence_after();
-          const uint64_t kst_k = umma_desc_adv(kv_k, st * kKVStage);
-#pragma unroll
-          for (int kk = 0; kk < DQK / 16; ++kk)
-            umma_ss(tmem + kColS, umma_desc_adv(q_k, (kk >> 2) * kQAtom + (kk & 3) * 32),
-                    umma_desc_adv(kst_k, (kk >> 2) * kKVAtom + (kk & 3) * 32), id_sdp,
-                    kk > 0 ? 1u : 0u);
-#pragma unroll
-          for (int kk = 0; kk < DV / 16; ++kk)
-            umma_ss(tmem + kColDP, umma_desc_adv(do_k, (kk >> 2) * kQAtom + (kk & 3) * 32),
-                    umma_desc_adv(kst_k, (3 + (kk >> 2)) * kKVAtom + (kk & 3) * 32), id_sdp,
-                    kk > 0 ? 1u : 0u);
-          umma_commit(&tail->sdp_full);
-          if (pend >= 0 && !issue_grads(pend, pend_flags, pend_row)) { ok = false; break; }
-          pend = g;
-          pend_flags = flags;
-          pend_row = nrow;
-          ++g;
         }
+        umma_commit(&tail->drain_g);
+        drain_wait_b(&tail->drain_g, 0, p.err);
+      } else {
+        for (int i = blockIdx.x; ok && i < nrows; i += gridDim.x, ++nrow) {
+          bool last = false;
+          while (ok && !last) {
+            const int st = g % kStages, kr = g % kKeyRing;
+            if (!mbar_wait(&tail->kv_full[st], (g / kStages) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
+            const int flags = tail->flags[kr];
+            last = (flags & 2) != 0;
+            if (flags & 1) {
+              // a new row: once the previous row's gradient MMAs are done its Q / dO
+              // tiles can be replaced by this row's (TMA)
+              if (nrow > 0 &&
+                  !mbar_wait(&tail->qdo_free, (nrow - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
+              mbar_arrive_expect_tx(&tail->qdo_full, 5 * kQAtom);
+              const int qrow = tail->row[kr] * H;
+#pragma unroll
+              for (int a = 0; a < 3; ++a)
+                tma_load_2d(smem + kQOff + a * kQAtom, &tm_q, &tail->qdo_full, a * 64, qrow);
+#pragma unroll
+              for (int a = 0; a < 2; ++a)
+                tma_load_2d(smem + kDOOff + a * kQAtom, &tm_do, &tail->qdo_full, a * 64, qrow);
+              if (!mbar_wait(&tail->qdo_full, nrow & 1, abort_flag, p.err, kErrB)) {
+                drain_wait_b(&tail->qdo_full, nrow & 1, p.err);   // let the copy land before exit
+                ok = false;
+                break;
+              }
+            }
+            // S / dP of this chunk need the softmax warps to have read the previous ones
+            if (g > 0 && !mbar_wait(&tail->sdp_free, (g - 1) & 1, abort_flag, p.err, kErrB)) { ok = false; break; }
+            fence_proxy_async_smem();
+            tc_fence_after();
+            const uint64_t kst_k = umma_desc_adv(kv_k, st * kKVStage);
+#pragma unroll
+            for (int kk = 0; kk < DQK / 16; ++kk)
+              umma_ss(tmem + kColS, umma_desc_adv(q_k, (kk >> 2) * kQAtom + (kk & 3) * 32),
+                      umma_desc_adv(kst_k, (kk >> 2) * kKVAtom + (kk & 3) * 32), id_sdp,
+                      kk > 0 ? 1u : 0u);
+#pragma unroll
+            for (int kk = 0; kk < DV / 16; ++kk)
+              umma_ss(tmem + kColDP, umma_desc_adv(do_k, (kk >> 2) * kQAtom + (kk & 3) * 32),
+                      umma_desc_adv(kst_k, (3 + (kk >> 2)) * kKVAtom + (kk & 3) * 32), id_sdp,
+                      kk > 0 ? 1u : 0u);
+            umma_commit(&tail->sdp_full);
+            ++g;
+          }
+        }
+        umma_commit(&tail->drain);
+        drain_wait_b(&tail->drain, 0, p.err);
       }
-      if (ok && pend >= 0) issue_grads(pend, pend_flags, pend_row);
-      umma_commit(&tail->drain);
-      drain_wait_b(&tail->drain, 0, p.err);
     }
   } else if (warp < 4) {
     // ================================================================ softmax
