@@ -201,6 +201,10 @@ ATTN_CASES = [
     (1, 200, 96, 192, 128, 97, 2),
     (2, 150, 128, 192, 128, 300, 0),
     (1, 700, 128, 192, 128, 512, 3),
+    # few heads on the tensor-core kernels (TMEM lanes >= H idle)
+    (1, 333, 1, 192, 128, 100, 0),
+    (2, 177, 3, 192, 128, 61, 2),
+    (1, 210, 5, 128, 128, 96, 0),
 ]
 
 
