@@ -122,6 +122,17 @@ __device__ __forceinline__ int load_key_b(const AttnParams& p, const int32_t* ir
   return s > t ? -1 : s;
 }
 
+__device__ __forceinline__ void tmem_ld_x16_b(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]),
+        "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 __device__ __forceinline__ float ex2b(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -595,29 +606,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          if (!(reg == 2 && q >= 2)) {
+          if (reg == 2 && q >= 2) {
+            // dims 192-255 of the dK^T hi region do not exist
+            tc_fence_before();
+            mbar_arrive(&tail->dkv_free[reg]);
+          } else {
             const uint32_t col = reg == 0 ? kColDV : (reg == 1 ? kColDKlo : kColDKhi);
             const int dim0 = (reg == 0 ? DQK : (reg == 1 ? 0 : 128)) + q * 32;
             const float sc = reg == 0 ? 1.f : p.scale;
-#pragma unroll 1
-            for (int j0 = hk * 32; j0 < hk * 32 + 32; j0 += 16) {
-              uint32_t v[16];
-              asm volatile(
-                  "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-                  "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-                  : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]),
-                    "=r"(v[6]), "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]),
-                    "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-                  : "r"(tmem + lane_off + col + j0)
-                  : "memory");
-              tmem_ld_wait();
+            // both 16-key blocks of this warp into registers with one wait; the TMEM
+            // region is then free for the next chunk's MMA while the reductions run
+            // (the key indices too: once every region is released the ring slot may
+            // be rewritten)
+            uint32_t va[16], vb[16];
+            tmem_ld_x16_b(tmem + lane_off + col + hk * 32, va);
+            tmem_ld_x16_b(tmem + lane_off + col + hk * 32 + 16, vb);
+            int kreg[2][4];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) tile[j * kDrainPitch + lane] = __uint_as_float(v[j]) * sc;
+            for (int half = 0; half < 2; ++half)
+#pragma unroll
+              for (int i4 = 0; i4 < 4; ++i4) kreg[half][i4] = keys[hk * 32 + half * 16 + rr + 4 * i4];
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&tail->dkv_free[reg]);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j)
+                tile[j * kDrainPitch + lane] = __uint_as_float(half == 0 ? va[j] : vb[j]) * sc;
               __syncwarp();
 #pragma unroll
               for (int i4 = 0; i4 < 4; ++i4) {
                 const int r = rr + 4 * i4;
-                const int key = keys[j0 + r];
+                const int key = kreg[half][i4];
                 if (key >= 0) {
                   const float4 x = *reinterpret_cast<const float4*>(tile + r * kDrainPitch + c4);
                   atomicAdd(reinterpret_cast<float4*>(ws + static_cast<long long>(key) * (DQK + DV) +
@@ -628,8 +649,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               __syncwarp();
             }
           }
-          tc_fence_before();
-          mbar_arrive(&tail->dkv_free[reg]);
         }
         if (!ok) break;
         ++g;
