@@ -25,7 +25,9 @@
 //               two warps per TMEM lane quarter, one per half of the chunk's keys)
 //   warp  12    TMEM owner; issues S and dP, and loads each row's Q / dO tiles (TMA)
 //               once the previous row's gradient MMAs have released them
-//   warp  13    issues dQ, dK^T and dV^T
+//   warp  13    issues dQ, dK^T and dV^T (in that order: dV^T, the one product that
+//               reads P, comes last, and dS is double-buffered, so the softmax warps
+//               write the next chunk's dS while this chunk's products still run)
 //   warps 14-15 gather: K/V rows of each chunk (cp.async, 2 stages; a stage is
 //               released as soon as the chunk's dQ product has read it)
 // TMEM: dQ [0,192) S [192,256) dP [256,320) dK^T lo [320,384) hi [384,448) dV^T [448,512).
@@ -58,11 +60,12 @@ constexpr uint32_t kKVAtom = NK * 128;           // [64 key rows x 64 dims]
 constexpr uint32_t kKVStage = 5 * kKVAtom;       // K: 3 atoms, V: 2 atoms
 constexpr uint32_t kKVOff = kDOOff + 2 * kQAtom;
 constexpr uint32_t kPOff = kKVOff + kStages * kKVStage;   // [128 heads x 64 keys]
-constexpr uint32_t kDSOff = kPOff + kQAtom;
-constexpr uint32_t kDrainOff = kDSOff + kQAtom;              // per drain warp: [16 keys x 36]
-constexpr int kDrainPitch = 36;                                // floats; rows stay 16-byte aligned
+constexpr uint32_t kDSOff = kPOff + kQAtom;                  // 2 buffers (chunk parity)
+constexpr uint32_t kDrainOff = kDSOff + 2 * kQAtom;          // per drain warp: [16 keys x 32]
+constexpr int kDrainPitch = 32;   // floats; a quarter-warp reads one 128-byte row: no conflicts
 constexpr uint32_t kDrainTile = 16 * kDrainPitch * 4;
 constexpr uint32_t kTailOff = kDrainOff + kDrainWarps * kDrainTile;
+static_assert(kTailOff + 2048 <= 232448, "shared memory: tiles + tail within 227 KB");
 constexpr uint32_t kColDQ = 0, kColS = 192, kColDP = 256, kColDKlo = 320, kColDKhi = 384,
                    kColDV = 448;
 
@@ -74,7 +77,9 @@ struct BwdTail {
   uint64_t keys_full[kKeyRing];   // the key list / flags of a ring slot are written
   uint64_t kv_full[kStages], kv_empty[kStages];
   uint64_t qdo_full, qdo_free;
-  uint64_t sdp_full, sdp_free, pds_full, pds_free;
+  uint64_t sdp_full, sdp_free;
+  uint64_t ds_full[2], ds_free[2];   // dS tiles, double-buffered by chunk parity
+  uint64_t p_full, p_free;           // the P tile
   uint64_t dkv_full[3], dkv_free[3];   // per region: dV^T, dK^T lo, dK^T hi
   uint64_t dq_full, dq_free;
   uint64_t drain, drain_g;
@@ -175,8 +180,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&tail->qdo_free, 1);
     mbar_init(&tail->sdp_full, 1);
     mbar_init(&tail->sdp_free, 128);
-    mbar_init(&tail->pds_full, 128);
-    mbar_init(&tail->pds_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tail->ds_full[i], 128);
+      mbar_init(&tail->ds_free[i], 1);
+    }
+    mbar_init(&tail->p_full, 128);
+    mbar_init(&tail->p_free, 1);
     for (int r = 0; r < 3; ++r) {
       mbar_init(&tail->dkv_full[r], 1);
       mbar_init(&tail->dkv_free[r], 32 * kDrainWarps);
@@ -203,24 +212,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ gather
     const int gt = threadIdx.x - 32 * kGatherWarp0;   // 0..95; gt < NK owns key slot gt
     const int gw = warp - kGatherWarp0;
-    constexpr int PK = DQK / 8, PV = DV / 8;          // 24 + 16 pieces of 16 bytes
-    constexpr int KI = PK / 8, VI = PV / 8;           // instructions per group of 4 keys
-    int k_kig[KI], k_off[KI], v_kig[VI], v_off[VI];
-    uint32_t k_dst[KI], v_dst[VI];
-#pragma unroll
-    for (int i = 0; i < KI; ++i) {
-      const int q = i * 32 + lane, pc = q % PK;
-      k_kig[i] = q / PK;
-      k_off[i] = pc * 8;
-      k_dst[i] = (pc >> 3) * kKVAtom + ((pc & 7) << 4);
-    }
-#pragma unroll
-    for (int i = 0; i < VI; ++i) {
-      const int q = i * 32 + lane, pv = q % PV;
-      v_kig[i] = q / PV;
-      v_off[i] = pv * 8;
-      v_dst[i] = (3 + (pv >> 3)) * kKVAtom + ((pv & 7) << 4);
-    }
+    // a warp copies 4 keys at a time: 8 lanes per key, one 16-byte piece of each
+    // 64-dim atom row per lane (K: 3 atoms, V: 2), 4 x 128 contiguous bytes per instruction
+    const int sub = lane >> 3, pc = lane & 7;
     // kend of a row (one past its last slot holding a causal key) needs the whole
     // index list; for k <= kPrefetch * kGatherThreads the next row's list is loaded
     // into registers while the current row is gathered
@@ -286,24 +280,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage = smem_u32(smem + kKVOff + st * kKVStage);
         const long long rowbase = static_cast<long long>(b) * p.S;
         for (int grp = gw; grp < NK / 4; grp += kGatherWarps) {
-          const int4 kq = *reinterpret_cast<const int4*>(&tail->key[kr][grp * 4]);
-          const int keys[4] = {kq.x, kq.y, kq.z, kq.w};
+          const int slot = grp * 4 + sub;
+          const int ks = tail->key[kr][slot];
+          const long long kv = rowbase + (ks >= 0 ? ks : 0);
+          const uint32_t n = ks >= 0 ? 16u : 0u;   // 0: zero-fill an empty slot
+          const auto* ksrc = p.K + kv * DQK + pc * 8;
+          const auto* vsrc = p.V + kv * DV + pc * 8;
+          const uint32_t dst = stage + slot * 128 + ((pc ^ (slot & 7)) << 4);
 #pragma unroll
-          for (int ii = 0; ii < KI; ++ii) {
-            const int kig = k_kig[ii], key = grp * 4 + kig;
-            const int ks = kig == 0 ? keys[0] : (kig == 1 ? keys[1] : (kig == 2 ? keys[2] : keys[3]));
-            const long long kv = rowbase + (ks >= 0 ? ks : 0);
-            cp_async_16(stage + key * 128 + (k_dst[ii] ^ ((key & 7) << 4)),
-                        p.K + kv * DQK + k_off[ii], ks >= 0 ? 16u : 0u);
-          }
+          for (int a = 0; a < 3; ++a) cp_async_16(dst + a * kKVAtom, ksrc + a * 64, n);
 #pragma unroll
-          for (int ii = 0; ii < VI; ++ii) {
-            const int kig = v_kig[ii], key = grp * 4 + kig;
-            const int ks = kig == 0 ? keys[0] : (kig == 1 ? keys[1] : (kig == 2 ? keys[2] : keys[3]));
-            const long long kv = rowbase + (ks >= 0 ? ks : 0);
-            cp_async_16(stage + key * 128 + (v_dst[ii] ^ ((key & 7) << 4)),
-                        p.V + kv * DV + v_off[ii], ks >= 0 ? 16u : 0u);
-          }
+          for (int a = 0; a < 2; ++a) cp_async_16(dst + (3 + a) * kKVAtom, vsrc + a * 64, n);
         }
         cp_async_mbar_arrive(&tail->kv_full[st]);
       }
@@ -337,38 +324,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       int g = 0, nrow = 0;
       bool ok = true;
       // dQ, dK^T, dV^T of chunk pg (its P / dS tiles are ready); prow = its row ordinal
+      // The next chunk's dS goes to the other buffer, so its dQ / dK^T MMAs can follow
+      // this chunk's at once; only dV^T (the one product that reads P) waits for the
+      // single P tile.
       auto issue_grads = [&](int pg, int flags, int prow) -> bool {
-        const int st = pg % kStages;
-        if (!mbar_wait(&tail->pds_full, pg & 1, abort_flag, p.err, kErrB)) return false;
+        const int st = pg % kStages, db = pg & 1;
+        if (!mbar_wait(&tail->ds_full[db], (pg >> 1) & 1, abort_flag, p.err, kErrB)) return false;
         if ((flags & 1) &&   // first chunk of a row: the previous row's dQ was read out
             !mbar_wait(&tail->dq_free, (prow & 1) ^ 1u, abort_flag, p.err, kErrB))
           return false;
         tc_fence_after();
         const uint64_t kst_mn = umma_desc_adv(kv_mn, st * kKVStage);
+        const uint64_t dsb_k = umma_desc_adv(ds_k, db * kQAtom);
+        const uint64_t dsb_mn = umma_desc_adv(ds_mn, db * kQAtom);
 #pragma unroll
         for (int kk = 0; kk < NK / 16; ++kk) {
-          umma_ss(tmem + kColDQ, umma_desc_adv(ds_k, kk * 32), umma_desc_adv(kst_mn, kk * 2048),
+          umma_ss(tmem + kColDQ, umma_desc_adv(dsb_k, kk * 32), umma_desc_adv(kst_mn, kk * 2048),
                   id_dq, ((flags & 1) && kk == 0) ? 0u : 1u);
         }
         if (flags & 2) umma_commit(&tail->dq_full);
         umma_commit(&tail->kv_empty[st]);   // K / V of this stage are no longer read
-        // dV^T, dK^T lo, dK^T hi of this chunk, each once the drain warps have emptied
-        // that region of the previous chunk (so draining and MMAs overlap by region);
-        // unrolled, so that each MMA is a constant advance of a base descriptor
+        // dK^T lo, dK^T hi, dV^T, each once the drain warps have emptied that region of
+        // the previous chunk (so draining and MMAs overlap by region); unrolled, so that
+        // each MMA is a constant advance of a base descriptor
 #pragma unroll
-        for (int reg = 0; reg < 3; ++reg) {
+        for (int ri = 0; ri < 3; ++ri) {
+          const int reg = ri == 2 ? 0 : ri + 1;
+          if (reg == 0) {
+            umma_commit(&tail->ds_free[db]);
+            if (!mbar_wait(&tail->p_full, pg & 1, abort_flag, p.err, kErrB)) return false;
+          }
           if (!mbar_wait(&tail->dkv_free[reg], (pg & 1) ^ 1u, abort_flag, p.err, kErrB)) return false;
           tc_fence_after();
           const uint32_t dcol = reg == 0 ? kColDV : (reg == 1 ? kColDKlo : kColDKhi);
           const uint64_t ad = reg == 0 ? do_mn : (reg == 1 ? q_mn : q_hi_mn);
-          const uint64_t bd = reg == 0 ? p_mn : ds_mn;
+          const uint64_t bd = reg == 0 ? p_mn : dsb_mn;
 #pragma unroll
           for (int kk = 0; kk < 128 / 16; ++kk)
             umma_ss(tmem + dcol, umma_desc_adv(ad, kk * 2048), umma_desc_adv(bd, kk * 2048), id_dkv,
                     kk > 0 ? 1u : 0u);
           umma_commit(&tail->dkv_full[reg]);
         }
-        umma_commit(&tail->pds_free);
+        umma_commit(&tail->p_free);
         if (flags & 2) umma_commit(&tail->qdo_free);
         return true;
       };
@@ -446,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const float c2 = p.scale_log2;
     uint8_t* prow = smem + kPOff + hrow * 128;
-    uint8_t* dsrow = smem + kDSOff + hrow * 128;
+    uint8_t* dsrow0 = smem + kDSOff + hrow * 128;
     const uint32_t sw = static_cast<uint32_t>(hrow & 7);
     int g = 0, nrow = 0;
     bool ok = true;
@@ -520,8 +517,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // S / dP are in registers: the next chunk's S / dP may overwrite them
         tc_fence_before();
         mbar_arrive(&tail->sdp_free);
-        // the previous chunk's P / dS tiles have been consumed by the tensor cores
-        if (g > 0 && !__all_sync(0xffffffffu, mbar_wait(&tail->pds_free, (g - 1) & 1, abort_flag,
+        // dS into its buffer once the chunk before the previous one has consumed it
+        const int db = g & 1;
+        if (g > 1 && !__all_sync(0xffffffffu, mbar_wait(&tail->ds_free[db], ((g >> 1) - 1) & 1,
+                                                         abort_flag, p.err, kErrB))) {
+          ok = false;
+          break;
+        }
+        uint8_t* dsrow = dsrow0 + db * kQAtom;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint32_t off = (static_cast<uint32_t>(cc) ^ sw) << 4;
+          *reinterpret_cast<uint4*>(dsrow + off) =
+              make_uint4(dw[cc * 4], dw[cc * 4 + 1], dw[cc * 4 + 2], dw[cc * 4 + 3]);
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&tail->ds_full[db]);
+        // P once the previous chunk's dV^T has read it
+        if (g > 0 && !__all_sync(0xffffffffu, mbar_wait(&tail->p_free, (g - 1) & 1, abort_flag,
                                                          p.err, kErrB))) {
           ok = false;
           break;
@@ -531,12 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t off = (static_cast<uint32_t>(cc) ^ sw) << 4;
           *reinterpret_cast<uint4*>(prow + off) =
               make_uint4(pw[cc * 4], pw[cc * 4 + 1], pw[cc * 4 + 2], pw[cc * 4 + 3]);
-          *reinterpret_cast<uint4*>(dsrow + off) =
-              make_uint4(dw[cc * 4], dw[cc * 4 + 1], dw[cc * 4 + 2], dw[cc * 4 + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&tail->pds_full);
+        mbar_arrive(&tail->p_full);
         ++g;
       }
       if (!ok) break;
@@ -593,13 +605,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = row / p.S;
         float* ws = p.ws + static_cast<long long>(b) * p.S * (DQK + DV);
         const int* keys = tail->key[kr];
-        // regions in the order the tensor cores produce them: dV^T, dK^T lo, dK^T hi
-        // (dims 128-191: quarters 0-1). Each 32-dim x 16-key block goes through a
+        // regions in the order the tensor cores produce them: dK^T lo, dK^T hi (dims
+        // 128-191: quarters 0-1), dV^T. Each 32-dim x 16-key block goes through a
         // shared tile so that a thread holds 4 consecutive dims of one key: one
         // 16-byte reduction per thread, 4 key rows x 128 contiguous bytes per warp
         // instruction.
 #pragma unroll 1
-        for (int reg = 0; reg < 3; ++reg) {
+        for (int ri = 0; ri < 3; ++ri) {
+          const int reg = ri == 2 ? 0 : ri + 1;
           if (!__all_sync(0xffffffffu,
                           mbar_wait(&tail->dkv_full[reg], g & 1, abort_flag, p.err, kErrB))) {
             ok = false;
