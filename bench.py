@@ -204,13 +204,18 @@ def run_ours(args, wl, rank, world, local_rank):
     device = torch.device("cuda", local_rank)
     wl_r = wl.replace(seed=wl.seed + 1000 * rank) if rank else wl
     ind, att = make_inputs(wl_r)
+    fp8 = args.indexer_dtype == "e4m3"
 
     def to_dev(a, bf16=False):
         t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf16 else a)
         t = t.to(device)
         return t.view(torch.bfloat16) if bf16 else t
 
-    q_idx, k_idx = to_dev(ind["q_idx"], True), to_dev(ind["k_idx"], True)
+    if fp8:   # the same dyadic values as e4m3 bytes (exact)
+        ind8 = synth.indexer_inputs_fp8(wl_r, "none")
+        q_idx, k_idx = to_dev(ind8["q_idx"]), to_dev(ind8["k_idx"])
+    else:
+        q_idx, k_idx = to_dev(ind["q_idx"], True), to_dev(ind["k_idx"], True)
     w = to_dev(ind["w"])
     seg = None if ind["seg"] is None else to_dev(ind["seg"])
     Q, K, V = to_dev(att["Q"], True), to_dev(att["K"], True), to_dev(att["V"], True)
@@ -235,7 +240,10 @@ def run_ours(args, wl, rank, world, local_rank):
 
     def step(ev):
         ev[0].record(stream)
-        dsa.dsa_index_scores(q_idx, k_idx, w, seg, scores=scores, stream=stream)
+        if fp8:
+            dsa.dsa_index_scores_fp8(q_idx, k_idx, w, seg, scores=scores, stream=stream)
+        else:
+            dsa.dsa_index_scores(q_idx, k_idx, w, seg, scores=scores, stream=stream)
         ev[1].record(stream)
         dsa.dsa_topk(scores, k, seg, idx=idx, count=count, stream=stream)
         ev[2].record(stream)
@@ -277,7 +285,9 @@ def run_ours(args, wl, rank, world, local_rank):
 
     # ---- end to end through the public API: pinned host in, host out
     e2e = None
-    if not args.no_e2e:
+    if fp8 and not args.no_e2e:
+        e2e = {"unavailable": "the host pipeline takes bf16 indexer inputs"}
+    if not args.no_e2e and not fp8:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
         h_in = {"q_idx": pin(ind["q_idx"]), "k_idx": pin(ind["k_idx"]), "w": pin(ind["w"]),
                 "Q": pin(att["Q"]), "K": pin(att["K"]), "V": pin(att["V"])}
@@ -398,6 +408,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--indexer-dtype", default="bf16", choices=["bf16", "e4m3"],
+                    help="e4m3: the indexer runs on fp8 inputs (the same dyadic values)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="rows in the CPU-baseline sample (default: 24 per host core)")
@@ -443,8 +455,10 @@ def main(argv=None):
         wk = work[s]
         if "flop" in wk:
             tf = wk["flop"] / (ms / 1e3) / 1e12
-            stages_out[s] = {"ms": ms, "tflops": tf, "bound": "tensor",
-                             "frac": tf / peaks["bf16_tflops_sustained"]}
+            # e4m3 contractions: the measured bf16 peak x the nominal fp8 / bf16 ratio (2)
+            pk = peaks["bf16_tflops_sustained"] * (2.0 if s == "indexer" and
+                                                   args.indexer_dtype == "e4m3" else 1.0)
+            stages_out[s] = {"ms": ms, "tflops": tf, "bound": "tensor", "frac": tf / pk}
         else:
             gbs = wk["bytes"] / (ms / 1e3) / 1e9
             stages_out[s] = {"ms": ms, "gbs": gbs, "bound": "hbm", "frac": gbs / peaks["hbm_gbs"]}
@@ -464,7 +478,8 @@ def main(argv=None):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded: dyadic indexer inputs, N(0,1) bf16 attention inputs)",
-        "config": workload_config(wl),
+        "config": dict(workload_config(wl), **({"indexer_dtype": "e4m3"}
+                                               if args.indexer_dtype == "e4m3" else {})),
         "tflops": total_flop / (r["ms_step"] / 1e3) / 1e12,
         "stages": stages_out,
         "roofline": roof,

@@ -103,6 +103,32 @@ int dsa_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_
                      int64_t ld_scores, void* stream);
 
 /*
+ * dsa_index_scores_fp8 - the same scores from 8-bit float inputs. The pages
+ * note that the original indexer is an fp8 kernel over quantized activations
+ * ("DeepSeek3.2: Onboard sparse attention", What this PR does, item 4). With a
+ * positive scale c_s per key (k = c_s * k8):
+ *
+ *     I[b,t,s] = c_s * sum_h w[b,t,h] * max(0, sum_d q8[b,t,h,d] * k8[b,s,d])
+ *
+ * which equals the bf16 definition on the dequantized k, because ReLU is
+ * positively homogeneous. A per-(query, head) scale of q belongs in w.
+ *
+ *   q_idx    e4m3 bytes [B, S, Hi, Di] (OCP FP8 E4M3: bias 7, no infinities)
+ *   k_idx    e4m3 bytes [B, S, Di]
+ *   k_scale  fp32 [B, S], every entry > 0, or NULL (all 1)
+ *   w, seg, scores, ld_scores, stream: as for dsa_index_scores
+ *
+ * Supported: Hi in {1, 2, 4, ..., 128}, Di in {32, 64, 128}. The products run at
+ * twice the bf16 tensor rate and accumulate in fp32; the scale is one fp32
+ * multiply of the reduced score. Inputs that are small dyadic values (exact in
+ * e4m3) with power-of-two scales give exact results, identical to
+ * dsa_index_scores on the same values.
+ */
+int dsa_index_scores_fp8(const void* q_idx, const void* k_idx, const float* k_scale,
+                         const void* w, int w_dtype, const int32_t* seg, int B, int S, int Hi,
+                         int Di, float* scores, int64_t ld_scores, void* stream);
+
+/*
  * dsa_topk - per-query top-k of the index scores ("DeepSeek3.2: Onboard
  * sparse attention", Background: non-parametric top-k token selection).
  *

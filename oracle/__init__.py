@@ -13,6 +13,9 @@ Functions and the passages they follow (details in ``dsa_oracle.c``):
   for CSA" (Description: per-head products reduced over heads), causal and
   document mask from "Support Ring Attention with DeepSeek DSA Sparse Indexer"
   (Forward Flow step 3).
+* ``index_scores_fp8`` / ``e4m3_decode`` - the indexer score from OCP FP8 E4M3
+  inputs with a per-key scale of k ("DeepSeek3.2: Onboard sparse attention",
+  What this PR does item 4: the original indexer is an fp8 kernel).
 * ``topk`` - per-query top-k index selection, ties to the lower index
   ("DeepSeek3.2: Onboard sparse attention", Background).
 * ``attn_fwd`` / ``attn_bwd`` - masked softmax attention over the selected
@@ -59,6 +62,11 @@ def _load():
             vp, ci, i64, cd = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_double
             lib.oracle_index_scores.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, vp, i64, vp, ci]
             lib.oracle_index_scores.restype = None
+            lib.oracle_index_scores_fp8.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, vp, i64,
+                                                    vp, ci]
+            lib.oracle_index_scores_fp8.restype = None
+            lib.oracle_e4m3_decode.argtypes = [vp, i64, vp]
+            lib.oracle_e4m3_decode.restype = None
             lib.oracle_topk.argtypes = [vp, vp, ci, ci, vp, i64, vp, vp, ci]
             lib.oracle_topk.restype = None
             lib.oracle_attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cd, vp,
@@ -109,6 +117,36 @@ def index_scores(q_idx, k_idx, w, seg, rows=None, threads=None) -> np.ndarray:
     out = np.empty((rows.size, S), dtype=np.float64)
     _load().oracle_index_scores(qp, kp, wp, sp, B, S, Hi, Di, rows.ctypes.data, rows.size,
                                 out.ctypes.data, threads or default_threads())
+    return out
+
+
+def e4m3_decode(b) -> np.ndarray:
+    """OCP FP8 E4M3 bytes (uint8, any shape) -> their exact fp64 values (NaN for S.1111.111)."""
+    a, ap = _c(b, np.uint8)
+    out = np.empty(a.shape, dtype=np.float64)
+    _load().oracle_e4m3_decode(ap, a.size, out.ctypes.data)
+    return out
+
+
+def index_scores_fp8(q8, k8, w, seg, k_scale=None, rows=None, threads=None) -> np.ndarray:
+    """q8 [B,S,Hi,Di], k8 [B,S,Di] e4m3 bytes, w [B,S,Hi] f32, seg [B,S] or None, k_scale [B,S].
+
+    Same output convention as ``index_scores``.
+    """
+    B, S, Hi, Di = q8.shape
+    assert k8.shape == (B, S, Di) and w.shape == (B, S, Hi)
+    q, qp = _c(q8, np.uint8)
+    k, kp = _c(k8, np.uint8)
+    ww, wp = _c(w, np.float32)
+    sp = cp = None
+    if seg is not None:
+        sg, sp = _c(seg, np.int32)
+    if k_scale is not None:
+        ks, cp = _c(k_scale, np.float32)
+    rows = _rows(rows, B, S)
+    out = np.empty((rows.size, S), dtype=np.float64)
+    _load().oracle_index_scores_fp8(qp, kp, cp, wp, sp, B, S, Hi, Di, rows.ctypes.data, rows.size,
+                                    out.ctypes.data, threads or default_threads())
     return out
 
 

@@ -25,6 +25,14 @@
  *                   I[t,s] = sum_h w[t,h] * max(0, sum_d q[t,h,d] * k[s,d])
  *               for valid (t,s); -inf elsewhere in s <= t.
  *
+ *  fp8 scores   Same page, What this PR does item 4: the original indexer is an
+ *               fp8 kernel over quantized activations. Inputs are OCP FP8
+ *               E4M3 bytes (1 sign, 4 exponent bits with bias 7, 3 mantissa
+ *               bits; exponent 0 is subnormal; S.1111.111 is NaN; no
+ *               infinities), decoded exactly, and k carries a per-key scale:
+ *                   I[t,s] = sum_h w[t,h] * max(0, sum_d q[t,h,d] * c_s * k[s,d])
+ *               computed as written (the scale inside the dot product).
+ *
  *  top-k        "DeepSeek3.2: Onboard sparse attention", Background / What
  *               this PR does: per query, the top-k keys by index score give
  *               the index mask. Ties go to the lower key index; -0.0 and +0.0
@@ -60,6 +68,16 @@ static double bf16_to_double(uint16_t b) {
   float f;
   memcpy(&f, &u, 4);
   return (double)f;
+}
+
+/* OCP FP8 E4M3 byte -> its exact value */
+static double e4m3_to_double(uint8_t b) {
+  const int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0) v = ldexp((double)m / 8.0, -6);          /* subnormal: 0.m * 2^(1-7) */
+  else v = ldexp(1.0 + (double)m / 8.0, e - 7);        /* normal: 1.m * 2^(e-7) */
+  return sign ? -v : v;
 }
 
 /* causal and same-document test */
@@ -107,13 +125,26 @@ static void for_rows(row_fn fn, void* ctx, int64_t nrows, int nthreads) {
 /* ------------------------------------------------------------ index scores */
 
 typedef struct {
-  const uint16_t *q, *k;
+  const uint16_t *q, *k;     /* bf16 inputs, or NULL when q8 / k8 are given */
+  const uint8_t *q8, *k8;    /* e4m3 inputs */
+  const float* kscale;       /* per-key scale of k8, or NULL */
   const float* w;
   const int32_t* seg;
   int B, S, Hi, Di;
   const int64_t* rows;
   double* out;
 } scores_ctx;
+
+static double q_value(const scores_ctx* c, int64_t i) {
+  return c->q8 ? e4m3_to_double(c->q8[i]) : bf16_to_double(c->q[i]);
+}
+
+static double k_value(const scores_ctx* c, int64_t b, int64_t s, int d) {
+  const int64_t i = (b * c->S + s) * c->Di + d;
+  if (!c->k8) return bf16_to_double(c->k[i]);
+  const double scale = c->kscale ? (double)c->kscale[b * c->S + s] : 1.0;
+  return scale * e4m3_to_double(c->k8[i]);
+}
 
 static void scores_row(void* p, int64_t r, int tid) {
   (void)tid;
@@ -124,15 +155,14 @@ static void scores_row(void* p, int64_t r, int tid) {
   double* out = c->out + r * (int64_t)c->S;
   double* qd = (double*)malloc(sizeof(double) * (size_t)c->Hi * c->Di);
   for (int64_t i = 0; i < (int64_t)c->Hi * c->Di; ++i)
-    qd[i] = bf16_to_double(c->q[row * c->Hi * c->Di + i]);
+    qd[i] = q_value(c, row * c->Hi * c->Di + i);
   for (int64_t s = 0; s < c->S; ++s) {
     if (s > t) { out[s] = NAN; continue; }              /* undefined above the diagonal */
     if (!valid_pair(seg_row, t, s)) { out[s] = -INFINITY; continue; }
-    const uint16_t* kr = c->k + (b * c->S + s) * c->Di;
     double acc = 0.0;
     for (int h = 0; h < c->Hi; ++h) {
       double dot = 0.0;
-      for (int d = 0; d < c->Di; ++d) dot += qd[h * c->Di + d] * bf16_to_double(kr[d]);
+      for (int d = 0; d < c->Di; ++d) dot += qd[h * c->Di + d] * k_value(c, b, s, d);
       double relu = dot > 0.0 ? dot : 0.0;
       acc += (double)c->w[row * c->Hi + h] * relu;
     }
@@ -149,8 +179,23 @@ static void scores_row(void* p, int64_t r, int tid) {
 void oracle_index_scores(const uint16_t* q_idx, const uint16_t* k_idx, const float* w,
                          const int32_t* seg, int B, int S, int Hi, int Di, const int64_t* rows,
                          int64_t nrows, double* out, int nthreads) {
-  scores_ctx c = {q_idx, k_idx, w, seg, B, S, Hi, Di, rows, out};
+  scores_ctx c = {q_idx, k_idx, NULL, NULL, NULL, w, seg, B, S, Hi, Di, rows, out};
   for_rows(scores_row, &c, nrows, nthreads);
+}
+
+/*
+ * The same scores from e4m3 bytes: q8 [B,S,Hi,Di], k8 [B,S,Di], kscale [B,S] or NULL.
+ */
+void oracle_index_scores_fp8(const uint8_t* q8, const uint8_t* k8, const float* kscale,
+                             const float* w, const int32_t* seg, int B, int S, int Hi, int Di,
+                             const int64_t* rows, int64_t nrows, double* out, int nthreads) {
+  scores_ctx c = {NULL, NULL, q8, k8, kscale, w, seg, B, S, Hi, Di, rows, out};
+  for_rows(scores_row, &c, nrows, nthreads);
+}
+
+/* Decode n e4m3 bytes. */
+void oracle_e4m3_decode(const uint8_t* in, int64_t n, double* out) {
+  for (int64_t i = 0; i < n; ++i) out[i] = e4m3_to_double(in[i]);
 }
 
 /* ------------------------------------------------------------------- top-k */

@@ -9,6 +9,7 @@ fallback path.
 Entry points (same names as the C ABI):
 
 * ``dsa_index_scores`` - lightning-indexer scores I[b,t,s] (causal / document mask)
+* ``dsa_index_scores_fp8`` - the same from e4m3 q_idx / k_idx, optional per-key scale
 * ``dsa_topk``         - per-query top-k key indices, ascending, -1 padded
 * ``dsa_sparse_attn_fwd`` - attention over the selected keys -> (O, lse)
 * ``dsa_sparse_attn_bwd`` - its gradients -> (dQ, dK, dV)
@@ -32,6 +33,7 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 
 # every symbol include/dsa.h declares
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa_index_scores",
+           "dsa_index_scores_fp8",
            "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
            "dsa_sparse_attn_bwd_noalloc")
@@ -55,6 +57,7 @@ def _load() -> ctypes.CDLL:
     lib.dsa_version.restype = ci
     lib.dsa_get_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int32)]
     lib.dsa_index_scores.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, vp, i64, vp]
+    lib.dsa_index_scores_fp8.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, vp, i64, vp]
     lib.dsa_topk_workspace_size.argtypes = [ci, ci, ci]
     lib.dsa_topk_workspace_size.restype = sz
     lib.dsa_topk.argtypes = [vp, i64, vp, ci, ci, ci, vp, vp, vp, sz, vp]
@@ -65,7 +68,7 @@ def _load() -> ctypes.CDLL:
                                         vp, vp, vp, vp, sz, vp]
     lib.dsa_sparse_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci,
                                                 ci, ci, cf, vp, vp, vp, vp]
-    for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_topk",
+    for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_index_scores_fp8", "dsa_topk",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_sparse_attn_bwd_noalloc"):
         getattr(lib, name).restype = ci
     return lib
@@ -123,6 +126,38 @@ def dsa_index_scores(q_idx, k_idx, w, seg=None, scores=None, ld: int | None = No
                               B, S, Hi, Di, _dev(scores, "scores", torch.float32), ld,
                               _stream(stream))
     _check(rc, "dsa_index_scores")
+    return scores
+
+
+_FP8_DTYPES = (torch.uint8,) + ((torch.float8_e4m3fn,) if hasattr(torch, "float8_e4m3fn") else ())
+
+
+def _dev8(t: torch.Tensor, name: str) -> int:
+    if isinstance(t, torch.Tensor) and t.dtype not in _FP8_DTYPES:
+        raise TypeError(f"{name} must hold e4m3 bytes (torch.uint8 or torch.float8_e4m3fn)")
+    return _dev(t, name)
+
+
+def dsa_index_scores_fp8(q_idx, k_idx, w, seg=None, k_scale=None, scores=None,
+                         ld: int | None = None, stream=None):
+    """q_idx [B,S,Hi,Di], k_idx [B,S,Di] as e4m3 bytes; k_scale fp32 [B,S] (> 0) or None.
+
+    Returns scores fp32 [B,S,ld]: k_scale[s] * sum_h w * relu(q . k); only s <= t is written.
+    """
+    B, S, Hi, Di = q_idx.shape
+    if ld is None:
+        ld = (S + 3) // 4 * 4
+    if scores is None:
+        scores = torch.empty((B, S, ld), dtype=torch.float32, device=q_idx.device)
+    ld = scores.shape[-1]
+    w_dtype = DSA_F32 if w.dtype == torch.float32 else DSA_BF16
+    rc = lib.dsa_index_scores_fp8(_dev8(q_idx, "q_idx"), _dev8(k_idx, "k_idx"),
+                                  None if k_scale is None else _dev(k_scale, "k_scale", torch.float32),
+                                  _dev(w, "w"), w_dtype,
+                                  None if seg is None else _dev(seg, "seg", torch.int32),
+                                  B, S, Hi, Di, _dev(scores, "scores", torch.float32), ld,
+                                  _stream(stream))
+    _check(rc, "dsa_index_scores_fp8")
     return scores
 
 

@@ -93,7 +93,24 @@ int dsa_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_
   if (!dsa::indexer_dims_supported(Hi, Di)) return DSA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * S * Hi >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
   return dsa::launch_index_scores(q_idx, k_idx, w, w_dtype == DSA_BF16, seg, B, S, Hi, Di,
-                                  scores, ld_scores, as_stream(stream));
+                                  scores, ld_scores, as_stream(stream), 0, nullptr);
+}
+
+int dsa_index_scores_fp8(const void* q_idx, const void* k_idx, const float* k_scale,
+                         const void* w, int w_dtype, const int32_t* seg, int B, int S, int Hi,
+                         int Di, float* scores, int64_t ld_scores, void* stream) {
+  if (!q_idx || !k_idx || !w || !scores) return DSA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || Hi < 1 || Di < 1) return DSA_ERR_INVALID_ARG;
+  if (w_dtype != DSA_F32 && w_dtype != DSA_BF16) return DSA_ERR_INVALID_ARG;
+  if (ld_scores < S || ld_scores % 4 != 0) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(scores) ||
+      (seg && !aligned16(seg)) || (k_scale && !aligned16(k_scale)))
+    return DSA_ERR_INVALID_ARG;
+  if (Di % 16 != 0) return DSA_ERR_INVALID_ARG;
+  if (!dsa::indexer_dims_supported(Hi, Di)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * S * Hi >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_index_scores(q_idx, k_idx, w, w_dtype == DSA_BF16, seg, B, S, Hi, Di,
+                                  scores, ld_scores, as_stream(stream), 1, k_scale);
 }
 
 size_t dsa_topk_workspace_size(int B, int S, int k) {

@@ -130,6 +130,18 @@ __device__ __forceinline__ void tc_fence_after() {
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulate.
+// D[tmem] (+)= A[smem] * B[smem]^T, 8-bit float inputs (K = 32 per instruction), fp32
+// accumulate.
+__device__ __forceinline__ void umma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                        uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                           uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -245,6 +257,14 @@ __host__ __device__ constexpr uint32_t umma_idesc_bf16_mn(int M, int N, bool b_m
 }
 
 // Instruction descriptor: kind::f16, A = B = bf16, D = fp32, both K-major.
+// Instruction descriptor: kind::f8f6f4 with A = B = e4m3 (format code 0), D = fp32.
+__host__ __device__ constexpr uint32_t umma_idesc_e4m3(int M, int N) {
+  return (1u << 4)                                   // D format fp32
+         | (0u << 7)                                 // A format e4m3
+         | (0u << 10)                                // B format e4m3
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
 __host__ __device__ constexpr uint32_t umma_idesc_bf16(int M, int N) {
   return (1u << 4)                                   // D format fp32
          | (1u << 7)                                 // A format bf16

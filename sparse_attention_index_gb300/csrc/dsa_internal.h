@@ -11,9 +11,11 @@ namespace dsa {
 // Device address of the library's error word on the current device.
 int* device_error_word();
 
+// fp8 != 0: q_idx / k_idx are e4m3 bytes and k_scale (fp32 [B, S] or nullptr) scales
+// each key's score.
 int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
                         const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
-                        int64_t ld, cudaStream_t stream);
+                        int64_t ld, cudaStream_t stream, int fp8, const float* k_scale);
 
 int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
                 int32_t* idx, int32_t* count, cudaStream_t stream);

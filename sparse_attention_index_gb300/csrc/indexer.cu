@@ -20,6 +20,14 @@
 //   warps 2-9  epilogue: tcgen05.ld, ReLU, x w, sum over heads, mask, store
 // Work item = (batch, query group); key blocks 0..t_max/128 of the item stream
 // through the ring. Items are handed out heaviest first, strided over CTAs.
+//
+// FP8 form ("DeepSeek3.2: Onboard sparse attention", unit tests: the original
+// indexer runs as an fp8 kernel on quantized activations): q_idx / k_idx as e4m3
+// bytes on kind::f8f6f4 (K = 32 per instruction, twice the bf16 rate), and an
+// optional positive scale per key. Since ReLU is positively homogeneous,
+//   sum_h w * max(0, q . (c_s k)) = c_s * sum_h w * max(0, q . k),
+// so the scale multiplies the reduced score; a per-(query, head) scale of q
+// belongs in w.
 
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -44,13 +52,15 @@ struct IndexerParams {
   int G;          // queries per tile (256 / Hi)
   int n_groups;   // ceil(S / G)
   int n_items;    // B * n_groups
-  int atom;       // K elements per swizzled row segment (16, 32 or 64)
+  int atom;       // K elements per swizzled row segment
   int n_atoms;    // Di / atom
+  uint32_t atom_bytes;   // bytes of one swizzled row segment (32, 64 or 128)
   uint32_t layout;
   uint32_t q_slot_bytes, k_stage_bytes;
   const void* w;
   int w_bf16;
   const int32_t* seg;
+  const float* k_scale;   // fp8 form: per-key scale [B, S] or nullptr
   float* scores;
   long long ld;
   int* err;
@@ -101,7 +111,7 @@ __device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(d));
 }
 
-template <int HI>
+template <int HI, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const IndexerParams p) {
@@ -151,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = tail->tmem_base;
 
-  const uint32_t atom_bytes = static_cast<uint32_t>(p.atom) * 2u;
+  const uint32_t atom_bytes = p.atom_bytes;
   const uint32_t sbo = 8u * atom_bytes;
 
   if (warp == 0) {
@@ -215,8 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ UMMA issuer
     if (lane == 0) {
-      const uint32_t idesc = umma_idesc_bf16(kKeysPerTile, kColsPerTile);
-      const int ksteps_per_atom = p.atom / 16;
+      const uint32_t idesc = F8 ? umma_idesc_e4m3(kKeysPerTile, kColsPerTile)
+                                : umma_idesc_bf16(kKeysPerTile, kColsPerTile);
+      const int ksteps_per_atom = static_cast<int>(atom_bytes / 32u);   // 32 bytes of K each
       int ks = 0, qs = 0, as = 0;
       uint32_t k_par = 0, q_par = 0, a_par = 1;
       bool ok = true;
@@ -238,7 +249,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                   umma_sdesc(k_addr + a * kKeysPerTile * atom_bytes + off, sbo, p.layout);
               const uint64_t bdesc =
                   umma_sdesc(q_addr + a * kColsPerTile * atom_bytes + off, sbo, p.layout);
-              umma_bf16(d_tmem, adesc, bdesc, idesc, (a | kk) != 0 ? 1u : 0u);
+              if (F8)
+                umma_f8(d_tmem, adesc, bdesc, idesc, (a | kk) != 0 ? 1u : 0u);
+              else
+                umma_bf16(d_tmem, adesc, bdesc, idesc, (a | kk) != 0 ? 1u : 0u);
             }
           }
           umma_commit(&tail->k_empty[ks]);
@@ -279,6 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const int s = j * kKeysPerTile + quarter * 32 + lane;
         const int seg_s = (p.seg != nullptr && s < p.S) ? __ldg(p.seg + b * p.S + s) : 0;
+        const float ks = (F8 && p.k_scale != nullptr && s < p.S) ? __ldg(p.k_scale + b * p.S + s) : 1.f;
         const uint32_t t_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                 static_cast<uint32_t>(as * kColsPerTile + half * 128);
         // this warp's 128 columns as two pairs of 32-column chunks, two TMEM loads
@@ -290,15 +305,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto chunk = [&](int ch, const uint32_t (&v)[32]) {
           const float* wrow = w_item + half * 128 + ch * 32;
 #pragma unroll
-          for (int jj = 0; jj < 32; jj += 2) {
-            const float2 w2 = *reinterpret_cast<const float2*>(wrow + jj);
-            const float2 r2 = make_float2(fmaxf(__uint_as_float(v[jj]), 0.f),
-                                          fmaxf(__uint_as_float(v[jj + 1]), 0.f));
-            if (HI >= 2) {
-              ffma2(acc2[jj / (32 / QPC)], r2, w2);
-            } else {   // one head per query: every column is its own query
-              acc2[jj].x = fmaf(w2.x, r2.x, acc2[jj].x);
-              acc2[jj + 1].x = fmaf(w2.y, r2.y, acc2[jj + 1].x);
+          for (int j4 = 0; j4 < 32; j4 += 4) {
+            const float4 w4 = *reinterpret_cast<const float4*>(wrow + j4);   // 4 weights per load
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+              const int jj = j4 + 2 * u;
+              const float2 w2 = u == 0 ? make_float2(w4.x, w4.y) : make_float2(w4.z, w4.w);
+              const float2 r2 = make_float2(fmaxf(__uint_as_float(v[jj]), 0.f),
+                                            fmaxf(__uint_as_float(v[jj + 1]), 0.f));
+              if (HI >= 2) {
+                ffma2(acc2[jj / (32 / QPC)], r2, w2);
+              } else {   // one head per query: every column is its own query
+                acc2[jj].x = fmaf(w2.x, r2.x, acc2[jj].x);
+                acc2[jj + 1].x = fmaf(w2.y, r2.y, acc2[jj + 1].x);
+              }
             }
           }
           if ((ch + 1) % CPQ == 0) {
@@ -309,6 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int t = t0 + qi;
               if (t < p.S && s <= t) {
                 float val = acc2[i].x + acc2[i].y;
+                if (F8 && p.k_scale != nullptr) val *= ks;
                 if (p.seg != nullptr && seg_s != __ldg(p.seg + b * p.S + t)) val = -INFINITY;
                 p.scores[(static_cast<long long>(b) * p.S + t) * p.ld + s] = val;
               }
@@ -364,22 +385,23 @@ EncodeTiledFn get_encode_fn() {
 }
 
 bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int cols, int box_cols,
-              int box_rows, CUtensorMapSwizzle swz) {
+              int box_rows, CUtensorMapSwizzle swz, bool f8) {
   EncodeTiledFn fn = get_encode_fn();
   if (fn == nullptr) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * (f8 ? 1 : 2)};
   cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+  return fn(map, f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            const_cast<void*>(base), dims, strides,
             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HI>
+template <int HI, bool F8>
 int launch_hi(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& p,
               size_t smem_bytes, cudaStream_t stream) {
-  auto kern = indexer_kernel<HI>;
+  auto kern = indexer_kernel<HI, F8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes)) != cudaSuccess)
     return DSA_ERR_CUDA;
@@ -400,9 +422,25 @@ bool indexer_dims_supported(int Hi, int Di) {
   return hi_ok && di_ok;
 }
 
+template <bool F8>
+int launch_hi_any(int Hi, const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& p,
+                  size_t smem_bytes, cudaStream_t stream) {
+  switch (Hi) {
+    case 1: return launch_hi<1, F8>(mq, mk, p, smem_bytes, stream);
+    case 2: return launch_hi<2, F8>(mq, mk, p, smem_bytes, stream);
+    case 4: return launch_hi<4, F8>(mq, mk, p, smem_bytes, stream);
+    case 8: return launch_hi<8, F8>(mq, mk, p, smem_bytes, stream);
+    case 16: return launch_hi<16, F8>(mq, mk, p, smem_bytes, stream);
+    case 32: return launch_hi<32, F8>(mq, mk, p, smem_bytes, stream);
+    case 64: return launch_hi<64, F8>(mq, mk, p, smem_bytes, stream);
+    case 128: return launch_hi<128, F8>(mq, mk, p, smem_bytes, stream);
+    default: return DSA_ERR_UNSUPPORTED;
+  }
+}
+
 int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
                         const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
-                        int64_t ld, cudaStream_t stream) {
+                        int64_t ld, cudaStream_t stream, int fp8, const float* k_scale) {
   IndexerParams p;
   p.B = B;
   p.S = S;
@@ -410,47 +448,44 @@ int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int
   p.G = kColsPerTile / Hi;
   p.n_groups = (S + p.G - 1) / p.G;
   p.n_items = B * p.n_groups;
-  p.atom = Di >= 64 ? 64 : Di;
+  // one swizzled row segment holds up to 128 bytes of K: 64 bf16 or 128 e4m3 values
+  const int ebytes = fp8 ? 1 : 2;
+  p.atom = Di * ebytes >= 128 ? 128 / ebytes : Di;
   p.n_atoms = Di / p.atom;
+  p.atom_bytes = static_cast<uint32_t>(p.atom * ebytes);
   CUtensorMapSwizzle swz;
-  if (p.atom == 64) {
+  if (p.atom_bytes == 128) {
     p.layout = kLayoutSw128;
     swz = CU_TENSOR_MAP_SWIZZLE_128B;
-  } else if (p.atom == 32) {
+  } else if (p.atom_bytes == 64) {
     p.layout = kLayoutSw64;
     swz = CU_TENSOR_MAP_SWIZZLE_64B;
   } else {
     p.layout = kLayoutSw32;
     swz = CU_TENSOR_MAP_SWIZZLE_32B;
   }
-  p.q_slot_bytes = static_cast<uint32_t>(kColsPerTile) * Di * 2;
-  p.k_stage_bytes = static_cast<uint32_t>(kKeysPerTile) * Di * 2;
+  p.q_slot_bytes = static_cast<uint32_t>(kColsPerTile) * Di * ebytes;
+  p.k_stage_bytes = static_cast<uint32_t>(kKeysPerTile) * Di * ebytes;
   p.w = w;
   p.w_bf16 = w_is_bf16;
   p.seg = seg;
+  p.k_scale = k_scale;
   p.scores = scores;
   p.ld = ld;
   p.err = device_error_word();
 
   CUtensorMap mq, mk;
-  if (!make_map(&mq, q_idx, static_cast<uint64_t>(B) * S * Hi, Di, p.atom, kColsPerTile, swz))
+  if (!make_map(&mq, q_idx, static_cast<uint64_t>(B) * S * Hi, Di, p.atom, kColsPerTile, swz,
+                fp8 != 0))
     return DSA_ERR_CUDA;
-  if (!make_map(&mk, k_idx, static_cast<uint64_t>(B) * S, Di, p.atom, kKeysPerTile, swz))
+  if (!make_map(&mk, k_idx, static_cast<uint64_t>(B) * S, Di, p.atom, kKeysPerTile, swz,
+                fp8 != 0))
     return DSA_ERR_CUDA;
 
   const size_t smem_bytes = kQSlots * static_cast<size_t>(p.q_slot_bytes) +
                             kKStages * static_cast<size_t>(p.k_stage_bytes) + sizeof(SmemTail);
-  switch (Hi) {
-    case 1: return launch_hi<1>(mq, mk, p, smem_bytes, stream);
-    case 2: return launch_hi<2>(mq, mk, p, smem_bytes, stream);
-    case 4: return launch_hi<4>(mq, mk, p, smem_bytes, stream);
-    case 8: return launch_hi<8>(mq, mk, p, smem_bytes, stream);
-    case 16: return launch_hi<16>(mq, mk, p, smem_bytes, stream);
-    case 32: return launch_hi<32>(mq, mk, p, smem_bytes, stream);
-    case 64: return launch_hi<64>(mq, mk, p, smem_bytes, stream);
-    case 128: return launch_hi<128>(mq, mk, p, smem_bytes, stream);
-    default: return DSA_ERR_UNSUPPORTED;
-  }
+  return fp8 ? launch_hi_any<true>(Hi, mq, mk, p, smem_bytes, stream)
+             : launch_hi_any<false>(Hi, mq, mk, p, smem_bytes, stream);
 }
 
 }  // namespace dsa

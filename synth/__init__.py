@@ -32,6 +32,7 @@ _lib = None
 STREAM_Q_IDX, STREAM_K_IDX, STREAM_W = 1, 2, 3
 STREAM_Q, STREAM_K, STREAM_V, STREAM_DO = 4, 5, 6, 7
 STREAM_SEG = 8
+STREAM_K_SCALE = 9
 STREAM_ROWS = 64
 
 
@@ -113,6 +114,25 @@ def words(seed: int, stream: int, n: int) -> np.ndarray:
 def bf16_to_f32(u16: np.ndarray) -> np.ndarray:
     """Widen bf16 bit patterns to float32 (exact)."""
     return (u16.astype(np.uint32) << 16).view(np.float32)
+
+
+def e4m3_bytes(values) -> np.ndarray:
+    """Exact OCP FP8 E4M3 bytes (uint8) of values that e4m3 represents exactly.
+
+    The conversion is torch's float8_e4m3fn cast; values that would round raise.
+    """
+    import torch
+    v = torch.from_numpy(np.ascontiguousarray(values, dtype=np.float32))
+    f8 = v.to(torch.float8_e4m3fn)
+    if not torch.equal(f8.to(torch.float32), v):
+        raise ValueError("value not exactly representable in e4m3")
+    return f8.view(torch.uint8).numpy().copy()
+
+
+def pow2_scales(shape, seed: int, stream: int, lo: int, hi: int) -> np.ndarray:
+    """2**j with j uniform on the integers lo..hi, float32."""
+    j = dyadic_f32(shape, seed, stream, lo, hi, 0)
+    return np.exp2(j).astype(np.float32)
 
 
 @dataclass(frozen=True)
@@ -198,6 +218,21 @@ def indexer_inputs(wl: Workload) -> dict:
                                wl.w_denom_log2)
     seg = segments(wl.B, wl.S, wl.ndocs, wl.seed) if wl.ndocs else None
     return {"q_idx": q, "k_idx": k, "w": w, "seg": seg}
+
+
+def indexer_inputs_fp8(wl: Workload, k_scale: str = "none") -> dict:
+    """indexer_inputs with q_idx / k_idx as e4m3 bytes (the same dyadic values) and a per-key
+    scale: "none" (None), "pow2" (2**j, j in -2..2) or "dyadic" (i/64, i in 33..127)."""
+    inp = indexer_inputs(wl)
+    inp["q_idx"] = e4m3_bytes(bf16_to_f32(inp["q_idx"]))
+    inp["k_idx"] = e4m3_bytes(bf16_to_f32(inp["k_idx"]))
+    if k_scale == "none":
+        inp["k_scale"] = None
+    elif k_scale == "pow2":
+        inp["k_scale"] = pow2_scales((wl.B, wl.S), wl.seed, STREAM_K_SCALE, -2, 2)
+    else:
+        inp["k_scale"] = dyadic_f32((wl.B, wl.S), wl.seed, STREAM_K_SCALE, 33, 127, 6)
+    return inp
 
 
 def attention_inputs(wl: Workload, with_grad: bool | None = None) -> dict:

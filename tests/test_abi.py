@@ -20,7 +20,7 @@ def dsa():
 def _declared():
     text = open(os.path.join(ROOT, "include", "dsa.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return set(re.findall(r"\b(dsa_[a-z_]+)\s*\(", text))
+    return set(re.findall(r"\b(dsa_[a-z0-9_]+)\s*\(", text))
 
 
 def test_every_declared_symbol_is_exported(dsa):

@@ -96,6 +96,74 @@ def test_index_scores_leading_dimension():
     assert torch.all(scores[..., 150:] == 7.0)   # padding columns untouched
 
 
+# ------------------------------------------------------------ fp8 indexer
+
+FP8_CASES = [
+    # B, S, Hi, Di, ndocs, k_scale
+    (1, 128, 4, 32, 0, "none"),
+    (2, 700, 64, 128, 0, "pow2"),
+    (1, 489, 64, 128, 3, "pow2"),
+    (1, 300, 1, 64, 0, "none"),
+    (1, 300, 8, 64, 2, "pow2"),
+    (1, 333, 16, 64, 0, "none"),
+    (1, 257, 32, 32, 0, "pow2"),
+    (2, 190, 128, 128, 0, "none"),
+]
+
+
+def _fp8_inputs(B, S, Hi, Di, ndocs, k_scale, seed):
+    wl = synth.Workload("fp8", seed=seed, B=B, S=S, Hi=Hi, Di=Di, topk=4, H=1, Dqk=32, Dv=32,
+                        backward=False, ndocs=ndocs)
+    return wl, synth.indexer_inputs_fp8(wl, k_scale)
+
+
+def _run_scores_fp8(inp):
+    dsa = _dsa()
+    seg = None if inp["seg"] is None else dev(inp["seg"])
+    ks = None if inp["k_scale"] is None else dev(inp["k_scale"])
+    sc = dsa.dsa_index_scores_fp8(dev(inp["q_idx"]), dev(inp["k_idx"]), dev(inp["w"]), seg, ks)
+    assert dsa.dsa_get_last_device_error() == 0
+    return sc
+
+
+@pytest.mark.parametrize("case", FP8_CASES)
+def test_index_scores_fp8_exact(case):
+    B, S, Hi, Di, ndocs, k_scale = case
+    _, inp = _fp8_inputs(B, S, Hi, Di, ndocs, k_scale, seed=300 + S)
+    sc = host_f64(_run_scores_fp8(inp))
+    ref = oracle.index_scores_fp8(inp["q_idx"], inp["k_idx"], inp["w"], inp["seg"], inp["k_scale"])
+    _check_scores(sc, ref, np.arange(B * S), S)
+
+
+def test_index_scores_fp8_equals_bf16_kernel():
+    """The same dyadic values through both kernels: identical scores."""
+    wl, f = _fp8_inputs(1, 611, 64, 128, 2, "none", seed=41)
+    a = synth.indexer_inputs(wl)
+    sc8 = host_f64(_run_scores_fp8(f))
+    sc16 = host_f64(_run_scores(a))
+    for t in range(611):
+        assert np.array_equal(sc8[0, t, : t + 1], sc16[0, t, : t + 1]), t
+
+
+def test_index_scores_fp8_general_key_scale():
+    """Scales that are not powers of two: one fp32 rounding of the scaled (exact) sum."""
+    B, S = 1, 400
+    _, inp = _fp8_inputs(B, S, 64, 128, 0, "dyadic", seed=42)
+    sc = host_f64(_run_scores_fp8(inp))
+    ref = oracle.index_scores_fp8(inp["q_idx"], inp["k_idx"], inp["w"], None, inp["k_scale"])
+    for t in range(S):
+        g, o = sc[0, t, : t + 1], ref[t, : t + 1]
+        assert np.all(np.abs(g - o) <= 2.0 ** -24 * np.abs(o)), t
+
+
+def test_index_scores_fp8_rejects_wide_dtypes():
+    dsa = _dsa()
+    _, inp = _fp8_inputs(1, 64, 4, 32, 0, "none", seed=43)
+    with pytest.raises(TypeError):
+        dsa.dsa_index_scores_fp8(bf16_dev(synth.dyadic_bf16((1, 64, 4, 32), 1, 1, -8, 8, 3)),
+                                 dev(inp["k_idx"]), dev(inp["w"]))
+
+
 # ------------------------------------------------------------------- top-k
 
 def _check_topk(idx_gpu, cnt_gpu, scores_f64, seg, S, k, rows):

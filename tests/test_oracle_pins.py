@@ -127,6 +127,78 @@ def test_indexer_weight_homogeneity_and_linearity():
         np.testing.assert_array_equal(ab[t, : t + 1], a[t, : t + 1] + b2[t, : t + 1])
 
 
+# ------------------------------------------------------- fp8 index scores
+
+# OCP 8-bit floating point specification, E4M3 (bias 7, exponent 0 subnormal,
+# S.1111.111 NaN, no infinities): byte -> value
+E4M3_SPEC = [(0x00, 0.0), (0x80, -0.0), (0x38, 1.0), (0xB8, -1.0), (0x30, 0.5), (0x3C, 1.5),
+             (0x40, 2.0), (0x44, 3.0), (0x7E, 448.0), (0xFE, -448.0), (0x08, 2.0 ** -6),
+             (0x01, 2.0 ** -9), (0x07, 7 * 2.0 ** -9), (0x77, 240.0), (0x28, 0.25), (0x20, 0.125)]
+
+
+def test_e4m3_decode_spec_values():
+    got = oracle.e4m3_decode(np.array([b for b, _ in E4M3_SPEC], dtype=np.uint8))
+    for (b, v), g in zip(E4M3_SPEC, got):
+        assert g == v and np.signbit(g) == np.signbit(v), (hex(b), g, v)
+    nan = oracle.e4m3_decode(np.array([0x7F, 0xFF], dtype=np.uint8))
+    assert np.all(np.isnan(nan))
+
+
+def test_e4m3_decode_all_codes_match_torch():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+    assert np.array_equal(np.signbit(got[fin]), np.signbit(ref[fin]))
+
+
+def _fp8_case(B, S, Hi, Di, seed, k_scale):
+    wl = synth.Workload("fp8pin", seed=seed, B=B, S=S, Hi=Hi, Di=Di, topk=4, H=1, Dqk=32, Dv=32,
+                        backward=False)
+    return synth.indexer_inputs_fp8(wl, k_scale)
+
+
+def test_indexer_fp8_brute_force_tiny():
+    """Against a numpy einsum on torch-decoded inputs, scale applied to k."""
+    B, S, Hi, Di = 1, 9, 3, 8
+    inp = _fp8_case(B, S, Hi, Di, seed=31, k_scale="dyadic")
+    dec = lambda a: torch.from_numpy(a).view(torch.float8_e4m3fn).to(torch.float64).numpy()  # noqa: E731
+    q, k = dec(inp["q_idx"])[0], dec(inp["k_idx"])[0] * inp["k_scale"][0][:, None]
+    dots = np.einsum("thd,sd->tsh", q, k)
+    ref = np.einsum("tsh,th->ts", np.maximum(dots, 0.0), inp["w"][0].astype(np.float64))
+    got = oracle.index_scores_fp8(inp["q_idx"], inp["k_idx"], inp["w"], None, inp["k_scale"])
+    for t in range(S):
+        np.testing.assert_allclose(got[t, : t + 1], ref[t, : t + 1], rtol=1e-14, atol=0)
+        assert np.all(np.isnan(got[t, t + 1:]))
+
+
+def test_indexer_fp8_equals_bf16_definition_on_same_values():
+    wl = synth.WORKLOADS["packed_s489"]
+    rows = synth.sample_rows(wl, 12)
+    a = synth.indexer_inputs(wl)
+    f = synth.indexer_inputs_fp8(wl, "none")
+    ref = oracle.index_scores(a["q_idx"], a["k_idx"], a["w"], a["seg"], rows=rows)
+    got = oracle.index_scores_fp8(f["q_idx"], f["k_idx"], f["w"], f["seg"], rows=rows)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(got[fin], ref[fin])
+
+
+def test_indexer_fp8_positive_key_scale_is_homogeneous():
+    """relu(q . c k) = c relu(q . k) for c > 0: a power-of-two scale multiplies each score."""
+    B, S, Hi, Di = 2, 40, 4, 16
+    f = _fp8_case(B, S, Hi, Di, seed=32, k_scale="pow2")
+    plain = oracle.index_scores_fp8(f["q_idx"], f["k_idx"], f["w"], None)
+    scaled = oracle.index_scores_fp8(f["q_idx"], f["k_idx"], f["w"], None, f["k_scale"])
+    for b in range(B):
+        for t in range(S):
+            r = b * S + t
+            np.testing.assert_array_equal(scaled[r, : t + 1],
+                                          plain[r, : t + 1] * f["k_scale"][b, : t + 1])
+
+
 # ------------------------------------------------------------------- top-k
 
 def _parse_golden():
