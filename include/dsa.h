@@ -163,10 +163,29 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* seg, int B, 
  *
  * Supported: Hkv = 1 (one K/V row shared by every head), 1 <= H <= 128,
  * (Dqk, Dv) in {(32, 32), (64, 64), (128, 128), (192, 128)}.
+ *
+ * Two tensor-core kernels compute it. One gathers each query's selected K/V
+ * rows and puts the heads on the 128 lanes of a tile. The other evaluates dense
+ * 128 x 128 (query, key) tiles of one head under a bitmap of the selection and
+ * skips tiles without a selected key (see dsa_sparse_attn_fwd_dense). The call
+ * takes the one with fewer tile products for the shape. The dense-tile kernel
+ * allocates its bitmap (B*S*ceil(S/128)*16 bytes) stream-ordered on `stream`.
  */
 int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
                         int S, int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O,
                         float* lse, void* stream);
+
+/*
+ * dsa_sparse_attn_fwd_dense - the same result from the dense-tile kernel only
+ * (the pages' own design evaluates the masked logits as dense blocks with
+ * partial mask blocks: "Support Ring Attention with DeepSeek DSA Sparse
+ * Indexer", Forward Flow). Arguments as for dsa_sparse_attn_fwd. Supported:
+ * Hkv = 1, 1 <= H <= 128, (Dqk, Dv) in {(128, 128), (192, 128)}, S <= 65536, a
+ * positive scale; DSA_ERR_UNSUPPORTED otherwise.
+ */
+int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
+                              int B, int S, int H, int Hkv, int Dqk, int Dv, int k, float scale,
+                              void* O, float* lse, void* stream);
 
 /*
  * dsa_sparse_attn_bwd - gradients of the sparse attention ("Support Ring

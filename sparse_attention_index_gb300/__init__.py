@@ -12,6 +12,7 @@ Entry points (same names as the C ABI):
 * ``dsa_index_scores_fp8`` - the same from e4m3 q_idx / k_idx, optional per-key scale
 * ``dsa_topk``         - per-query top-k key indices, ascending, -1 padded
 * ``dsa_sparse_attn_fwd`` - attention over the selected keys -> (O, lse)
+* ``dsa_sparse_attn_fwd_dense`` - the same from the dense-tile kernel only
 * ``dsa_sparse_attn_bwd`` - its gradients -> (dQ, dK, dV)
 """
 from __future__ import annotations
@@ -34,7 +35,7 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 # every symbol include/dsa.h declares
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa_index_scores",
            "dsa_index_scores_fp8",
-           "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd",
+           "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
            "dsa_sparse_attn_bwd_noalloc")
 
@@ -62,6 +63,7 @@ def _load() -> ctypes.CDLL:
     lib.dsa_topk_workspace_size.restype = sz
     lib.dsa_topk.argtypes = [vp, i64, vp, ci, ci, ci, vp, vp, vp, sz, vp]
     lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp]
+    lib.dsa_sparse_attn_fwd_dense.argtypes = lib.dsa_sparse_attn_fwd.argtypes
     lib.dsa_sparse_attn_bwd_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
     lib.dsa_sparse_attn_bwd_workspace_size.restype = sz
     lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
@@ -69,7 +71,8 @@ def _load() -> ctypes.CDLL:
     lib.dsa_sparse_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci,
                                                 ci, ci, cf, vp, vp, vp, vp]
     for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_index_scores_fp8", "dsa_topk",
-                 "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_sparse_attn_bwd_noalloc"):
+                 "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense", "dsa_sparse_attn_bwd",
+                 "dsa_sparse_attn_bwd_noalloc"):
         getattr(lib, name).restype = ci
     return lib
 
@@ -177,7 +180,8 @@ def dsa_topk(scores, k: int, seg=None, S: int | None = None, idx=None, count=Non
     return idx, count
 
 
-def dsa_sparse_attn_fwd(Q, K, V, idx, scale: float, O=None, lse=None, stream=None):
+def dsa_sparse_attn_fwd(Q, K, V, idx, scale: float, O=None, lse=None, stream=None,
+                        _entry: str = "dsa_sparse_attn_fwd"):
     """Q [B,S,H,Dqk], K [B,S,Hkv,Dqk], V [B,S,Hkv,Dv] bf16, idx [B,S,k] -> (O bf16, lse fp32)."""
     B, S, H, Dqk = Q.shape
     Hkv, Dv = V.shape[2], V.shape[3]
@@ -186,13 +190,19 @@ def dsa_sparse_attn_fwd(Q, K, V, idx, scale: float, O=None, lse=None, stream=Non
         O = torch.empty((B, S, H, Dv), dtype=torch.bfloat16, device=Q.device)
     if lse is None:
         lse = torch.empty((B, S, H), dtype=torch.float32, device=Q.device)
-    rc = lib.dsa_sparse_attn_fwd(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
-                                 _dev(V, "V", torch.bfloat16), _dev(idx, "idx", torch.int32),
-                                 B, S, H, Hkv, Dqk, Dv, k, float(scale),
-                                 _dev(O, "O", torch.bfloat16), _dev(lse, "lse", torch.float32),
-                                 _stream(stream))
-    _check(rc, "dsa_sparse_attn_fwd")
+    rc = getattr(lib, _entry)(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
+                              _dev(V, "V", torch.bfloat16), _dev(idx, "idx", torch.int32),
+                              B, S, H, Hkv, Dqk, Dv, k, float(scale),
+                              _dev(O, "O", torch.bfloat16), _dev(lse, "lse", torch.float32),
+                              _stream(stream))
+    _check(rc, _entry)
     return O, lse
+
+
+def dsa_sparse_attn_fwd_dense(Q, K, V, idx, scale: float, O=None, lse=None, stream=None):
+    """dsa_sparse_attn_fwd through the dense-tile kernel only (same arguments and result)."""
+    return dsa_sparse_attn_fwd(Q, K, V, idx, scale, O=O, lse=lse, stream=stream,
+                               _entry="dsa_sparse_attn_fwd_dense")
 
 
 def bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv) -> int:

@@ -185,12 +185,17 @@ int launch_fwd_dims(const AttnParams& p, long long rows, cudaStream_t stream) {
 
 int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
                     int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, int path) {
   AttnParams p = make_attn_params(Q, K, V, idx, B, S, H, k, scale);
   p.O = static_cast<uint16_t*>(O);
   p.lse = lse;
   const long long rows = static_cast<long long>(B) * S;
   if (rows * H > 0x7fffffffLL || H > 128) return DSA_ERR_UNSUPPORTED;
+  const bool dense_ok = attn_fwd_dense_supported(B, S, H, Dqk, Dv, scale);
+  if (path == kFwdPathDense)
+    return dense_ok ? launch_attn_fwd_dense(p, Dqk, Dv, stream) : DSA_ERR_UNSUPPORTED;
+  if (dense_ok && attn_fwd_dense_preferred(B, S, H, k))
+    return launch_attn_fwd_dense(p, Dqk, Dv, stream);
   if (attn_fwd_tc_supported(H, Dqk, Dv, scale)) return launch_attn_fwd_tc(p, Dqk, Dv, stream);
   if (Dqk == 192 && Dv == 128) return launch_fwd_dims<192, 128>(p, rows, stream);
   if (Dqk == 128 && Dv == 128) return launch_fwd_dims<128, 128>(p, rows, stream);

@@ -144,6 +144,16 @@ int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32
                               as_stream(stream));
 }
 
+int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
+                        int S, int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O,
+                        float* lse, void* stream) {
+  if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
+  if (!O || !lse || !aligned16(O) || !aligned16(lse)) return DSA_ERR_INVALID_ARG;
+  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  return dsa::launch_attn_fwd(Q, K, V, idx, B, S, H, Dqk, Dv, k, scale, O, lse,
+                              as_stream(stream), dsa::kFwdPathDense);
+}
+
 size_t dsa_sparse_attn_bwd_workspace_size(int B, int S, int H, int Hkv, int Dqk, int Dv) {
   (void)H;
   if (B < 1 || S < 1 || Hkv < 1 || Dqk < 1 || Dv < 1) return 0;

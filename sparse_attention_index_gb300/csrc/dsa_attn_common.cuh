@@ -43,6 +43,12 @@ inline AttnParams make_attn_params(const void* Q, const void* K, const void* V,
 bool attn_fwd_tc_supported(int H, int Dqk, int Dv, float scale);
 int launch_attn_fwd_tc(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream);
 
+// tcgen05 forward on dense 128 x 128 tiles with a selection bitmap (attn_fwd_dense.cu):
+// one query row per TMEM lane, so few heads still fill the M = 128 tile.
+bool attn_fwd_dense_supported(int B, int S, int H, int Dqk, int Dv, float scale);
+bool attn_fwd_dense_preferred(int B, int S, int H, int k);
+int launch_attn_fwd_dense(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream);
+
 // tcgen05 backward (attn_bwd_tc.cu): H <= 128, Dqk = 192, Dv = 128, positive scale.
 // The fp32 dK/dV accumulator p.ws must already be zero on the stream.
 bool attn_bwd_tc_supported(int H, int Dqk, int Dv, float scale);

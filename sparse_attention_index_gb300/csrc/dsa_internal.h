@@ -20,9 +20,12 @@ int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int
 int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
                 int32_t* idx, int32_t* count, cudaStream_t stream);
 
+// path: kFwdPathAuto (the cheaper of the gathered-key and dense-tile kernels) or
+// kFwdPathDense (the dense-tile kernel, DSA_ERR_UNSUPPORTED where it does not apply)
+constexpr int kFwdPathAuto = 0, kFwdPathDense = 1;
 int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
                     int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
-                    cudaStream_t stream);
+                    cudaStream_t stream, int path = kFwdPathAuto);
 
 int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                     const void* O, const float* lse, const void* dO, int B, int S, int H, int Dqk,

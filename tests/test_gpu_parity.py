@@ -337,6 +337,89 @@ def test_sparse_attn_user_index_lists(H):
     assert rel_err(host_f64(dV), dV_ref) <= TOL
 
 
+# ------------------------------------------------- dense-tile forward kernel
+
+DENSE_CASES = [
+    # B, S, H, Dqk, Dv, k, ndocs
+    (1, 489, 16, 192, 128, 512, 3),
+    (2, 200, 16, 192, 128, 100, 0),
+    (1, 129, 1, 192, 128, 64, 0),      # the last query tile holds one row
+    (1, 300, 128, 192, 128, 64, 0),    # many heads (the call would pick the other kernel)
+    (1, 260, 8, 128, 128, 300, 0),     # k >= S: every causal key
+    (2, 177, 3, 192, 128, 61, 2),
+    (1, 700, 16, 192, 128, 96, 0),     # many skipped key tiles
+]
+
+
+def _fwd_check(O, lse, Q, K, V, idx, scale):
+    O_ref, lse_ref = oracle.attn_fwd(Q, K, V, idx, scale)
+    assert rel_err(host_f64(O).reshape(O_ref.shape), O_ref) <= TOL
+    lg = host_f64(lse).reshape(lse_ref.shape)
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lse_ref))
+    fin = np.isfinite(lse_ref)
+    assert rel_err(lg[fin], lse_ref[fin]) <= TOL
+
+
+@pytest.mark.parametrize("case", DENSE_CASES)
+def test_dense_fwd_matches_oracle(case):
+    dsa = _dsa()
+    B, S, H, Dqk, Dv, k, ndocs = case
+    Q, K, V, dO, idx = _attn_case(*case, seed=900 + S + H)
+    scale = 1.0 / np.sqrt(Dqk)
+    O, lse = dsa.dsa_sparse_attn_fwd_dense(bf16_dev(Q), bf16_dev(K), bf16_dev(V), dev(idx), scale)
+    assert dsa.dsa_get_last_device_error() == 0
+    _fwd_check(O, lse, Q, K, V, idx, scale)
+
+
+@pytest.mark.parametrize("H", [16, 128])
+def test_dense_fwd_user_index_lists(H):
+    """-1 anywhere, entries above the diagonal, empty rows, unsorted lists."""
+    dsa = _dsa()
+    B, S, Dqk, Dv, k = 1, 300, 192, 128, 150
+    Q, K, V, dO, _ = _attn_case(B, S, H, Dqk, Dv, 8, 0, seed=15)
+    rng = np.random.default_rng(12)
+    idx = np.full((B, S, k), -1, dtype=np.int32)
+    for t in range(S):
+        if t % 9 == 4 or 128 <= t < 140:
+            continue                                    # empty rows
+        pick = rng.choice(S, size=min(S, k), replace=False).astype(np.int32)
+        pick[rng.random(pick.size) < 0.2] = -1          # holes
+        idx[0, t] = pick                                # some above the diagonal
+    O, lse = dsa.dsa_sparse_attn_fwd_dense(bf16_dev(Q), bf16_dev(K), bf16_dev(V), dev(idx), 0.1)
+    assert dsa.dsa_get_last_device_error() == 0
+    _fwd_check(O, lse, Q, K, V, idx, 0.1)
+
+
+def test_dense_fwd_query_tile_without_keys():
+    """A whole query tile that selects nothing: O = 0, LSE = -inf, the others unaffected."""
+    dsa = _dsa()
+    B, S, H, k = 1, 300, 4, 32
+    Q, K, V, dO, idx = _attn_case(B, S, H, 192, 128, k, 0, seed=16)
+    idx = idx.copy()
+    idx[0, 128:256] = -1
+    O, lse = dsa.dsa_sparse_attn_fwd_dense(bf16_dev(Q), bf16_dev(K), bf16_dev(V), dev(idx), 0.07)
+    assert dsa.dsa_get_last_device_error() == 0
+    _fwd_check(O, lse, Q, K, V, idx, 0.07)
+    assert torch.all(O[0, 128:256] == 0)
+
+
+def test_dense_fwd_bad_index_and_unsupported():
+    dsa = _dsa()
+    B, S, H, k = 1, 140, 16, 8
+    Q, K, V, dO, idx = _attn_case(B, S, H, 192, 128, k, 0, seed=17)
+    idx = idx.copy()
+    idx[0, 100, 0] = S + 3      # out of range: skipped and reported
+    dsa.dsa_get_last_device_error()
+    O, lse = dsa.dsa_sparse_attn_fwd_dense(bf16_dev(Q), bf16_dev(K), bf16_dev(V), dev(idx), 0.125)
+    assert dsa.dsa_get_last_device_error() == (0x300 | 0x02)
+    idx_ok = idx.copy()
+    idx_ok[0, 100, 0] = -1
+    _fwd_check(O, lse, Q, K, V, idx_ok, 0.125)
+    Q6, K6, V6, _, idx6 = _attn_case(1, 64, 4, 64, 64, 8, 0, seed=18)
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_sparse_attn_fwd_dense(bf16_dev(Q6), bf16_dev(K6), bf16_dev(V6), dev(idx6), 0.125)
+
+
 def test_bad_index_is_reported_not_faulted():
     dsa = _dsa()
     B, S, H, D, k = 1, 40, 16, 64, 8
