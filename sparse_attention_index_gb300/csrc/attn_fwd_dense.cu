@@ -12,16 +12,18 @@
 //   P  = exp2(S * scale*log2e - m) where the row selects the key, else 0
 //   O += P [128 x 128] . V_tile [128 x Dv]   A = P from TMEM, B = V tile in smem (MN-major)
 // The selection is a bitmap built from the index lists (dense_mask_kernel): bit s of
-// row t is set when row t lists key s (0 <= s <= t). A key tile in which no row of
+// row t is set when row t lists key s (0 <= s <= t); a row's words past its own query
+// tile are never written nor read. A key tile in which no row of
 // the query tile selects anything is skipped; the others stream through a 2-stage
 // TMA ring. The running max is refreshed only when it grows by more than 2^8 (in
 // exp2 units), as in the gathered-key kernel.
 //
-// Persistent CTA (one per SM), 192 threads:
+// Persistent CTA (one per SM), 320 threads:
 //   warp  0     TMA producer: the active key tiles of each item, K and V (128B swizzle)
 //   warp  1     TMEM owner and single-thread UMMA issuer
-//   warps 2-5   softmax / output: Q rows -> TMEM, masked softmax, P -> TMEM, final O, LSE
-//               (TMEM lane quarters 2, 3, 0, 1)
+//   warps 2-9   softmax / output: Q rows -> TMEM, masked softmax, P -> TMEM, final O, LSE;
+//               two warps per TMEM lane quarter, each on half of a tile's keys and of
+//               the O columns
 // TMEM: [Q: Dqk/2 cols][S/P: 2 x 128 cols][O: Dv cols].
 // Items are handed out heaviest (last query tile) first, strided over CTAs.
 
@@ -32,7 +34,8 @@ namespace {
 
 constexpr int kTile = 128;            // query rows and keys per tile
 constexpr int kStages = 2;            // K/V stages == S/P buffers
-constexpr int kThreads = 192;
+constexpr int kSoftWarps = 8;
+constexpr int kThreads = 32 * (2 + kSoftWarps);
 constexpr int kSoftWarp0 = 2;
 constexpr int kErrD = DSA_STAGE_FWD | DSA_DEVERR_TIMEOUT;
 constexpr float kRescaleLog2D = 8.f;  // refresh the running max when it grows by > 2^8
@@ -62,6 +65,9 @@ struct DenseTail {
   uint64_t s_full[kStages], s_empty[kStages], p_full[kStages];
   uint64_t q_full, o_free;
   uint64_t drain;
+  float xmax[2][2][kTile];   // per tile parity and half: the half's row max
+  float xl[2][kTile];        // per half: the row sum at the end of an item
+  uint64_t pairbar[4];       // per TMEM lane quarter: the two warps' exchange barrier
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -73,26 +79,42 @@ struct DenseParams {
   int W4, QT;
 };
 
-// Selection bitmap and tile flags from the index lists (both zeroed beforehand).
-// Entries -1 and entries above the diagonal are skipped; out-of-range entries
-// set the device error word and are skipped, as in the other attention kernels.
-__global__ void dense_mask_kernel(const int32_t* idx, int B, int S, int k, int W4, int QT,
-                                  uint32_t* bits, uint8_t* any, int* err) {
-  const long long total = static_cast<long long>(B) * S * k;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += stride) {
-    const long long row = i / k;
-    const int s = __ldg(idx + i);
+// Selection bitmap and tile flags from the index lists, one row per CTA at a time:
+// the row's words are built in shared memory and written out whole up to the row's
+// own query tile (the only words the attention kernel reads); the tile flags must be
+// zero beforehand. Entries -1 and entries above the diagonal are skipped;
+// out-of-range entries set the device error word and are skipped, as in the other
+// attention kernels.
+__global__ void __launch_bounds__(256) dense_mask_kernel(const int32_t* idx, int B, int S, int k,
+                                                         int W4, int QT, uint32_t* bits,
+                                                         uint8_t* any, int* err) {
+  extern __shared__ __align__(16) uint32_t words[];   // W4 words
+  const long long rows = static_cast<long long>(B) * S;
+  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const int b = static_cast<int>(row / S);
     const int t = static_cast<int>(row - static_cast<long long>(b) * S);
-    if (s < -1 || s >= S) {
-      report_error(err, DSA_STAGE_FWD | DSA_DEVERR_BAD_INDEX);
-      continue;
+    const int nw = ((t >> 7) + 1) * 4;   // words of the key tiles up to the row's own
+    for (int w = threadIdx.x; w < nw; w += blockDim.x) words[w] = 0u;
+    __syncthreads();
+    const int32_t* ir = idx + row * k;
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+      const int s = __ldg(ir + j);
+      if (s < -1 || s >= S) {
+        report_error(err, DSA_STAGE_FWD | DSA_DEVERR_BAD_INDEX);
+        continue;
+      }
+      if (s < 0 || s > t) continue;
+      atomicOr(&words[s >> 5], 1u << (s & 31));
     }
-    if (s < 0 || s > t) continue;
-    atomicOr(bits + row * W4 + (s >> 5), 1u << (s & 31));
-    any[(static_cast<long long>(b) * QT + (t >> 7)) * QT + (s >> 7)] = 1;
+    __syncthreads();
+    uint4* dst = reinterpret_cast<uint4*>(bits + row * W4);
+    uint8_t* arow = any + (static_cast<long long>(b) * QT + (t >> 7)) * QT;
+    for (int q = threadIdx.x; q < nw / 4; q += blockDim.x) {
+      const uint4 v = reinterpret_cast<const uint4*>(words)[q];
+      dst[q] = v;
+      if ((v.x | v.y | v.z | v.w) != 0u) arow[q] = 1;   // key tile q has a selected key
+    }
+    __syncthreads();
   }
 }
 
@@ -155,11 +177,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&tail->kv_empty[i], 1);
       mbar_init(&tail->s_full[i], 1);
       mbar_init(&tail->s_empty[i], 1);
-      mbar_init(&tail->p_full[i], 128);
+      mbar_init(&tail->p_full[i], 32 * kSoftWarps);
     }
-    mbar_init(&tail->q_full, 128);
-    mbar_init(&tail->o_free, 128);
+    mbar_init(&tail->q_full, 32 * kSoftWarps);
+    mbar_init(&tail->o_free, 32 * kSoftWarps);
     mbar_init(&tail->drain, 1);
+    for (int q = 0; q < 4; ++q) mbar_init(&tail->pairbar[q], 64);
     tail->abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_k);
@@ -316,34 +339,44 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // ================================================================ softmax / output
-    const int quarter = warp & 3;                          // TMEM lane quarter
+    // warp 2 + q' + 4 * half: TMEM lane quarter (warp & 3), keys 64 * half.. of every
+    // tile, Q / O columns of that half; the two warps of a quarter share each tile's
+    // row max (and at the end the row sum) through shared memory
+    const int quarter = warp & 3;
+    const int half = (warp - kSoftWarp0) >> 2;
     const int r = quarter * 32 + lane;                     // query row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float c2 = p.scale_log2;
+    // the pair's exchanges go through an mbarrier with a bounded wait, so that a
+    // failure elsewhere ends both warps instead of leaving one in a barrier
+    uint32_t nx = 0;
+    auto pair_sync = [&]() -> bool {
+      mbar_arrive(&tail->pairbar[quarter]);
+      const bool r = mbar_wait(&tail->pairbar[quarter], nx & 1u, abort_flag, p.err, kErrD);
+      ++nx;
+      return __all_sync(0xffffffffu, r);
+    };
     int g = 0;
     bool ok = true;
 
-    // Q row (b, t = qt*128 + r, head h) -> this thread's TMEM lane as packed bf16
-    // pairs; rows past S load zeros and store nothing
+    // this half of the Q row (b, t = qt*128 + r, head h) -> TMEM as packed bf16 pairs;
+    // rows past S load zeros and store nothing
     auto load_q = [&](int i) {
       int b, h, qt;
       item_of(i, B, H, QT, b, h, qt);
       const int t = qt * kTile + r;
       const bool in = t < S;
       const long long qrow = (static_cast<long long>(b) * S + (in ? t : 0)) * H + h;
-      const uint4* src = reinterpret_cast<const uint4*>(p.Q + qrow * DQK);
+      const uint4* src = reinterpret_cast<const uint4*>(p.Q + qrow * DQK) + half * (DQK / 16);
 #pragma unroll
-      for (int a = 0; a < DQK / 64; ++a) {
-        uint32_t lo[16], hi[16];
+      for (int c = 0; c < DQK / 64; ++c) {
+        uint32_t v[16];
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
-          const uint4 x = in ? __ldg(src + a * 8 + cc) : make_uint4(0, 0, 0, 0);
-          const uint4 y = in ? __ldg(src + a * 8 + 4 + cc) : make_uint4(0, 0, 0, 0);
-          lo[cc * 4 + 0] = x.x; lo[cc * 4 + 1] = x.y; lo[cc * 4 + 2] = x.z; lo[cc * 4 + 3] = x.w;
-          hi[cc * 4 + 0] = y.x; hi[cc * 4 + 1] = y.y; hi[cc * 4 + 2] = y.z; hi[cc * 4 + 3] = y.w;
+          const uint4 x = in ? __ldg(src + c * 4 + cc) : make_uint4(0, 0, 0, 0);
+          v[cc * 4 + 0] = x.x; v[cc * 4 + 1] = x.y; v[cc * 4 + 2] = x.z; v[cc * 4 + 3] = x.w;
         }
-        tmem_st_x16(tmem + lane_off + L::kColQ + a * 32, lo);
-        tmem_st_x16(tmem + lane_off + L::kColQ + a * 32 + 16, hi);
+        tmem_st_x16(tmem + lane_off + L::kColQ + half * (DQK / 4) + c * 16, v);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -357,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = qt * kTile + r;
       const bool in = t < S;
       const uint32_t* brow = dp.bits + (static_cast<long long>(b) * S + (in ? t : 0)) * dp.W4;
-      float m = -INFINITY, l = 0.f;   // running max (raw logits) and sum
+      float m = -INFINITY, l = 0.f;   // running max (raw logits) and this half's sum
       bool last = false;
       while (!last) {
         const int sb = g % kStages;
@@ -378,27 +411,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const DenseHdr& hd = tail->hdr[sb];
         last = hd.last != 0;
         const bool first = hd.first != 0;
-        const uint4 mw = in ? __ldg(reinterpret_cast<const uint4*>(brow + hd.kt * 4))
-                            : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t mwv[4] = {mw.x, mw.y, mw.z, mw.w};
+        const uint2 mw = in ? __ldg(reinterpret_cast<const uint2*>(brow + hd.kt * 4 + half * 2))
+                            : make_uint2(0u, 0u);
         const uint32_t sbase = tmem + lane_off + L::kColS + sb * kTile;
-        // row max over the selected keys, 32 columns per TMEM load
+        uint32_t sv0[32], sv1[32];
+        tmem_ld_x32(sbase + half * 64, sv0);
+        tmem_ld_x32(sbase + half * 64 + 32, sv1);
+        tmem_ld_wait();
         float mx = -INFINITY;
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          uint32_t sv[32];
-          tmem_ld_x32(sbase + part * 32, sv);
-          tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if ((mwv[part] >> j) & 1u) mx = fmaxf(mx, __uint_as_float(sv[j]));
+        for (int j = 0; j < 32; ++j) {
+          if ((mw.x >> j) & 1u) mx = fmaxf(mx, __uint_as_float(sv0[j]));
+          if ((mw.y >> j) & 1u) mx = fmaxf(mx, __uint_as_float(sv1[j]));
         }
+        // both halves' S are in registers after this barrier, so P may overwrite them
+        tail->xmax[g & 1][half][r] = mx;
+        if (!pair_sync()) {
+          ok = false;
+          break;
+        }
+        mx = fmaxf(mx, tail->xmax[g & 1][half ^ 1][r]);
         if (first) {
           m = mx;
         } else if (__any_sync(0xffffffffu,
                               mx > m && (m == -INFINITY || (mx - m) * c2 > kRescaleLog2D))) {
           // refresh the running max of every row of the warp (a no-op where it has not
-          // grown): rescale O (every earlier PV product is done) and l
+          // grown; the other warp of the quarter decides the same): rescale this half of
+          // O (every earlier PV product is done) and l
           const int pg = g - 1;
           if (!__all_sync(0xffffffffu,
                           mbar_wait(&tail->s_empty[pg % kStages], (pg / kStages) & 1, abort_flag,
@@ -410,39 +449,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mnew = fmaxf(m, mx);
           const float f = m == -INFINITY ? 0.f : exp2f((m - mnew) * c2);
 #pragma unroll
-          for (int d0 = 0; d0 < DV; d0 += 16) {
+          for (int d0 = 0; d0 < DV / 2; d0 += 16) {
             uint32_t ov[16];
-            tmem_ld_x16d(tmem + lane_off + L::kColO + d0, ov);
+            tmem_ld_x16d(tmem + lane_off + L::kColO + half * (DV / 2) + d0, ov);
             tmem_ld_wait();
 #pragma unroll
             for (int j = 0; j < 16; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * f);
-            tmem_st_x16(tmem + lane_off + L::kColO + d0, ov);
+            tmem_st_x16(tmem + lane_off + L::kColO + half * (DV / 2) + d0, ov);
           }
           tmem_st_wait();
           l *= f;
           m = mnew;
         }
-        // P = exp2(S*c2 - m*c2) on the selected keys, 0 elsewhere -> bf16 pairs in the
-        // buffer's first 64 columns (columns 2j, 2j+1 -> column j: each part's 32 values
-        // are read before its 16 packed words are written over columns already read)
+        // P = exp2(S*c2 - m*c2) on the selected keys, 0 elsewhere -> bf16 pairs: keys
+        // 64*half.. go to columns 32*half.. of the buffer
         const float base = m == -INFINITY ? 0.f : m * c2;
         float ls = 0.f;
 #pragma unroll
-        for (int part = 0; part < 4; ++part) {
-          uint32_t sv[32];
-          tmem_ld_x32(sbase + part * 32, sv);
-          tmem_ld_wait();
+        for (int part = 0; part < 2; ++part) {
+          const uint32_t* sv = part == 0 ? sv0 : sv1;
+          const uint32_t mwp = part == 0 ? mw.x : mw.y;
           uint32_t pk[16];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             float e0 = ex2d(fmaf(__uint_as_float(sv[j]), c2, -base));
             float e1 = ex2d(fmaf(__uint_as_float(sv[j + 1]), c2, -base));
-            e0 = ((mwv[part] >> j) & 1u) ? e0 : 0.f;
-            e1 = ((mwv[part] >> (j + 1)) & 1u) ? e1 : 0.f;
+            e0 = ((mwp >> j) & 1u) ? e0 : 0.f;
+            e1 = ((mwp >> (j + 1)) & 1u) ? e1 : 0.f;
             ls += e0 + e1;
             pk[j >> 1] = pack_bf16(e0, e1);
           }
-          tmem_st_x16(sbase + part * 16, pk);
+          tmem_st_x16(sbase + half * 32 + part * 16, pk);
         }
         tmem_st_wait();
         tc_fence_before();
@@ -463,13 +500,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      tail->xl[half][r] = l;
+      if (!pair_sync()) {
+        ok = false;
+        break;
+      }
+      const float lt = l + tail->xl[half ^ 1][r];
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
       uint4* orow = reinterpret_cast<uint4*>(
-          p.O + ((static_cast<long long>(b) * S + (in ? t : 0)) * H + h) * DV);
+          p.O + ((static_cast<long long>(b) * S + (in ? t : 0)) * H + h) * DV + half * (DV / 2));
 #pragma unroll
-      for (int d0 = 0; d0 < DV; d0 += 32) {
+      for (int d0 = 0; d0 < DV / 2; d0 += 32) {
         uint32_t ov[32];
-        tmem_ld_x32(tmem + lane_off + L::kColO + d0, ov);
+        tmem_ld_x32(tmem + lane_off + L::kColO + half * (DV / 2) + d0, ov);
         tmem_ld_wait();
         if (in) {
 #pragma unroll
@@ -485,9 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       mbar_arrive(&tail->o_free);
-      if (in)
+      if (in && half == 0)
         p.lse[(static_cast<long long>(b) * S + t) * H + h] =
-            l > 0.f ? (m * c2 + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+            lt > 0.f ? (m * c2 + log2f(lt)) * 0.69314718055994530942f : -INFINITY;
     }
   }
 
@@ -543,18 +586,19 @@ int launch_dense(const AttnParams& p, cudaStream_t stream) {
   const long long krows = static_cast<long long>(p.B) * p.S;
   const size_t smem = L::kTailOff + sizeof(DenseTail);
   auto kern = attn_fwd_dense_kernel<DQK, DV>;
-  if (cudaMemsetAsync(ws, 0, any_off + any_bytes, stream) != cudaSuccess ||
+  if (cudaMemsetAsync(any, 0, any_bytes, stream) != cudaSuccess ||
       !make_tile_map(&mk, p.K, krows, DQK) || !make_tile_map(&mv, p.V, krows, DV) ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
     rc = DSA_ERR_CUDA;
   } else {
-    const long long total = static_cast<long long>(p.B) * p.S * p.k;
-    const int mgrid = static_cast<int>(total / 256 + 1 < 4096 ? total / 256 + 1 : 4096);
-    dense_mask_kernel<<<mgrid, 256, 0, stream>>>(p.idx, p.B, p.S, p.k, W4, QT, bits, any, p.err);
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long mrows = static_cast<long long>(p.B) * p.S;
+    const int mgrid = static_cast<int>(mrows < 8LL * sms ? mrows : 8LL * sms);
+    dense_mask_kernel<<<mgrid, 256, static_cast<size_t>(W4) * 4, stream>>>(p.idx, p.B, p.S, p.k,
+                                                                         W4, QT, bits, any, p.err);
     const long long items = static_cast<long long>(QT) * p.B * p.H;
     const int grid = static_cast<int>(items < sms ? items : sms);
     DenseParams dp;
