@@ -236,7 +236,11 @@ def run_ours(args, wl, rank, world, local_rank):
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device=device)
     stages = ["indexer", "topk", "attn_fwd"] + (["attn_bwd"] if wl.backward else [])
-    launches_per_step = 3 + (2 if wl.backward else 0)
+    # indexer, top-k, the forward (two launches on the dense-tile kernel: bitmap build +
+    # attention), the backward and its finalize
+    fwd_launches = 2 if dsa.dsa_sparse_attn_fwd_kernel(B, S, wl.H, 1, wl.Dqk, wl.Dv, k, wl.scale) \
+        == dsa.DSA_FWD_DENSE_TC else 1
+    launches_per_step = 2 + fwd_launches + (2 if wl.backward else 0)
 
     def step(ev):
         ev[0].record(stream)

@@ -176,6 +176,20 @@ int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32
                         float* lse, void* stream);
 
 /*
+ * dsa_sparse_attn_fwd_kernel - which kernel dsa_sparse_attn_fwd runs for a shape:
+ * DSA_FWD_GATHER_TC (the gathered-key tensor-core kernel, one launch),
+ * DSA_FWD_DENSE_TC (the dense-tile tensor-core kernel: a bitmap build and the
+ * attention, two launches) or DSA_FWD_MMA_SYNC (one launch); the negated status
+ * (-DSA_ERR_INVALID_ARG, -DSA_ERR_UNSUPPORTED) when the call would refuse the shape.
+ * Launches nothing.
+ */
+#define DSA_FWD_GATHER_TC 0
+#define DSA_FWD_DENSE_TC 1
+#define DSA_FWD_MMA_SYNC 2
+int dsa_sparse_attn_fwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, int k,
+                               float scale);
+
+/*
  * dsa_sparse_attn_fwd_dense - the same result from the dense-tile kernel only
  * (the pages' own design evaluates the masked logits as dense blocks with
  * partial mask blocks: "Support Ring Attention with DeepSeek DSA Sparse

@@ -36,6 +36,7 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa_index_scores",
            "dsa_index_scores_fp8",
            "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense",
+           "dsa_sparse_attn_fwd_kernel",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
            "dsa_sparse_attn_bwd_noalloc")
 
@@ -64,6 +65,8 @@ def _load() -> ctypes.CDLL:
     lib.dsa_topk.argtypes = [vp, i64, vp, ci, ci, ci, vp, vp, vp, sz, vp]
     lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp]
     lib.dsa_sparse_attn_fwd_dense.argtypes = lib.dsa_sparse_attn_fwd.argtypes
+    lib.dsa_sparse_attn_fwd_kernel.argtypes = [ci, ci, ci, ci, ci, ci, ci, cf]
+    lib.dsa_sparse_attn_fwd_kernel.restype = ci
     lib.dsa_sparse_attn_bwd_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
     lib.dsa_sparse_attn_bwd_workspace_size.restype = sz
     lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
@@ -197,6 +200,17 @@ def dsa_sparse_attn_fwd(Q, K, V, idx, scale: float, O=None, lse=None, stream=Non
                               _stream(stream))
     _check(rc, _entry)
     return O, lse
+
+
+DSA_FWD_GATHER_TC, DSA_FWD_DENSE_TC, DSA_FWD_MMA_SYNC = 0, 1, 2
+
+
+def dsa_sparse_attn_fwd_kernel(B, S, H, Hkv, Dqk, Dv, k, scale: float) -> int:
+    """Which kernel dsa_sparse_attn_fwd runs for this shape (DSA_FWD_*; launches nothing)."""
+    r = lib.dsa_sparse_attn_fwd_kernel(B, S, H, Hkv, Dqk, Dv, k, float(scale))
+    if r < 0:
+        raise DsaError(-r, "dsa_sparse_attn_fwd_kernel")
+    return r
 
 
 def dsa_sparse_attn_fwd_dense(Q, K, V, idx, scale: float, O=None, lse=None, stream=None):

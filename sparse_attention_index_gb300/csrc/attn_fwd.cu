@@ -191,17 +191,24 @@ int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* 
   p.lse = lse;
   const long long rows = static_cast<long long>(B) * S;
   if (rows * H > 0x7fffffffLL || H > 128) return DSA_ERR_UNSUPPORTED;
-  const bool dense_ok = attn_fwd_dense_supported(B, S, H, Dqk, Dv, scale);
   if (path == kFwdPathDense)
-    return dense_ok ? launch_attn_fwd_dense(p, Dqk, Dv, stream) : DSA_ERR_UNSUPPORTED;
-  if (dense_ok && attn_fwd_dense_preferred(B, S, H, k))
-    return launch_attn_fwd_dense(p, Dqk, Dv, stream);
-  if (attn_fwd_tc_supported(H, Dqk, Dv, scale)) return launch_attn_fwd_tc(p, Dqk, Dv, stream);
+    return attn_fwd_dense_supported(B, S, H, Dqk, Dv, scale) ? launch_attn_fwd_dense(p, Dqk, Dv, stream)
+                                                             : DSA_ERR_UNSUPPORTED;
+  const int kind = attn_fwd_kernel_kind(B, S, H, Dqk, Dv, k, scale);
+  if (kind == kFwdDenseTc) return launch_attn_fwd_dense(p, Dqk, Dv, stream);
+  if (kind == kFwdGatherTc) return launch_attn_fwd_tc(p, Dqk, Dv, stream);
   if (Dqk == 192 && Dv == 128) return launch_fwd_dims<192, 128>(p, rows, stream);
   if (Dqk == 128 && Dv == 128) return launch_fwd_dims<128, 128>(p, rows, stream);
   if (Dqk == 64 && Dv == 64) return launch_fwd_dims<64, 64>(p, rows, stream);
   if (Dqk == 32 && Dv == 32) return launch_fwd_dims<32, 32>(p, rows, stream);
   return DSA_ERR_UNSUPPORTED;
+}
+
+int attn_fwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale) {
+  if (attn_fwd_dense_supported(B, S, H, Dqk, Dv, scale) && attn_fwd_dense_preferred(B, S, H, k))
+    return kFwdDenseTc;
+  if (attn_fwd_tc_supported(H, Dqk, Dv, scale)) return kFwdGatherTc;
+  return kFwdMmaSync;
 }
 
 bool attn_dims_supported(int Dqk, int Dv) {

@@ -625,10 +625,11 @@ bool attn_fwd_dense_supported(int B, int S, int H, int Dqk, int Dv, float scale)
 }
 
 // The dense-tile kernel does about H * (causal 128 x 128 tiles) tile products; the
-// gathered-key kernel about one 96-key chunk per row and 96 selected keys, at a
-// similar cost per unit. Choose the dense kernel when it has fewer units and enough
-// work items (batch x head x query tile) to give every SM one: below that its
-// per-tile pipeline latency and the bitmap set-up are not hidden.
+// gathered-key kernel about one 96-key chunk per row and 96 selected keys. Measured on
+// GB300, a tile product costs about 5/3 of a chunk (15 against 9 ns of whole-GPU time).
+// Choose the dense kernel when it is the cheaper by that count and has enough work
+// items (batch x head x query tile) to give every SM one: below that its per-tile
+// pipeline latency and the bitmap set-up are not hidden.
 bool attn_fwd_dense_preferred(int B, int S, int H, int k) {
   const long long QT = (S + kTile - 1) / kTile;
   int dev = 0, sms = 0;
@@ -640,7 +641,7 @@ bool attn_fwd_dense_preferred(int B, int S, int H, int k) {
   const long long N = S < k ? S : k, q = N / 96, rem = N % 96;
   const long long chunks = 96 * q * (q + 1) / 2 + rem * (q + 1) + (S - N) * ((k + 95) / 96);
   (void)B;
-  return dense_units < chunks;
+  return 5 * dense_units < 3 * chunks;
 }
 
 int launch_attn_fwd_dense(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream) {

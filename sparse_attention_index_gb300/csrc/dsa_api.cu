@@ -144,6 +144,13 @@ int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32
                               as_stream(stream));
 }
 
+int dsa_sparse_attn_fwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, int k,
+                               float scale) {
+  if (B < 1 || S < 1 || H < 1 || k < 1) return -DSA_ERR_INVALID_ARG;
+  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return -DSA_ERR_UNSUPPORTED;
+  return dsa::attn_fwd_kernel_kind(B, S, H, Dqk, Dv, k, scale);
+}
+
 int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
                         int S, int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O,
                         float* lse, void* stream) {

@@ -23,6 +23,10 @@ int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int 
 // path: kFwdPathAuto (the cheaper of the gathered-key and dense-tile kernels) or
 // kFwdPathDense (the dense-tile kernel, DSA_ERR_UNSUPPORTED where it does not apply)
 constexpr int kFwdPathAuto = 0, kFwdPathDense = 1;
+// the kernel the automatic path runs: gathered-key tcgen05 (1 launch), dense-tile
+// tcgen05 (bitmap build + attention: 2 launches) or mma.sync (1 launch)
+constexpr int kFwdGatherTc = 0, kFwdDenseTc = 1, kFwdMmaSync = 2;
+int attn_fwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale);
 int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
                     int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
                     cudaStream_t stream, int path = kFwdPathAuto);

@@ -403,6 +403,22 @@ def test_dense_fwd_query_tile_without_keys():
     assert torch.all(O[0, 128:256] == 0)
 
 
+def test_fwd_kernel_choice():
+    """The automatic forward picks the dense-tile kernel for few heads and many selected keys,
+    the gathered-key kernel for 128 heads, mma.sync for small head dims; it refuses Hkv > 1."""
+    dsa = _dsa()
+    sc = 1.0 / np.sqrt(192)
+    assert dsa.dsa_sparse_attn_fwd_kernel(2, 4096, 16, 1, 192, 128, 2048, sc) == dsa.DSA_FWD_DENSE_TC
+    assert dsa.dsa_sparse_attn_fwd_kernel(4, 4096, 16, 1, 192, 128, 512, sc) == dsa.DSA_FWD_DENSE_TC
+    assert dsa.dsa_sparse_attn_fwd_kernel(1, 16384, 128, 1, 192, 128, 2048, sc) == \
+        dsa.DSA_FWD_GATHER_TC
+    assert dsa.dsa_sparse_attn_fwd_kernel(1, 489, 16, 1, 192, 128, 512, sc) == \
+        dsa.DSA_FWD_GATHER_TC   # too few work items to fill the GPU
+    assert dsa.dsa_sparse_attn_fwd_kernel(1, 128, 2, 1, 32, 32, 4, 0.2) == dsa.DSA_FWD_MMA_SYNC
+    with pytest.raises(dsa.DsaError):
+        dsa.dsa_sparse_attn_fwd_kernel(1, 128, 2, 2, 192, 128, 4, 0.2)
+
+
 def test_dense_fwd_bad_index_and_unsupported():
     dsa = _dsa()
     B, S, H, k = 1, 140, 16, 8
