@@ -237,10 +237,13 @@ def run_ours(args, wl, rank, world, local_rank):
     stream = torch.cuda.Stream(device=device)
     stages = ["indexer", "topk", "attn_fwd"] + (["attn_bwd"] if wl.backward else [])
     # indexer, top-k, the forward (two launches on the dense-tile kernel: bitmap build +
-    # attention), the backward and its finalize
+    # attention), the backward and its finalize (four on the dense-tile kernels: bitmap,
+    # dQ pass, dK / dV pass, finalize)
     fwd_launches = 2 if dsa.dsa_sparse_attn_fwd_kernel(B, S, wl.H, 1, wl.Dqk, wl.Dv, k, wl.scale) \
         == dsa.DSA_FWD_DENSE_TC else 1
-    launches_per_step = 2 + fwd_launches + (2 if wl.backward else 0)
+    bwd_launches = (4 if dsa.dsa_sparse_attn_bwd_kernel(B, S, wl.H, 1, wl.Dqk, wl.Dv, k, wl.scale)
+                    == dsa.DSA_BWD_DENSE_TC else 2) if wl.backward else 0
+    launches_per_step = 2 + fwd_launches + bwd_launches
 
     def step(ev):
         ev[0].record(stream)

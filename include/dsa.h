@@ -226,6 +226,37 @@ int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32
                         void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * dsa_sparse_attn_bwd_dense - the same gradients from the dense-tile kernels only:
+ * a dQ pass over (batch, head, query tile) items and a key-major dK / dV pass over
+ * (batch, key tile, group of heads) items, both under the bitmap of the selection
+ * (the pages' design: dense blocks with partial mask blocks and a key-major pass
+ * for dK / dV, "Support Ring Attention with DeepSeek DSA Sparse Indexer",
+ * Backward Flow). Arguments as for dsa_sparse_attn_bwd; the bitmap and Delta
+ * (B*S*ceil(S/128)*16 + B*S*H*4 bytes) are allocated stream-ordered on `stream`.
+ * Supported: Hkv = 1, 1 <= H <= 128, (Dqk, Dv) in {(128, 128), (192, 128)},
+ * S <= 65536, a positive scale; DSA_ERR_UNSUPPORTED otherwise.
+ * dsa_sparse_attn_bwd takes these kernels when they have fewer tile products for
+ * the shape; dsa_sparse_attn_bwd_noalloc never does.
+ */
+int dsa_sparse_attn_bwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
+                              const void* O, const float* lse, const void* dO, int B, int S, int H,
+                              int Hkv, int Dqk, int Dv, int k, float scale, void* dQ, void* dK, void* dV,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dsa_sparse_attn_bwd_kernel - which kernels dsa_sparse_attn_bwd runs for a shape:
+ * DSA_BWD_GATHER_TC (gathered-key tensor-core kernel + finalize: 2 launches),
+ * DSA_BWD_DENSE_TC (bitmap, dQ pass, dK / dV pass, finalize: 4 launches) or
+ * DSA_BWD_MMA_SYNC (2 launches); the negated status when the call would refuse the
+ * shape. Launches nothing.
+ */
+#define DSA_BWD_GATHER_TC 0
+#define DSA_BWD_DENSE_TC 1
+#define DSA_BWD_MMA_SYNC 2
+int dsa_sparse_attn_bwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, int k,
+                               float scale);
+
+/*
  * dsa_sparse_attn_bwd_noalloc - dsa_sparse_attn_bwd for callers that cannot
  * allocate device memory. The pages have no counterpart: this is a
  * deployment variant of the same backward pass, not part of the method.

@@ -36,7 +36,7 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa_index_scores",
            "dsa_index_scores_fp8",
            "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense",
-           "dsa_sparse_attn_fwd_kernel",
+           "dsa_sparse_attn_fwd_kernel", "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_kernel",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
            "dsa_sparse_attn_bwd_noalloc")
 
@@ -67,14 +67,18 @@ def _load() -> ctypes.CDLL:
     lib.dsa_sparse_attn_fwd_dense.argtypes = lib.dsa_sparse_attn_fwd.argtypes
     lib.dsa_sparse_attn_fwd_kernel.argtypes = [ci, ci, ci, ci, ci, ci, ci, cf]
     lib.dsa_sparse_attn_fwd_kernel.restype = ci
+    lib.dsa_sparse_attn_bwd_kernel.argtypes = [ci, ci, ci, ci, ci, ci, ci, cf]
+    lib.dsa_sparse_attn_bwd_kernel.restype = ci
     lib.dsa_sparse_attn_bwd_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
     lib.dsa_sparse_attn_bwd_workspace_size.restype = sz
     lib.dsa_sparse_attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf,
                                         vp, vp, vp, vp, sz, vp]
+    lib.dsa_sparse_attn_bwd_dense.argtypes = lib.dsa_sparse_attn_bwd.argtypes
     lib.dsa_sparse_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci,
                                                 ci, ci, cf, vp, vp, vp, vp]
     for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_index_scores_fp8", "dsa_topk",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense", "dsa_sparse_attn_bwd",
+                 "dsa_sparse_attn_bwd_dense",
                  "dsa_sparse_attn_bwd_noalloc"):
         getattr(lib, name).restype = ci
     return lib
@@ -224,7 +228,7 @@ def bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv) -> int:
 
 
 def dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, scale: float, dQ=None, dK=None, dV=None,
-                        ws=None, stream=None):
+                        ws=None, stream=None, _entry: str = "dsa_sparse_attn_bwd"):
     """Gradients of the sparse attention -> (dQ [B,S,H,Dqk], dK [B,S,Hkv,Dqk], dV [B,S,Hkv,Dv])."""
     B, S, H, Dqk = Q.shape
     Hkv, Dv = V.shape[2], V.shape[3]
@@ -239,15 +243,33 @@ def dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, scale: float, dQ=None, dK=None
     need = bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv)
     if ws is None:
         ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
-    rc = lib.dsa_sparse_attn_bwd(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
-                                 _dev(V, "V", torch.bfloat16), _dev(idx, "idx", torch.int32),
-                                 _dev(O, "O", torch.bfloat16), _dev(lse, "lse", torch.float32),
-                                 _dev(dO, "dO", torch.bfloat16), B, S, H, Hkv, Dqk, Dv, k,
-                                 float(scale), _dev(dQ, "dQ", torch.bfloat16),
-                                 _dev(dK, "dK", torch.bfloat16), _dev(dV, "dV", torch.bfloat16),
-                                 _dev(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
-    _check(rc, "dsa_sparse_attn_bwd")
+    rc = getattr(lib, _entry)(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
+                              _dev(V, "V", torch.bfloat16), _dev(idx, "idx", torch.int32),
+                              _dev(O, "O", torch.bfloat16), _dev(lse, "lse", torch.float32),
+                              _dev(dO, "dO", torch.bfloat16), B, S, H, Hkv, Dqk, Dv, k,
+                              float(scale), _dev(dQ, "dQ", torch.bfloat16),
+                              _dev(dK, "dK", torch.bfloat16), _dev(dV, "dV", torch.bfloat16),
+                              _dev(ws, "ws"), ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, _entry)
     return dQ, dK, dV
+
+
+def dsa_sparse_attn_bwd_dense(Q, K, V, idx, O, lse, dO, scale: float, dQ=None, dK=None,
+                              dV=None, ws=None, stream=None):
+    """dsa_sparse_attn_bwd through the dense-tile kernels only (same arguments and result)."""
+    return dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, scale, dQ=dQ, dK=dK, dV=dV, ws=ws,
+                               stream=stream, _entry="dsa_sparse_attn_bwd_dense")
+
+
+DSA_BWD_GATHER_TC, DSA_BWD_DENSE_TC, DSA_BWD_MMA_SYNC = 0, 1, 2
+
+
+def dsa_sparse_attn_bwd_kernel(B, S, H, Hkv, Dqk, Dv, k, scale: float) -> int:
+    """Which kernels dsa_sparse_attn_bwd runs for this shape (DSA_BWD_*; launches nothing)."""
+    r = lib.dsa_sparse_attn_bwd_kernel(B, S, H, Hkv, Dqk, Dv, k, float(scale))
+    if r < 0:
+        raise DsaError(-r, "dsa_sparse_attn_bwd_kernel")
+    return r
 
 
 def dsa_sparse_attn_bwd_noalloc(Q, K, V, idx, O, lse, dO, scale: float, dQ=None, dK=None,

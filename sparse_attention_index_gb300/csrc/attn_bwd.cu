@@ -300,10 +300,17 @@ int launch_bwd_dims(const AttnParams& p, long long rows, cudaStream_t stream) {
 
 }  // namespace
 
+int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale) {
+  if (attn_bwd_dense_supported(B, S, H, Dqk, Dv, scale) && attn_bwd_dense_preferred(B, S, H, k))
+    return kBwdDenseTc;
+  if (attn_bwd_tc_supported(H, Dqk, Dv, scale)) return kBwdGatherTc;
+  return kBwdMmaSync;
+}
+
 int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                     const void* O, const float* lse, const void* dO, int B, int S, int H, int Dqk,
                     int Dv, int k, float scale, void* dQ, void* dK, void* dV, float* ws_dkv,
-                    cudaStream_t stream) {
+                    cudaStream_t stream, int path) {
   AttnParams p = make_attn_params(Q, K, V, idx, B, S, H, k, scale);
   p.O_in = static_cast<const uint16_t*>(O);
   p.lse_in = lse;
@@ -315,8 +322,13 @@ int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* 
   if (cudaMemsetAsync(ws_dkv, 0, static_cast<size_t>(rows) * (Dqk + Dv) * sizeof(float),
                       stream) != cudaSuccess)
     return DSA_ERR_CUDA;
+  const bool dense_ok = attn_bwd_dense_supported(B, S, H, Dqk, Dv, scale);
+  if (path == kBwdPathDense && !dense_ok) return DSA_ERR_UNSUPPORTED;
+  const bool dense = dense_ok && (path == kBwdPathDense ||
+                                  (path == kBwdPathAuto && attn_bwd_dense_preferred(B, S, H, k)));
   int rc;
-  if (attn_bwd_tc_supported(H, Dqk, Dv, scale)) rc = launch_attn_bwd_tc(p, stream);
+  if (dense) rc = launch_attn_bwd_dense(p, Dqk, Dv, stream);
+  else if (attn_bwd_tc_supported(H, Dqk, Dv, scale)) rc = launch_attn_bwd_tc(p, stream);
   else if (Dqk == 192 && Dv == 128) rc = launch_bwd_dims<192, 128>(p, rows, stream);
   else if (Dqk == 128 && Dv == 128) rc = launch_bwd_dims<128, 128>(p, rows, stream);
   else if (Dqk == 64 && Dv == 64) rc = launch_bwd_dims<64, 64>(p, rows, stream);

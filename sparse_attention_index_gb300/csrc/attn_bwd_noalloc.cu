@@ -77,5 +77,5 @@ extern "C" int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const v
   if (ws == nullptr) return DSA_ERR_CUDA;
   // launch_attn_bwd zeroes the rows it uses (cudaMemsetAsync) before accumulating
   return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
-                              ws, static_cast<cudaStream_t>(stream));
+                              ws, static_cast<cudaStream_t>(stream), dsa::kBwdPathNoAlloc);
 }

@@ -595,10 +595,7 @@ int launch_dense(const AttnParams& p, cudaStream_t stream) {
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long mrows = static_cast<long long>(p.B) * p.S;
-    const int mgrid = static_cast<int>(mrows < 8LL * sms ? mrows : 8LL * sms);
-    dense_mask_kernel<<<mgrid, 256, static_cast<size_t>(W4) * 4, stream>>>(p.idx, p.B, p.S, p.k,
-                                                                         W4, QT, bits, any, p.err);
+    launch_dense_mask(p.idx, p.B, p.S, p.k, W4, QT, bits, any, p.err, stream);
     const long long items = static_cast<long long>(QT) * p.B * p.H;
     const int grid = static_cast<int>(items < sms ? items : sms);
     DenseParams dp;
@@ -615,6 +612,17 @@ int launch_dense(const AttnParams& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+void launch_dense_mask(const int32_t* idx, int B, int S, int k, int W4, int QT, uint32_t* bits,
+                       uint8_t* any, int* err, cudaStream_t stream) {
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long rows = static_cast<long long>(B) * S;
+  const int grid = static_cast<int>(rows < 8LL * sms ? rows : 8LL * sms);
+  dense_mask_kernel<<<grid, 256, static_cast<size_t>(W4) * 4, stream>>>(idx, B, S, k, W4, QT, bits,
+                                                                       any, err);
+}
 
 // (Dqk, Dv) = (192, 128) or (128, 128), Hkv = 1, a positive scale; the bitmap holds
 // B*S*ceil(S/128)*16 bytes, so S is limited to 65536.

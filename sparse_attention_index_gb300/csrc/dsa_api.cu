@@ -183,4 +183,27 @@ int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32
                               static_cast<float*>(ws), as_stream(stream));
 }
 
+int dsa_sparse_attn_bwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
+                        const void* O, const float* lse, const void* dO, int B, int S, int H,
+                        int Hkv, int Dqk, int Dv, int k, float scale, void* dQ, void* dK, void* dV,
+                        void* ws, size_t ws_bytes, void* stream) {
+  if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
+  if (!O || !lse || !dO || !dQ || !dK || !dV) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(O) || !aligned16(lse) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
+      !aligned16(dV))
+    return DSA_ERR_INVALID_ARG;
+  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  const size_t need = dsa_sparse_attn_bwd_workspace_size(B, S, H, Hkv, Dqk, Dv);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+  return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
+                              static_cast<float*>(ws), as_stream(stream), dsa::kBwdPathDense);
+}
+
+int dsa_sparse_attn_bwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, int k,
+                               float scale) {
+  if (B < 1 || S < 1 || H < 1 || k < 1) return -DSA_ERR_INVALID_ARG;
+  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return -DSA_ERR_UNSUPPORTED;
+  return dsa::attn_bwd_kernel_kind(B, S, H, Dqk, Dv, k, scale);
+}
+
 }  // extern "C"

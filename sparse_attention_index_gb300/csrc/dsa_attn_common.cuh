@@ -48,6 +48,16 @@ int launch_attn_fwd_tc(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream
 bool attn_fwd_dense_supported(int B, int S, int H, int Dqk, int Dv, float scale);
 bool attn_fwd_dense_preferred(int B, int S, int H, int k);
 int launch_attn_fwd_dense(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream);
+// The selection bitmap of the dense-tile kernels (attn_fwd_dense.cu): bits [B*S, W4]
+// (W4 = 4 * QT words per row, written up to each row's own query tile), tile flags
+// any [B, QT, QT] (zeroed by the caller), QT = ceil(S / 128).
+void launch_dense_mask(const int32_t* idx, int B, int S, int k, int W4, int QT, uint32_t* bits,
+                       uint8_t* any, int* err, cudaStream_t stream);
+// Dense-tile backward (attn_bwd_dense.cu): dQ written directly, dK / dV added into the
+// zeroed fp32 workspace p.ws like the other backward kernels.
+bool attn_bwd_dense_supported(int B, int S, int H, int Dqk, int Dv, float scale);
+bool attn_bwd_dense_preferred(int B, int S, int H, int k);
+int launch_attn_bwd_dense(const AttnParams& p, int Dqk, int Dv, cudaStream_t stream);
 
 // tcgen05 backward (attn_bwd_tc.cu): H <= 128, Dqk = 192, Dv = 128, positive scale.
 // The fp32 dK/dV accumulator p.ws must already be zero on the stream.

@@ -31,10 +31,18 @@ int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* 
                     int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
                     cudaStream_t stream, int path = kFwdPathAuto);
 
+// path: kBwdPathAuto (the cheaper of the gathered-key and dense-tile kernels),
+// kBwdPathNoAlloc (never the dense-tile kernels, which allocate their bitmap) or
+// kBwdPathDense (the dense-tile kernels, DSA_ERR_UNSUPPORTED where they do not apply)
+constexpr int kBwdPathAuto = 0, kBwdPathNoAlloc = 1, kBwdPathDense = 2;
+// the kernels the automatic path runs: gathered-key tcgen05 (+ finalize: 2 launches),
+// dense-tile tcgen05 (bitmap, dq, dk/dv, finalize: 4) or mma.sync (+ finalize: 2)
+constexpr int kBwdGatherTc = 0, kBwdDenseTc = 1, kBwdMmaSync = 2;
+int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale);
 int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                     const void* O, const float* lse, const void* dO, int B, int S, int H, int Dqk,
                     int Dv, int k, float scale, void* dQ, void* dK, void* dV, float* ws_dkv,
-                    cudaStream_t stream);
+                    cudaStream_t stream, int path = kBwdPathAuto);
 
 bool attn_dims_supported(int Dqk, int Dv);
 bool indexer_dims_supported(int Hi, int Di);

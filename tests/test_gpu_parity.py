@@ -403,6 +403,58 @@ def test_dense_fwd_query_tile_without_keys():
     assert torch.all(O[0, 128:256] == 0)
 
 
+def _bwd_check(dQ, dK, dV, Q, K, V, idx, dO, scale):
+    dQ_ref, dK_ref, dV_ref = oracle.attn_bwd(Q, K, V, idx, dO, scale)
+    assert rel_err(host_f64(dQ).reshape(dQ_ref.shape), dQ_ref) <= TOL
+    assert rel_err(host_f64(dK), dK_ref) <= TOL
+    assert rel_err(host_f64(dV), dV_ref) <= TOL
+
+
+@pytest.mark.parametrize("case", DENSE_CASES)
+def test_dense_bwd_matches_oracle(case):
+    dsa = _dsa()
+    B, S, H, Dqk, Dv, k, ndocs = case
+    Q, K, V, dO, idx = _attn_case(*case, seed=950 + S + H)
+    scale = 1.0 / np.sqrt(Dqk)
+    Qd, Kd, Vd, dOd, idxd = bf16_dev(Q), bf16_dev(K), bf16_dev(V), bf16_dev(dO), dev(idx)
+    O, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, idxd, scale)
+    dQ, dK, dV = dsa.dsa_sparse_attn_bwd_dense(Qd, Kd, Vd, idxd, O, lse, dOd, scale)
+    assert dsa.dsa_get_last_device_error() == 0
+    _bwd_check(dQ, dK, dV, Q, K, V, idx, dO, scale)
+
+
+@pytest.mark.parametrize("H", [5, 16])
+def test_dense_bwd_user_lists_and_empty_tiles(H):
+    """Holes, entries above the diagonal, empty rows and a whole query tile without keys;
+    H = 5 leaves a partial group of heads in the dK / dV pass."""
+    dsa = _dsa()
+    B, S, Dqk, Dv, k = 1, 300, 192, 128, 150
+    Q, K, V, dO, _ = _attn_case(B, S, H, Dqk, Dv, 8, 0, seed=21)
+    rng = np.random.default_rng(22)
+    idx = np.full((B, S, k), -1, dtype=np.int32)
+    for t in range(S):
+        if t % 9 == 4 or 128 <= t < 256:
+            continue
+        pick = rng.choice(S, size=min(S, k), replace=False).astype(np.int32)
+        pick[rng.random(pick.size) < 0.2] = -1
+        idx[0, t] = pick
+    Qd, Kd, Vd, dOd, idxd = bf16_dev(Q), bf16_dev(K), bf16_dev(V), bf16_dev(dO), dev(idx)
+    O, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, idxd, 0.1)
+    dQ, dK, dV = dsa.dsa_sparse_attn_bwd_dense(Qd, Kd, Vd, idxd, O, lse, dOd, 0.1)
+    assert dsa.dsa_get_last_device_error() == 0
+    _bwd_check(dQ, dK, dV, Q, K, V, idx, dO, 0.1)
+    assert torch.all(dQ[0, 128:256] == 0)
+
+
+def test_bwd_kernel_choice():
+    dsa = _dsa()
+    sc = 1.0 / np.sqrt(192)
+    assert dsa.dsa_sparse_attn_bwd_kernel(4, 4096, 16, 1, 192, 128, 512, sc) == dsa.DSA_BWD_DENSE_TC
+    assert dsa.dsa_sparse_attn_bwd_kernel(1, 16384, 128, 1, 192, 128, 2048, sc) == \
+        dsa.DSA_BWD_GATHER_TC
+    assert dsa.dsa_sparse_attn_bwd_kernel(1, 128, 2, 1, 32, 32, 4, 0.2) == dsa.DSA_BWD_MMA_SYNC
+
+
 def test_fwd_kernel_choice():
     """The automatic forward picks the dense-tile kernel for few heads and many selected keys,
     the gathered-key kernel for 128 heads, mma.sync for small head dims; it refuses Hkv > 1."""
