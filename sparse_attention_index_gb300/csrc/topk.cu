@@ -649,6 +649,8 @@ struct Smem {
   int wgt[NW], weq[NW];
   int bcast[4];
   uint32_t ubc[8];
+  int wcnt[NW];               // one-pass path: candidates appended by each warp
+  uint32_t ckey[kLongCand];   // one-pass path: the order key of each candidate
 };
 
 // keys of one row read from global memory (tail of the last group and other
@@ -855,6 +857,65 @@ __device__ __forceinline__ void select_sweep(const RowKeys& rk, int nq, uint32_t
   __syncthreads();   // wgt / weq are reused by the next row
 }
 
+// The selection from the candidate list sm->cand[0..in_bin) (every key that can still
+// be selected beyond those already marked in sm->gtw): the remaining digits below
+// (prefix, mask), the candidates marked above / equal to the threshold, and the
+// ascending emission of the gtw keys and the first `need` eqw keys.
+__device__ __forceinline__ void finish_candidates(const RowKeys& rk, bool inner, uint32_t prefix,
+                                                  uint32_t mask, int need, int in_bin, int nwords,
+                                                  const TopkParams& p, int32_t* out, Smem* sm) {
+  const int tid = threadIdx.x;
+  const int ncand = min(in_bin, kLongCand);
+  const int shifts_in[2] = {8, 0}, nbins_in[2] = {512, 256};
+  const int shifts_out[4] = {24, 16, 8, 0}, nbins_out[4] = {256, 256, 256, 256};
+  resolve_levels(
+      [&](auto fn) {
+        for (int j = tid; j < ncand; j += NT) fn(rk.key(static_cast<int>(sm->cand[j])));
+      },
+      sm->hist, inner ? 2 : 4, inner ? shifts_in : shifts_out, inner ? nbins_in : nbins_out,
+      prefix, mask, need, in_bin, sm);
+  for (int j = tid; j < ncand; j += NT) {
+    const int sj = static_cast<int>(sm->cand[j]);
+    const uint32_t km = rk.key(sj) & mask;
+    if (km > prefix) atomicOr(&sm->gtw[sj >> 5], 1u << (sj & 31));
+    else if (km == prefix) atomicOr(&sm->eqw[sj >> 5], 1u << (sj & 31));
+  }
+  __syncthreads();
+  uint32_t g[kWpt], q[kWpt];
+  int own = 0;
+#pragma unroll
+  for (int i = 0; i < kWpt; ++i) {
+    const int wd = tid * kWpt + i;
+    g[i] = wd < nwords ? sm->gtw[wd] : 0u;
+    q[i] = wd < nwords ? sm->eqw[wd] : 0u;
+    own += __popc(g[i]) | (__popc(q[i]) << 16);
+  }
+  int tot;
+  const int excl = block_scan(own, tot, sm) - own;   // every word is read before this returns
+  int gb = excl & 0xFFFF, eb = excl >> 16;
+  int32_t* ost = p.k <= kLongCand ? reinterpret_cast<int32_t*>(sm->cand) : out;
+#pragma unroll
+  for (int i = 0; i < kWpt; ++i) {
+    uint32_t bits = g[i] | q[i];
+    while (bits) {
+      const int bb = __ffs(bits) - 1;
+      bits &= bits - 1u;
+      const int sj = (tid * kWpt + i) * 32 + bb;
+      if ((g[i] >> bb) & 1u) {
+        const int pos = gb + min(eb, need);
+        if (pos < p.k) ost[pos] = sj;
+        ++gb;
+      } else {
+        if (eb < need && gb + eb < p.k) ost[gb + eb] = sj;
+        ++eb;
+      }
+    }
+  }
+  __syncthreads();
+  if (ost != out)
+    for (int j = tid; j < p.k; j += NT) out[j] = ost[j];
+}
+
 __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, const TopkParams& p,
                                            int32_t* out, long long row, Smem* sm) {
   const int tid = threadIdx.x, lane = tid & 31;
@@ -867,6 +928,145 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
     for (int j = n + tid; j < p.k; j += NT) out[j] = -1;
     if (p.count && tid == 0) p.count[row] = n;
     return;
+  }
+  // ---- one pass: every key at or above a threshold placed from a strided sample (one
+  // group of 4 keys per thread, evenly spaced over the row) at the sample rank that k
+  // takes in the row plus four standard deviations. When that leaves between k and
+  // kLongCand keys, the top k are among them and the candidate finish selects them
+  // exactly; otherwise the two-pass path below runs.
+  const int nwords0 = (4 * nq + 31) >> 5;
+  if (nwords0 <= kLongWords) {
+    for (int i = tid; i < 2048; i += NT) sm->hist[i] = 0u;
+    if (tid < 8) sm->ubc[tid] = 0u;
+    const int cs = static_cast<int>((static_cast<long long>(tid) * nq) / NT);
+    const uint4 smp = rk.load4(cs);
+    const uint32_t sk[4] = {smp.x, smp.y, smp.z, smp.w};
+    uint32_t ap = 0u, an = 0u, cp = 0u, cv = 0u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (sk[e] == 0u) continue;
+      const bool pos = sk[e] >= 0x80000000u;
+      if (pos) ap = max(ap, sk[e] & 0x7FFFFFFFu);
+      else an = max(an, ~sk[e] & 0x7FFFFFFFu);
+      cp += pos;
+      ++cv;
+    }
+    ap = __reduce_max_sync(0xffffffffu, ap);
+    an = __reduce_max_sync(0xffffffffu, an);
+    cp = __reduce_add_sync(0xffffffffu, cp);
+    cv = __reduce_add_sync(0xffffffffu, cv);
+    __syncthreads();
+    if (lane == 0) {
+      atomicMax(&sm->ubc[0], ap);
+      atomicMax(&sm->ubc[1], an);
+      atomicAdd(&sm->ubc[2], cp);
+      atomicAdd(&sm->ubc[3], cv);
+    }
+    __syncthreads();
+    const uint32_t npos = sm->ubc[2], nval = sm->ubc[3];
+    if (nval > 0u) {
+      const bool positive_side = static_cast<unsigned long long>(npos) * n >=
+                                 static_cast<unsigned long long>(nval) * p.k;
+      const LevelOne ws = LevelOne::make(sm->ubc[0], sm->ubc[1], positive_side);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (sk[e] != 0u) atomicAdd(&sm->hist[ws.bucket(sk[e])], 1u);
+      __syncthreads();
+      const float mu = static_cast<float>(p.k) * static_cast<float>(nval) / static_cast<float>(n);
+      int rs = static_cast<int>(mu + 4.f * sqrtf(mu) + 8.f);
+      if (rs > static_cast<int>(nval)) rs = static_cast<int>(nval);
+      int sbin, sabove, sin_bin;
+      find_bin(sm->hist, 2048, rs, sm, sbin, sabove, sin_bin);
+      if (ws.interior(static_cast<uint32_t>(sbin))) {
+        const uint32_t L = ws.prefix(static_cast<uint32_t>(sbin));
+        for (int i = tid; i < nwords0; i += NT) {
+          sm->gtw[i] = 0u;
+          sm->eqw[i] = 0u;
+        }
+        for (int i = tid; i < 2048; i += NT) sm->hist[i] = 0u;   // now: the candidates' bins
+        if (tid == 0) {
+          sm->ubc[6] = 0u;
+          sm->ubc[7] = 0u;
+        }
+        __syncthreads();
+        // each warp appends to its own segment of the list, so that no counter is
+        // shared between warps; a warp that fills its segment sends the row to the
+        // two-pass path
+        constexpr int kSeg = kLongCand / NW;
+        const int wid = tid >> 5;
+        uint32_t* seg = sm->cand + wid * kSeg;
+        uint32_t* segk = sm->ckey + wid * kSeg;
+        int wc = 0;
+        const uint32_t lt = (1u << lane) - 1u;
+        for (int c0 = 0; c0 < nq; c0 += 4 * NT) {
+          uint4 kv[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u * NT + tid;
+            kv[u] = c < nq ? rk.load4(c) : make_uint4(0u, 0u, 0u, 0u);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint32_t kk[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
+            const int c = c0 + u * NT + tid;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const bool cd = kk[e] != 0u && kk[e] >= L;
+              const uint32_t bal = __ballot_sync(0xffffffffu, cd);
+              const int r = wc + __popc(bal & lt);
+              if (cd && r < kSeg) {
+                seg[r] = static_cast<uint32_t>(4 * c + e);
+                segk[r] = kk[e];
+              }
+              wc += __popc(bal);
+            }
+          }
+        }
+        if (lane == 0) {
+          sm->wcnt[wid] = wc;
+          if (wc > kSeg) sm->ubc[6] = 1u;   // a segment overflowed
+          atomicAdd(&sm->ubc[7], static_cast<uint32_t>(wc));
+        }
+        // the candidates' first-level bins, after the pass (a few thousand keys)
+        for (int j = lane; j < min(wc, kSeg); j += 32) atomicAdd(&sm->hist[ws.bucket(segk[j])], 1u);
+        __syncthreads();
+        const int C = static_cast<int>(sm->ubc[7]);
+        const bool fits = sm->ubc[6] == 0u;
+        __syncthreads();
+        if (tid == 0) sm->ubc[7] = 0u;   // reused as the in-bin counter below
+        __syncthreads();
+        if (fits && C >= p.k) {
+          // every key >= L is a candidate and there are at least k: the bin of the k-th
+          // largest candidate is the row's threshold bin. Candidates above it go to the
+          // bitmap, those in it become the list (staged in eqw, which is zeroed after).
+          int bin, above, in_bin;
+          find_bin(sm->hist, 2048, p.k, sm, bin, above, in_bin);
+          const uint32_t b1 = static_cast<uint32_t>(bin);
+          for (int j = lane; j < sm->wcnt[wid]; j += 32) {
+            const uint32_t sj = seg[j];
+            const uint32_t bk = ws.bucket(segk[j]);
+            if (bk > b1) {
+              atomicOr(&sm->gtw[sj >> 5], 1u << (sj & 31));
+            } else if (bk == b1) {
+              const uint32_t r = atomicAdd(&sm->ubc[7], 1u);
+              sm->eqw[r] = sj;
+            }
+          }
+          __syncthreads();
+          for (int j = tid; j < in_bin; j += NT) sm->cand[j] = sm->eqw[j];
+          __syncthreads();
+          for (int i = tid; i < nwords0; i += NT) sm->eqw[i] = 0u;
+          __syncthreads();
+          const bool inner = ws.interior(b1);
+          finish_candidates(rk, inner, inner ? ws.prefix(b1) : 0u, inner ? 0xFFFE0000u : 0u,
+                            p.k - above, in_bin, nwords0, p, out, sm);
+          if (p.count && tid == 0) p.count[row] = p.k;
+          __syncthreads();   // the shared state is reused by the next row
+          return;
+        }
+        __syncthreads();   // C is read before the two-pass path resets the counters
+      }
+    }
   }
   for (int i = tid; i < 2048; i += NT) sm->hist[i] = 0u;
   if (tid < 4) sm->ubc[tid] = 0u;
@@ -970,55 +1170,7 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
       }
     }
     __syncthreads();
-    const int ncand = min(in_bin, kLongCand);
-    const int shifts_in[2] = {8, 0}, nbins_in[2] = {512, 256};
-    const int shifts_out[4] = {24, 16, 8, 0}, nbins_out[4] = {256, 256, 256, 256};
-    resolve_levels(
-        [&](auto fn) {
-          for (int j = tid; j < ncand; j += NT) fn(rk.key(static_cast<int>(sm->cand[j])));
-        },
-        sm->hist, inner ? 2 : 4, inner ? shifts_in : shifts_out, inner ? nbins_in : nbins_out,
-        prefix, mask, need, in_bin, sm);
-    for (int j = tid; j < ncand; j += NT) {
-      const int sj = static_cast<int>(sm->cand[j]);
-      const uint32_t km = rk.key(sj) & mask;
-      if (km > prefix) atomicOr(&sm->gtw[sj >> 5], 1u << (sj & 31));
-      else if (km == prefix) atomicOr(&sm->eqw[sj >> 5], 1u << (sj & 31));
-    }
-    __syncthreads();
-    uint32_t g[kWpt], q[kWpt];
-    int own = 0;
-#pragma unroll
-    for (int i = 0; i < kWpt; ++i) {
-      const int wd = tid * kWpt + i;
-      g[i] = wd < nwords ? sm->gtw[wd] : 0u;
-      q[i] = wd < nwords ? sm->eqw[wd] : 0u;
-      own += __popc(g[i]) | (__popc(q[i]) << 16);
-    }
-    int tot;
-    const int excl = block_scan(own, tot, sm) - own;   // every word is read before this returns
-    int gb = excl & 0xFFFF, eb = excl >> 16;
-    int32_t* ost = p.k <= kLongCand ? reinterpret_cast<int32_t*>(sm->cand) : out;
-#pragma unroll
-    for (int i = 0; i < kWpt; ++i) {
-      uint32_t bits = g[i] | q[i];
-      while (bits) {
-        const int bb = __ffs(bits) - 1;
-        bits &= bits - 1u;
-        const int sj = (tid * kWpt + i) * 32 + bb;
-        if ((g[i] >> bb) & 1u) {
-          const int pos = gb + min(eb, need);
-          if (pos < p.k) ost[pos] = sj;
-          ++gb;
-        } else {
-          if (eb < need && gb + eb < p.k) ost[gb + eb] = sj;
-          ++eb;
-        }
-      }
-    }
-    __syncthreads();
-    if (ost != out)
-      for (int j = tid; j < p.k; j += NT) out[j] = ost[j];
+    finish_candidates(rk, inner, prefix, mask, need, in_bin, nwords, p, out, sm);
   } else {
     // ---- further levels over the whole row
     uint32_t prefix = 0u, mask = 0u;
