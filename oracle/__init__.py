@@ -21,6 +21,13 @@ Functions and the passages they follow (details in ``dsa_oracle.c``):
 * ``attn_fwd`` / ``attn_bwd`` - masked softmax attention over the selected
   keys and its gradients ("Support Ring Attention with DeepSeek DSA Sparse
   Indexer", Forward Flow step 5, Backward Flow step 6).
+* ``indexer_loss`` / ``indexer_loss_bwd`` - the indexer's auxiliary loss: a
+  head-summed fp32 softmax target of the attention scores over the valid
+  tokens, held constant ("Implement QK attention head chunking for CSA", the
+  indexer-loss teacher), added to the objective so that its gradient trains
+  the indexer ("Support Ring Attention with DeepSeek DSA Sparse Indexer", Loss
+  Harvesting & Objective Injection); KL form and normalisation as read in
+  ``dsa_oracle.c``.
 
 Pins (tests/test_oracle_pins.py): exact rational arithmetic, brute-force
 sorting, dense masked attention through torch in fp64, autograd and finite
@@ -75,6 +82,12 @@ def _load():
             lib.oracle_attn_bwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cd,
                                             vp, i64, vp, vp, vp, ci]
             lib.oracle_attn_bwd.restype = ci
+            lib.oracle_indexer_loss.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, cd, cd,
+                                                vp, i64, vp, vp, vp, ci]
+            lib.oracle_indexer_loss.restype = ci
+            lib.oracle_indexer_loss_bwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp,
+                                                    i64, vp, vp, vp, ci]
+            lib.oracle_indexer_loss_bwd.restype = ci
             _lib = lib
     return _lib
 
@@ -211,3 +224,59 @@ def attn_bwd(Q, K, V, idx, dO, scale: float, rows=None, threads=None):
     if rc:
         raise ValueError(f"oracle_attn_bwd: bad input (code {rc})")
     return dQ, dK, dV
+
+
+def indexer_loss(Q, K, idx, scores, scale: float, grad_scale: float = 1.0, rows=None,
+                 threads=None, want_pbar: bool = False):
+    """Q [B,S,H,Dqk], K [B,S,Hkv,Dqk] (bf16 bits), idx [B,S,k], scores [n,S] (any float).
+
+    Returns (kl [n], dI [n,k]) in fp64, plus pbar [n,k] (the target) if asked.
+    """
+    B, S, H, Dqk = Q.shape
+    Hkv = K.shape[2]
+    k = idx.shape[2]
+    q, qp = _c(Q, np.uint16)
+    kk, kp = _c(K, np.uint16)
+    ix, ip = _c(idx, np.int32)
+    rows = _rows(rows, B, S)
+    sc, sp = _c(scores, np.float64)
+    if sc.shape != (rows.size, S):
+        raise ValueError("scores must be [len(rows), S]")
+    kl = np.empty((rows.size,), dtype=np.float64)
+    dI = np.empty((rows.size, k), dtype=np.float64)
+    pbar = np.empty((rows.size, k), dtype=np.float64) if want_pbar else None
+    rc = _load().oracle_indexer_loss(qp, kp, ip, sp, B, S, H, Hkv, Dqk, k, float(scale),
+                                     float(grad_scale), rows.ctypes.data, rows.size,
+                                     kl.ctypes.data, dI.ctypes.data,
+                                     pbar.ctypes.data if want_pbar else None,
+                                     threads or default_threads())
+    if rc:
+        raise ValueError(f"oracle_indexer_loss: bad input (code {rc})")
+    return (kl, dI, pbar) if want_pbar else (kl, dI)
+
+
+def indexer_loss_bwd(q_idx, k_idx, w, idx, dI, rows=None, threads=None):
+    """q_idx [B,S,Hi,Di], k_idx [B,S,Di] (bf16 bits), w [B,S,Hi] f32, idx [B,S,k], dI [n,k].
+
+    Returns (dq [n,Hi,Di], dk [B,S,Di], dw [n,Hi]) in fp64; dk holds the listed rows'
+    contributions (all rows: the full gradient).
+    """
+    B, S, Hi, Di = q_idx.shape
+    k = idx.shape[2]
+    q, qp = _c(q_idx, np.uint16)
+    kk, kp = _c(k_idx, np.uint16)
+    ww, wp = _c(w, np.float32)
+    ix, ip = _c(idx, np.int32)
+    rows = _rows(rows, B, S)
+    g, gp = _c(dI, np.float64)
+    if g.shape != (rows.size, k):
+        raise ValueError("dI must be [len(rows), k]")
+    dq = np.empty((rows.size, Hi, Di), dtype=np.float64)
+    dk = np.empty((B, S, Di), dtype=np.float64)
+    dw = np.empty((rows.size, Hi), dtype=np.float64)
+    rc = _load().oracle_indexer_loss_bwd(qp, kp, wp, ip, gp, B, S, Hi, Di, k, rows.ctypes.data,
+                                         rows.size, dq.ctypes.data, dk.ctypes.data,
+                                         dw.ctypes.data, threads or default_threads())
+    if rc:
+        raise ValueError(f"oracle_indexer_loss_bwd: bad input (code {rc})")
+    return dq, dk, dw

@@ -422,3 +422,201 @@ int oracle_attn_bwd(const uint16_t* Q, const uint16_t* K, const uint16_t* V, con
   free(c.dV_part);
   return c.bad_index;
 }
+
+/* ------------------------------------------------------ indexer loss (f3) */
+/*
+ * The indexer's auxiliary loss. "Implement QK attention head chunking for CSA"
+ * (the teacher of the indexer loss): the attention scores of every head are
+ * turned into fp32 softmax probabilities over the keys, zeroed outside the
+ * valid tokens and summed over the heads; the result is a stop-gradient target.
+ * "Support Ring Attention with DeepSeek DSA Sparse Indexer" (Loss Harvesting &
+ * Objective Injection): the loss is added to the training objective and its
+ * gradient reaches the indexer's query and key projections.
+ *
+ * Plainest reading of what the pages leave open:
+ *   - the valid tokens are the attention's own mask, the selected slots j of
+ *     the row with 0 <= idx[t,j] <= t (a key listed twice counts twice);
+ *   - the target is made a distribution by dividing the head sum by H:
+ *         pbar_j = (1/H) sum_h softmax_j(scale * Q[t,h] . K[s_j, g(h)]);
+ *   - the student is the softmax of the index scores over the same slots,
+ *         q_j = exp(I[t,s_j]) / sum_i exp(I[t,s_i]);
+ *   - the loss of row t is KL(pbar || q) = sum_j pbar_j (log pbar_j - log q_j),
+ *     with 0 log 0 = 0; a row without a selected key has loss 0;
+ *   - dL/dI[t,s_j] = g (q_j - pbar_j) for the objective g * sum_t L_t (the
+ *     target is constant), and the chain rule through
+ *         I[t,s] = sum_h w[t,h] max(0, z_h),  z_h = q_idx[t,h] . k_idx[s]
+ *     takes the derivative of max(0, z) at z = 0 as 0:
+ *         dw[t,h]      = sum_j dI_j max(0, z_hj)
+ *         dq_idx[t,h]  = sum_j dI_j w[t,h] [z_hj > 0] k_idx[s_j]
+ *         dk_idx[s_j] += sum_h dI_j w[t,h] [z_hj > 0] q_idx[t,h]
+ */
+
+typedef struct {
+  const uint16_t *Q, *K;
+  const int32_t* idx;
+  const double* scores;   /* [nrows, S]: the index scores of each listed row */
+  int B, S, H, Hkv, Dqk, k;
+  double scale, grad_scale;
+  const int64_t* rows;
+  double *kl, *dI, *pbar;  /* [nrows], [nrows,k], [nrows,k] (pbar may be NULL) */
+  int bad_index;
+} iloss_ctx;
+
+static void iloss_row(void* p, int64_t r, int tid) {
+  (void)tid;
+  iloss_ctx* c = (iloss_ctx*)p;
+  int64_t row = c->rows[r];
+  int64_t b = row / c->S, t = row % c->S;
+  int kk = c->k > 0 ? c->k : 1;
+  int* slot = (int*)malloc(sizeof(int) * (size_t)kk);
+  int32_t* keys = (int32_t*)malloc(sizeof(int32_t) * (size_t)kk);
+  double* pb = (double*)calloc((size_t)kk, sizeof(double));
+  double* l = (double*)malloc(sizeof(double) * (size_t)kk);
+  int64_t m = 0;
+  for (int j = 0; j < c->k; ++j) {
+    int32_t s = c->idx[row * c->k + j];
+    if (s < -1 || s >= c->S) { c->bad_index = 1; continue; }
+    if (s < 0 || s > t) continue;
+    slot[m] = j;
+    keys[m] = s;
+    ++m;
+  }
+  for (int j = 0; j < c->k; ++j) c->dI[r * c->k + j] = 0.0;
+  if (c->pbar)
+    for (int j = 0; j < c->k; ++j) c->pbar[r * c->k + j] = 0.0;
+  c->kl[r] = 0.0;
+  if (m > 0) {
+    /* teacher: per-head softmax of the attention logits, averaged over heads */
+    for (int h = 0; h < c->H; ++h) {
+      int g = h / (c->H / c->Hkv);
+      const uint16_t* q = c->Q + (row * c->H + h) * c->Dqk;
+      double mx = -INFINITY;
+      for (int64_t i = 0; i < m; ++i) {
+        const uint16_t* kr = c->K + ((b * c->S + keys[i]) * c->Hkv + g) * c->Dqk;
+        double dot = 0.0;
+        for (int d = 0; d < c->Dqk; ++d) dot += bf16_to_double(q[d]) * bf16_to_double(kr[d]);
+        l[i] = dot * c->scale;
+        if (l[i] > mx) mx = l[i];
+      }
+      double z = 0.0;
+      for (int64_t i = 0; i < m; ++i) { l[i] = exp(l[i] - mx); z += l[i]; }
+      for (int64_t i = 0; i < m; ++i) pb[i] += l[i] / z;
+    }
+    for (int64_t i = 0; i < m; ++i) pb[i] /= c->H;
+    /* student: softmax of the index scores over the same slots */
+    const double* I = c->scores + r * (int64_t)c->S;
+    double mx = -INFINITY;
+    for (int64_t i = 0; i < m; ++i)
+      if (I[keys[i]] > mx) mx = I[keys[i]];
+    double z = 0.0;
+    for (int64_t i = 0; i < m; ++i) z += exp(I[keys[i]] - mx);
+    double logz = mx + log(z);
+    double kl = 0.0;
+    for (int64_t i = 0; i < m; ++i) {
+      double logq = I[keys[i]] - logz;
+      if (pb[i] > 0.0) kl += pb[i] * (log(pb[i]) - logq);
+      c->dI[r * c->k + slot[i]] = c->grad_scale * (exp(logq) - pb[i]);
+      if (c->pbar) c->pbar[r * c->k + slot[i]] = pb[i];
+    }
+    c->kl[r] = kl;
+  }
+  free(slot);
+  free(keys);
+  free(pb);
+  free(l);
+}
+
+/*
+ * Indexer loss of the listed rows. Q [B,S,H,Dqk], K [B,S,Hkv,Dqk] bf16, idx
+ * [B,S,k], scores [nrows,S] (the listed rows' index scores; only the selected
+ * keys are read). kl [nrows]; dI [nrows,k] = dL/dI at each slot (0 at slots
+ * that hold no selected key); pbar [nrows,k] (optional) = the target. Returns
+ * 0, 1 if an index was outside [-1, S), 2 on bad head counts.
+ */
+int oracle_indexer_loss(const uint16_t* Q, const uint16_t* K, const int32_t* idx,
+                        const double* scores, int B, int S, int H, int Hkv, int Dqk, int k,
+                        double scale, double grad_scale, const int64_t* rows, int64_t nrows,
+                        double* kl, double* dI, double* pbar, int nthreads) {
+  if (Hkv < 1 || H % Hkv != 0) return 2;
+  iloss_ctx c;
+  memset(&c, 0, sizeof(c));
+  c.Q = Q; c.K = K; c.idx = idx; c.scores = scores;
+  c.B = B; c.S = S; c.H = H; c.Hkv = Hkv; c.Dqk = Dqk; c.k = k;
+  c.scale = scale; c.grad_scale = grad_scale;
+  c.rows = rows; c.kl = kl; c.dI = dI; c.pbar = pbar;
+  for_rows(iloss_row, &c, nrows, nthreads);
+  return c.bad_index;
+}
+
+typedef struct {
+  const uint16_t *qi, *ki; /* q_idx [B,S,Hi,Di], k_idx [B,S,Di] bf16 */
+  const float* w;          /* [B,S,Hi] */
+  const int32_t* idx;
+  const double* dI;        /* [nrows,k] */
+  int B, S, Hi, Di, k;
+  const int64_t* rows;
+  double *dq, *dw;         /* [nrows,Hi,Di], [nrows,Hi] */
+  double* dk_part;         /* per thread [B*S*Di] */
+  int bad_index;
+} ibwd_ctx;
+
+static void ibwd_row(void* p, int64_t r, int tid) {
+  ibwd_ctx* c = (ibwd_ctx*)p;
+  int64_t row = c->rows[r];
+  int64_t b = row / c->S, t = row % c->S;
+  double* dq = c->dq + r * (int64_t)c->Hi * c->Di;
+  double* dw = c->dw + r * (int64_t)c->Hi;
+  double* dk = c->dk_part + (size_t)tid * (size_t)c->B * c->S * c->Di;
+  for (int64_t i = 0; i < (int64_t)c->Hi * c->Di; ++i) dq[i] = 0.0;
+  for (int h = 0; h < c->Hi; ++h) dw[h] = 0.0;
+  for (int j = 0; j < c->k; ++j) {
+    int32_t s = c->idx[row * c->k + j];
+    if (s < -1 || s >= c->S) { c->bad_index = 1; continue; }
+    if (s < 0 || s > t) continue;
+    double g = c->dI[r * c->k + j];
+    const uint16_t* kr = c->ki + (b * c->S + s) * c->Di;
+    for (int h = 0; h < c->Hi; ++h) {
+      const uint16_t* qr = c->qi + (row * c->Hi + h) * c->Di;
+      double z = 0.0;
+      for (int d = 0; d < c->Di; ++d) z += bf16_to_double(qr[d]) * bf16_to_double(kr[d]);
+      if (z > 0.0) {
+        dw[h] += g * z;
+        double gw = g * (double)c->w[row * c->Hi + h];
+        for (int d = 0; d < c->Di; ++d) {
+          dq[h * c->Di + d] += gw * bf16_to_double(kr[d]);
+          dk[(b * c->S + s) * c->Di + d] += gw * bf16_to_double(qr[d]);
+        }
+      }
+    }
+  }
+}
+
+/*
+ * Gradient of the indexer loss into the indexer inputs, given dI [nrows,k]
+ * (dL/dI at each slot of the listed rows). dq [nrows,Hi,Di], dw [nrows,Hi] for
+ * the listed rows; dk [B,S,Di] collects the contributions of the listed rows
+ * (all rows: the full gradient). Returns as oracle_indexer_loss.
+ */
+int oracle_indexer_loss_bwd(const uint16_t* q_idx, const uint16_t* k_idx, const float* w,
+                            const int32_t* idx, const double* dI, int B, int S, int Hi, int Di,
+                            int k, const int64_t* rows, int64_t nrows, double* dq, double* dk,
+                            double* dw, int nthreads) {
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 512) nthreads = 512;
+  size_t nk = (size_t)B * S * Di;
+  ibwd_ctx c;
+  memset(&c, 0, sizeof(c));
+  c.qi = q_idx; c.ki = k_idx; c.w = w; c.idx = idx; c.dI = dI;
+  c.B = B; c.S = S; c.Hi = Hi; c.Di = Di; c.k = k;
+  c.rows = rows; c.dq = dq; c.dw = dw;
+  c.dk_part = (double*)calloc(nk * (size_t)nthreads, sizeof(double));
+  if (!c.dk_part) return 3;
+  for_rows(ibwd_row, &c, nrows, nthreads);
+  for (size_t i = 0; i < nk; ++i) {
+    double a = 0.0;
+    for (int tI = 0; tI < nthreads; ++tI) a += c.dk_part[(size_t)tI * nk + i];
+    dk[i] = a;
+  }
+  free(c.dk_part);
+  return c.bad_index;
+}

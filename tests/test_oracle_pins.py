@@ -493,3 +493,204 @@ def test_attn_bwd_closed_form_sums():
     _, dKb, dVb = oracle.attn_bwd(Q, K, V, idx, dO, scale, rows=rows_b)
     np.testing.assert_allclose(dKa + dKb, dK, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(dVa + dVb, dV, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------------- indexer loss
+
+def _iloss_case(B, S, H, Dqk, seed, k, Hi=3, Di=16, seg_docs=0):
+    Q = synth.normal_bf16((B, S, H, Dqk), seed, 4)
+    K = synth.normal_bf16((B, S, 1, Dqk), seed, 5)
+    seg = synth.segments(B, S, seg_docs, seed) if seg_docs else None
+    q_idx = synth.dyadic_bf16((B, S, Hi, Di), seed, 1, -8, 8, 3)
+    k_idx = synth.dyadic_bf16((B, S, Di), seed, 2, -8, 8, 3)
+    w = synth.dyadic_f32((B, S, Hi), seed, 3, -4, 4, 4)
+    sc = oracle.index_scores(q_idx, k_idx, w, seg)
+    idx, _ = oracle.topk(sc, seg, S, k, B=B)
+    return Q, K, q_idx, k_idx, w, seg, sc, idx.reshape(B, S, k)
+
+
+def _torch_teacher_student(Q, K, idx, scores, scale, H):
+    """Dense fp64 torch: target pbar [B,S,S] and log-student [B,S,S] under the index mask."""
+    B, S = Q.shape[:2]
+    mask = torch.from_numpy(_dense_mask(idx, S))
+    q = torch.from_numpy(bf16_bits_to_f64(Q))                       # [B,S,H,D]
+    kk = torch.from_numpy(bf16_bits_to_f64(K))[:, :, 0]              # [B,S,D]
+    logits = torch.einsum("bthd,bsd->bhts", q, kk) * scale
+    logits = logits.masked_fill(~mask[:, None], float("-inf"))
+    probs = torch.softmax(logits, dim=-1)
+    probs = torch.nan_to_num(probs, nan=0.0)                         # rows without a key
+    pbar = probs.sum(dim=1) / H
+    I = torch.from_numpy(np.nan_to_num(scores.reshape(B, S, S), nan=-np.inf))
+    return pbar, I, mask
+
+
+def _slots_to_dense(vals, idx, S):
+    B, _, k = idx.shape
+    out = np.zeros((B, S, S))
+    v = vals.reshape(B, S, k)
+    for b in range(B):
+        for t in range(S):
+            for j in range(k):
+                s = idx[b, t, j]
+                if 0 <= s <= t:
+                    out[b, t, s] += v[b, t, j]
+    return out
+
+
+@pytest.mark.parametrize("seg_docs", [0, 3])
+def test_indexer_loss_matches_torch_kl_div_and_autograd(seg_docs):
+    B, S, H, Dqk, k = 2, 36, 5, 24, 6
+    Q, K, _, _, _, seg, sc, idx = _iloss_case(B, S, H, Dqk, seed=41, k=k, seg_docs=seg_docs)
+    scale, g = 0.25, 0.75
+    kl, dI, pbar = oracle.indexer_loss(Q, K, idx, sc, scale, g, want_pbar=True)
+    tp, I, mask = _torch_teacher_student(Q, K, idx, sc, scale, H)
+    np.testing.assert_allclose(_slots_to_dense(pbar, idx, S), tp.numpy(), rtol=1e-12, atol=1e-15)
+    I = I.clone().requires_grad_(True)
+    logq = torch.log_softmax(I.masked_fill(~mask, float("-inf")), dim=-1)
+    # KL(p || q) through torch's kl_div (input log q, target p), zero outside the mask
+    terms = torch.nn.functional.kl_div(torch.where(mask, logq, torch.zeros_like(logq)), tp,
+                                       reduction="none")
+    row_kl = torch.where(mask, terms, torch.zeros_like(terms)).sum(-1)
+    np.testing.assert_allclose(kl, row_kl.reshape(-1).detach().numpy(), rtol=1e-11, atol=1e-14)
+    (g * row_kl.sum()).backward()
+    np.testing.assert_allclose(_slots_to_dense(dI, idx, S), I.grad.numpy(), rtol=1e-10,
+                               atol=1e-14)
+
+
+def test_indexer_loss_two_key_closed_form():
+    """One head, two selected keys: Bernoulli KL written with the logistic function."""
+    B, S, H, Dqk, k = 1, 6, 1, 8, 2
+    Q, K, _, _, _, _, _, _ = _iloss_case(B, S, H, Dqk, seed=42, k=k)
+    t, s0, s1 = 5, 1, 4
+    idx = np.full((B, S, k), -1, dtype=np.int32)
+    idx[0, t] = [s0, s1]
+    scores = np.full((B * S, S), np.nan)
+    c0, c1 = 0.375, -1.25
+    scores[t, s0], scores[t, s1] = c0, c1
+    scale, g = 0.5, 2.0
+    kl, dI = oracle.indexer_loss(Q, K, idx, scores[t:t + 1], scale, g, rows=np.array([t]))
+    qv = bf16_bits_to_f64(Q)[0, t, 0]
+    kv = bf16_bits_to_f64(K)[0, :, 0]
+    a0, a1 = scale * float(qv @ kv[s0]), scale * float(qv @ kv[s1])
+    p = 1.0 / (1.0 + np.exp(a1 - a0))      # teacher weight of s0
+    q = 1.0 / (1.0 + np.exp(c1 - c0))      # student weight of s0
+    want = p * np.log(p / q) + (1 - p) * np.log((1 - p) / (1 - q))
+    assert abs(kl[0] - want) <= 1e-13
+    np.testing.assert_allclose(dI[0], [g * (q - p), g * (p - q)], rtol=1e-12, atol=1e-15)
+
+
+def test_indexer_loss_invariants():
+    B, S, H, Dqk, k = 2, 30, 4, 16, 5
+    Q, K, _, _, _, _, sc, idx = _iloss_case(B, S, H, Dqk, seed=43, k=k)
+    scale = 0.3
+    kl, dI, pbar = oracle.indexer_loss(Q, K, idx, sc, scale, 1.0, want_pbar=True)
+    assert (kl >= -1e-15).all()
+    np.testing.assert_allclose(pbar.sum(axis=1), 1.0, rtol=1e-13)     # every row has key t
+    np.testing.assert_allclose(dI.sum(axis=1), 0.0, atol=1e-14)
+    # a constant shift of a row's scores changes neither the loss nor its gradient
+    kl2, dI2 = oracle.indexer_loss(Q, K, idx, sc + 3.5, scale, 1.0)
+    np.testing.assert_allclose(kl2, kl, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dI2, dI, rtol=1e-10, atol=1e-15)
+    # a student equal to the target has zero loss and zero gradient
+    st = np.full_like(sc, -np.inf)
+    for r in range(B * S):
+        for j in range(k):
+            s = idx.reshape(-1, k)[r, j]
+            if s >= 0 and pbar[r, j] > 0:
+                st[r, s] = np.log(pbar[r, j])
+    kl3, dI3 = oracle.indexer_loss(Q, K, idx, st, scale, 1.0)
+    assert np.max(np.abs(kl3)) < 1e-13 and np.max(np.abs(dI3)) < 1e-15
+    # one head: the target is the attention's own softmax weights (exp(l - LSE))
+    kl1, dI1, p1 = oracle.indexer_loss(Q[:, :, :1], K, idx, sc, scale, 1.0, want_pbar=True)
+    _, lse = oracle.attn_fwd(Q[:, :, :1], K, K[..., :8], idx, scale)
+    qv, kv = bf16_bits_to_f64(Q)[:, :, 0], bf16_bits_to_f64(K)[:, :, 0]
+    for r in (0, 17, 29, 45):
+        b, t = divmod(r, S)
+        for j in range(k):
+            s = idx[b, t, j]
+            if 0 <= s <= t:
+                want = np.exp(scale * float(qv[b, t] @ kv[b, s]) - lse[r, 0])
+                assert abs(p1[r, j] - want) <= 1e-13
+
+
+def _torch_indexer_loss(q_idx, k_idx, w, tp, mask, g):
+    q = torch.from_numpy(bf16_bits_to_f64(q_idx)).requires_grad_(True)
+    kk = torch.from_numpy(bf16_bits_to_f64(k_idx)).requires_grad_(True)
+    ww = torch.from_numpy(w.astype(np.float64)).requires_grad_(True)
+    z = torch.einsum("bthd,bsd->bths", q, kk)
+    I = (ww[..., None] * torch.relu(z)).sum(dim=2)
+    logq = torch.log_softmax(I.masked_fill(~mask, float("-inf")), dim=-1)
+    safe = torch.where(mask & (tp > 0), tp, torch.ones_like(tp))
+    kl = torch.where(mask & (tp > 0), tp * (torch.log(safe) - logq), torch.zeros_like(tp))
+    (g * kl.sum()).backward()
+    return q.grad.numpy(), kk.grad.numpy(), ww.grad.numpy()
+
+
+@pytest.mark.parametrize("seg_docs", [0, 2])
+def test_indexer_loss_bwd_matches_torch_autograd(seg_docs):
+    """Autograd through I = sum_h w relu(q.k) (relu'(0) = 0 in torch too, and the dyadic
+    inputs make many z exactly 0) into the KL with a constant target."""
+    B, S, H, Dqk, k, Hi, Di = 2, 28, 3, 16, 5, 4, 16
+    Q, K, q_idx, k_idx, w, seg, sc, idx = _iloss_case(B, S, H, Dqk, seed=44, k=k, Hi=Hi, Di=Di,
+                                                      seg_docs=seg_docs)
+    scale, g = 0.4, 1.5
+    _, dI = oracle.indexer_loss(Q, K, idx, sc, scale, g)
+    dq, dk, dw = oracle.indexer_loss_bwd(q_idx, k_idx, w, idx, dI)
+    tp, _, mask = _torch_teacher_student(Q, K, idx, sc, scale, H)
+    z = np.einsum("bthd,bsd->bths", bf16_bits_to_f64(q_idx), bf16_bits_to_f64(k_idx))
+    assert (z[np.broadcast_to(mask[:, :, None].numpy(), z.shape)] == 0).any()
+    gq, gk, gw = _torch_indexer_loss(q_idx, k_idx, w, tp, mask, g)
+    np.testing.assert_allclose(dq.reshape(gq.shape), gq, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dk, gk, rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(dw.reshape(gw.shape), gw, rtol=1e-10, atol=1e-13)
+    # rows split in two contribute parts of dk that add up
+    rows_a, rows_b = np.arange(0, B * S, 2), np.arange(1, B * S, 2)
+    _, dka, _ = oracle.indexer_loss_bwd(q_idx, k_idx, w, idx, dI[rows_a], rows=rows_a)
+    _, dkb, _ = oracle.indexer_loss_bwd(q_idx, k_idx, w, idx, dI[rows_b], rows=rows_b)
+    np.testing.assert_allclose(dka + dkb, dk, rtol=1e-12, atol=1e-14)
+
+
+def test_indexer_loss_bwd_finite_differences():
+    """Central differences of the whole chain q_idx, k_idx, w -> scores -> loss."""
+    B, S, H, Dqk, k, Hi, Di = 1, 14, 2, 16, 4, 3, 8
+    Q, K, q_idx, k_idx, w, _, sc, idx = _iloss_case(B, S, H, Dqk, seed=45, k=k, Hi=Hi, Di=Di)
+    scale, g = 0.5, 1.0
+    one = f64_to_bf16_bits(np.array([1.0]))[0]
+    arrs = {"q": q_idx.copy(), "k": k_idx.copy(), "w": w.copy()}
+    probes = [("q", (0, 11, 1, 2)), ("q", (0, 6, 0, 5)), ("k", (0, 3, 1)), ("k", (0, 9, 6)),
+              ("w", (0, 12, 2)), ("w", (0, 8, 0))]
+    for name, ix in probes:
+        arrs[name][ix] = 1.0 if name == "w" else one
+    sc0 = oracle.index_scores(arrs["q"], arrs["k"], arrs["w"], None)
+    _, dI = oracle.indexer_loss(Q, K, idx, sc0, scale, g)
+    dq, dk, dw = oracle.indexer_loss_bwd(arrs["q"], arrs["k"], arrs["w"], idx, dI)
+    grads = {"q": dq.reshape(q_idx.shape), "k": dk, "w": dw.reshape(w.shape)}
+    z = np.einsum("bthd,bsd->bths", bf16_bits_to_f64(arrs["q"]), bf16_bits_to_f64(arrs["k"]))
+    eps = 2.0 ** -7          # 1 +- 2^-7 are bf16 values; no z of the rows crosses 0 (checked)
+
+    def loss(a):
+        s = oracle.index_scores(a["q"], a["k"], a["w"], None)
+        kl, _ = oracle.indexer_loss(Q, K, idx, s, scale, g)
+        return float(g * kl.sum())
+
+    checked = 0
+    for name, ix in probes:
+        if name == "q":
+            zz = z[0, ix[1], ix[2], : ix[1] + 1]
+        elif name == "k":
+            zz = z[0, ix[1]:, :, ix[1]]
+        else:
+            zz = np.ones(1)
+        if (zz == 0).any():
+            continue
+        vals = []
+        for sgn in (+1, -1):
+            a = {n: x.copy() for n, x in arrs.items()}
+            a[name][ix] = (1.0 + sgn * eps) if name == "w" else \
+                f64_to_bf16_bits(np.array([1.0 + sgn * eps]))[0]
+            vals.append(loss(a))
+        fd = (vals[0] - vals[1]) / (2 * eps)
+        an = grads[name][ix]
+        assert abs(fd - an) <= 2e-3 * max(1e-2, abs(an)), (name, ix, fd, an)
+        checked += 1
+    assert checked >= 4
