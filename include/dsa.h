@@ -62,6 +62,8 @@ typedef enum { DSA_BF16 = 0, DSA_F32 = 1 } dsa_dtype;
 #define DSA_STAGE_TOPK 0x200
 #define DSA_STAGE_FWD 0x300
 #define DSA_STAGE_BWD 0x400
+#define DSA_STAGE_LOSS 0x500
+#define DSA_STAGE_LOSS_BWD 0x600
 
 /* Human-readable name of a status. Never NULL. */
 const char* dsa_status_string(int status);
@@ -286,6 +288,66 @@ int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
                                 const void* O, const float* lse, const void* dO, int B, int S,
                                 int H, int Hkv, int Dqk, int Dv, int k, float scale, void* dQ,
                                 void* dK, void* dV, void* stream);
+
+/*
+ * dsa_indexer_loss - the indexer's auxiliary loss and its gradient with respect
+ * to the index scores.
+ *
+ * "Implement QK attention head chunking for CSA" gives the target: every head's
+ * attention scores go through an fp32 softmax over the valid tokens, are zeroed
+ * elsewhere, summed over the heads and held constant. "Support Ring Attention
+ * with DeepSeek DSA Sparse Indexer" (Loss Harvesting & Objective Injection) adds
+ * the loss to the objective so that its gradient trains the indexer. The pages
+ * do not print the loss itself; this library reads it as the KL divergence
+ * between the head-averaged target and the softmax of the index scores, both
+ * over the query's selected keys (slots j with 0 <= s_j = idx[b,t,j] <= t):
+ *
+ *   pbar_j = (1/H) sum_h exp(scale Q[b,t,h].K[b,s_j] - lse[b,t,h])
+ *   q_j    = softmax_j(scores[b,t,s_j])
+ *   kl[b,t]   = sum_j pbar_j (log pbar_j - log q_j)          (0 log 0 = 0)
+ *   dI[b,t,j] = grad_scale (q_j - pbar_j)   (0 at slots without a selected key)
+ *
+ * dI is the gradient of grad_scale * sum_{b,t} kl[b,t] with respect to the score
+ * at each slot: pass it to dsa_indexer_loss_bwd.
+ *
+ *   Q      bf16 [B, S, H, Dqk]     K    bf16 [B, S, Hkv, Dqk]
+ *   idx    int32 [B, S, k]          lse  fp32 [B, S, H] (from dsa_sparse_attn_fwd)
+ *   scores fp32 [B, S, ld_scores]   only the selected entries are read
+ *   kl     fp32 [B, S] out          dI   fp32 [B, S, k] out
+ *
+ * Supported: Hkv = 1, 1 <= H <= 128, Dqk in {128, 192}, scale > 0. Rows with no
+ * selected key get kl = 0 and dI = 0. An index outside [-1, S) is skipped and
+ * recorded as DSA_STAGE_LOSS | DSA_DEVERR_BAD_INDEX. kl is accumulated with
+ * atomics (summation order unspecified).
+ */
+int dsa_indexer_loss(const void* Q, const void* K, const int32_t* idx, const float* lse,
+                     const float* scores, int64_t ld_scores, int B, int S, int H, int Hkv,
+                     int Dqk, int k, float scale, float grad_scale, float* kl, float* dI,
+                     void* stream);
+
+/*
+ * dsa_indexer_loss_bwd - the gradient of the indexer loss with respect to the
+ * indexer's inputs, given dI from dsa_indexer_loss. With
+ * I[t,s] = sum_h w[t,h] max(0, z_h), z_h = q_idx[t,h].k_idx[s] (the index score
+ * of dsa_index_scores) and the derivative of max(0, z) at z = 0 taken as 0:
+ *
+ *   dw[b,t,h]     = sum_j dI[b,t,j] max(0, z_hj)
+ *   dq_idx[b,t,h] = sum_j dI[b,t,j] w[b,t,h] [z_hj > 0] k_idx[b,s_j]
+ *   dk_idx[b,s]   = sum over (t, j) with s_j = s of sum_h dI[b,t,j] w[b,t,h] [z_hj > 0] q_idx[b,t,h]
+ *
+ * over the selected slots (0 <= s_j <= t).
+ *
+ *   q_idx  bf16 [B, S, Hi, Di]   k_idx bf16 [B, S, Di]   w fp32 [B, S, Hi]
+ *   idx    int32 [B, S, k]       dI    fp32 [B, S, k]
+ *   dq_idx fp32 [B, S, Hi, Di] out   dk_idx fp32 [B, S, Di] out   dw fp32 [B, S, Hi] out
+ *
+ * Supported: Hi = 64, Di = 128. The products run on the tensor cores with
+ * G = dI w [z > 0] rounded to bf16 and fp32 accumulation; dk_idx is accumulated
+ * with fp32 atomics (summation order unspecified).
+ */
+int dsa_indexer_loss_bwd(const void* q_idx, const void* k_idx, const float* w,
+                         const int32_t* idx, const float* dI, int B, int S, int Hi, int Di,
+                         int k, float* dq_idx, float* dk_idx, float* dw, void* stream);
 
 #ifdef __cplusplus
 }

@@ -29,6 +29,8 @@ DSA_BF16, DSA_F32 = 0, 1
 # device error codes (dsa_get_last_device_error): kind | stage
 DSA_DEVERR_TIMEOUT, DSA_DEVERR_BAD_INDEX, DSA_DEVERR_MISALIGNED = 0x01, 0x02, 0x03
 DSA_STAGE_INDEXER, DSA_STAGE_TOPK, DSA_STAGE_FWD, DSA_STAGE_BWD = 0x100, 0x200, 0x300, 0x400
+DSA_STAGE_LOSS, DSA_STAGE_LOSS_BWD = 0x500, 0x600
+DSA_OK, DSA_ERR_INVALID_ARG, DSA_ERR_UNSUPPORTED = 0, 1, 2
 STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
           4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_DEVICE"}
 
@@ -38,7 +40,7 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa
            "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense",
            "dsa_sparse_attn_fwd_kernel", "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_kernel",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
-           "dsa_sparse_attn_bwd_noalloc")
+           "dsa_sparse_attn_bwd_noalloc", "dsa_indexer_loss", "dsa_indexer_loss_bwd")
 
 
 class DsaError(RuntimeError):
@@ -76,10 +78,14 @@ def _load() -> ctypes.CDLL:
     lib.dsa_sparse_attn_bwd_dense.argtypes = lib.dsa_sparse_attn_bwd.argtypes
     lib.dsa_sparse_attn_bwd_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, vp, ci, ci, ci, ci, ci,
                                                 ci, ci, cf, vp, vp, vp, vp]
+    lib.dsa_indexer_loss.argtypes = [vp, vp, vp, vp, vp, i64, ci, ci, ci, ci, ci, ci, cf, cf, vp,
+                                     vp, vp]
+    lib.dsa_indexer_loss_bwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp, vp]
     for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_index_scores_fp8", "dsa_topk",
+                 "dsa_indexer_loss", "dsa_indexer_loss_bwd",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense", "dsa_sparse_attn_bwd",
                  "dsa_sparse_attn_bwd_dense",
-                 "dsa_sparse_attn_bwd_noalloc"):
+                 "dsa_sparse_attn_bwd_noalloc", "dsa_indexer_loss", "dsa_indexer_loss_bwd"):
         getattr(lib, name).restype = ci
     return lib
 
@@ -419,6 +425,57 @@ class HostPipeline:
         self.ev_out1, self.ev_out2, self.ev_out3 = out1, out2, out3
         self.n += 1
         return out3
+
+
+def dsa_indexer_loss(Q, K, idx, lse, scores, scale: float, grad_scale: float = 1.0, kl=None,
+                     dI=None, stream=None):
+    """Indexer auxiliary loss -> (kl fp32 [B,S], dI fp32 [B,S,k]).
+
+    Q [B,S,H,Dqk] bf16, K [B,S,1,Dqk] bf16, idx [B,S,k] int32, lse [B,S,H] fp32 (the
+    attention forward's), scores [B,S,ld] fp32 (the index scores). dI is the gradient of
+    grad_scale * kl.sum() with respect to the score at each slot of idx.
+    """
+    B, S, H, Dqk = Q.shape
+    Hkv = K.shape[2]
+    k = idx.shape[2]
+    if kl is None:
+        kl = torch.empty((B, S), dtype=torch.float32, device=Q.device)
+    if dI is None:
+        dI = torch.empty((B, S, k), dtype=torch.float32, device=Q.device)
+    rc = lib.dsa_indexer_loss(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
+                              _dev(idx, "idx", torch.int32), _dev(lse, "lse", torch.float32),
+                              _dev(scores, "scores", torch.float32), scores.shape[-1], B, S, H,
+                              Hkv, Dqk, k, float(scale), float(grad_scale),
+                              _dev(kl, "kl", torch.float32), _dev(dI, "dI", torch.float32),
+                              _stream(stream))
+    _check(rc, "dsa_indexer_loss")
+    return kl, dI
+
+
+def dsa_indexer_loss_bwd(q_idx, k_idx, w, idx, dI, dq_idx=None, dk_idx=None, dw=None,
+                         stream=None):
+    """Gradient of the indexer loss into the indexer inputs -> (dq_idx, dk_idx, dw), fp32.
+
+    q_idx [B,S,Hi,Di] bf16, k_idx [B,S,Di] bf16, w [B,S,Hi] fp32, idx [B,S,k] int32,
+    dI [B,S,k] fp32 (from dsa_indexer_loss).
+    """
+    B, S, Hi, Di = q_idx.shape
+    k = idx.shape[2]
+    dev = q_idx.device
+    if dq_idx is None:
+        dq_idx = torch.empty((B, S, Hi, Di), dtype=torch.float32, device=dev)
+    if dk_idx is None:
+        dk_idx = torch.empty((B, S, Di), dtype=torch.float32, device=dev)
+    if dw is None:
+        dw = torch.empty((B, S, Hi), dtype=torch.float32, device=dev)
+    rc = lib.dsa_indexer_loss_bwd(_dev(q_idx, "q_idx", torch.bfloat16),
+                                  _dev(k_idx, "k_idx", torch.bfloat16), _dev(w, "w", torch.float32),
+                                  _dev(idx, "idx", torch.int32), _dev(dI, "dI", torch.float32),
+                                  B, S, Hi, Di, k, _dev(dq_idx, "dq_idx", torch.float32),
+                                  _dev(dk_idx, "dk_idx", torch.float32), _dev(dw, "dw", torch.float32),
+                                  _stream(stream))
+    _check(rc, "dsa_indexer_loss_bwd")
+    return dq_idx, dk_idx, dw
 
 
 def dsa_layer(q_idx, k_idx, w, Q, K, V, topk: int, scale: float, seg=None, dO=None, stream=None):

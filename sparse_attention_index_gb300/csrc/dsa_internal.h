@@ -45,6 +45,18 @@ int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* 
                     cudaStream_t stream, int path = kBwdPathAuto);
 
 bool attn_dims_supported(int Dqk, int Dv);
+
+// indexer auxiliary loss: target, KL and dI (kl zeroed here), then the gradient into
+// q_idx, k_idx and w (dk zeroed here)
+bool indexer_loss_supported(int H, int Dqk, float scale);
+bool indexer_loss_bwd_supported(int Hi, int Di);
+int launch_indexer_loss(const void* Q, const void* K, const int32_t* idx, const float* lse,
+                        const float* scores, int64_t ld, int B, int S, int H, int Dqk, int k,
+                        float scale, float grad_scale, float* kl, float* dI,
+                        cudaStream_t stream);
+int launch_indexer_loss_bwd(const void* q_idx, const void* k_idx, const float* w,
+                            const int32_t* idx, const float* dI, int B, int S, int Hi, int Di,
+                            int k, float* dq, float* dk, float* dw, cudaStream_t stream);
 bool indexer_dims_supported(int Hi, int Di);
 
 }  // namespace dsa
