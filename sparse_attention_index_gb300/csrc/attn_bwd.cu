@@ -300,7 +300,9 @@ int launch_bwd_dims(const AttnParams& p, long long rows, cudaStream_t stream) {
 
 }  // namespace
 
-int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale) {
+int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale, int Hkv) {
+  if (Hkv > 1)
+    return attn_bwd_dense_supported(B, S, H, Dqk, Dv, scale) ? kBwdDenseTc : -DSA_ERR_UNSUPPORTED;
   if (attn_bwd_dense_supported(B, S, H, Dqk, Dv, scale) && attn_bwd_dense_preferred(B, S, H, k))
     return kBwdDenseTc;
   if (attn_bwd_tc_supported(H, Dqk, Dv, scale)) return kBwdGatherTc;
@@ -310,21 +312,24 @@ int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scal
 int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                     const void* O, const float* lse, const void* dO, int B, int S, int H, int Dqk,
                     int Dv, int k, float scale, void* dQ, void* dK, void* dV, float* ws_dkv,
-                    cudaStream_t stream, int path) {
+                    cudaStream_t stream, int path, int Hkv) {
   AttnParams p = make_attn_params(Q, K, V, idx, B, S, H, k, scale);
+  p.Hkv = Hkv;
   p.O_in = static_cast<const uint16_t*>(O);
   p.lse_in = lse;
   p.dO = static_cast<const uint16_t*>(dO);
   p.dQ = static_cast<uint16_t*>(dQ);
   p.ws = ws_dkv;
   const long long rows = static_cast<long long>(B) * S;
-  if (rows * H > 0x7fffffffLL || H > 128) return DSA_ERR_UNSUPPORTED;
-  if (cudaMemsetAsync(ws_dkv, 0, static_cast<size_t>(rows) * (Dqk + Dv) * sizeof(float),
+  if (rows * H > 0x7fffffffLL || H > 128 || Hkv < 1 || H % Hkv != 0) return DSA_ERR_UNSUPPORTED;
+  const bool dense_ok = attn_bwd_dense_supported(B, S, H, Dqk, Dv, scale);
+  // per-head or grouped K / V: the dense-tile kernels only (they allocate their bitmap)
+  if (Hkv > 1 && (!dense_ok || path == kBwdPathNoAlloc)) return DSA_ERR_UNSUPPORTED;
+  if (path == kBwdPathDense && !dense_ok) return DSA_ERR_UNSUPPORTED;
+  if (cudaMemsetAsync(ws_dkv, 0, static_cast<size_t>(rows) * Hkv * (Dqk + Dv) * sizeof(float),
                       stream) != cudaSuccess)
     return DSA_ERR_CUDA;
-  const bool dense_ok = attn_bwd_dense_supported(B, S, H, Dqk, Dv, scale);
-  if (path == kBwdPathDense && !dense_ok) return DSA_ERR_UNSUPPORTED;
-  const bool dense = dense_ok && (path == kBwdPathDense ||
+  const bool dense = dense_ok && (Hkv > 1 || path == kBwdPathDense ||
                                   (path == kBwdPathAuto && attn_bwd_dense_preferred(B, S, H, k)));
   int rc;
   if (dense) rc = launch_attn_bwd_dense(p, Dqk, Dv, stream);
@@ -339,7 +344,8 @@ int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* 
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   finalize_dkv_kernel<<<sms * 4, 256, 0, stream>>>(ws_dkv, static_cast<uint16_t*>(dK),
-                                                   static_cast<uint16_t*>(dV), rows, Dqk, Dv);
+                                                   static_cast<uint16_t*>(dV), rows * Hkv, Dqk,
+                                                   Dv);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

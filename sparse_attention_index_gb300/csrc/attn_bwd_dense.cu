@@ -49,6 +49,8 @@ constexpr int kH = 64;                // keys (dq) or queries (dk/dv) per half s
 constexpr int kThreadsB = 192;
 constexpr int kErrB2 = DSA_STAGE_BWD | DSA_DEVERR_TIMEOUT;
 constexpr int kGroupHeads = 1;        // heads per dk/dv item (1, 2, 4 measured: 1 is fastest)
+// every head of an item reads one K / V head (with per-head K / V only single-head items do)
+static_assert(kGroupHeads == 1, "an item's heads must share one K / V head");
 
 struct DenseBwdParams {
   AttnParams a;
@@ -211,14 +213,15 @@ __global__ void __launch_bounds__(kThreadsB, 1)
               hd.last = kt == lastkt ? 1 : 0;
               mbar_arrive_expect_tx(&tail->kv_full[st], L::kStage);
               const int krow = b * S + kt * kT;
+              const int kvh = h / (p.H / p.Hkv);   // the K / V head of query head h
               uint8_t* stage = smem + st * L::kStage;
 #pragma unroll
               for (int a = 0; a < L::KA; ++a)
-                tma_load_2d(stage + a * L::kAtom, &tm_k, &tail->kv_full[st], a * 64, krow);
+                tma_load_3d(stage + a * L::kAtom, &tm_k, &tail->kv_full[st], a * 64, kvh, krow);
 #pragma unroll
               for (int a = 0; a < L::VA; ++a)
-                tma_load_2d(stage + (L::KA + a) * L::kAtom, &tm_v, &tail->kv_full[st], a * 64,
-                            krow);
+                tma_load_3d(stage + (L::KA + a) * L::kAtom, &tm_v, &tail->kv_full[st], a * 64,
+                            kvh, krow);
               issued[st] = true;
               last_par[st] = (g >> 1) & 1;
             }
@@ -621,12 +624,14 @@ __global__ void __launch_bounds__(kThreadsB, 1)
         if (go) {
           mbar_arrive_expect_tx(&tail->kv_full, L::kKv);
           const int krow = b * S + kt * kT;
+          const int kvh = hg * kGroupHeads / (p.H / p.Hkv);   // the item's K / V head
 #pragma unroll
           for (int a = 0; a < L::KA; ++a)
-            tma_load_2d(smem + a * L::kKvAtom, &tm_k, &tail->kv_full, a * 64, krow);
+            tma_load_3d(smem + a * L::kKvAtom, &tm_k, &tail->kv_full, a * 64, kvh, krow);
 #pragma unroll
           for (int a = 0; a < L::VA; ++a)
-            tma_load_2d(smem + (L::KA + a) * L::kKvAtom, &tm_v, &tail->kv_full, a * 64, krow);
+            tma_load_3d(smem + (L::KA + a) * L::kKvAtom, &tm_v, &tail->kv_full, a * 64, kvh,
+                        krow);
           kv_issued = true;
           kv_last = n & 1;
         }
@@ -879,7 +884,9 @@ __global__ void __launch_bounds__(kThreadsB, 1)
       }
       dkv_par ^= 1u;
       tc_fence_after();
-      float* wrow = p.ws + (static_cast<long long>(b) * S + (kin ? s : 0)) * (DQK + DV);
+      const int kvh = hg * kGroupHeads / (p.H / p.Hkv);
+      float* wrow =
+          p.ws + ((static_cast<long long>(b) * S + (kin ? s : 0)) * p.Hkv + kvh) * (DQK + DV);
 #pragma unroll 1
       for (int d0 = 0; d0 < DQK + DV; d0 += 32) {
         uint32_t v[32];
@@ -924,15 +931,18 @@ EncodeTiledFnBd encode_fn_bd() {
   return fn;
 }
 
-// K / V rows [rows, cols] bf16: boxes of 64 columns x 128 rows, 128-byte swizzle
-bool make_kv_map(CUtensorMap* map, const void* base, long long rows, int cols) {
+// K / V [rows, Hkv, cols] bf16 as (column, K/V head, row): boxes of 64 columns x 1 head
+// x 128 rows, 128-byte swizzle (the shared-memory tile of a [128 x 64] 2-D box)
+bool make_kv_map(CUtensorMap* map, const void* base, long long rows, int Hkv, int cols) {
   EncodeTiledFnBd fn = encode_fn_bd();
   if (fn == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kT)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(Hkv),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                           static_cast<cuuint64_t>(cols) * 2 * static_cast<cuuint64_t>(Hkv)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kT)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -979,7 +989,7 @@ int launch_bwd_dense_dims(const AttnParams& p, cudaStream_t stream) {
   auto ka = attn_bwd_dense_dq_kernel<DQK, DV>;
   auto kb = attn_bwd_dense_dkv_kernel<DQK, DV>;
   if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + any_off, 0, any_bytes, stream) != cudaSuccess ||
-      !make_kv_map(&mk, p.K, rows, DQK) || !make_kv_map(&mv, p.V, rows, DV) ||
+      !make_kv_map(&mk, p.K, rows, p.Hkv, DQK) || !make_kv_map(&mv, p.V, rows, p.Hkv, DV) ||
       !make_head_rows_map(&mq, p.Q, rows, p.H, DQK) ||
       !make_head_rows_map(&mdo, p.dO, rows, p.H, DV) ||
       cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize,

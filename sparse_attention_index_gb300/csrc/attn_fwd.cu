@@ -185,13 +185,14 @@ int launch_fwd_dims(const AttnParams& p, long long rows, cudaStream_t stream) {
 
 int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
                     int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
-                    cudaStream_t stream, int path) {
+                    cudaStream_t stream, int path, int Hkv) {
   AttnParams p = make_attn_params(Q, K, V, idx, B, S, H, k, scale);
   p.O = static_cast<uint16_t*>(O);
   p.lse = lse;
+  p.Hkv = Hkv;
   const long long rows = static_cast<long long>(B) * S;
-  if (rows * H > 0x7fffffffLL || H > 128) return DSA_ERR_UNSUPPORTED;
-  if (path == kFwdPathDense)
+  if (rows * H > 0x7fffffffLL || H > 128 || Hkv < 1 || H % Hkv != 0) return DSA_ERR_UNSUPPORTED;
+  if (Hkv > 1 || path == kFwdPathDense)
     return attn_fwd_dense_supported(B, S, H, Dqk, Dv, scale) ? launch_attn_fwd_dense(p, Dqk, Dv, stream)
                                                              : DSA_ERR_UNSUPPORTED;
   const int kind = attn_fwd_kernel_kind(B, S, H, Dqk, Dv, k, scale);
@@ -204,7 +205,9 @@ int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* 
   return DSA_ERR_UNSUPPORTED;
 }
 
-int attn_fwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale) {
+int attn_fwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale, int Hkv) {
+  if (Hkv > 1)
+    return attn_fwd_dense_supported(B, S, H, Dqk, Dv, scale) ? kFwdDenseTc : -DSA_ERR_UNSUPPORTED;
   if (attn_fwd_dense_supported(B, S, H, Dqk, Dv, scale) && attn_fwd_dense_preferred(B, S, H, k))
     return kFwdDenseTc;
   if (attn_fwd_tc_supported(H, Dqk, Dv, scale)) return kFwdGatherTc;

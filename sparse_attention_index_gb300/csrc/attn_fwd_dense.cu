@@ -242,14 +242,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               // the arrive releases the header; the copies complete the phase
               mbar_arrive_expect_tx(&tail->kv_full[st], L::kStage);
               const int krow = b * S + kt * kTile;
+              const int kvh = h / (p.H / p.Hkv);   // the K / V head of query head h
               uint8_t* stage = smem + st * L::kStage;
 #pragma unroll
               for (int a = 0; a < L::KA; ++a)
-                tma_load_2d(stage + a * L::kAtom, &tm_k, &tail->kv_full[st], a * 64, krow);
+                tma_load_3d(stage + a * L::kAtom, &tm_k, &tail->kv_full[st], a * 64, kvh, krow);
 #pragma unroll
               for (int a = 0; a < L::VA; ++a)
-                tma_load_2d(stage + (L::KA + a) * L::kAtom, &tm_v, &tail->kv_full[st], a * 64,
-                            krow);
+                tma_load_3d(stage + (L::KA + a) * L::kAtom, &tm_v, &tail->kv_full[st], a * 64,
+                            kvh, krow);
               issued[st] = true;
               last_par[st] = (g / kStages) & 1;
             }
@@ -546,9 +547,10 @@ typedef CUresult (*EncodeTiledFnDense)(CUtensorMap*, CUtensorMapDataType, cuuint
                                        CUtensorMapSwizzle, CUtensorMapL2promotion,
                                        CUtensorMapFloatOOBfill);
 
-// [rows, cols] bf16 rows, a box of 64 columns x 128 rows, 128-byte swizzle; rows past
+// [rows, Hkv, cols] bf16 as (column, K/V head, row): a box of 64 columns x 1 head x 128
+// rows, 128-byte swizzle (the same shared-memory tile as a [128 x 64] 2-D box); rows past
 // the end read as zeros
-bool make_tile_map(CUtensorMap* map, const void* base, long long rows, int cols) {
+bool make_tile_map(CUtensorMap* map, const void* base, long long rows, int Hkv, int cols) {
   static EncodeTiledFnDense fn = nullptr;
   if (fn == nullptr) {
     void* ptr = nullptr;
@@ -559,11 +561,13 @@ bool make_tile_map(CUtensorMap* map, const void* base, long long rows, int cols)
       return false;
     fn = reinterpret_cast<EncodeTiledFnDense>(ptr);
   }
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kTile)};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(Hkv),
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2,
+                           static_cast<cuuint64_t>(cols) * 2 * static_cast<cuuint64_t>(Hkv)};
+  cuuint32_t box[3] = {64, 1, static_cast<cuuint32_t>(kTile)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -587,7 +591,7 @@ int launch_dense(const AttnParams& p, cudaStream_t stream) {
   const size_t smem = L::kTailOff + sizeof(DenseTail);
   auto kern = attn_fwd_dense_kernel<DQK, DV>;
   if (cudaMemsetAsync(any, 0, any_bytes, stream) != cudaSuccess ||
-      !make_tile_map(&mk, p.K, krows, DQK) || !make_tile_map(&mv, p.V, krows, DV) ||
+      !make_tile_map(&mk, p.K, krows, p.Hkv, DQK) || !make_tile_map(&mv, p.V, krows, p.Hkv, DV) ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess) {
     rc = DSA_ERR_CUDA;
@@ -624,8 +628,9 @@ void launch_dense_mask(const int32_t* idx, int B, int S, int k, int W4, int QT, 
                                                                        any, err);
 }
 
-// (Dqk, Dv) = (192, 128) or (128, 128), Hkv = 1, a positive scale; the bitmap holds
-// B*S*ceil(S/128)*16 bytes, so S is limited to 65536.
+// (Dqk, Dv) = (192, 128) or (128, 128), a positive scale, any Hkv dividing H (each tile is
+// one head's product, so per-head K / V only changes which rows its tiles load); the
+// bitmap holds B*S*ceil(S/128)*16 bytes, so S is limited to 65536.
 bool attn_fwd_dense_supported(int B, int S, int H, int Dqk, int Dv, float scale) {
   const long long items = static_cast<long long>((S + kTile - 1) / kTile) * B * H;
   return scale > 0.f && S >= 1 && S <= 65536 && H >= 1 && items < (1LL << 31) &&

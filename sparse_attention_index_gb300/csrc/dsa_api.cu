@@ -139,16 +139,18 @@ int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32
                         float* lse, void* stream) {
   if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
   if (!O || !lse || !aligned16(O) || !aligned16(lse)) return DSA_ERR_INVALID_ARG;
-  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
+  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
   return dsa::launch_attn_fwd(Q, K, V, idx, B, S, H, Dqk, Dv, k, scale, O, lse,
-                              as_stream(stream));
+                              as_stream(stream), dsa::kFwdPathAuto, Hkv);
 }
 
 int dsa_sparse_attn_fwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, int k,
                                float scale) {
   if (B < 1 || S < 1 || H < 1 || k < 1) return -DSA_ERR_INVALID_ARG;
-  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return -DSA_ERR_UNSUPPORTED;
-  return dsa::attn_fwd_kernel_kind(B, S, H, Dqk, Dv, k, scale);
+  if (Hkv < 1 || H % Hkv != 0) return -DSA_ERR_INVALID_ARG;
+  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return -DSA_ERR_UNSUPPORTED;
+  return dsa::attn_fwd_kernel_kind(B, S, H, Dqk, Dv, k, scale, Hkv);
 }
 
 int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
@@ -156,9 +158,10 @@ int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const
                         float* lse, void* stream) {
   if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
   if (!O || !lse || !aligned16(O) || !aligned16(lse)) return DSA_ERR_INVALID_ARG;
-  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
+  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
   return dsa::launch_attn_fwd(Q, K, V, idx, B, S, H, Dqk, Dv, k, scale, O, lse,
-                              as_stream(stream), dsa::kFwdPathDense);
+                              as_stream(stream), dsa::kFwdPathDense, Hkv);
 }
 
 size_t dsa_sparse_attn_bwd_workspace_size(int B, int S, int H, int Hkv, int Dqk, int Dv) {
@@ -176,11 +179,12 @@ int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32
   if (!aligned16(O) || !aligned16(lse) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
       !aligned16(dV))
     return DSA_ERR_INVALID_ARG;
-  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
+  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
   const size_t need = dsa_sparse_attn_bwd_workspace_size(B, S, H, Hkv, Dqk, Dv);
   if (!ws || ws_bytes < need || !aligned16(ws)) return DSA_ERR_WORKSPACE;
   return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
-                              static_cast<float*>(ws), as_stream(stream));
+                              static_cast<float*>(ws), as_stream(stream), dsa::kBwdPathAuto, Hkv);
 }
 
 int dsa_sparse_attn_bwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
@@ -192,18 +196,20 @@ int dsa_sparse_attn_bwd_dense(const void* Q, const void* K, const void* V, const
   if (!aligned16(O) || !aligned16(lse) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
       !aligned16(dV))
     return DSA_ERR_INVALID_ARG;
-  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
+  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
   const size_t need = dsa_sparse_attn_bwd_workspace_size(B, S, H, Hkv, Dqk, Dv);
   if (!ws || ws_bytes < need || !aligned16(ws)) return DSA_ERR_WORKSPACE;
   return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
-                              static_cast<float*>(ws), as_stream(stream), dsa::kBwdPathDense);
+                              static_cast<float*>(ws), as_stream(stream), dsa::kBwdPathDense, Hkv);
 }
 
 int dsa_sparse_attn_bwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, int k,
                                float scale) {
   if (B < 1 || S < 1 || H < 1 || k < 1) return -DSA_ERR_INVALID_ARG;
-  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return -DSA_ERR_UNSUPPORTED;
-  return dsa::attn_bwd_kernel_kind(B, S, H, Dqk, Dv, k, scale);
+  if (Hkv < 1 || H % Hkv != 0) return -DSA_ERR_INVALID_ARG;
+  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return -DSA_ERR_UNSUPPORTED;
+  return dsa::attn_bwd_kernel_kind(B, S, H, Dqk, Dv, k, scale, Hkv);
 }
 
 

@@ -12,6 +12,7 @@ struct AttnParams {
   const int32_t* idx;
   const float* lse_in;
   int B, S, H, k;
+  int Hkv;     // K / V heads: head h reads K / V head h / (H / Hkv)
   float scale, scale_log2;
   uint16_t* O;
   float* lse;
@@ -31,6 +32,7 @@ inline AttnParams make_attn_params(const void* Q, const void* K, const void* V,
   p.B = B;
   p.S = S;
   p.H = H;
+  p.Hkv = 1;
   p.k = k;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -26,10 +26,12 @@ constexpr int kFwdPathAuto = 0, kFwdPathDense = 1;
 // the kernel the automatic path runs: gathered-key tcgen05 (1 launch), dense-tile
 // tcgen05 (bitmap build + attention: 2 launches) or mma.sync (1 launch)
 constexpr int kFwdGatherTc = 0, kFwdDenseTc = 1, kFwdMmaSync = 2;
-int attn_fwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale);
+// Hkv > 1 (per-head or grouped K / V) runs on the dense-tile kernels only: the others
+// share one K / V row between all heads. Returns -DSA_ERR_UNSUPPORTED where no kernel applies.
+int attn_fwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale, int Hkv = 1);
 int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
                     int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
-                    cudaStream_t stream, int path = kFwdPathAuto);
+                    cudaStream_t stream, int path = kFwdPathAuto, int Hkv = 1);
 
 // path: kBwdPathAuto (the cheaper of the gathered-key and dense-tile kernels),
 // kBwdPathNoAlloc (never the dense-tile kernels, which allocate their bitmap) or
@@ -38,11 +40,11 @@ constexpr int kBwdPathAuto = 0, kBwdPathNoAlloc = 1, kBwdPathDense = 2;
 // the kernels the automatic path runs: gathered-key tcgen05 (+ finalize: 2 launches),
 // dense-tile tcgen05 (bitmap, dq, dk/dv, finalize: 4) or mma.sync (+ finalize: 2)
 constexpr int kBwdGatherTc = 0, kBwdDenseTc = 1, kBwdMmaSync = 2;
-int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale);
+int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale, int Hkv = 1);
 int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                     const void* O, const float* lse, const void* dO, int B, int S, int H, int Dqk,
                     int Dv, int k, float scale, void* dQ, void* dK, void* dV, float* ws_dkv,
-                    cudaStream_t stream, int path = kBwdPathAuto);
+                    cudaStream_t stream, int path = kBwdPathAuto, int Hkv = 1);
 
 bool attn_dims_supported(int Dqk, int Dv);
 

@@ -32,12 +32,15 @@
 // accumulates in TMEM over the row's chunks; each dk row is added to the output with
 // 16-byte fp32 reductions; dw is reduced over the keys with a warp reduce-scatter.
 //
-// Both kernels: persistent CTA per SM, 288 threads:
-//   warps 0-3   epilogue (TMEM lane quarters: one key, or one dimension of dq, per thread)
-//   warp  4     TMEM owner and single-thread UMMA issuer
-//   warps 5-8   gather: 16-byte cp.async of the selected key rows into 128B-swizzled
-//               tiles, four keys per group so that every copy instruction uses all 32
-//               lanes; the row's Q (q_idx) tile alongside the row's first chunk
+// Both kernels: persistent CTA per SM, warp-specialised:
+//   epilogue    forward: warps 0-7, two per TMEM lane quarter, each summing half of the
+//               heads of a key; backward: warps 0-3 (one key, or one dimension of dq,
+//               per thread)
+//   issuer      forward: warp 8, backward: warp 4 - TMEM owner and single-thread UMMA
+//               issuer
+//   gather      the last 4 warps: 16-byte cp.async of the selected key rows into
+//               128B-swizzled tiles, four keys per group so that every copy instruction
+//               uses all 32 lanes; the row's Q (q_idx) tile alongside its first chunk
 // Every wait is bounded (the library's 2 s limit); a wait that runs out sets the
 // CTA's abort flag and the error word, and every role then leaves its loops.
 
@@ -50,10 +53,11 @@ namespace dsa {
 namespace {
 
 constexpr int kNK = 128;                 // keys per chunk (UMMA M)
-constexpr int kGatherWarp0 = 5;
 constexpr int kGatherWarps = 4;
 constexpr int kGatherThreads = 32 * kGatherWarps;
-constexpr int kThreads = 288;
+// forward: 8 epilogue warps, the issuer, 4 gather warps; backward: 4, 1, 4
+constexpr int kFwdIssuer = 8, kFwdGather0 = 9, kFwdThreads = 416;
+constexpr int kBwdIssuer = 4, kBwdGather0 = 5, kBwdThreads = 288;
 constexpr uint32_t kAtom = kNK * 128;    // [128 rows x 128 B] swizzle atom
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -70,8 +74,9 @@ __device__ __forceinline__ void bar_gather() {
 // thread 0 samples the abort flag before the barrier and everyone reads that one
 // sample after it (two slots, so that a fast thread 0 cannot overwrite a verdict
 // a slow thread has yet to read).
+template <int W0>
 __device__ __forceinline__ bool bar_gather_ok(int* okb, int& nb, volatile int* abort_flag) {
-  if (threadIdx.x == 32 * kGatherWarp0) okb[nb & 1] = (*abort_flag == 0);
+  if (threadIdx.x == 32 * W0) okb[nb & 1] = (*abort_flag == 0);
   bar_gather();
   const bool ok = reinterpret_cast<volatile int*>(okb)[nb & 1] != 0;
   ++nb;
@@ -110,19 +115,27 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
 // The gather threads' index list pass: one past the last slot that holds a key the
 // row may attend to (0 <= s <= t), agreed by all gather threads. Returns false when
 // the CTA is aborting.
+template <int W0>
 __device__ __forceinline__ bool row_kend(const int32_t* irow, int k, int t, int S, int gt,
                                          int lane, int gw, int* red, int* okb, int& nb,
                                          volatile int* abort_flag, int& kend) {
   int last = 0;
-#pragma unroll 4
-  for (int j = gt; j < k; j += kGatherThreads) {
-    const int s = __ldg(irow + j);
-    if (s >= 0 && s <= t && s < S) last = j + 1;
+#pragma unroll 1
+  for (int j0 = gt; j0 < k; j0 += 16 * kGatherThreads) {
+    int sv[16];   // sixteen loads in flight per thread
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int j = j0 + u * kGatherThreads;
+      sv[u] = j < k ? __ldg(irow + j) : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u)
+      if (sv[u] >= 0 && sv[u] <= t && sv[u] < S) last = j0 + u * kGatherThreads + 1;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
   if (lane == 0) red[gw] = last;
-  if (!bar_gather_ok(okb, nb, abort_flag)) return false;
+  if (!bar_gather_ok<W0>(okb, nb, abort_flag)) return false;
   kend = 0;
 #pragma unroll
   for (int w2 = 0; w2 < kGatherWarps; ++w2) kend = max(kend, red[w2]);
@@ -178,6 +191,7 @@ struct LossFwdParams {
 };
 
 constexpr int kFwdStages = 2;
+constexpr int kFwdKeepChunks = 16;   // chunks whose scores the epilogue keeps from its pre-pass
 
 template <int DQK>
 struct LossFwdLayout {
@@ -193,6 +207,7 @@ struct LossFwdTail {
   __align__(16) int key[kFwdStages][kNK];   // read as int4 by gather_rows
   uint64_t kv_full[kFwdStages], kv_empty[kFwdStages];
   uint64_t s_full[kFwdStages], s_empty[kFwdStages];
+  uint64_t e_full[kFwdStages];
   uint64_t q_empty[2];
   uint64_t lz_bar;
   uint64_t drain;
@@ -201,12 +216,16 @@ struct LossFwdTail {
   int okb[2];
   int red[kGatherWarps];
   __align__(16) float lse2[2][128];   // the row's LSE in log2 units, by row parity
-  float lzm[2][4], lzl[2][4];         // per-warp partial log-sum-exp of the scores
-  int lzk[2][4];                      // per-warp partial kend
+  float lzm[2][8], lzl[2][8];         // per-warp partial log-sum-exp of the scores
+  int lzk[2][8];                      // per-warp partial kend
+  float ebuf[kFwdStages][128];        // the upper epilogue warps' partial head sums
+  float sv[2][kFwdKeepChunks * 128];  // by row parity: the score (log2 units) at slot j of
+                                      // the row's first kFwdKeepChunks chunks, NaN where
+                                      // the slot holds no selected key
 };
 
 template <int DQK>
-__global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdParams p) {
+__global__ void __launch_bounds__(kFwdThreads, 1) loss_fwd_kernel(const LossFwdParams p) {
   using L = LossFwdLayout<DQK>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if ((smem_u32(smem) & 1023u) != 0) {
@@ -225,16 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
       mbar_init(&tail->kv_full[i], 2 * kGatherThreads);
       mbar_init(&tail->kv_empty[i], 1);
       mbar_init(&tail->s_full[i], 1);
-      mbar_init(&tail->s_empty[i], 128);
+      mbar_init(&tail->s_empty[i], 256);   // both epilogue warps of each lane quarter
+      mbar_init(&tail->e_full[i], 128);    // the upper epilogue warps
     }
     mbar_init(&tail->q_empty[0], 1);
     mbar_init(&tail->q_empty[1], 1);
-    mbar_init(&tail->lz_bar, 4);
+    mbar_init(&tail->lz_bar, 8);
     mbar_init(&tail->drain, 1);
     tail->abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 4) {
+  if (warp == kFwdIssuer) {
     tmem_alloc(&tail->tmem_base, 256);
     tmem_relinquish();
   }
@@ -243,10 +263,10 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
   tc_fence_after();
   const uint32_t tmem = tail->tmem_base;
 
-  if (warp >= kGatherWarp0) {
+  if (warp >= kFwdGather0) {
     // ================================================================ gather
-    const int gt = threadIdx.x - 32 * kGatherWarp0;
-    const int gw = warp - kGatherWarp0;
+    const int gt = threadIdx.x - 32 * kFwdGather0;
+    const int gw = warp - kFwdGather0;
     constexpr int PQ = DQK / 8;
     int g = 0, nb = 0, ri = 0;
     for (int i = blockIdx.x; i < nrows; i += gridDim.x, ++ri) {
@@ -255,13 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
       const int t = static_cast<int>(row - static_cast<long long>(b) * p.S);
       const int32_t* irow = p.idx + row * p.k;
       int kend = 0;
-      if (!row_kend(irow, p.k, t, p.S, gt, lane, gw, tail->red, tail->okb, nb, abort_flag, kend))
+      if (!row_kend<kFwdGather0>(irow, p.k, t, p.S, gt, lane, gw, tail->red, tail->okb, nb, abort_flag, kend))
         break;
       const int nch = kend > 0 ? (kend + kNK - 1) / kNK : 1;
       // the row's Q tile, once the MMAs of the row two back have read the buffer
       const int qb = ri & 1;
       mbar_wait(&tail->q_empty[qb], ((ri >> 1) & 1) ^ 1u, abort_flag, p.err, kErrFwd);
-      if (!bar_gather_ok(tail->okb, nb, abort_flag)) break;
+      if (!bar_gather_ok<kFwdGather0>(tail->okb, nb, abort_flag)) break;
       const uint32_t qbuf = smem_u32(smem + L::kQOff + qb * L::kQBuf);
       const __nv_bfloat16* qsrc = p.Q + row * p.H * DQK;
 #pragma unroll 2
@@ -281,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
           tail->first[st] = c == 0;
           tail->last[st] = c == nch - 1;
         }
-        if (!bar_gather_ok(tail->okb, nb, abort_flag)) { stop = true; break; }
+        if (!bar_gather_ok<kFwdGather0>(tail->okb, nb, abort_flag)) { stop = true; break; }
         mbar_arrive(&tail->kv_full[st]);   // releases the header writes
         gather_rows<DQK>(smem_u32(smem + st * L::kStage), tail->key[st],
                          p.K + static_cast<long long>(b) * p.S * DQK, gw, lane);
@@ -292,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
       if (stop) break;
     }
     cp_async_wait<0>();
-  } else if (warp == 4) {
+  } else if (warp == kFwdIssuer) {
     // ================================================================ UMMA issuer
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(128, Hp, false, false);
@@ -330,8 +350,12 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
     }
   } else {
     // ================================================================ epilogue
-    const int tid = threadIdx.x;                 // key slot of a chunk; TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    // Warps w and w + 4 share TMEM lane quarter w % 4: the lower warp sums the heads of
+    // the even 32-column blocks, the upper warp those of the odd blocks and hands its
+    // partial sum over through ebuf; the lower warp finishes the slot (dI, the loss).
+    const bool upper = warp >= 4;
+    const int tid = threadIdx.x & 127;           // key slot of a chunk; TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const int H = p.H;
     const float invH = 1.f / static_cast<float>(H);
     int g = 0, ri = 0;
@@ -343,18 +367,41 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
       const int32_t* irow = p.idx + row * p.k;
       const float* srow = p.scores + row * p.ld;
       (void)b;
-      // the row's LSE (log2 units) and the log-sum-exp of its selected index scores
-      if (tid < H) tail->lse2[par][tid] = __ldg(p.lse + row * H + tid) * kLog2e;
+      // the row's LSE (log2 units) and the log-sum-exp of its selected index scores:
+      // the 256 epilogue threads read slots j = e + 256 u (sixteen loads in flight per
+      // thread) and keep the scores of the first kFwdKeepChunks chunks in sv[par]
+      const int et = threadIdx.x;   // 0..255
+      if (et < H) tail->lse2[par][et] = __ldg(p.lse + row * H + et) * kLog2e;
       float m = -INFINITY, l = 0.f;
       int kl_end = 0;
-#pragma unroll 2
-      for (int j = tid; j < p.k; j += 128) {
-        const int s = __ldg(irow + j);
-        if (s < -1 || s >= p.S) {
-          report_error(p.err, DSA_STAGE_LOSS | DSA_DEVERR_BAD_INDEX);
-        } else if (s >= 0 && s <= t) {
+      float* svr = tail->sv[par];
+#pragma unroll 1
+      for (int j0 = et; j0 < p.k; j0 += 16 * 256) {
+        int sk[16];
+        float vv[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int j = j0 + u * 256;
+          sk[u] = j < p.k ? __ldg(irow + j) : -1;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int s = sk[u];
+          if (s < -1 || s >= p.S) {
+            report_error(p.err, DSA_STAGE_LOSS | DSA_DEVERR_BAD_INDEX);
+            sk[u] = -1;
+          } else if (s > t) {
+            sk[u] = -1;
+          }
+          vv[u] = sk[u] >= 0 ? __ldg(srow + sk[u]) * kLog2e : 0.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+          const int j = j0 + u * 256;
+          if (j < kFwdKeepChunks * 128) svr[j] = sk[u] >= 0 ? vv[u] : __int_as_float(0x7fc00000);
+          if (sk[u] < 0) continue;
           kl_end = j + 1;
-          const float v = __ldg(srow + s) * kLog2e;
+          const float v = vv[u];
           if (v > m) {
             l = l * ex2(m - v) + 1.f;
             m = v;
@@ -363,6 +410,8 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
           }
         }
       }
+      // slots of the kept chunks past k read as "no key"
+      for (int j = p.k + et; j < kFwdKeepChunks * 128; j += 256) svr[j] = __int_as_float(0x7fc00000);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float om = __shfl_xor_sync(0xffffffffu, m, o);
@@ -372,6 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
         l = (m > -INFINITY ? l * ex2(m - mm) : 0.f) + (om > -INFINITY ? ol * ex2(om - mm) : 0.f);
         m = mm;
       }
+      // every epilogue warp arrives, so that no warp starts row ri + 2, and rewrites this
+      // row's slots, before all have left row ri
       __syncwarp();
       if (lane == 0) {
         tail->lzm[par][warp] = m;
@@ -384,13 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
       float M = -INFINITY;
       int kend = 0;
 #pragma unroll
-      for (int w2 = 0; w2 < 4; ++w2) {
+      for (int w2 = 0; w2 < 8; ++w2) {
         M = fmaxf(M, tail->lzm[par][w2]);
         kend = max(kend, tail->lzk[par][w2]);
       }
       float Lsum = 0.f;
 #pragma unroll
-      for (int w2 = 0; w2 < 4; ++w2) {
+      for (int w2 = 0; w2 < 8; ++w2) {
         const float mw = tail->lzm[par][w2];
         if (mw > -INFINITY) Lsum += tail->lzl[par][w2] * ex2(mw - M);
       }
@@ -408,12 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
           break;
         }
         tc_fence_after();
-        const int j = c * kNK + tid;
-        const int s = slot_key(irow, j, kend, t, p.S);
-        // sum over heads of exp2(S * c2 - LSE2[h])
+        // sum over this warp's heads of exp2(S * c2 - LSE2[h])
         float e = 0.f;
 #pragma unroll 1
-        for (int cb = 0; cb < Hp; cb += 32) {
+        for (int cb = upper ? 32 : 0; cb < Hp; cb += 64) {
           uint32_t v[32];
           tmem_ld_x32(tmem + lane_off + st * 128 + cb, v);
           tmem_ld_wait();
@@ -432,13 +481,40 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
             }
           }
         }
+        if (upper) {
+          tail->ebuf[st][tid] = e;
+          tc_fence_before();
+          mbar_arrive(&tail->e_full[st]);
+          mbar_arrive(&tail->s_empty[st]);
+          continue;
+        }
+        // the partner's half; the TMEM buffer (and with it ebuf[st]) is released only
+        // after it has been read
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&tail->e_full[st], ph, abort_flag, p.err, kErrFwd))) {
+          ok = false;
+          break;
+        }
+        e += tail->ebuf[st][tid];
         tc_fence_before();
         mbar_arrive(&tail->s_empty[st]);
+        const int j = c * kNK + tid;
+        // this slot's key and score: from the pre-pass, or read again past its reach
+        bool valid;
+        float v2 = 0.f;
+        if (c < kFwdKeepChunks) {
+          v2 = svr[j];
+          valid = !isnan(v2);
+        } else {
+          const int s = slot_key(irow, j, kend, t, p.S);
+          valid = s >= 0;
+          if (valid) v2 = __ldg(srow + s) * kLog2e;
+        }
         if (j < p.k) {
           float d = 0.f;
-          if (s >= 0) {
+          if (valid) {
             const float pbar = e * invH;
-            const float lq2 = __ldg(srow + s) * kLog2e - logz2;   // log2 of the student
+            const float lq2 = v2 - logz2;   // log2 of the student
             d = p.grad_scale * (ex2(lq2) - pbar);
             if (pbar > 0.f) kl_acc += pbar * (log2f(pbar) - lq2);
           }
@@ -446,17 +522,19 @@ __global__ void __launch_bounds__(kThreads, 1) loss_fwd_kernel(const LossFwdPara
         }
       }
       if (!ok) break;
-      for (int j = nch * kNK + tid; j < p.k; j += 128) p.dI[row * p.k + j] = 0.f;
+      if (!upper) {
+        for (int j = nch * kNK + tid; j < p.k; j += 128) p.dI[row * p.k + j] = 0.f;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) kl_acc += __shfl_xor_sync(0xffffffffu, kl_acc, o);
-      if (lane == 0 && kl_acc != 0.f) atomicAdd(p.kl + row, kl_acc * kLn2);
+        for (int o = 16; o > 0; o >>= 1) kl_acc += __shfl_xor_sync(0xffffffffu, kl_acc, o);
+        if (lane == 0 && kl_acc != 0.f) atomicAdd(p.kl + row, kl_acc * kLn2);
+      }
     }
   }
 
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, 256);
+  if (warp == kFwdIssuer) tmem_dealloc(tmem, 256);
 }
 
 // ==================================================================== backward
@@ -499,7 +577,8 @@ struct LossBwdLayout {
   static constexpr uint32_t kQBuf = (DI / 64) * kQAtom;
   static constexpr uint32_t kGOff = kQOff + 2 * kQBuf;         // G tiles [128 keys x HI] bf16
   static constexpr uint32_t kGBuf = (HI / 64) * kAtom;
-  static constexpr uint32_t kTailOff = kGOff + 2 * kGBuf;
+  static constexpr uint32_t kXOff = kGOff + 2 * kGBuf;          // dk transpose, 4 KB per warp
+  static constexpr uint32_t kTailOff = kXOff + 4 * 4096;
   // TMEM columns
   static constexpr uint32_t kColZ = 0;              // 2 x HI
   static constexpr uint32_t kColDk = 2 * HI;        // 2 x DI
@@ -529,7 +608,7 @@ struct LossBwdTail {
 };
 
 template <int HI, int DI>
-__global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdParams p) {
+__global__ void __launch_bounds__(kBwdThreads, 1) loss_bwd_kernel(const LossBwdParams p) {
   using L = LossBwdLayout<HI, DI>;
   using Tail = LossBwdTail<HI>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -564,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < 2 * HI; i += blockDim.x) (&tail->dw_acc[0][0])[i] = 0.f;
-  if (warp == 4) {
+  if (warp == kBwdIssuer) {
     tmem_alloc(&tail->tmem_base, 512);
     tmem_relinquish();
   }
@@ -573,10 +652,10 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
   tc_fence_after();
   const uint32_t tmem = tail->tmem_base;
 
-  if (warp >= kGatherWarp0) {
+  if (warp >= kBwdGather0) {
     // ================================================================ gather
-    const int gt = threadIdx.x - 32 * kGatherWarp0;
-    const int gw = warp - kGatherWarp0;
+    const int gt = threadIdx.x - 32 * kBwdGather0;
+    const int gw = warp - kBwdGather0;
     constexpr int PQ = DI / 8;
     int g = 0, nb = 0, ri = 0;
     for (int i = blockIdx.x; i < nrows; i += gridDim.x, ++ri) {
@@ -585,12 +664,12 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
       const int t = static_cast<int>(row - static_cast<long long>(b) * p.S);
       const int32_t* irow = p.idx + row * p.k;
       int kend = 0;
-      if (!row_kend(irow, p.k, t, p.S, gt, lane, gw, tail->red, tail->okb, nb, abort_flag, kend))
+      if (!row_kend<kBwdGather0>(irow, p.k, t, p.S, gt, lane, gw, tail->red, tail->okb, nb, abort_flag, kend))
         break;
       const int nch = kend > 0 ? (kend + kNK - 1) / kNK : 1;
       const int qb = ri & 1;
       mbar_wait(&tail->q_empty[qb], ((ri >> 1) & 1) ^ 1u, abort_flag, p.err, kErrBwd);
-      if (!bar_gather_ok(tail->okb, nb, abort_flag)) break;
+      if (!bar_gather_ok<kBwdGather0>(tail->okb, nb, abort_flag)) break;
       // q_idx[t] as [DI/64 atoms][HI rows][128 B] and w[t, :]
       const uint32_t qbuf = smem_u32(smem + L::kQOff + qb * L::kQBuf);
       const __nv_bfloat16* qsrc = p.q + row * HI * DI;
@@ -602,11 +681,20 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
       }
       if (gt < HI) tail->wrow[qb][gt] = __ldg(p.w + row * HI + gt);
       bool stop = false;
+      // this slot's key and dI one chunk ahead (two independent loads), so that their
+      // latency overlaps the previous chunk's wait and copies
+      const float* drow = p.dI + row * p.k;
+      int s_next = slot_key(irow, gt, kend, t, p.S);
+      float dv_next = gt < p.k ? __ldg(drow + gt) : 0.f;
       for (int c = 0; c < nch; ++c, ++g) {
         const int st = g % kBwdStages;
-        const int j = c * kNK + gt;
-        const int s = slot_key(irow, j, kend, t, p.S);
-        const float dv = s >= 0 ? __ldg(p.dI + row * p.k + j) : 0.f;
+        const int s = s_next;
+        const float dv = s >= 0 ? dv_next : 0.f;
+        if (c + 1 < nch) {
+          const int jn = (c + 1) * kNK + gt;
+          s_next = slot_key(irow, jn, kend, t, p.S);
+          dv_next = jn < p.k ? __ldg(drow + jn) : 0.f;
+        }
         mbar_wait(&tail->kv_empty[st], ((g / kBwdStages) & 1) ^ 1u, abort_flag, p.err, kErrBwd);
         tail->key[st][gt] = s;
         tail->dval[st][gt] = dv;
@@ -614,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
           tail->first[st] = c == 0;
           tail->last[st] = c == nch - 1;
         }
-        if (!bar_gather_ok(tail->okb, nb, abort_flag)) { stop = true; break; }
+        if (!bar_gather_ok<kBwdGather0>(tail->okb, nb, abort_flag)) { stop = true; break; }
         mbar_arrive(&tail->kv_full[st]);   // releases the header (and w row) writes
         gather_rows<DI>(smem_u32(smem + st * L::kStage), tail->key[st],
                         p.kx + static_cast<long long>(b) * p.S * DI, gw, lane);
@@ -623,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
       if (stop) break;
     }
     cp_async_wait<0>();
-  } else if (warp == 4) {
+  } else if (warp == kBwdIssuer) {
     // ================================================================ UMMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_z = idesc_bf16(128, HI, false, false);    // Z^T = K . q^T
@@ -721,7 +809,10 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     int g = 0, ri = 0;
     bool ok = true;
-    // dk rows of chunk gp: thread tid adds its key's row into dk
+    // dk rows of chunk gp. Each thread holds its key's row in TMEM; the warp passes 32
+    // columns of its 32 keys through a swizzled shared tile so that each quarter-warp adds
+    // one key's 128 contiguous bytes per reduction instruction.
+    const uint32_t xt = smem_u32(smem + L::kXOff) + warp * 4096;
     auto drain_dk = [&](int gp, int s, float d, long long kvbase) -> bool {
       const int db = gp & 1;
       if (!__all_sync(0xffffffffu, mbar_wait(&tail->dk_full[db], (gp >> 1) & 1, abort_flag,
@@ -729,18 +820,32 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
         return false;
       tc_fence_after();
       const bool add = s >= 0 && d != 0.f;
-      float* dst = p.dk + (kvbase + (s >= 0 ? s : 0)) * DI;
+      const int sub = lane >> 3, pc = lane & 7;
 #pragma unroll 1
       for (int c0 = 0; c0 < DI; c0 += 32) {
         uint32_t v[32];
         tmem_ld_x32(tmem + lane_off + L::kColDk + db * DI + c0, v);
         tmem_ld_wait();
-        if (add) {
+        __syncwarp();
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
-            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + c0 + e),
-                         "f"(__uint_as_float(v[e])), "f"(__uint_as_float(v[e + 1])),
-                         "f"(__uint_as_float(v[e + 2])), "f"(__uint_as_float(v[e + 3]))
+        for (int c = 0; c < 8; ++c)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                           xt + lane * 128 + ((c ^ (lane & 7)) << 4)),
+                       "r"(v[4 * c]), "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
+                       : "memory");
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int kr = 4 * i + sub;   // key row of this quarter-warp
+          const int sk = __shfl_sync(0xffffffffu, add ? s : -1, kr);
+          float4 x;
+          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                       : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                       : "r"(xt + kr * 128 + ((pc ^ (kr & 7)) << 4)));
+          if (sk >= 0) {
+            float* dst = p.dk + (kvbase + sk) * DI + c0 + pc * 4;
+            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x.x),
+                         "f"(x.y), "f"(x.z), "f"(x.w)
                          : "memory");
           }
         }
@@ -869,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1) loss_bwd_kernel(const LossBwdPara
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) tmem_dealloc(tmem, 512);
+  if (warp == kBwdIssuer) tmem_dealloc(tmem, 512);
 }
 
 int sm_count() {
@@ -889,7 +994,7 @@ int launch_fwd(const LossFwdParams& p, cudaStream_t stream) {
     return DSA_ERR_CUDA;
   const long long rows = static_cast<long long>(p.B) * p.S;
   const int sms = sm_count();
-  kern<<<static_cast<int>(rows < sms ? rows : sms), kThreads, smem, stream>>>(p);
+  kern<<<static_cast<int>(rows < sms ? rows : sms), kFwdThreads, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -903,7 +1008,7 @@ int launch_bwd(const LossBwdParams& p, cudaStream_t stream) {
     return DSA_ERR_CUDA;
   const long long rows = static_cast<long long>(p.B) * p.S;
   const int sms = sm_count();
-  kern<<<static_cast<int>(rows < sms ? rows : sms), kThreads, smem, stream>>>(p);
+  kern<<<static_cast<int>(rows < sms ? rows : sms), kBwdThreads, smem, stream>>>(p);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -76,7 +76,9 @@ def test_attention_validation(dsa):
     # B, S, H, Hkv, Dqk, Dv, k
     assert fwd(P, P, P, P, 1, 64, 16, 1, 192, 128, 8, 0.1, None, P, None) == 1   # null O
     assert fwd(P, P, P, P, 1, 64, 16, 3, 192, 128, 8, 0.1, P, P, None) == 1      # H % Hkv
-    assert fwd(P, P, P, P, 1, 64, 16, 16, 192, 128, 8, 0.1, P, P, None) == 2     # Hkv = H
+    # per-head K / V runs on the dense-tile kernels only, which take (192, 128) / (128, 128)
+    assert fwd(P, P, P, P, 1, 64, 16, 16, 64, 64, 8, 0.1, P, P, None) == 2       # Hkv = H, 64
+    assert fwd(P, P, P, P, 1, 70000, 16, 16, 192, 128, 8, 0.1, P, P, None) == 2  # Hkv = H, S
     assert fwd(P, P, P, P, 1, 64, 256, 1, 192, 128, 8, 0.1, P, P, None) == 2     # H > 128
     assert fwd(P, P, P, P, 1, 64, 16, 1, 96, 128, 8, 0.1, P, P, None) == 2       # dims
     assert fwd(P, P, P, P, 1, 64, 16, 1, 100, 128, 8, 0.1, P, P, None) == 1      # Dqk % 16

@@ -457,7 +457,8 @@ def test_bwd_kernel_choice():
 
 def test_fwd_kernel_choice():
     """The automatic forward picks the dense-tile kernel for few heads and many selected keys,
-    the gathered-key kernel for 128 heads, mma.sync for small head dims; it refuses Hkv > 1."""
+    the gathered-key kernel for 128 heads, mma.sync for small head dims; Hkv > 1 always
+    takes the dense-tile kernel, and is refused where that kernel does not apply."""
     dsa = _dsa()
     sc = 1.0 / np.sqrt(192)
     assert dsa.dsa_sparse_attn_fwd_kernel(2, 4096, 16, 1, 192, 128, 2048, sc) == dsa.DSA_FWD_DENSE_TC
@@ -467,8 +468,9 @@ def test_fwd_kernel_choice():
     assert dsa.dsa_sparse_attn_fwd_kernel(1, 489, 16, 1, 192, 128, 512, sc) == \
         dsa.DSA_FWD_GATHER_TC   # too few work items to fill the GPU
     assert dsa.dsa_sparse_attn_fwd_kernel(1, 128, 2, 1, 32, 32, 4, 0.2) == dsa.DSA_FWD_MMA_SYNC
+    assert dsa.dsa_sparse_attn_fwd_kernel(1, 128, 2, 2, 192, 128, 4, 0.2) == dsa.DSA_FWD_DENSE_TC
     with pytest.raises(dsa.DsaError):
-        dsa.dsa_sparse_attn_fwd_kernel(1, 128, 2, 2, 192, 128, 4, 0.2)
+        dsa.dsa_sparse_attn_fwd_kernel(1, 128, 2, 2, 32, 32, 4, 0.2)
 
 
 def test_dense_fwd_bad_index_and_unsupported():
@@ -504,3 +506,100 @@ def test_bad_index_is_reported_not_faulted():
     idx_ok[0, 30, 0] = -1
     O_ref, _ = oracle.attn_fwd(Q, K, V, idx_ok, 0.125)
     assert rel_err(host_f64(O).reshape(O_ref.shape), O_ref) <= TOL
+
+
+# ------------------------------------- per-head and grouped K / V (Hkv > 1)
+
+HKV_CASES = [
+    # B, S, H, Hkv, Dqk, Dv, k, ndocs
+    (1, 300, 16, 16, 192, 128, 64, 0),     # one K / V head per query head
+    (2, 200, 8, 2, 192, 128, 100, 0),      # groups of four heads
+    (1, 260, 4, 4, 128, 128, 300, 0),      # k >= S: every causal key
+    (1, 489, 16, 4, 192, 128, 512, 3),     # packed documents, ragged last tile
+    (1, 129, 2, 2, 192, 128, 64, 0),
+    (1, 200, 128, 128, 192, 128, 100, 0),  # 128 heads, each with its own K / V
+]
+
+
+def _hkv_case(B, S, H, Hkv, Dqk, Dv, k, ndocs, seed):
+    Q = synth.normal_bf16((B, S, H, Dqk), seed, synth.STREAM_Q)
+    K = synth.normal_bf16((B, S, Hkv, Dqk), seed, synth.STREAM_K)
+    V = synth.normal_bf16((B, S, Hkv, Dv), seed, synth.STREAM_V)
+    dO = synth.normal_bf16((B, S, H, Dv), seed, synth.STREAM_DO)
+    ind = _indexer_case(B, S, 4, 32, seed, ndocs=ndocs)
+    sc = oracle.index_scores(ind["q_idx"], ind["k_idx"], ind["w"], ind["seg"])
+    idx, _ = oracle.topk(sc, ind["seg"], S, k, B=B)
+    return Q, K, V, dO, idx.reshape(B, S, k)
+
+
+@pytest.mark.parametrize("case", HKV_CASES)
+def test_per_head_kv_fwd_bwd(case):
+    dsa = _dsa()
+    B, S, H, Hkv, Dqk, Dv, k, ndocs = case
+    Q, K, V, dO, idx = _hkv_case(*case, seed=900 + S + H + Hkv)
+    scale = 1.0 / np.sqrt(Dqk)
+    assert dsa.dsa_sparse_attn_fwd_kernel(B, S, H, Hkv, Dqk, Dv, k, scale) == dsa.DSA_FWD_DENSE_TC
+    assert dsa.dsa_sparse_attn_bwd_kernel(B, S, H, Hkv, Dqk, Dv, k, scale) == dsa.DSA_BWD_DENSE_TC
+    Qd, Kd, Vd, dOd, idxd = bf16_dev(Q), bf16_dev(K), bf16_dev(V), bf16_dev(dO), dev(idx)
+    O, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, idxd, scale)
+    dQ, dK, dV = dsa.dsa_sparse_attn_bwd(Qd, Kd, Vd, idxd, O, lse, dOd, scale)
+    assert dsa.dsa_get_last_device_error() == 0
+    O_ref, lse_ref = oracle.attn_fwd(Q, K, V, idx, scale)
+    assert rel_err(host_f64(O).reshape(O_ref.shape), O_ref) <= TOL
+    assert rel_err(host_f64(lse).reshape(lse_ref.shape), lse_ref) <= TOL
+    dQ_ref, dK_ref, dV_ref = oracle.attn_bwd(Q, K, V, idx, dO, scale)
+    assert rel_err(host_f64(dQ).reshape(dQ_ref.shape), dQ_ref) <= TOL
+    assert rel_err(host_f64(dK), dK_ref) <= TOL
+    assert rel_err(host_f64(dV), dV_ref) <= TOL
+    # each K / V head's gradient on its own (a mix-up of heads would hide in the max norm)
+    for g in range(Hkv):
+        assert rel_err(host_f64(dK)[:, :, g], dK_ref[:, :, g]) <= TOL
+        assert rel_err(host_f64(dV)[:, :, g], dV_ref[:, :, g]) <= TOL
+
+
+def test_per_head_kv_user_lists():
+    """-1 holes, entries above the diagonal and empty rows with Hkv = H."""
+    dsa = _dsa()
+    B, S, H, Hkv, Dqk, Dv, k = 1, 150, 8, 8, 192, 128, 60
+    Q, K, V, dO, _ = _hkv_case(B, S, H, Hkv, Dqk, Dv, 8, 0, seed=77)
+    rng = np.random.default_rng(19)
+    idx = np.full((B, S, k), -1, dtype=np.int32)
+    for t in range(S):
+        if t % 13 == 5:
+            continue
+        pick = rng.choice(S, size=k, replace=False).astype(np.int32)
+        pick[rng.random(k) < 0.25] = -1
+        idx[0, t] = pick
+    scale = 0.09
+    Qd, Kd, Vd, dOd, idxd = bf16_dev(Q), bf16_dev(K), bf16_dev(V), bf16_dev(dO), dev(idx)
+    O, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, idxd, scale)
+    dQ, dK, dV = dsa.dsa_sparse_attn_bwd(Qd, Kd, Vd, idxd, O, lse, dOd, scale)
+    assert dsa.dsa_get_last_device_error() == 0
+    O_ref, lse_ref = oracle.attn_fwd(Q, K, V, idx, scale)
+    assert rel_err(host_f64(O).reshape(O_ref.shape), O_ref) <= TOL
+    lg = host_f64(lse).reshape(lse_ref.shape)
+    assert np.array_equal(np.isneginf(lg), np.isneginf(lse_ref))
+    dQ_ref, dK_ref, dV_ref = oracle.attn_bwd(Q, K, V, idx, dO, scale)
+    assert rel_err(host_f64(dQ).reshape(dQ_ref.shape), dQ_ref) <= TOL
+    assert rel_err(host_f64(dK), dK_ref) <= TOL
+    assert rel_err(host_f64(dV), dV_ref) <= TOL
+
+
+def test_per_head_kv_unsupported_forms():
+    """Hkv > 1 needs the dense-tile kernels: other dims, the no-allocation backward and a
+    head count that Hkv does not divide are refused before anything runs."""
+    dsa = _dsa()
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_sparse_attn_fwd_kernel(1, 64, 4, 2, 64, 64, 8, 0.1)
+    assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_sparse_attn_bwd_kernel(1, 64, 6, 4, 192, 128, 8, 0.1)
+    assert e.value.status == dsa.DSA_ERR_INVALID_ARG
+    B, S, H, Hkv, Dqk, Dv, k = 1, 64, 4, 2, 192, 128, 8
+    Q, K, V, dO, idx = _hkv_case(B, S, H, Hkv, Dqk, Dv, k, 0, seed=5)
+    Qd, Kd, Vd, dOd, idxd = bf16_dev(Q), bf16_dev(K), bf16_dev(V), bf16_dev(dO), dev(idx)
+    O, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, idxd, 0.1)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.dsa_sparse_attn_bwd_noalloc(Qd, Kd, Vd, idxd, O, lse, dOd, 0.1)
+    assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
+    assert dsa.dsa_get_last_device_error() == 0
