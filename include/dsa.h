@@ -163,8 +163,14 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* seg, int B, 
  *   Q    bf16 [B, S, H, Dqk]     K  bf16 [B, S, Hkv, Dqk]    V  bf16 [B, S, Hkv, Dv]
  *   idx  int32 [B, S, k]         O  bf16 [B, S, H, Dv] out   lse fp32 [B, S, H] out
  *
- * Supported: Hkv = 1 (one K/V row shared by every head), 1 <= H <= 128,
- * (Dqk, Dv) in {(32, 32), (64, 64), (128, 128), (192, 128)}.
+ * Supported: 1 <= H <= 128 and
+ *  - Hkv = 1 (one K/V row shared by every head, the form the indexer's
+ *    selection is built for): (Dqk, Dv) in {(32, 32), (64, 64), (128, 128),
+ *    (192, 128)};
+ *  - Hkv > 1 dividing H (per-head K/V, Hkv = H, or groups of H / Hkv heads;
+ *    head h reads K/V head h / (H / Hkv)): the dense-tile kernel only, so
+ *    (Dqk, Dv) in {(128, 128), (192, 128)}, S <= 65536 and a positive scale;
+ *    DSA_ERR_UNSUPPORTED otherwise.
  *
  * Two tensor-core kernels compute it. One gathers each query's selected K/V
  * rows and puts the heads on the 128 lanes of a tile. The other evaluates dense
@@ -196,8 +202,8 @@ int dsa_sparse_attn_fwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, in
  * (the pages' own design evaluates the masked logits as dense blocks with
  * partial mask blocks: "Support Ring Attention with DeepSeek DSA Sparse
  * Indexer", Forward Flow). Arguments as for dsa_sparse_attn_fwd. Supported:
- * Hkv = 1, 1 <= H <= 128, (Dqk, Dv) in {(128, 128), (192, 128)}, S <= 65536, a
- * positive scale; DSA_ERR_UNSUPPORTED otherwise.
+ * any Hkv dividing H, 1 <= H <= 128, (Dqk, Dv) in {(128, 128), (192, 128)},
+ * S <= 65536, a positive scale; DSA_ERR_UNSUPPORTED otherwise.
  */
 int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
                               int B, int S, int H, int Hkv, int Dqk, int Dv, int k, float scale,
@@ -235,10 +241,11 @@ int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32
  * for dK / dV, "Support Ring Attention with DeepSeek DSA Sparse Indexer",
  * Backward Flow). Arguments as for dsa_sparse_attn_bwd; the bitmap and Delta
  * (B*S*ceil(S/128)*16 + B*S*H*4 bytes) are allocated stream-ordered on `stream`.
- * Supported: Hkv = 1, 1 <= H <= 128, (Dqk, Dv) in {(128, 128), (192, 128)},
- * S <= 65536, a positive scale; DSA_ERR_UNSUPPORTED otherwise.
+ * Supported: any Hkv dividing H, 1 <= H <= 128, (Dqk, Dv) in {(128, 128),
+ * (192, 128)}, S <= 65536, a positive scale; DSA_ERR_UNSUPPORTED otherwise.
  * dsa_sparse_attn_bwd takes these kernels when they have fewer tile products for
- * the shape; dsa_sparse_attn_bwd_noalloc never does.
+ * the shape, and always for Hkv > 1; dsa_sparse_attn_bwd_noalloc never does (so
+ * it takes Hkv = 1 only).
  */
 int dsa_sparse_attn_bwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
                               const void* O, const float* lse, const void* dO, int B, int S, int H,
@@ -281,7 +288,8 @@ int dsa_sparse_attn_bwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, in
  *  - Every call shares the one array and zeroes the part it uses before
  *    accumulating, so calls whose work overlaps on the GPU (two streams, or
  *    two host threads) race and corrupt each other's dK/dV. Serialise them.
- *  - Arguments, supported shapes and results are those of dsa_sparse_attn_bwd.
+ *  - Arguments, supported shapes and results are those of dsa_sparse_attn_bwd
+ *    with Hkv = 1 (per-head K/V needs the dense-tile kernels, which allocate).
  */
 #define DSA_NOALLOC_BWD_MAX_FLOATS 8388608
 int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const void* V, const int32_t* idx,
