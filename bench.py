@@ -62,13 +62,19 @@ def pair_counts(wl: synth.Workload):
 
 
 def stage_work(wl: synth.Workload):
-    """Algorithmic work per step: FLOP for the contractions, bytes for top-k."""
+    """Algorithmic work per step: FLOP for the contractions, bytes for top-k.
+
+    The indexer loss: its forward is the target's logit product (H x Dqk per selected
+    pair); its backward the three products Z, dq and dk (Hi x Di each per selected pair).
+    """
     causal, sel = pair_counts(wl)
     return {
         "indexer": {"flop": 2.0 * wl.Hi * wl.Di * causal},
         "topk": {"bytes": 4.0 * causal + 4.0 * wl.topk * wl.B * wl.S},
         "attn_fwd": {"flop": 2.0 * wl.H * (wl.Dqk + wl.Dv) * sel},
         "attn_bwd": {"flop": 2.0 * wl.H * (3 * wl.Dqk + 2 * wl.Dv) * sel} if wl.backward else None,
+        "loss_fwd": {"flop": 2.0 * wl.H * wl.Dqk * sel},
+        "loss_bwd": {"flop": 3 * 2.0 * wl.Hi * wl.Di * sel},
     }
 
 
@@ -87,7 +93,8 @@ def load_peaks():
 def kernel_source_hash(stage: str) -> str:
     files = {"indexer": ["indexer.cu"], "topk": ["topk.cu"],
              "attn_fwd": ["attn_fwd.cu", "attn_fwd_tc.cu"],
-             "attn_bwd": ["attn_bwd.cu", "attn_bwd_tc.cu"]}[stage]
+             "attn_bwd": ["attn_bwd.cu", "attn_bwd_tc.cu"],
+             "loss_fwd": ["iloss.cu"], "loss_bwd": ["iloss.cu"]}[stage]
     h = hashlib.sha256()
     for f in files + ["dsa_common.cuh", "dsa_attn_common.cuh"]:
         with open(os.path.join(ROOT, "sparse_attention_index_gb300", "csrc", f), "rb") as fh:
@@ -231,19 +238,28 @@ def run_ours(args, wl, rank, world, local_rank):
         dQ = torch.empty_like(Q)
         dK = torch.empty_like(K)
         dV = torch.empty_like(V)
-        ws = torch.empty((dsa.bwd_workspace_bytes(B, S, wl.H, 1, wl.Dqk, wl.Dv),), dtype=torch.uint8,
+        ws = torch.empty((dsa.bwd_workspace_bytes(B, S, wl.H, wl.Hkv, wl.Dqk, wl.Dv),), dtype=torch.uint8,
                          device=device)
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device=device)
     stages = ["indexer", "topk", "attn_fwd"] + (["attn_bwd"] if wl.backward else [])
+    loss = args.indexer_loss
+    if loss:
+        # the indexer's auxiliary loss and its gradient into the indexer inputs
+        stages += ["loss_fwd", "loss_bwd"]
+        kl = torch.empty((B, S), dtype=torch.float32, device=device)
+        dI = torch.empty((B, S, k), dtype=torch.float32, device=device)
+        dq_idx = torch.empty((B, S, wl.Hi, wl.Di), dtype=torch.float32, device=device)
+        dk_idx = torch.empty((B, S, wl.Di), dtype=torch.float32, device=device)
+        dw = torch.empty((B, S, wl.Hi), dtype=torch.float32, device=device)
     # indexer, top-k, the forward (two launches on the dense-tile kernel: bitmap build +
     # attention), the backward and its finalize (four on the dense-tile kernels: bitmap,
     # dQ pass, dK / dV pass, finalize)
-    fwd_launches = 2 if dsa.dsa_sparse_attn_fwd_kernel(B, S, wl.H, 1, wl.Dqk, wl.Dv, k, wl.scale) \
+    fwd_launches = 2 if dsa.dsa_sparse_attn_fwd_kernel(B, S, wl.H, wl.Hkv, wl.Dqk, wl.Dv, k, wl.scale) \
         == dsa.DSA_FWD_DENSE_TC else 1
-    bwd_launches = (4 if dsa.dsa_sparse_attn_bwd_kernel(B, S, wl.H, 1, wl.Dqk, wl.Dv, k, wl.scale)
+    bwd_launches = (4 if dsa.dsa_sparse_attn_bwd_kernel(B, S, wl.H, wl.Hkv, wl.Dqk, wl.Dv, k, wl.scale)
                     == dsa.DSA_BWD_DENSE_TC else 2) if wl.backward else 0
-    launches_per_step = 2 + fwd_launches + bwd_launches
+    launches_per_step = 2 + fwd_launches + bwd_launches + (2 if loss else 0)
 
     def step(ev):
         ev[0].record(stream)
@@ -260,6 +276,14 @@ def run_ours(args, wl, rank, world, local_rank):
             dsa.dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, wl.scale, dQ=dQ, dK=dK, dV=dV, ws=ws,
                                     stream=stream)
             ev[4].record(stream)
+        if loss:
+            e = 5 if wl.backward else 4
+            dsa.dsa_indexer_loss(Q, K, idx, lse, scores, wl.scale, 1.0 / (B * S), kl=kl, dI=dI,
+                                 stream=stream)
+            ev[e].record(stream)
+            dsa.dsa_indexer_loss_bwd(q_idx, k_idx, w, idx, dI, dq_idx=dq_idx, dk_idx=dk_idx,
+                                     dw=dw, stream=stream)
+            ev[e + 1].record(stream)
 
     n_ev = len(stages) + 1
     with torch.cuda.stream(stream):
@@ -294,7 +318,9 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e = None
     if fp8 and not args.no_e2e:
         e2e = {"unavailable": "the host pipeline takes bf16 indexer inputs"}
-    if not args.no_e2e and not fp8:
+    if loss and not args.no_e2e:
+        e2e = {"unavailable": "the host pipeline runs the four stages without the indexer loss"}
+    if not args.no_e2e and not fp8 and not loss:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
         h_in = {"q_idx": pin(ind["q_idx"]), "k_idx": pin(ind["k_idx"]), "w": pin(ind["w"]),
                 "Q": pin(att["Q"]), "K": pin(att["K"]), "V": pin(att["V"])}
@@ -305,7 +331,8 @@ def run_ours(args, wl, rank, world, local_rank):
         # the public host-to-host API: copies in, the four stages and copies out on
         # three streams, overlapped (sparse_attention_index_gb300.HostPipeline)
         pipe = dsa.HostPipeline(B, S, wl.Hi, wl.Di, wl.H, wl.Dqk, wl.Dv, k, wl.scale,
-                                backward=wl.backward, segments=seg is not None, device=device)
+                                backward=wl.backward, segments=seg is not None, device=device,
+                                Hkv=wl.Hkv)
         h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in pipe.out.items()}
         h2d = sum(t.numel() * t.element_size() for t in h_in.values())
         d2h = sum(t.numel() * t.element_size() for t in h_out.values())
@@ -333,8 +360,9 @@ def run_ours(args, wl, rank, world, local_rank):
 
 # ------------------------------------------------------------------ CPU oracle
 
-def oracle_sample(wl, ind, att, rows):
-    """The oracle's full per-row work (scores, top-k, fwd, bwd) on the listed query rows."""
+def oracle_sample(wl, ind, att, rows, loss=False):
+    """The oracle's full per-row work (scores, top-k, fwd, bwd; with loss, the indexer loss
+    and its gradient) on the listed query rows."""
     import oracle
     S, k = wl.S, wl.topk
     sc = oracle.index_scores(ind["q_idx"], ind["k_idx"], ind["w"], ind["seg"], rows=rows)
@@ -345,6 +373,10 @@ def oracle_sample(wl, ind, att, rows):
     oracle.attn_fwd(att["Q"], att["K"], att["V"], idx, wl.scale, rows=rows)
     if wl.backward:
         oracle.attn_bwd(att["Q"], att["K"], att["V"], idx, att["dO"], wl.scale, rows=rows)
+    if loss:
+        _, dI = oracle.indexer_loss(att["Q"], att["K"], idx, sc, wl.scale, 1.0 / wl.tokens,
+                                    rows=rows)
+        oracle.indexer_loss_bwd(ind["q_idx"], ind["k_idx"], ind["w"], idx, dI, rows=rows)
 
 
 def sample_rows(wl, n, salt):
@@ -352,18 +384,19 @@ def sample_rows(wl, n, salt):
     return np.sort(rng.choice(wl.B * wl.S, size=min(n, wl.B * wl.S), replace=False)).astype(np.int64)
 
 
-def cpu_baseline(wl, n_rows):
+def cpu_baseline(wl, n_rows, loss=False):
     import oracle
     ind, att = make_inputs(wl)
     rows = sample_rows(wl, n_rows, 1)
     t0 = time.perf_counter()
-    oracle_sample(wl, ind, att, rows)
+    oracle_sample(wl, ind, att, rows, loss)
     dt = time.perf_counter() - t0
     return {"value": rows.size / dt, "unit": "tokens/s", "cores": oracle.default_threads(),
             "kind": "oracle", "seconds": dt,
             "sample": f"{rows.size} uniformly drawn query rows of {wl.name} (B*S={wl.tokens}); "
                       "each row gets its full indexer, top-k, forward"
-                      + (" and backward" if wl.backward else "") + " work; tokens/s = rows / s"}
+                      + (" and backward" if wl.backward else "")
+                      + (" and indexer-loss" if loss else "") + " work; tokens/s = rows / s"}
 
 
 def run_reference(args, wl, rank, world):
@@ -373,12 +406,12 @@ def run_reference(args, wl, rank, world):
     ind, att = make_inputs(wl)
     per_step = args.cpu_rows_per_step
     for i in range(args.warmup):
-        oracle_sample(wl, ind, att, sample_rows(wl, per_step, 100 + i))
+        oracle_sample(wl, ind, att, sample_rows(wl, per_step, 100 + i), args.indexer_loss)
     times = []
     for i in range(args.steps):
         rows = sample_rows(wl, per_step, 1000 + i)
         t0 = time.perf_counter()
-        oracle_sample(wl, ind, att, rows)
+        oracle_sample(wl, ind, att, rows, args.indexer_loss)
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = args.steps * per_step / total
@@ -386,7 +419,7 @@ def run_reference(args, wl, rank, world):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(wl),
+        "data": "synthetic", "config": workload_config(wl, args),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "kind": "oracle",
                          "cores": oracle.default_threads(),
                          "sample": f"each step: {per_step} uniformly drawn query rows of {wl.name}, "
@@ -399,12 +432,17 @@ def run_reference(args, wl, rank, world):
     return 0
 
 
-def workload_config(wl):
-    return {"workload": f"{wl.name}: {wl.description}", "B": wl.B, "S": wl.S,
-            "index_heads": wl.Hi, "index_head_dim": wl.Di, "index_topk": wl.topk,
-            "heads": wl.H, "kv_heads": 1, "qk_dim": wl.Dqk, "v_dim": wl.Dv,
-            "backward": wl.backward, "segments": wl.ndocs,
-            "l2": "flushed between steps (256 MiB write outside the timed events)"}
+def workload_config(wl, args=None):
+    cfg = {"workload": f"{wl.name}: {wl.description}", "B": wl.B, "S": wl.S,
+           "index_heads": wl.Hi, "index_head_dim": wl.Di, "index_topk": wl.topk,
+           "heads": wl.H, "kv_heads": wl.Hkv, "qk_dim": wl.Dqk, "v_dim": wl.Dv,
+           "backward": wl.backward, "segments": wl.ndocs,
+           "l2": "flushed between steps (256 MiB write outside the timed events)"}
+    if args is not None and getattr(args, "indexer_dtype", "bf16") == "e4m3":
+        cfg["indexer_dtype"] = "e4m3"
+    if args is not None and getattr(args, "indexer_loss", False):
+        cfg["indexer_loss"] = True
+    return cfg
 
 
 def main(argv=None):
@@ -417,12 +455,20 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--indexer-dtype", default="bf16", choices=["bf16", "e4m3"],
                     help="e4m3: the indexer runs on fp8 inputs (the same dyadic values)")
+    ap.add_argument("--indexer-loss", action="store_true",
+                    help="add the indexer auxiliary loss and its gradient to every step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=0,
                     help="rows in the CPU-baseline sample (default: 24 per host core)")
     ap.add_argument("--cpu-rows-per-step", type=int, default=0,
                     help="rows per reference-arm step (default: 4 per host core)")
     args = ap.parse_args(argv)
+    if args.indexer_loss:
+        wl0 = synth.WORKLOADS[args.workload]
+        if (wl0.Hi, wl0.Di) != (64, 128) or wl0.Dqk not in (128, 192):
+            ap.error("--indexer-loss runs on Hi = 64, Di = 128 and Dqk in {128, 192}")
+        if args.indexer_dtype != "bf16":
+            ap.error("--indexer-loss takes the bf16 indexer (its backward reads bf16 inputs)")
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     wl = synth.WORKLOADS[args.workload]
@@ -485,8 +531,7 @@ def main(argv=None):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded: dyadic indexer inputs, N(0,1) bf16 attention inputs)",
-        "config": dict(workload_config(wl), **({"indexer_dtype": "e4m3"}
-                                               if args.indexer_dtype == "e4m3" else {})),
+        "config": workload_config(wl, args),
         "tflops": total_flop / (r["ms_step"] / 1e3) / 1e12,
         "stages": stages_out,
         "roofline": roof,
@@ -496,7 +541,7 @@ def main(argv=None):
         "device_error": r["device_error"],
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_rows, args.indexer_loss)
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

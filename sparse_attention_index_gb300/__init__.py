@@ -316,7 +316,7 @@ class HostPipeline:
     """
 
     def __init__(self, B, S, Hi, Di, H, Dqk, Dv, topk, scale, backward=True, segments=False,
-                 device=None):
+                 device=None, Hkv=1):
         dev = torch.device("cuda") if device is None else torch.device(device)
         self.dev, self.topk, self.scale, self.backward = dev, topk, scale, backward
         e = lambda *shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
@@ -325,7 +325,7 @@ class HostPipeline:
             self.d["seg"] = e(B, S, dt=torch.int32)
         self.big = []
         for _ in range(2):
-            sets = {"Q": e(B, S, H, Dqk), "K": e(B, S, 1, Dqk), "V": e(B, S, 1, Dv)}
+            sets = {"Q": e(B, S, H, Dqk), "K": e(B, S, Hkv, Dqk), "V": e(B, S, Hkv, Dv)}
             if backward:
                 sets["dO"] = e(B, S, H, Dv)
             self.big.append(sets)
@@ -335,8 +335,9 @@ class HostPipeline:
         self.out = {"idx": e(B, S, topk, dt=torch.int32), "count": e(B, S, dt=torch.int32),
                     "O": e(B, S, H, Dv), "lse": e(B, S, H, dt=torch.float32)}
         if backward:
-            self.out.update({"dQ": e(B, S, H, Dqk), "dK": e(B, S, 1, Dqk), "dV": e(B, S, 1, Dv)})
-            self.ws = e(bwd_workspace_bytes(B, S, H, 1, Dqk, Dv), dt=torch.uint8)
+            self.out.update({"dQ": e(B, S, H, Dqk), "dK": e(B, S, Hkv, Dqk),
+                             "dV": e(B, S, Hkv, Dv)})
+            self.ws = e(bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv), dt=torch.uint8)
         self.s_in, self.s_c, self.s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
         ev = lambda: torch.cuda.Event()  # noqa: E731
         # events of earlier steps that the next one must respect

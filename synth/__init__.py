@@ -198,6 +198,11 @@ WORKLOADS = {
         "packed_s4096", seed=4, B=4, S=4096, Hi=64, Di=128, topk=512, H=16, Dqk=192, Dv=128,
         backward=True, ndocs=3,
         description="packed training step: 3 documents per row, top-512, 16 heads, fwd+bwd"),
+    "mla_perhead_s4096": Workload(
+        "mla_perhead_s4096", seed=5, B=1, S=4096, Hi=64, Di=128, topk=2048, H=128, Hkv=128,
+        Dqk=192, Dv=128, backward=True,
+        description="DS-v3.2 layer shape at S=4096 with per-head K/V (each of the 128 heads "
+                    "has its own 192/128 K/V rows), top-2048, fwd+bwd"),
     "packed_s489": Workload(
         "packed_s489", seed=4, B=1, S=489, Hi=64, Di=128, topk=512, H=16, Dqk=192, Dv=128,
         backward=True, ndocs=3,

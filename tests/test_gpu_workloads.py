@@ -40,25 +40,32 @@ def _check(wl, n_uniform):
     ind, att, out = _run(wl)
     rows = synth.sample_rows(wl, n_uniform)
     S, k = wl.S, wl.topk
-    b_idx, t_idx = rows // S, rows % S
 
-    # index scores, bit-exact on the sampled rows
-    ref_sc = oracle.index_scores(ind["q_idx"], ind["k_idx"], ind["w"], ind["seg"], rows=rows)
-    gsc = out["scores"][torch.as_tensor(b_idx), torch.as_tensor(t_idx), :S].double().cpu().numpy()
-    for r in range(rows.size):
-        t = t_idx[r]
+    # index scores, bit-exact on the sampled rows (and on the last TAIL rows of every batch
+    # row, whose selections give the oracle's dK / dV of the last keys)
+    tail_rows = np.concatenate([b * S + np.arange(S - TAIL, S) for b in range(wl.B)]) \
+        if wl.backward else np.zeros(0, dtype=np.int64)
+    all_rows = np.union1d(rows, tail_rows).astype(np.int64)
+    ref_sc = oracle.index_scores(ind["q_idx"], ind["k_idx"], ind["w"], ind["seg"], rows=all_rows)
+    ab, at = all_rows // S, all_rows % S
+    gsc = out["scores"][torch.as_tensor(ab), torch.as_tensor(at), :S].double().cpu().numpy()
+    for r in range(all_rows.size):
+        t = at[r]
         g, o = gsc[r, : t + 1], ref_sc[r, : t + 1]
         assert np.array_equal(np.isneginf(g), np.isneginf(o))
         fin = np.isfinite(o)
-        assert np.array_equal(g[fin], o[fin]), (int(rows[r]),)
+        assert np.array_equal(g[fin], o[fin]), (int(all_rows[r]),)
 
-    # top-k sets, bit-exact
-    ref_idx, ref_cnt = oracle.topk(ref_sc, ind["seg"], S, k, rows=rows, B=wl.B)
-    idx = out["idx"].cpu().numpy()
-    assert np.array_equal(idx.reshape(-1, k)[rows], ref_idx)
-    assert np.array_equal(out["count"].cpu().numpy().reshape(-1)[rows], ref_cnt)
+    # top-k sets, bit-exact; the oracle's own lists feed every oracle call below
+    ref_idx, ref_cnt = oracle.topk(ref_sc, ind["seg"], S, k, rows=all_rows, B=wl.B)
+    gidx = out["idx"].cpu().numpy().reshape(-1, k)
+    assert np.array_equal(gidx[all_rows], ref_idx)
+    assert np.array_equal(out["count"].cpu().numpy().reshape(-1)[all_rows], ref_cnt)
+    idx = np.full((wl.B * S, k), -1, dtype=np.int32)
+    idx[all_rows] = ref_idx
+    idx = idx.reshape(wl.B, S, k)
 
-    # attention forward on the sampled rows (GPU selection == oracle selection there)
+    # attention forward on the sampled rows
     O_ref, lse_ref = oracle.attn_fwd(att["Q"], att["K"], att["V"], idx, wl.scale, rows=rows)
     O = out["O"].reshape(wl.B * S, wl.H, wl.Dv)[torch.as_tensor(rows)]
     lse = out["lse"].reshape(wl.B * S, wl.H)[torch.as_tensor(rows)]
@@ -71,7 +78,6 @@ def _check(wl, n_uniform):
                                    rows=rows)
     dQ = out["dQ"].reshape(wl.B * S, wl.H, wl.Dqk)[torch.as_tensor(rows)]
     assert rel_err(host_f64(dQ), dQ_ref) <= TOL
-    tail_rows = np.concatenate([b * S + np.arange(S - TAIL, S) for b in range(wl.B)])
     _, dK_ref, dV_ref = oracle.attn_bwd(att["Q"], att["K"], att["V"], idx, att["dO"], wl.scale,
                                         rows=tail_rows)
     dK = host_f64(out["dK"][:, S - TAIL:])
@@ -85,7 +91,7 @@ def _check(wl, n_uniform):
 
 
 @pytest.mark.parametrize("name", ["tiny_s128", "packed_s489", "small2b_s4096", "packed_s4096",
-                                  "v32_671b_s16k"])
+                                  "v32_671b_s16k", "mla_perhead_s4096"])
 def test_workload(name):
     _check(synth.WORKLOADS[name], n_uniform=12)
 
