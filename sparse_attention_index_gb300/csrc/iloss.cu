@@ -38,9 +38,12 @@
 //               per thread)
 //   issuer      forward: warp 8, backward: warp 4 - TMEM owner and single-thread UMMA
 //               issuer
-//   gather      the last 4 warps: 16-byte cp.async of the selected key rows into
-//               128B-swizzled tiles, four keys per group so that every copy instruction
-//               uses all 32 lanes; the row's Q (q_idx) tile alongside its first chunk
+//   gather      forward: warps 9-12, backward: warps 5-8 - 16-byte cp.async of the
+//               selected key rows into 128B-swizzled tiles, four keys per group so that
+//               every copy instruction uses all 32 lanes; the row's Q (q_idx) tile
+//               alongside its first chunk
+//   drain       backward: warps 9-12 - the dk rows from TMEM into dk_idx (fp32
+//               reductions), overlapping the epilogue's next chunk
 // Every wait is bounded (the library's 2 s limit); a wait that runs out sets the
 // CTA's abort flag and the error word, and every role then leaves its loops.
 
@@ -55,9 +58,10 @@ namespace {
 constexpr int kNK = 128;                 // keys per chunk (UMMA M)
 constexpr int kGatherWarps = 4;
 constexpr int kGatherThreads = 32 * kGatherWarps;
-// forward: 8 epilogue warps, the issuer, 4 gather warps; backward: 4, 1, 4
+// forward: 8 epilogue warps, the issuer, 4 gather warps; backward: 4 epilogue warps, the
+// issuer, 4 gather warps, 4 dk drain warps
 constexpr int kFwdIssuer = 8, kFwdGather0 = 9, kFwdThreads = 416;
-constexpr int kBwdIssuer = 4, kBwdGather0 = 5, kBwdThreads = 288;
+constexpr int kBwdIssuer = 4, kBwdGather0 = 5, kBwdDrain0 = 9, kBwdThreads = 416;
 constexpr uint32_t kAtom = kNK * 128;    // [128 rows x 128 B] swizzle atom
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -605,6 +609,8 @@ struct LossBwdTail {
   int red[kGatherWarps];
   __align__(16) float wrow[2][HI];   // w[t, :] by row parity
   float dw_acc[2][HI];
+  int dk_key[2][kNK];                // by chunk parity: each slot's key, -1 where nothing is added
+  int dk_last[2];                    // by chunk parity: the row's last chunk
 };
 
 template <int HI, int DI>
@@ -636,13 +642,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) loss_bwd_kernel(const LossBwdP
       mbar_init(&tail->q_empty[i], 1);
     }
     mbar_init(&tail->dq_full, 1);
-    mbar_init(&tail->dq_free, 128);
+    mbar_init(&tail->dq_free, 128);   // the epilogue warps; dk_empty counts the drain warps
     mbar_init(&tail->dw_bar, 4);
     mbar_init(&tail->drain, 1);
     tail->abort_flag = 0;
     fence_mbar_init();
   }
   for (int i = threadIdx.x; i < 2 * HI; i += blockDim.x) (&tail->dw_acc[0][0])[i] = 0.f;
+  static_assert(kBwdDrain0 == kBwdGather0 + kGatherWarps && kBwdThreads == 32 * (kBwdDrain0 + 4),
+                "backward roles: 4 epilogue, 1 issuer, 4 gather, 4 drain warps");
   if (warp == kBwdIssuer) {
     tmem_alloc(&tail->tmem_base, 512);
     tmem_relinquish();
@@ -652,7 +660,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) loss_bwd_kernel(const LossBwdP
   tc_fence_after();
   const uint32_t tmem = tail->tmem_base;
 
-  if (warp >= kBwdGather0) {
+  if (warp >= kBwdGather0 && warp < kBwdDrain0) {
     // ================================================================ gather
     const int gt = threadIdx.x - 32 * kBwdGather0;
     const int gw = warp - kBwdGather0;
@@ -803,65 +811,80 @@ __global__ void __launch_bounds__(kBwdThreads, 1) loss_bwd_kernel(const LossBwdP
       umma_commit(&tail->drain);
       drain_wait(&tail->drain, 0, p.err, kErrBwd);
     }
+  } else if (warp >= kBwdDrain0) {
+    // ================================================================ dk drain
+    // Thread tq holds key slot tq's dk row in TMEM (lane quarter warp % 4). The warp passes
+    // 32 columns of its 32 keys through a swizzled shared tile so that each quarter-warp adds
+    // one key's 128 contiguous bytes per reduction instruction.
+    const int quarter = warp & 3;
+    const int tq = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t xt = smem_u32(smem + L::kXOff) + quarter * 4096;
+    const int sub = lane >> 3, pc = lane & 7;
+    int g = 0;
+    bool ok = true;
+    for (int i = blockIdx.x; ok && i < nrows; i += gridDim.x) {
+      const long long row = row_of(i, nrows);
+      const long long kvbase = row / p.S * p.S;
+      bool last = false;
+      while (!last) {
+        const int db = g & 1;
+        const uint32_t ph = (g >> 1) & 1;
+        // the epilogue's handover (g_full) and the dk products (dk_full) of chunk g
+        if (!__all_sync(0xffffffffu, mbar_wait(&tail->g_full[db], ph, abort_flag, p.err,
+                                               kErrBwd)) ||
+            !__all_sync(0xffffffffu, mbar_wait(&tail->dk_full[db], ph, abort_flag, p.err,
+                                               kErrBwd))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        last = tail->dk_last[db] != 0;
+        const int s = tail->dk_key[db][tq];
+#pragma unroll 1
+        for (int c0 = 0; c0 < DI; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld_x32(tmem + lane_off + L::kColDk + db * DI + c0, v);
+          tmem_ld_wait();
+          __syncwarp();
+#pragma unroll
+          for (int c = 0; c < 8; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                             xt + lane * 128 + ((c ^ (lane & 7)) << 4)),
+                         "r"(v[4 * c]), "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
+                         : "memory");
+          __syncwarp();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int kr = 4 * u + sub;   // key row of this quarter-warp
+            const int sk = __shfl_sync(0xffffffffu, s, kr);
+            float4 x;
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
+                         : "r"(xt + kr * 128 + ((pc ^ (kr & 7)) << 4)));
+            if (sk >= 0) {
+              float* dst = p.dk + (kvbase + sk) * DI + c0 + pc * 4;
+              asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x.x),
+                           "f"(x.y), "f"(x.z), "f"(x.w)
+                           : "memory");
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tail->dk_empty[db]);
+        ++g;
+      }
+    }
   } else {
     // ================================================================ epilogue
-    const int tid = threadIdx.x;   // key slot of a chunk (Z, G, dk); dimension of dq
+    const int tid = threadIdx.x;   // key slot of a chunk (Z, G); dimension of dq
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     int g = 0, ri = 0;
     bool ok = true;
-    // dk rows of chunk gp. Each thread holds its key's row in TMEM; the warp passes 32
-    // columns of its 32 keys through a swizzled shared tile so that each quarter-warp adds
-    // one key's 128 contiguous bytes per reduction instruction.
-    const uint32_t xt = smem_u32(smem + L::kXOff) + warp * 4096;
-    auto drain_dk = [&](int gp, int s, float d, long long kvbase) -> bool {
-      const int db = gp & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&tail->dk_full[db], (gp >> 1) & 1, abort_flag,
-                                             p.err, kErrBwd)))
-        return false;
-      tc_fence_after();
-      const bool add = s >= 0 && d != 0.f;
-      const int sub = lane >> 3, pc = lane & 7;
-#pragma unroll 1
-      for (int c0 = 0; c0 < DI; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld_x32(tmem + lane_off + L::kColDk + db * DI + c0, v);
-        tmem_ld_wait();
-        __syncwarp();
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
-                           xt + lane * 128 + ((c ^ (lane & 7)) << 4)),
-                       "r"(v[4 * c]), "r"(v[4 * c + 1]), "r"(v[4 * c + 2]), "r"(v[4 * c + 3])
-                       : "memory");
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int kr = 4 * i + sub;   // key row of this quarter-warp
-          const int sk = __shfl_sync(0xffffffffu, add ? s : -1, kr);
-          float4 x;
-          asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                       : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w)
-                       : "r"(xt + kr * 128 + ((pc ^ (kr & 7)) << 4)));
-          if (sk >= 0) {
-            float* dst = p.dk + (kvbase + sk) * DI + c0 + pc * 4;
-            asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(x.x),
-                         "f"(x.y), "f"(x.z), "f"(x.w)
-                         : "memory");
-          }
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(&tail->dk_empty[db]);
-      return true;
-    };
     for (int i = blockIdx.x; i < nrows; i += gridDim.x, ++ri) {
       const long long row = row_of(i, nrows);
-      const int b = static_cast<int>(row / p.S);
-      const long long kvbase = static_cast<long long>(b) * p.S;
       const int par = ri & 1;
-      bool last = false, have_prev = false;
-      int s_prev = -1;
-      float d_prev = 0.f;
+      bool last = false;
       while (!last) {
         const int st = g % kBwdStages, zb = g & 1;
         const uint32_t ph = (g >> 1) & 1;
@@ -910,6 +933,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) loss_bwd_kernel(const LossBwdP
           ok = false;
           break;
         }
+        // hand this chunk's keys to the drain warps, once they have drained the chunk that
+        // used the buffer two chunks back (dk_key / dk_last are released by g_full)
+        if (!__all_sync(0xffffffffu,
+                        mbar_wait(&tail->dk_empty[gb], ph ^ 1u, abort_flag, p.err, kErrBwd))) {
+          ok = false;
+          break;
+        }
+        tail->dk_key[gb][tid] = (s >= 0 && d != 0.f) ? s : -1;
+        if (tid == 0) tail->dk_last[gb] = last ? 1 : 0;
         const uint32_t grow = smem_u32(smem + L::kGOff + gb * L::kGBuf) + tid * 128;
 #pragma unroll
         for (int a = 0; a < HI / 64; ++a) {
@@ -935,15 +967,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1) loss_bwd_kernel(const LossBwdP
         reduce_scatter_step<2, 1>(r, lane);
         atomicAdd(&tail->dw_acc[par][2 * lane], r[0]);
         atomicAdd(&tail->dw_acc[par][2 * lane + 1], r[1]);
-        // dk rows of the previous chunk of the row
-        if (have_prev && !drain_dk(g - 1, s_prev, d_prev, kvbase)) { ok = false; break; }
-        have_prev = true;
-        s_prev = s;
-        d_prev = d;
         ++g;
       }
       if (!ok) break;
-      if (!drain_dk(g - 1, s_prev, d_prev, kvbase)) break;
       // dq^T of the row: thread tid holds dimension tid of every head
       if (!__all_sync(0xffffffffu, mbar_wait(&tail->dq_full, par, abort_flag, p.err, kErrBwd)))
         break;
