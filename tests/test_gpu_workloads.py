@@ -99,3 +99,53 @@ def test_workload(name):
 @pytest.mark.slow
 def test_long_context_workload():
     _check(synth.WORKLOADS["long_s128k"], n_uniform=6)
+
+
+def test_indexer_loss_full_size():
+    """The indexer loss and its gradient at v32_671b_s16k, the step bench.py --indexer-loss times.
+
+    Sampled rows against the oracle (its own scores and selection); dk_idx, which gathers every
+    row, through an identity that holds at any size: I is positively homogeneous of degree 1 in
+    q_idx and in k_idx, so sum_s <dk_s, k_s> = sum_{t,h} <dq_th, q_th> = sum_{t,h} w dw
+    = sum_{t,j} dI_tj I[t, s_tj]."""
+    import sparse_attention_index_gb300 as dsa
+    wl = synth.WORKLOADS["v32_671b_s16k"]
+    ind = synth.indexer_inputs(wl)
+    att = synth.attention_inputs(wl, with_grad=False)
+    S, k, g = wl.S, wl.topk, 1.0 / wl.S
+    qd, kd, wd = bf16_dev(ind["q_idx"]), bf16_dev(ind["k_idx"]), dev(ind["w"])
+    Qd, Kd, Vd = bf16_dev(att["Q"]), bf16_dev(att["K"]), bf16_dev(att["V"])
+    scores = dsa.dsa_index_scores(qd, kd, wd)
+    idx, _ = dsa.dsa_topk(scores, k)
+    _, lse = dsa.dsa_sparse_attn_fwd(Qd, Kd, Vd, idx, wl.scale)
+    kl, dI = dsa.dsa_indexer_loss(Qd, Kd, idx, lse, scores, wl.scale, g)
+    dq, dk, dw = dsa.dsa_indexer_loss_bwd(qd, kd, wd, idx, dI)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_last_device_error() == 0
+
+    rows = synth.sample_rows(wl, 8)
+    sc = oracle.index_scores(ind["q_idx"], ind["k_idx"], ind["w"], None, rows=rows)
+    ref_idx, _ = oracle.topk(sc, None, S, k, rows=rows, B=wl.B)
+    assert np.array_equal(idx.cpu().numpy().reshape(-1, k)[rows], ref_idx)
+    full_idx = np.full((wl.B * S, k), -1, dtype=np.int32)
+    full_idx[rows] = ref_idx
+    full_idx = full_idx.reshape(wl.B, S, k)
+    kl_ref, dI_ref = oracle.indexer_loss(att["Q"], att["K"], full_idx, sc, wl.scale, g, rows=rows)
+    rt = torch.as_tensor(rows)
+    assert rel_err(host_f64(kl.reshape(-1)[rt]), kl_ref) <= 1e-3
+    assert rel_err(host_f64(dI.reshape(-1, k)[rt]), dI_ref) <= 1e-3
+    dq_ref, _, dw_ref = oracle.indexer_loss_bwd(ind["q_idx"], ind["k_idx"], ind["w"], full_idx,
+                                                dI_ref, rows=rows)
+    assert rel_err(host_f64(dq.reshape(wl.B * S, wl.Hi, wl.Di)[rt]), dq_ref) <= TOL
+    # dw from the GPU's dI (within 1e-3 of the oracle's); its sum over keys can cancel
+    assert rel_err(host_f64(dw.reshape(wl.B * S, wl.Hi)[rt]), dw_ref) <= TOL
+
+    sel = idx.long().clamp(min=0)
+    I_sel = torch.gather(scores[:, :, :S], 2, sel).double() * (idx >= 0)
+    rhs = (dI.double() * I_sel).sum().item()
+    via_dk = (dk.double() * kd.double()).sum().item()
+    via_dq = (dq.double() * qd.double()).sum().item()
+    via_dw = (dw.double() * wd.double()).sum().item()
+    assert abs(via_dw - rhs) <= 1e-4 * abs(rhs)
+    assert abs(via_dk - rhs) <= 2e-3 * abs(rhs)      # G in bf16 (2^-9) in the dk, dq products
+    assert abs(via_dq - rhs) <= 2e-3 * abs(rhs)
