@@ -318,9 +318,7 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e = None
     if fp8 and not args.no_e2e:
         e2e = {"unavailable": "the host pipeline takes bf16 indexer inputs"}
-    if loss and not args.no_e2e:
-        e2e = {"unavailable": "the host pipeline runs the four stages without the indexer loss"}
-    if not args.no_e2e and not fp8 and not loss:
+    if not args.no_e2e and not fp8:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
         h_in = {"q_idx": pin(ind["q_idx"]), "k_idx": pin(ind["k_idx"]), "w": pin(ind["w"]),
                 "Q": pin(att["Q"]), "K": pin(att["K"]), "V": pin(att["V"])}
@@ -332,7 +330,7 @@ def run_ours(args, wl, rank, world, local_rank):
         # three streams, overlapped (sparse_attention_index_gb300.HostPipeline)
         pipe = dsa.HostPipeline(B, S, wl.Hi, wl.Di, wl.H, wl.Dqk, wl.Dv, k, wl.scale,
                                 backward=wl.backward, segments=seg is not None, device=device,
-                                Hkv=wl.Hkv)
+                                Hkv=wl.Hkv, indexer_loss=loss)
         h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in pipe.out.items()}
         h2d = sum(t.numel() * t.element_size() for t in h_in.values())
         d2h = sum(t.numel() * t.element_size() for t in h_out.values())

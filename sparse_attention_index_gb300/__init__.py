@@ -316,9 +316,14 @@ class HostPipeline:
     """
 
     def __init__(self, B, S, Hi, Di, H, Dqk, Dv, topk, scale, backward=True, segments=False,
-                 device=None, Hkv=1):
+                 device=None, Hkv=1, indexer_loss=False, grad_scale=None):
+        """indexer_loss: also run the indexer loss (objective grad_scale * sum of the
+        per-query losses, default 1/(B*S)) and its gradient each step, returning kl,
+        dq_idx, dk_idx and dw."""
         dev = torch.device("cuda") if device is None else torch.device(device)
         self.dev, self.topk, self.scale, self.backward = dev, topk, scale, backward
+        self.loss = indexer_loss
+        self.grad_scale = 1.0 / (B * S) if grad_scale is None else grad_scale
         e = lambda *shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
         self.d = {"q_idx": e(B, S, Hi, Di), "k_idx": e(B, S, Di), "w": e(B, S, Hi, dt=torch.float32)}
         if segments:
@@ -338,12 +343,17 @@ class HostPipeline:
             self.out.update({"dQ": e(B, S, H, Dqk), "dK": e(B, S, Hkv, Dqk),
                              "dV": e(B, S, Hkv, Dv)})
             self.ws = e(bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv), dt=torch.uint8)
+        if indexer_loss:
+            f32 = torch.float32
+            self.dI = e(B, S, topk, dt=f32)
+            self.out.update({"kl": e(B, S, dt=f32), "dq_idx": e(B, S, Hi, Di, dt=f32),
+                             "dk_idx": e(B, S, Di, dt=f32), "dw": e(B, S, Hi, dt=f32)})
         self.s_in, self.s_c, self.s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
         ev = lambda: torch.cuda.Event()  # noqa: E731
         # events of earlier steps that the next one must respect
         self.ev_idx_read = None
         self.ev_attn_read = [None, None]   # per Q/K/V/dO set: its last reader is done
-        self.ev_out1 = self.ev_out2 = self.ev_out3 = None
+        self.ev_out1 = self.ev_out2 = self.ev_out3 = self.ev_out4 = None
         self._ev = ev
 
     def _wait(self, stream, event):
@@ -359,7 +369,8 @@ class HostPipeline:
     def step(self, h_in: dict, h_out: dict):
         """Enqueue one step: h_in / h_out hold pinned host tensors named like the
         device buffers (inputs q_idx, k_idx, w, [seg], Q, K, V, [dO]; outputs idx,
-        count, O, lse, [dQ, dK, dV]). Returns the event that completes the step."""
+        count, O, lse, [dQ, dK, dV], [kl, dq_idx, dk_idx, dw]). Returns the event that
+        completes the step."""
         d, o, ev = self.d, self.out, self._ev
         par = self.n & 1
         bd = self.big[par]
@@ -402,6 +413,18 @@ class HostPipeline:
                                 stream=sc)
             bwd_done = ev()
             bwd_done.record(sc)
+        attn_read = bwd_done
+        if self.loss:
+            # reads Q, K, the scores and the indexer inputs: the next step's copies into
+            # them wait for it (idx_read, attn_read)
+            self._wait(sc, self.ev_out4)
+            dsa_indexer_loss(bd["Q"], bd["K"], o["idx"], o["lse"], self.scores, self.scale,
+                             self.grad_scale, kl=o["kl"], dI=self.dI, stream=sc)
+            dsa_indexer_loss_bwd(d["q_idx"], d["k_idx"], d["w"], o["idx"], self.dI,
+                                 dq_idx=o["dq_idx"], dk_idx=o["dk_idx"], dw=o["dw"], stream=sc)
+            loss_done = ev()
+            loss_done.record(sc)
+            idx_read = attn_read = loss_done
         # device -> host
         with torch.cuda.stream(self.s_out):
             self.s_out.wait_event(topk_done)
@@ -421,11 +444,18 @@ class HostPipeline:
                     h_out[n].copy_(self._bits(o[n], h_out[n]), non_blocking=True)
                 out3 = ev()
                 out3.record(self.s_out)
+            out4 = out3
+            if self.loss:
+                self.s_out.wait_event(loss_done)
+                for n in ("kl", "dq_idx", "dk_idx", "dw"):
+                    h_out[n].copy_(o[n], non_blocking=True)
+                out4 = ev()
+                out4.record(self.s_out)
         self.ev_idx_read = idx_read
-        self.ev_attn_read[par] = bwd_done
-        self.ev_out1, self.ev_out2, self.ev_out3 = out1, out2, out3
+        self.ev_attn_read[par] = attn_read
+        self.ev_out1, self.ev_out2, self.ev_out3, self.ev_out4 = out1, out2, out3, out4
         self.n += 1
-        return out3
+        return out4
 
 
 def dsa_indexer_loss(Q, K, idx, lse, scores, scale: float, grad_scale: float = 1.0, kl=None,

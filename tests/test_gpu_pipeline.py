@@ -46,3 +46,38 @@ def test_host_pipeline_matches_device_path(name):
     if wl.backward:
         for n in ("dK", "dV"):
             assert rel_err(host_f64(h_out[n]), host_f64(ref[n])) <= TOL, n
+
+
+def test_host_pipeline_with_indexer_loss():
+    """The pipeline's loss stage (it reads the scores, Q, K and the indexer inputs, so the next
+    step's copies wait for it) gives the device-resident path's kl, dq_idx and dw exactly and
+    dk_idx within the fp32-atomic tolerance, over consecutive overlapped steps."""
+    import sparse_attention_index_gb300 as dsa
+    wl = synth.WORKLOADS["packed_s489"]
+    ind = synth.indexer_inputs(wl)
+    att = synth.attention_inputs(wl)
+    seg = dev(ind["seg"])
+    qd, kd, wd = bf16_dev(ind["q_idx"]), bf16_dev(ind["k_idx"]), dev(ind["w"])
+    ref = dsa.dsa_layer(qd, kd, wd, bf16_dev(att["Q"]), bf16_dev(att["K"]), bf16_dev(att["V"]),
+                        wl.topk, wl.scale, seg=seg, dO=bf16_dev(att["dO"]))
+    g = 1.0 / (wl.B * wl.S)
+    kl, dI = dsa.dsa_indexer_loss(bf16_dev(att["Q"]), bf16_dev(att["K"]), ref["idx"], ref["lse"],
+                                  ref["scores"], wl.scale, g)
+    dq, dk, dw = dsa.dsa_indexer_loss_bwd(qd, kd, wd, ref["idx"], dI)
+    torch.cuda.synchronize()
+
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    h_in = {n: pin(ind[n]) for n in ("q_idx", "k_idx", "w", "seg")}
+    h_in.update({n: pin(att[n]) for n in ("Q", "K", "V", "dO")})
+    pipe = dsa.HostPipeline(wl.B, wl.S, wl.Hi, wl.Di, wl.H, wl.Dqk, wl.Dv, wl.topk, wl.scale,
+                            backward=True, segments=True, indexer_loss=True)
+    h_out = {n: torch.zeros(t.shape, dtype=t.dtype).pin_memory() for n, t in pipe.out.items()}
+    for _ in range(3):
+        pipe.step(h_in, h_out)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_last_device_error() == 0
+    assert torch.equal(h_out["idx"], ref["idx"].cpu())
+    assert rel_err(host_f64(h_out["kl"]), host_f64(kl)) <= 1e-6       # atomic order of the sum
+    assert torch.equal(h_out["dq_idx"], dq.cpu())
+    assert rel_err(host_f64(h_out["dw"]), host_f64(dw)) <= 1e-6
+    assert rel_err(host_f64(h_out["dk_idx"]), host_f64(dk)) <= 1e-5
