@@ -70,6 +70,7 @@ def stage_work(wl: synth.Workload):
     causal, sel = pair_counts(wl)
     return {
         "indexer": {"flop": 2.0 * wl.Hi * wl.Di * causal},
+        "indexer_topk": {"flop": 2.0 * wl.Hi * wl.Di * causal},
         "topk": {"bytes": 4.0 * causal + 4.0 * wl.topk * wl.B * wl.S},
         "attn_fwd": {"flop": 2.0 * wl.H * (wl.Dqk + wl.Dv) * sel},
         "attn_bwd": {"flop": 2.0 * wl.H * (3 * wl.Dqk + 2 * wl.Dv) * sel} if wl.backward else None,
@@ -229,7 +230,14 @@ def run_ours(args, wl, rank, world, local_rank):
     dO = to_dev(att["dO"], True) if wl.backward else None
     B, S, k = wl.B, wl.S, wl.topk
     ld = (S + 3) // 4 * 4
-    scores = torch.empty((B, S, ld), dtype=torch.float32, device=device)
+    fused = args.fused_topk > 0
+    if fused:   # one block of query rows of scores instead of the [B, S, S] matrix
+        R = args.fused_topk
+        topk_ws = torch.empty((dsa.index_topk_workspace_bytes(B, S, R),), dtype=torch.uint8,
+                              device=device)
+        scores = None
+    else:
+        scores = torch.empty((B, S, ld), dtype=torch.float32, device=device)
     idx = torch.empty((B, S, k), dtype=torch.int32, device=device)
     count = torch.empty((B, S), dtype=torch.int32, device=device)
     O = torch.empty((B, S, wl.H, wl.Dv), dtype=torch.bfloat16, device=device)
@@ -242,7 +250,8 @@ def run_ours(args, wl, rank, world, local_rank):
                          device=device)
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=device)
     stream = torch.cuda.Stream(device=device)
-    stages = ["indexer", "topk", "attn_fwd"] + (["attn_bwd"] if wl.backward else [])
+    stages = (["indexer_topk"] if fused else ["indexer", "topk"]) + ["attn_fwd"] + \
+        (["attn_bwd"] if wl.backward else [])
     loss = args.indexer_loss
     if loss:
         # the indexer's auxiliary loss and its gradient into the indexer inputs
@@ -259,25 +268,38 @@ def run_ours(args, wl, rank, world, local_rank):
         == dsa.DSA_FWD_DENSE_TC else 1
     bwd_launches = (4 if dsa.dsa_sparse_attn_bwd_kernel(B, S, wl.H, wl.Hkv, wl.Dqk, wl.Dv, k, wl.scale)
                     == dsa.DSA_BWD_DENSE_TC else 2) if wl.backward else 0
-    launches_per_step = 2 + fwd_launches + bwd_launches + (2 if loss else 0)
+    if fused:   # per block of query rows: the indexer, the staged and / or the long-row top-k
+        idx_launches = sum(1 + (t_lo < 16384) + (min(t_lo + R, S) > 16384)
+                           for t_lo in range(0, S, R))
+    else:
+        idx_launches = 2
+    launches_per_step = idx_launches + fwd_launches + bwd_launches + (2 if loss else 0)
 
     def step(ev):
         ev[0].record(stream)
-        if fp8:
-            dsa.dsa_index_scores_fp8(q_idx, k_idx, w, seg, scores=scores, stream=stream)
+        e = 1
+        if fused:
+            dsa.dsa_index_topk(q_idx, k_idx, w, k, seg, block_rows=R, idx=idx, count=count,
+                               ws=topk_ws, stream=stream)
         else:
-            dsa.dsa_index_scores(q_idx, k_idx, w, seg, scores=scores, stream=stream)
-        ev[1].record(stream)
-        dsa.dsa_topk(scores, k, seg, idx=idx, count=count, stream=stream)
-        ev[2].record(stream)
+            if fp8:
+                dsa.dsa_index_scores_fp8(q_idx, k_idx, w, seg, scores=scores, stream=stream)
+            else:
+                dsa.dsa_index_scores(q_idx, k_idx, w, seg, scores=scores, stream=stream)
+            ev[e].record(stream)
+            e += 1
+            dsa.dsa_topk(scores, k, seg, idx=idx, count=count, stream=stream)
+        ev[e].record(stream)
+        e += 1
         dsa.dsa_sparse_attn_fwd(Q, K, V, idx, wl.scale, O=O, lse=lse, stream=stream)
-        ev[3].record(stream)
+        ev[e].record(stream)
+        e += 1
         if wl.backward:
             dsa.dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, wl.scale, dQ=dQ, dK=dK, dV=dV, ws=ws,
                                     stream=stream)
-            ev[4].record(stream)
+            ev[e].record(stream)
+            e += 1
         if loss:
-            e = 5 if wl.backward else 4
             dsa.dsa_indexer_loss(Q, K, idx, lse, scores, wl.scale, 1.0 / (B * S), kl=kl, dI=dI,
                                  stream=stream)
             ev[e].record(stream)
@@ -318,7 +340,9 @@ def run_ours(args, wl, rank, world, local_rank):
     e2e = None
     if fp8 and not args.no_e2e:
         e2e = {"unavailable": "the host pipeline takes bf16 indexer inputs"}
-    if not args.no_e2e and not fp8:
+    if fused and not args.no_e2e:
+        e2e = {"unavailable": "the host pipeline runs the unfused indexer and top-k"}
+    if not args.no_e2e and not fp8 and not fused:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
         h_in = {"q_idx": pin(ind["q_idx"]), "k_idx": pin(ind["k_idx"]), "w": pin(ind["w"]),
                 "Q": pin(att["Q"]), "K": pin(att["K"]), "V": pin(att["V"])}
@@ -440,6 +464,8 @@ def workload_config(wl, args=None):
         cfg["indexer_dtype"] = "e4m3"
     if args is not None and getattr(args, "indexer_loss", False):
         cfg["indexer_loss"] = True
+    if args is not None and getattr(args, "fused_topk", 0):
+        cfg["fused_topk_block_rows"] = args.fused_topk
     return cfg
 
 
@@ -453,6 +479,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--indexer-dtype", default="bf16", choices=["bf16", "e4m3"],
                     help="e4m3: the indexer runs on fp8 inputs (the same dyadic values)")
+    ap.add_argument("--fused-topk", type=int, default=0, metavar="BLOCK_ROWS",
+                    help="run the indexer and the top-k fused through blocks of this many query "
+                         "rows (a multiple of 256): no [B, S, S] score matrix")
     ap.add_argument("--indexer-loss", action="store_true",
                     help="add the indexer auxiliary loss and its gradient to every step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -461,6 +490,10 @@ def main(argv=None):
     ap.add_argument("--cpu-rows-per-step", type=int, default=0,
                     help="rows per reference-arm step (default: 4 per host core)")
     args = ap.parse_args(argv)
+    if args.fused_topk and (args.fused_topk % 256 or args.indexer_loss or
+                            args.indexer_dtype != "bf16"):
+        ap.error("--fused-topk takes a multiple of 256, the bf16 indexer and no --indexer-loss "
+                 "(the loss reads the score matrix)")
     if args.indexer_loss:
         wl0 = synth.WORKLOADS[args.workload]
         if (wl0.Hi, wl0.Di) != (64, 128) or wl0.Dqk not in (128, 192):

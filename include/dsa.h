@@ -298,6 +298,30 @@ int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
                                 void* dK, void* dV, void* stream);
 
 /*
+ * dsa_index_topk - dsa_index_scores followed by dsa_topk, fused through blocks of
+ * query rows: the [B, S, S] score matrix never exists. Each block of block_rows
+ * query rows is scored into a [B, block_rows, ld] fp32 buffer in `ws` (ld = S
+ * rounded up to a multiple of 4) and its top-k is taken before the next block
+ * reuses the buffer, so the scores' memory is B * block_rows * ld * 4 bytes instead
+ * of B * S * ld * 4 (at S = 131072 and block_rows = 2048: 1 GiB instead of 64 GiB),
+ * and a small block keeps them in L2. "DeepSeek3.2: Onboard sparse attention"
+ * (Background: the top-k of the index scores gives the index mask) and "Implement QK
+ * attention head chunking for CSA" (the dense score products run out of memory at
+ * long context).
+ *
+ *   q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di as for dsa_index_scores;
+ *   k, idx [B, S, k], count [B, S] (or NULL) as for dsa_topk (identical results);
+ *   block_rows  query rows per block: a positive multiple of 256;
+ *   ws          at least dsa_index_topk_workspace_size(B, S, block_rows) bytes.
+ *
+ * Supported as for dsa_index_scores (bf16 inputs). DSA_ERR_WORKSPACE if ws is too small.
+ */
+size_t dsa_index_topk_workspace_size(int B, int S, int block_rows);
+int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
+                   const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
+                   int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * dsa_indexer_loss - the indexer's auxiliary loss and its gradient with respect
  * to the index scores.
  *

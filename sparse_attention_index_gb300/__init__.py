@@ -40,7 +40,8 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa
            "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense",
            "dsa_sparse_attn_fwd_kernel", "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_kernel",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
-           "dsa_sparse_attn_bwd_noalloc", "dsa_indexer_loss", "dsa_indexer_loss_bwd")
+           "dsa_sparse_attn_bwd_noalloc", "dsa_indexer_loss", "dsa_indexer_loss_bwd",
+           "dsa_index_topk_workspace_size", "dsa_index_topk")
 
 
 class DsaError(RuntimeError):
@@ -81,11 +82,13 @@ def _load() -> ctypes.CDLL:
     lib.dsa_indexer_loss.argtypes = [vp, vp, vp, vp, vp, i64, ci, ci, ci, ci, ci, ci, cf, cf, vp,
                                      vp, vp]
     lib.dsa_indexer_loss_bwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp, vp]
+    lib.dsa_index_topk_workspace_size.argtypes = [ci, ci, ci]
+    lib.dsa_index_topk_workspace_size.restype = sz
+    lib.dsa_index_topk.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, sz, vp]
     for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_index_scores_fp8", "dsa_topk",
-                 "dsa_indexer_loss", "dsa_indexer_loss_bwd",
+                 "dsa_indexer_loss", "dsa_indexer_loss_bwd", "dsa_index_topk",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense", "dsa_sparse_attn_bwd",
-                 "dsa_sparse_attn_bwd_dense",
-                 "dsa_sparse_attn_bwd_noalloc", "dsa_indexer_loss", "dsa_indexer_loss_bwd"):
+                 "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_noalloc"):
         getattr(lib, name).restype = ci
     return lib
 
@@ -456,6 +459,37 @@ class HostPipeline:
         self.ev_out1, self.ev_out2, self.ev_out3, self.ev_out4 = out1, out2, out3, out4
         self.n += 1
         return out4
+
+
+def index_topk_workspace_bytes(B, S, block_rows) -> int:
+    return int(lib.dsa_index_topk_workspace_size(B, S, block_rows))
+
+
+def dsa_index_topk(q_idx, k_idx, w, k: int, seg=None, block_rows: int = 2048, idx=None,
+                   count=None, ws=None, stream=None):
+    """Indexer scores and top-k fused through blocks of query rows (no [B,S,S] scores).
+
+    Same arguments and results as dsa_index_scores followed by dsa_topk; the scores of
+    one block of block_rows query rows (a multiple of 256) live in `ws`.
+    """
+    B, S, Hi, Di = q_idx.shape
+    dev = q_idx.device
+    if idx is None:
+        idx = torch.empty((B, S, k), dtype=torch.int32, device=dev)
+    if count is None:
+        count = torch.empty((B, S), dtype=torch.int32, device=dev)
+    need = index_topk_workspace_bytes(B, S, block_rows)
+    if ws is None:
+        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    w_dtype = DSA_F32 if w.dtype == torch.float32 else DSA_BF16
+    rc = lib.dsa_index_topk(_dev(q_idx, "q_idx", torch.bfloat16), _dev(k_idx, "k_idx", torch.bfloat16),
+                            _dev(w, "w"), w_dtype,
+                            None if seg is None else _dev(seg, "seg", torch.int32),
+                            B, S, Hi, Di, k, block_rows, _dev(idx, "idx", torch.int32),
+                            _dev(count, "count", torch.int32), _dev(ws, "ws"),
+                            ws.numel() * ws.element_size(), _stream(stream))
+    _check(rc, "dsa_index_topk")
+    return idx, count
 
 
 def dsa_indexer_loss(Q, K, idx, lse, scores, scale: float, grad_scale: float = 1.0, kl=None,

@@ -213,6 +213,44 @@ int dsa_sparse_attn_bwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, in
 }
 
 
+size_t dsa_index_topk_workspace_size(int B, int S, int block_rows) {
+  if (B < 1 || S < 1 || block_rows < 1) return 0;
+  const long long ld = (static_cast<long long>(S) + 3) / 4 * 4;
+  const long long rows = block_rows < S ? block_rows : S;
+  return static_cast<size_t>(B) * rows * ld * sizeof(float);
+}
+
+int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
+                   const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
+                   int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream) {
+  if (!q_idx || !k_idx || !w || !idx) return DSA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || Hi < 1 || Di < 1 || k < 1) return DSA_ERR_INVALID_ARG;
+  if (block_rows < 256 || block_rows % 256 != 0) return DSA_ERR_INVALID_ARG;
+  if (w_dtype != DSA_F32 && w_dtype != DSA_BF16) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(idx) ||
+      (count && !aligned16(count)) || (seg && !aligned16(seg)))
+    return DSA_ERR_INVALID_ARG;
+  if (Di % 8 != 0) return DSA_ERR_INVALID_ARG;
+  if (!dsa::indexer_dims_supported(Hi, Di)) return DSA_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * S * Hi >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
+  const size_t need = dsa_index_topk_workspace_size(B, S, block_rows);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+  const long long ld = (static_cast<long long>(S) + 3) / 4 * 4;
+  const int R = block_rows < S ? block_rows : S;
+  float* buf = static_cast<float*>(ws);
+  for (int t_lo = 0; t_lo < S; t_lo += R) {
+    const int t_hi = t_lo + R < S ? t_lo + R : S;
+    int rc = dsa::launch_index_scores_rows(q_idx, k_idx, w, w_dtype == DSA_BF16, seg, B, S, Hi,
+                                           Di, buf, ld, as_stream(stream), 0, nullptr, t_lo,
+                                           t_hi, R);
+    if (rc != DSA_OK) return rc;
+    rc = dsa::launch_topk_rows(buf, ld, seg, B, S, k, idx, count, as_stream(stream), t_lo, t_hi,
+                               R);
+    if (rc != DSA_OK) return rc;
+  }
+  return DSA_OK;
+}
+
 int dsa_indexer_loss(const void* Q, const void* K, const int32_t* idx, const float* lse,
                      const float* scores, int64_t ld_scores, int B, int S, int H, int Hkv,
                      int Dqk, int k, float scale, float grad_scale, float* kl, float* dI,

@@ -17,8 +17,19 @@ int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int
                         const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
                         int64_t ld, cudaStream_t stream, int fp8, const float* k_scale);
 
+// rows [t_lo, t_hi) of every batch row only, scores of row t at row t - t_lo of a buffer with
+// rows_blk rows per batch (the query-block form of the fused indexer + top-k; t_lo a
+// multiple of 256)
+int launch_index_scores_rows(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                             const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
+                             int64_t ld, cudaStream_t stream, int fp8, const float* k_scale,
+                             int t_lo, int t_hi, long long rows_blk);
+
 int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
                 int32_t* idx, int32_t* count, cudaStream_t stream);
+int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
+                     int32_t* idx, int32_t* count, cudaStream_t stream, int t_lo, int t_hi,
+                     long long rows_blk);
 
 // path: kFwdPathAuto (the cheaper of the gathered-key and dense-tile kernels) or
 // kFwdPathDense (the dense-tile kernel, DSA_ERR_UNSUPPORTED where it does not apply)

@@ -51,7 +51,11 @@ struct IndexerParams {
   int B, S, Di;
   int G;          // queries per tile (256 / Hi)
   int n_groups;   // ceil(S / G)
-  int n_items;    // B * n_groups
+  int g_lo, g_hi; // the query groups of this launch (all of them, or one block of rows)
+  int n_items;    // B * (g_hi - g_lo)
+  int t_base;     // the first query row of the launch: row t is stored at row t - t_base
+  int t_end;      // one past its last query row
+  long long rows_blk;   // rows per batch of the score buffer
   int atom;       // K elements per swizzled row segment
   int n_atoms;    // Di / atom
   uint32_t atom_bytes;   // bytes of one swizzled row segment (32, 64 or 128)
@@ -82,7 +86,7 @@ __device__ __forceinline__ void item_coords(const IndexerParams& p, int item, in
   // heaviest items (largest t) first
   const int gi = item / p.B;
   b = item - gi * p.B;
-  const int g = p.n_groups - 1 - gi;
+  const int g = p.g_hi - 1 - gi;
   t0 = g * p.G;
   int t_last = t0 + p.G - 1;
   if (t_last > p.S - 1) t_last = p.S - 1;
@@ -327,11 +331,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < QPC; ++i) {
               const int qi = (half * 128 + cq * 32) / HI + i;
               const int t = t0 + qi;
-              if (t < p.S && s <= t) {
+              if (t < p.t_end && s <= t) {
                 float val = acc2[i].x + acc2[i].y;
                 if (F8 && p.k_scale != nullptr) val *= ks;
                 if (p.seg != nullptr && seg_s != __ldg(p.seg + b * p.S + t)) val = -INFINITY;
-                p.scores[(static_cast<long long>(b) * p.S + t) * p.ld + s] = val;
+                p.scores[(static_cast<long long>(b) * p.rows_blk + (t - p.t_base)) * p.ld + s] =
+                    val;
               }
               acc2[i] = make_float2(0.f, 0.f);
             }
@@ -441,13 +446,27 @@ int launch_hi_any(int Hi, const CUtensorMap& mq, const CUtensorMap& mk, const In
 int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
                         const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
                         int64_t ld, cudaStream_t stream, int fp8, const float* k_scale) {
+  return launch_index_scores_rows(q_idx, k_idx, w, w_is_bf16, seg, B, S, Hi, Di, scores, ld,
+                                  stream, fp8, k_scale, 0, S, S);
+}
+
+int launch_index_scores_rows(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                             const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
+                             int64_t ld, cudaStream_t stream, int fp8, const float* k_scale,
+                             int t_lo, int t_hi, long long rows_blk) {
   IndexerParams p;
   p.B = B;
   p.S = S;
   p.Di = Di;
   p.G = kColsPerTile / Hi;
   p.n_groups = (S + p.G - 1) / p.G;
-  p.n_items = B * p.n_groups;
+  // t_lo is a multiple of G (the callers' blocks are multiples of 256 rows)
+  p.g_lo = t_lo / p.G;
+  p.g_hi = (t_hi + p.G - 1) / p.G;
+  p.n_items = B * (p.g_hi - p.g_lo);
+  p.t_base = t_lo;
+  p.t_end = t_hi < S ? t_hi : S;
+  p.rows_blk = rows_blk;
   // one swizzled row segment holds up to 128 bytes of K: 64 bf16 or 128 e4m3 values
   const int ebytes = fp8 ? 1 : 2;
   p.atom = Di * ebytes >= 128 ? 128 / ebytes : Di;

@@ -46,7 +46,14 @@ struct TopkParams {
   int32_t* idx;
   int32_t* count;
   int stage_cap;
+  int t_lo, t_hi;        // the query rows of this launch (all of them, or one block)
+  long long rows_blk;    // rows per batch of the score buffer: row t is its row t - t_lo
 };
+
+// the scores of query row t of batch row b
+__device__ __forceinline__ const float* score_row(const TopkParams& p, int b, int t) {
+  return p.scores + (static_cast<long long>(b) * p.rows_blk + (t - p.t_lo)) * p.ld;
+}
 
 struct TopkSmem {
   uint32_t hist[2048];
@@ -431,18 +438,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
   TopkSmem* sm = reinterpret_cast<TopkSmem*>(smem_raw);
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkSmem));
 
-  // rows t < stage_cap of every batch row, long rows first
-  const int sc = min(p.S, p.stage_cap);
+  // rows t_lo <= t < min(t_hi, stage_cap) of every batch row, long rows first
+  const int sc = min(p.t_hi, p.stage_cap) - p.t_lo;
   const long long i = static_cast<long long>(gridDim.x) - 1 - blockIdx.x;
   const int b = static_cast<int>(i / sc);
-  const int t = static_cast<int>(i - static_cast<long long>(b) * sc);
+  const int t = p.t_lo + static_cast<int>(i - static_cast<long long>(b) * sc);
   const long long row = static_cast<long long>(b) * p.S + t;
   const int len = t + 1;
   const int tid = threadIdx.x;
   const int lane = tid & 31;
   const int32_t* seg_row = p.seg ? p.seg + static_cast<long long>(b) * p.S : nullptr;
   const int seg_t = seg_row ? seg_row[t] : 0;
-  const float* srow = p.scores + row * p.ld;
+  const float* srow = score_row(p, b, t);
   int32_t* out = p.idx + row * p.k;
 
   // number of valid keys
@@ -1204,15 +1211,15 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
 
 }  // namespace lr
 
-// rows t >= t0 of every batch row; persistent, longest rows first
+// rows t0 <= t < t_hi of every batch row; persistent, longest rows first
 __global__ void __launch_bounds__(lr::NT, 1) topk_long_kernel(const TopkParams p, int t0) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   lr::Smem* sm = reinterpret_cast<lr::Smem*>(smem_raw);
   const int tid = threadIdx.x;
-  const long long nlong = static_cast<long long>(p.B) * (p.S - t0);
+  const long long nlong = static_cast<long long>(p.B) * (p.t_hi - t0);
   for (long long j = blockIdx.x; j < nlong; j += gridDim.x) {
     const int b = static_cast<int>(j % p.B);
-    const int t = p.S - 1 - static_cast<int>(j / p.B);
+    const int t = p.t_hi - 1 - static_cast<int>(j / p.B);
     const long long row = static_cast<long long>(b) * p.S + t;
     const int32_t* seg_row = p.seg ? p.seg + static_cast<long long>(b) * p.S : nullptr;
     const int seg_t = seg_row ? seg_row[t] : 0;
@@ -1224,7 +1231,7 @@ __global__ void __launch_bounds__(lr::NT, 1) topk_long_kernel(const TopkParams p
       lr::block_scan(c, tot, sm);
       n = tot;
     }
-    const lr::RowKeys rk{p.scores + row * p.ld, seg_row, t + 1, seg_t};
+    const lr::RowKeys rk{score_row(p, b, t), seg_row, t + 1, seg_t};
     lr::select_row(rk, t, n, p, p.idx + row * p.k, row, sm);
   }
 }
@@ -1232,6 +1239,12 @@ __global__ void __launch_bounds__(lr::NT, 1) topk_long_kernel(const TopkParams p
 
 int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
                 int32_t* idx, int32_t* count, cudaStream_t stream) {
+  return launch_topk_rows(scores, ld, seg, B, S, k, idx, count, stream, 0, S, S);
+}
+
+int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
+                     int32_t* idx, int32_t* count, cudaStream_t stream, int t_lo, int t_hi,
+                     long long rows_blk) {
   TopkParams p;
   p.scores = scores;
   p.ld = ld;
@@ -1241,6 +1254,9 @@ int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int 
   p.k = k;
   p.idx = idx;
   p.count = count;
+  p.t_lo = t_lo;
+  p.t_hi = t_hi;
+  p.rows_blk = rows_blk;
   p.stage_cap = S < kStageMax ? S : kStageMax;
   p.stage_cap = (p.stage_cap + 3) & ~3;   // whole uint4 groups
   const size_t smem = sizeof(TopkSmem) + static_cast<size_t>(p.stage_cap) * 4;
@@ -1250,10 +1266,14 @@ int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int 
   const long long rows = static_cast<long long>(B) * S;
   if (rows > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
   // rows t < stage_cap: one CTA per row with the row staged in shared memory
-  const long long nshort = static_cast<long long>(B) * (S < p.stage_cap ? S : p.stage_cap);
-  topk_kernel<<<static_cast<unsigned>(nshort), kThreads, smem, stream>>>(p);
-  if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
-  if (S > kStageMax) {
+  const int short_hi = t_hi < p.stage_cap ? t_hi : p.stage_cap;
+  if (short_hi > t_lo) {
+    const long long nshort = static_cast<long long>(B) * (short_hi - t_lo);
+    topk_kernel<<<static_cast<unsigned>(nshort), kThreads, smem, stream>>>(p);
+    if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  const int long_lo = t_lo > kStageMax ? t_lo : kStageMax;
+  if (S > kStageMax && t_hi > long_lo) {
     // longer rows: persistent CTAs, one per SM
     const size_t lsmem = sizeof(lr::Smem);
     if (cudaFuncSetAttribute(topk_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1262,9 +1282,9 @@ int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int 
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long nlong = static_cast<long long>(B) * (S - kStageMax);
+    const long long nlong = static_cast<long long>(B) * (t_hi - long_lo);
     const int grid = static_cast<int>(nlong < sms ? nlong : sms);
-    topk_long_kernel<<<grid, lr::NT, lsmem, stream>>>(p, kStageMax);
+    topk_long_kernel<<<grid, lr::NT, lsmem, stream>>>(p, long_lo);
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   }
   return DSA_OK;

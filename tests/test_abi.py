@@ -88,3 +88,20 @@ def test_attention_validation(dsa):
     assert bwd(*args, None, need, None) == 3                                      # no ws
     assert bwd(*args, P, need - 4, None) == 3                                     # small ws
     assert bwd(*([P] * 6 + [None] + args[7:]), P, need, None) == 1                # null dO
+
+
+def test_index_topk_validation(dsa):
+    """The fused indexer + top-k: its workspace is one block of query rows, and bad
+    arguments are refused before anything is launched."""
+    assert dsa.lib.dsa_index_topk_workspace_size(1, 131072, 2048) == 2048 * 131072 * 4
+    assert dsa.lib.dsa_index_topk_workspace_size(2, 489, 2048) == 2 * 489 * 492 * 4   # S < block
+    assert dsa.lib.dsa_index_topk_workspace_size(0, 128, 256) == 0
+    f = dsa.lib.dsa_index_topk
+    need = dsa.lib.dsa_index_topk_workspace_size(1, 1024, 256)
+    # q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di, k, block_rows, idx, count, ws, ws_bytes, stream
+    assert f(None, P, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need, None) == 1   # null q_idx
+    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 100, P, P, P, need, None) == 1     # block % 256
+    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 0, 256, P, P, P, need, None) == 1     # k = 0
+    assert f(P, P, P, 1, None, 1, 1024, 48, 128, 8, 256, P, P, P, need, None) == 2     # Hi not 2^n
+    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need - 16, None) == 3  # small ws
+    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, None, need, None) == 3   # no ws

@@ -603,3 +603,45 @@ def test_per_head_kv_unsupported_forms():
         dsa.dsa_sparse_attn_bwd_noalloc(Qd, Kd, Vd, idxd, O, lse, dOd, 0.1)
     assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
     assert dsa.dsa_get_last_device_error() == 0
+
+
+# --------------------------------------- fused indexer + top-k by query blocks
+
+@pytest.mark.parametrize("case", [
+    # B, S, Hi, Di, k, ndocs, block_rows
+    (2, 700, 64, 128, 64, 0, 256),     # three full blocks and a ragged one
+    (1, 700, 64, 128, 300, 3, 512),    # packed documents, k larger than early rows
+    (1, 333, 4, 32, 100, 0, 256),      # 64 queries per indexer tile
+    (1, 200, 16, 64, 8, 0, 2048),      # one block larger than S
+])
+def test_index_topk_matches_oracle(case):
+    dsa = _dsa()
+    B, S, Hi, Di, k, ndocs, R = case
+    inp = _indexer_case(B, S, Hi, Di, seed=610 + S + Hi, ndocs=ndocs)
+    seg = None if inp["seg"] is None else dev(inp["seg"])
+    idx, cnt = dsa.dsa_index_topk(bf16_dev(inp["q_idx"]), bf16_dev(inp["k_idx"]), dev(inp["w"]),
+                                  k, seg, block_rows=R)
+    assert dsa.dsa_get_last_device_error() == 0
+    sc = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], inp["seg"])
+    ref_idx, ref_cnt = oracle.topk(sc, inp["seg"], S, k, B=B)
+    assert np.array_equal(idx.cpu().numpy().reshape(-1, k), ref_idx)
+    assert np.array_equal(cnt.cpu().numpy().reshape(-1), ref_cnt)
+
+
+def test_index_topk_long_rows_match_unfused_path():
+    """S = 20000 crosses the 16384-key boundary of the staged top-k inside a block: the fused
+    call equals the unfused path bit for bit, and the oracle on rows around the boundary."""
+    dsa = _dsa()
+    B, S, Hi, Di, k, R = 1, 20000, 64, 128, 2048, 4096
+    inp = _indexer_case(B, S, Hi, Di, seed=77)
+    q, kk, w = bf16_dev(inp["q_idx"]), bf16_dev(inp["k_idx"]), dev(inp["w"])
+    idx_f, cnt_f = dsa.dsa_index_topk(q, kk, w, k, block_rows=R)
+    scores = dsa.dsa_index_scores(q, kk, w)
+    idx_u, cnt_u = dsa.dsa_topk(scores, k)
+    assert dsa.dsa_get_last_device_error() == 0
+    assert torch.equal(idx_f, idx_u) and torch.equal(cnt_f, cnt_u)
+    rows = np.array([0, 2047, 2048, 4095, 4096, 16383, 16384, 16385, 19999], dtype=np.int64)
+    sc = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], None, rows=rows)
+    ref_idx, ref_cnt = oracle.topk(sc, None, S, k, rows=rows, B=B)
+    assert np.array_equal(idx_f.cpu().numpy().reshape(-1, k)[rows], ref_idx)
+    assert np.array_equal(cnt_f.cpu().numpy().reshape(-1)[rows], ref_cnt)
