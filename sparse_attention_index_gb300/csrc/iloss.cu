@@ -365,12 +365,10 @@ __global__ void __launch_bounds__(kFwdThreads, 1) loss_fwd_kernel(const LossFwdP
     int g = 0, ri = 0;
     for (int i = blockIdx.x; i < nrows; i += gridDim.x, ++ri) {
       const long long row = row_of(i, nrows);
-      const int b = static_cast<int>(row / p.S);
-      const int t = static_cast<int>(row - static_cast<long long>(b) * p.S);
+      const int t = static_cast<int>(row % p.S);
       const int par = ri & 1;
       const int32_t* irow = p.idx + row * p.k;
       const float* srow = p.scores + row * p.ld;
-      (void)b;
       // the row's LSE (log2 units) and the log-sum-exp of its selected index scores:
       // the 256 epilogue threads read slots j = e + 256 u (sixteen loads in flight per
       // thread) and keep the scores of the first kFwdKeepChunks chunks in sv[par]
