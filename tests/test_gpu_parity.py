@@ -613,6 +613,8 @@ def test_per_head_kv_unsupported_forms():
     (1, 700, 64, 128, 300, 3, 512),    # packed documents, k larger than early rows
     (1, 333, 4, 32, 100, 0, 256),      # 64 queries per indexer tile
     (1, 200, 16, 64, 8, 0, 2048),      # one block larger than S
+    (1, 2000, 4, 32, 64, 0, 256),      # eight blocks through one reused buffer
+    (2, 1500, 4, 32, 200, 3, 256),
 ])
 def test_index_topk_matches_oracle(case):
     dsa = _dsa()
