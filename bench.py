@@ -495,9 +495,6 @@ def main(argv=None):
         ap.error("--fused-topk takes a multiple of 256, the bf16 indexer and no --indexer-loss "
                  "(the loss reads the score matrix)")
     if args.indexer_loss:
-        wl0 = synth.WORKLOADS[args.workload]
-        if (wl0.Hi, wl0.Di) != (64, 128) or wl0.Dqk not in (128, 192):
-            ap.error("--indexer-loss runs on Hi = 64, Di = 128 and Dqk in {128, 192}")
         if args.indexer_dtype != "bf16":
             ap.error("--indexer-loss takes the bf16 indexer (its backward reads bf16 inputs)")
     if args.warmup < 3 and args.impl == "ours":

@@ -347,8 +347,10 @@ int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dt
  *   scores fp32 [B, S, ld_scores]   only the selected entries are read
  *   kl     fp32 [B, S] out          dI   fp32 [B, S, k] out
  *
- * Supported: Hkv = 1, 1 <= H <= 128, Dqk in {128, 192}, scale > 0. Rows with no
- * selected key get kl = 0 and dI = 0. An index outside [-1, S) is skipped and
+ * Hkv divides H (head h reads K head h / (H / Hkv)). The tensor-core kernel takes
+ * Hkv = 1, 1 <= H <= 128, Dqk in {128, 192} and scale > 0; every other shape runs on
+ * the CUDA cores (one CTA per query row, far slower). Rows with no selected key get
+ * kl = 0 and dI = 0. An index outside [-1, S) is skipped and
  * recorded as DSA_STAGE_LOSS | DSA_DEVERR_BAD_INDEX. kl is accumulated with
  * atomics (summation order unspecified).
  */
@@ -373,9 +375,10 @@ int dsa_indexer_loss(const void* Q, const void* K, const int32_t* idx, const flo
  *   idx    int32 [B, S, k]       dI    fp32 [B, S, k]
  *   dq_idx fp32 [B, S, Hi, Di] out   dk_idx fp32 [B, S, Di] out   dw fp32 [B, S, Hi] out
  *
- * Supported: Hi = 64, Di = 128. The products run on the tensor cores with
- * G = dI w [z > 0] rounded to bf16 and fp32 accumulation; dk_idx is accumulated
- * with fp32 atomics (summation order unspecified).
+ * Hi = 64, Di = 128 run on the tensor cores, with G = dI w [z > 0] rounded to bf16
+ * and fp32 accumulation; other shapes on the CUDA cores in fp32 (one CTA per query
+ * row, far slower), up to Hi * (Di + 1) <= 51200 (DSA_ERR_UNSUPPORTED above). dk_idx
+ * is accumulated with fp32 atomics (summation order unspecified).
  */
 int dsa_indexer_loss_bwd(const void* q_idx, const void* k_idx, const float* w,
                          const int32_t* idx, const float* dI, int B, int S, int Hi, int Di,

@@ -257,14 +257,16 @@ int dsa_indexer_loss(const void* Q, const void* K, const int32_t* idx, const flo
                      void* stream) {
   if (!Q || !K || !idx || !lse || !scores || !kl || !dI) return DSA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || H < 1 || Hkv < 1 || Dqk < 1 || k < 1) return DSA_ERR_INVALID_ARG;
-  if (ld_scores < S) return DSA_ERR_INVALID_ARG;
+  if (H % Hkv != 0 || ld_scores < S) return DSA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(idx) || !aligned16(lse) ||
       !aligned16(scores) || !aligned16(kl) || !aligned16(dI))
     return DSA_ERR_INVALID_ARG;
-  if (Hkv != 1 || !dsa::indexer_loss_supported(H, Dqk, scale)) return DSA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * S >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
-  return dsa::launch_indexer_loss(Q, K, idx, lse, scores, ld_scores, B, S, H, Dqk, k, scale,
-                                  grad_scale, kl, dI, as_stream(stream));
+  if (Hkv == 1 && dsa::indexer_loss_supported(H, Dqk, scale))
+    return dsa::launch_indexer_loss(Q, K, idx, lse, scores, ld_scores, B, S, H, Dqk, k, scale,
+                                    grad_scale, kl, dI, as_stream(stream));
+  return dsa::launch_indexer_loss_simt(Q, K, idx, lse, scores, ld_scores, B, S, H, Hkv, Dqk, k,
+                                       scale, grad_scale, kl, dI, as_stream(stream));
 }
 
 int dsa_indexer_loss_bwd(const void* q_idx, const void* k_idx, const float* w,
@@ -276,10 +278,12 @@ int dsa_indexer_loss_bwd(const void* q_idx, const void* k_idx, const float* w,
   if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(idx) ||
       !aligned16(dI) || !aligned16(dq_idx) || !aligned16(dk_idx) || !aligned16(dw))
     return DSA_ERR_INVALID_ARG;
-  if (!dsa::indexer_loss_bwd_supported(Hi, Di)) return DSA_ERR_UNSUPPORTED;
   if (static_cast<long long>(B) * S >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
-  return dsa::launch_indexer_loss_bwd(q_idx, k_idx, w, idx, dI, B, S, Hi, Di, k, dq_idx, dk_idx,
-                                      dw, as_stream(stream));
+  if (dsa::indexer_loss_bwd_supported(Hi, Di))
+    return dsa::launch_indexer_loss_bwd(q_idx, k_idx, w, idx, dI, B, S, Hi, Di, k, dq_idx, dk_idx,
+                                        dw, as_stream(stream));
+  return dsa::launch_indexer_loss_bwd_simt(q_idx, k_idx, w, idx, dI, B, S, Hi, Di, k, dq_idx,
+                                           dk_idx, dw, as_stream(stream));
 }
 
 }  // extern "C"

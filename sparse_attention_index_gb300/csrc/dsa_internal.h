@@ -70,6 +70,14 @@ int launch_indexer_loss(const void* Q, const void* K, const int32_t* idx, const 
 int launch_indexer_loss_bwd(const void* q_idx, const void* k_idx, const float* w,
                             const int32_t* idx, const float* dI, int B, int S, int Hi, int Di,
                             int k, float* dq, float* dk, float* dw, cudaStream_t stream);
+// the same on the CUDA cores, for every other shape (iloss_simt.cu)
+int launch_indexer_loss_simt(const void* Q, const void* K, const int32_t* idx, const float* lse,
+                             const float* scores, int64_t ld, int B, int S, int H, int Hkv,
+                             int Dqk, int k, float scale, float grad_scale, float* kl, float* dI,
+                             cudaStream_t stream);
+int launch_indexer_loss_bwd_simt(const void* q_idx, const void* k_idx, const float* w,
+                                 const int32_t* idx, const float* dI, int B, int S, int Hi, int Di,
+                                 int k, float* dq, float* dk, float* dw, cudaStream_t stream);
 bool indexer_dims_supported(int Hi, int Di);
 
 }  // namespace dsa

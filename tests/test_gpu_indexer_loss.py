@@ -15,6 +15,7 @@ import torch
 import oracle
 import synth
 from gpu_util import TOL, bf16_dev, dev, host_f64, rel_err
+from synth import bf16_to_f32
 
 pytestmark = pytest.mark.gpu
 
@@ -184,28 +185,81 @@ def test_indexer_loss_chain_on_gpu_inputs():
     assert rel_err(host_f64(dw).reshape(dw_ref.shape), dw_ref) <= TOL_LOSS
 
 
-def test_indexer_loss_unsupported_and_invalid():
+SIMT_LOSS_CASES = [
+    # B, S, H, Hkv, Dqk, k: shapes the tensor-core kernel does not take
+    (1, 128, 2, 1, 32, 4),        # the tiny workload's attention shape
+    (1, 150, 8, 8, 64, 40),       # per-head K/V
+    (2, 100, 6, 2, 48, 30),       # grouped heads, Dqk not a multiple of 64
+]
+
+
+def _simt_loss_case(B, S, H, Hkv, Dqk, k, seed):
+    Q = synth.normal_bf16((B, S, H, Dqk), seed, synth.STREAM_Q)
+    K = synth.normal_bf16((B, S, Hkv, Dqk), seed, synth.STREAM_K)
+    V = synth.normal_bf16((B, S, Hkv, 32), seed, synth.STREAM_V)
+    q_idx = synth.dyadic_bf16((B, S, 4, 32), seed, synth.STREAM_Q_IDX, -8, 8, 3)
+    k_idx = synth.dyadic_bf16((B, S, 32), seed, synth.STREAM_K_IDX, -8, 8, 3)
+    w = synth.dyadic_f32((B, S, 4), seed, synth.STREAM_W, -1, 1, 4)
+    sc = oracle.index_scores(q_idx, k_idx, w, None)
+    idx, _ = oracle.topk(sc, None, S, k, B=B)
+    idx = idx.reshape(B, S, k)
+    scale = 1.0 / np.sqrt(Dqk)
+    _, lse = oracle.attn_fwd(Q, K, V, idx, scale)
+    return dict(Q=Q, K=K, sc=sc, idx=idx, lse=lse, scale=scale)
+
+
+@pytest.mark.parametrize("case", SIMT_LOSS_CASES)
+def test_indexer_loss_cuda_core_shapes(case):
+    """Shapes outside the tensor-core kernel (head dims, per-head or grouped K/V) run on the
+    CUDA cores: same definition, same tolerances."""
+    B, S, H, Hkv, Dqk, k = case
+    c = _simt_loss_case(B, S, H, Hkv, Dqk, k, seed=930 + S + H)
+    kl, dI = _run_loss(c, B, S, 0.5)
+    kl_ref, dI_ref = oracle.indexer_loss(c["Q"], c["K"], c["idx"], c["sc"], c["scale"], 0.5)
+    assert rel_err(kl, kl_ref) <= TOL_LOSS
+    assert rel_err(dI, dI_ref) <= TOL_LOSS
+
+
+@pytest.mark.parametrize("Hi, Di", [(4, 32), (32, 64), (16, 128)])
+def test_indexer_loss_bwd_cuda_core_shapes(Hi, Di):
+    """Index shapes other than 64 x 128 run on the CUDA cores in fp32 (no bf16 rounding of G)."""
     dsa = _dsa()
-    B, S, H, k = 1, 64, 8, 16
-    Q = torch.zeros((B, S, H, 64), dtype=torch.bfloat16, device="cuda")
-    K = torch.zeros((B, S, 1, 64), dtype=torch.bfloat16, device="cuda")
+    B, S, k = 1, 160, 48
+    seed = 940 + Hi + Di
+    q_idx = synth.dyadic_bf16((B, S, Hi, Di), seed, synth.STREAM_Q_IDX, -8, 8, 3)
+    k_idx = synth.dyadic_bf16((B, S, Di), seed, synth.STREAM_K_IDX, -8, 8, 3)
+    w = synth.dyadic_f32((B, S, Hi), seed, synth.STREAM_W, -1, 1, 4)
+    sc = oracle.index_scores(q_idx, k_idx, w, None)
+    idx, _ = oracle.topk(sc, None, S, k, B=B)
+    idx = idx.reshape(B, S, k)
+    dI = synth.normal_bf16((B * S, k), seed, synth.STREAM_DO)
+    dI = np.where(idx.reshape(B * S, k) >= 0, bf16_to_f32(dI), 0.0).astype(np.float32)
+    dq, dk, dw = dsa.dsa_indexer_loss_bwd(bf16_dev(q_idx), bf16_dev(k_idx), dev(w), dev(idx),
+                                          dev(dI.reshape(B, S, k)))
+    assert dsa.dsa_get_last_device_error() == 0
+    dq_ref, dk_ref, dw_ref = oracle.indexer_loss_bwd(q_idx, k_idx, w, idx, dI.astype(np.float64))
+    assert rel_err(host_f64(dq).reshape(dq_ref.shape), dq_ref) <= TOL_LOSS
+    assert rel_err(host_f64(dk), dk_ref) <= TOL_LOSS
+    assert rel_err(host_f64(dw).reshape(dw_ref.shape), dw_ref) <= TOL_LOSS
+
+
+def test_indexer_loss_refusals():
+    dsa = _dsa()
+    B, S, k = 1, 64, 16
     idx = torch.full((B, S, k), -1, dtype=torch.int32, device="cuda")
-    lse = torch.zeros((B, S, H), device="cuda")
+    lse = torch.zeros((B, S, 6), device="cuda")
     sc = torch.zeros((B, S, S), device="cuda")
+    Q = torch.zeros((B, S, 6, 64), dtype=torch.bfloat16, device="cuda")
+    K = torch.zeros((B, S, 4, 64), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(dsa.DsaError) as e:
-        dsa.dsa_indexer_loss(Q, K, idx, lse, sc, 0.1)       # Dqk = 64
-    assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
-    Q2 = torch.zeros((B, S, H, 128), dtype=torch.bfloat16, device="cuda")
-    K2 = torch.zeros((B, S, 2, 128), dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(dsa.DsaError) as e:
-        dsa.dsa_indexer_loss(Q2, K2, idx, lse, sc, 0.1)     # Hkv = 2
-    assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
-    qi = torch.zeros((B, S, 32, 128), dtype=torch.bfloat16, device="cuda")
-    ki = torch.zeros((B, S, 128), dtype=torch.bfloat16, device="cuda")
-    wi = torch.zeros((B, S, 32), device="cuda")
+        dsa.dsa_indexer_loss(Q, K, idx, lse, sc, 0.1)        # 4 K/V heads do not divide 6
+    assert e.value.status == dsa.DSA_ERR_INVALID_ARG
+    qi = torch.zeros((B, S, 128, 512), dtype=torch.bfloat16, device="cuda")
+    ki = torch.zeros((B, S, 512), dtype=torch.bfloat16, device="cuda")
+    wi = torch.zeros((B, S, 128), device="cuda")
     dI = torch.zeros((B, S, k), device="cuda")
     with pytest.raises(dsa.DsaError) as e:
-        dsa.dsa_indexer_loss_bwd(qi, ki, wi, idx, dI)         # Hi = 32
+        dsa.dsa_indexer_loss_bwd(qi, ki, wi, idx, dI)          # Hi * (Di + 1) > 51200
     assert e.value.status == dsa.DSA_ERR_UNSUPPORTED
     assert dsa.dsa_get_last_device_error() == 0
 
