@@ -280,7 +280,7 @@ def run_ours(args, wl, rank, world, local_rank):
         e = 1
         if fused:
             dsa.dsa_index_topk(q_idx, k_idx, w, k, seg, block_rows=R, idx=idx, count=count,
-                               ws=topk_ws, stream=stream)
+                               ws=topk_ws, stream=stream)   # e4m3 inputs: the fp8 indexer
         else:
             if fp8:
                 dsa.dsa_index_scores_fp8(q_idx, k_idx, w, seg, scores=scores, stream=stream)
@@ -490,9 +490,8 @@ def main(argv=None):
     ap.add_argument("--cpu-rows-per-step", type=int, default=0,
                     help="rows per reference-arm step (default: 4 per host core)")
     args = ap.parse_args(argv)
-    if args.fused_topk and (args.fused_topk % 256 or args.indexer_loss or
-                            args.indexer_dtype != "bf16"):
-        ap.error("--fused-topk takes a multiple of 256, the bf16 indexer and no --indexer-loss "
+    if args.fused_topk and (args.fused_topk % 256 or args.indexer_loss):
+        ap.error("--fused-topk takes a multiple of 256 and no --indexer-loss "
                  "(the loss reads the score matrix)")
     if args.indexer_loss:
         if args.indexer_dtype != "bf16":
@@ -529,7 +528,7 @@ def main(argv=None):
     peaks = load_peaks()
     work = stage_work(wl)
     tokens = wl.B * wl.S
-    total_flop = sum(v["flop"] for v in work.values() if v and "flop" in v)
+    total_flop = sum(work[s]["flop"] for s in r["stages"] if "flop" in work[s])
     stages_out = {}
     for s in r["stages"]:
         ms = r["stage_ms"][s]
@@ -537,7 +536,7 @@ def main(argv=None):
         if "flop" in wk:
             tf = wk["flop"] / (ms / 1e3) / 1e12
             # e4m3 contractions: the measured bf16 peak x the nominal fp8 / bf16 ratio (2)
-            pk = peaks["bf16_tflops_sustained"] * (2.0 if s == "indexer" and
+            pk = peaks["bf16_tflops_sustained"] * (2.0 if s in ("indexer", "indexer_topk") and
                                                    args.indexer_dtype == "e4m3" else 1.0)
             stages_out[s] = {"ms": ms, "tflops": tf, "bound": "tensor", "frac": tf / pk}
         else:

@@ -322,6 +322,17 @@ int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dt
                    int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * dsa_index_topk_fp8 - dsa_index_topk on e4m3 q_idx / k_idx with an optional
+ * per-key scale of k: dsa_index_scores_fp8 followed by dsa_topk, through blocks of
+ * query rows. Arguments as for dsa_index_topk, plus k_scale as for
+ * dsa_index_scores_fp8 (Di a multiple of 16).
+ */
+int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scale, const void* w,
+                       int w_dtype, const int32_t* seg, int B, int S, int Hi, int Di, int k,
+                       int block_rows, int32_t* idx, int32_t* count, void* ws, size_t ws_bytes,
+                       void* stream);
+
+/*
  * dsa_indexer_loss - the indexer's auxiliary loss and its gradient with respect
  * to the index scores.
  *

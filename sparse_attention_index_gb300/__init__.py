@@ -41,7 +41,7 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa
            "dsa_sparse_attn_fwd_kernel", "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_kernel",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
            "dsa_sparse_attn_bwd_noalloc", "dsa_indexer_loss", "dsa_indexer_loss_bwd",
-           "dsa_index_topk_workspace_size", "dsa_index_topk")
+           "dsa_index_topk_workspace_size", "dsa_index_topk", "dsa_index_topk_fp8")
 
 
 class DsaError(RuntimeError):
@@ -85,8 +85,11 @@ def _load() -> ctypes.CDLL:
     lib.dsa_index_topk_workspace_size.argtypes = [ci, ci, ci]
     lib.dsa_index_topk_workspace_size.restype = sz
     lib.dsa_index_topk.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, sz, vp]
+    lib.dsa_index_topk_fp8.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp,
+                                       sz, vp]
     for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_index_scores_fp8", "dsa_topk",
                  "dsa_indexer_loss", "dsa_indexer_loss_bwd", "dsa_index_topk",
+                 "dsa_index_topk_fp8",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense", "dsa_sparse_attn_bwd",
                  "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_noalloc"):
         getattr(lib, name).restype = ci
@@ -466,11 +469,12 @@ def index_topk_workspace_bytes(B, S, block_rows) -> int:
 
 
 def dsa_index_topk(q_idx, k_idx, w, k: int, seg=None, block_rows: int = 2048, idx=None,
-                   count=None, ws=None, stream=None):
+                   count=None, ws=None, stream=None, k_scale=None):
     """Indexer scores and top-k fused through blocks of query rows (no [B,S,S] scores).
 
-    Same arguments and results as dsa_index_scores followed by dsa_topk; the scores of
-    one block of block_rows query rows (a multiple of 256) live in `ws`.
+    Same arguments and results as dsa_index_scores (or dsa_index_scores_fp8, for e4m3
+    q_idx / k_idx, with k_scale) followed by dsa_topk; the scores of one block of
+    block_rows query rows (a multiple of 256) live in `ws`.
     """
     B, S, Hi, Di = q_idx.shape
     dev = q_idx.device
@@ -482,13 +486,20 @@ def dsa_index_topk(q_idx, k_idx, w, k: int, seg=None, block_rows: int = 2048, id
     if ws is None:
         ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
     w_dtype = DSA_F32 if w.dtype == torch.float32 else DSA_BF16
-    rc = lib.dsa_index_topk(_dev(q_idx, "q_idx", torch.bfloat16), _dev(k_idx, "k_idx", torch.bfloat16),
-                            _dev(w, "w"), w_dtype,
-                            None if seg is None else _dev(seg, "seg", torch.int32),
-                            B, S, Hi, Di, k, block_rows, _dev(idx, "idx", torch.int32),
-                            _dev(count, "count", torch.int32), _dev(ws, "ws"),
-                            ws.numel() * ws.element_size(), _stream(stream))
-    _check(rc, "dsa_index_topk")
+    tail = (None if seg is None else _dev(seg, "seg", torch.int32), B, S, Hi, Di, k, block_rows,
+            _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32), _dev(ws, "ws"),
+            ws.numel() * ws.element_size(), _stream(stream))
+    if q_idx.dtype in _FP8_DTYPES:
+        rc = lib.dsa_index_topk_fp8(_dev8(q_idx, "q_idx"), _dev8(k_idx, "k_idx"),
+                                    None if k_scale is None else _dev(k_scale, "k_scale",
+                                                                      torch.float32),
+                                    _dev(w, "w"), w_dtype, *tail)
+        _check(rc, "dsa_index_topk_fp8")
+    else:
+        rc = lib.dsa_index_topk(_dev(q_idx, "q_idx", torch.bfloat16),
+                                _dev(k_idx, "k_idx", torch.bfloat16), _dev(w, "w"), w_dtype,
+                                *tail)
+        _check(rc, "dsa_index_topk")
     return idx, count
 
 

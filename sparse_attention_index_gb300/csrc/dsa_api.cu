@@ -220,10 +220,17 @@ size_t dsa_index_topk_workspace_size(int B, int S, int block_rows) {
   return static_cast<size_t>(B) * rows * ld * sizeof(float);
 }
 
-int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
-                   const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
-                   int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+int index_topk_impl(const void* q_idx, const void* k_idx, const float* k_scale, const void* w,
+                    int w_dtype, const int32_t* seg, int B, int S, int Hi, int Di, int k,
+                    int block_rows, int32_t* idx, int32_t* count, void* ws, size_t ws_bytes,
+                    void* stream, int fp8) {
   if (!q_idx || !k_idx || !w || !idx) return DSA_ERR_INVALID_ARG;
+  if (k_scale && !aligned16(k_scale)) return DSA_ERR_INVALID_ARG;
+  if (fp8 && Di % 16 != 0) return DSA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || Hi < 1 || Di < 1 || k < 1) return DSA_ERR_INVALID_ARG;
   if (block_rows < 256 || block_rows % 256 != 0) return DSA_ERR_INVALID_ARG;
   if (w_dtype != DSA_F32 && w_dtype != DSA_BF16) return DSA_ERR_INVALID_ARG;
@@ -241,7 +248,7 @@ int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dt
   for (int t_lo = 0; t_lo < S; t_lo += R) {
     const int t_hi = t_lo + R < S ? t_lo + R : S;
     int rc = dsa::launch_index_scores_rows(q_idx, k_idx, w, w_dtype == DSA_BF16, seg, B, S, Hi,
-                                           Di, buf, ld, as_stream(stream), 0, nullptr, t_lo,
+                                           Di, buf, ld, as_stream(stream), fp8, k_scale, t_lo,
                                            t_hi, R);
     if (rc != DSA_OK) return rc;
     rc = dsa::launch_topk_rows(buf, ld, seg, B, S, k, idx, count, as_stream(stream), t_lo, t_hi,
@@ -249,6 +256,25 @@ int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dt
     if (rc != DSA_OK) return rc;
   }
   return DSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
+                   const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
+                   int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream) {
+  return index_topk_impl(q_idx, k_idx, nullptr, w, w_dtype, seg, B, S, Hi, Di, k, block_rows,
+                         idx, count, ws, ws_bytes, stream, 0);
+}
+
+int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scale, const void* w,
+                       int w_dtype, const int32_t* seg, int B, int S, int Hi, int Di, int k,
+                       int block_rows, int32_t* idx, int32_t* count, void* ws, size_t ws_bytes,
+                       void* stream) {
+  return index_topk_impl(q_idx, k_idx, k_scale, w, w_dtype, seg, B, S, Hi, Di, k, block_rows,
+                         idx, count, ws, ws_bytes, stream, 1);
 }
 
 int dsa_indexer_loss(const void* Q, const void* K, const int32_t* idx, const float* lse,

@@ -647,3 +647,25 @@ def test_index_topk_long_rows_match_unfused_path():
     ref_idx, ref_cnt = oracle.topk(sc, None, S, k, rows=rows, B=B)
     assert np.array_equal(idx_f.cpu().numpy().reshape(-1, k)[rows], ref_idx)
     assert np.array_equal(cnt_f.cpu().numpy().reshape(-1)[rows], ref_cnt)
+
+
+@pytest.mark.parametrize("case", [
+    # B, S, Hi, Di, k, ndocs, k_scale, block_rows
+    (2, 700, 64, 128, 64, 0, "pow2", 256),
+    (1, 489, 64, 128, 200, 3, "pow2", 256),
+    (1, 1000, 8, 64, 100, 2, "none", 512),
+])
+def test_index_topk_fp8_matches_oracle(case):
+    """The e4m3 indexer through query blocks: the oracle's e4m3 scores, then its top-k."""
+    dsa = _dsa()
+    B, S, Hi, Di, k, ndocs, k_scale, R = case
+    _, inp = _fp8_inputs(B, S, Hi, Di, ndocs, k_scale, seed=640 + S)
+    seg = None if inp["seg"] is None else dev(inp["seg"])
+    ks = None if inp["k_scale"] is None else dev(inp["k_scale"])
+    idx, cnt = dsa.dsa_index_topk(dev(inp["q_idx"]), dev(inp["k_idx"]), dev(inp["w"]), k, seg,
+                                  block_rows=R, k_scale=ks)
+    assert dsa.dsa_get_last_device_error() == 0
+    sc = oracle.index_scores_fp8(inp["q_idx"], inp["k_idx"], inp["w"], inp["seg"], inp["k_scale"])
+    ref_idx, ref_cnt = oracle.topk(sc, inp["seg"], S, k, B=B)
+    assert np.array_equal(idx.cpu().numpy().reshape(-1, k), ref_idx)
+    assert np.array_equal(cnt.cpu().numpy().reshape(-1), ref_cnt)
