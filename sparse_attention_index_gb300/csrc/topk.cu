@@ -644,7 +644,10 @@ namespace lr {
 constexpr int NT = 1024;
 constexpr int NW = NT / 32;
 constexpr int kLongWords = 4096;   // bitmap words: rows up to 131072 keys
-constexpr int kLongCand = 4096;
+// candidates of the one-pass path: each warp appends to its own segment of 256; at
+// S = 131072 a row leaves about 3.3K candidates, ~105 per warp, and segments of 128
+// overflowed on about half of the rows beyond t = 90K
+constexpr int kLongCand = 8192;
 constexpr int kWpt = kLongWords / NT;   // bitmap words per thread
 
 struct Smem {
@@ -1042,12 +1045,13 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
         __syncthreads();
         if (tid == 0) sm->ubc[7] = 0u;   // reused as the in-bin counter below
         __syncthreads();
-        if (fits && C >= p.k) {
-          // every key >= L is a candidate and there are at least k: the bin of the k-th
-          // largest candidate is the row's threshold bin. Candidates above it go to the
-          // bitmap, those in it become the list (staged in eqw, which is zeroed after).
-          int bin, above, in_bin;
-          find_bin(sm->hist, 2048, p.k, sm, bin, above, in_bin);
+        int bin = 0, above = 0, in_bin = 0;
+        // every key >= L is a candidate and there are at least k: the bin of the k-th
+        // largest candidate is the row's threshold bin
+        if (fits && C >= p.k) find_bin(sm->hist, 2048, p.k, sm, bin, above, in_bin);
+        if (fits && C >= p.k && in_bin <= kLongWords) {
+          // candidates above the threshold bin go to the bitmap, those in it become the
+          // list (staged in eqw, which is zeroed after)
           const uint32_t b1 = static_cast<uint32_t>(bin);
           for (int j = lane; j < sm->wcnt[wid]; j += 32) {
             const uint32_t sj = seg[j];
