@@ -241,6 +241,20 @@ def test_topk_rows_longer_than_the_shared_stage():
                 k, rows)
 
 
+def test_topk_long_rows_k2048():
+    """Rows of 16384 to 32767 keys with k = 2048, the long-context regime of the long-row
+    kernel's one-pass path (thousands of candidates per row): sampled rows against the oracle."""
+    dsa = _dsa()
+    S, k = 32768, 2048
+    rng = np.random.default_rng(11)
+    sc = rng.standard_normal((1, S, S), dtype=np.float32)
+    idx, cnt = dsa.dsa_topk(dev(sc), k)
+    assert dsa.dsa_get_last_device_error() == 0
+    rows = np.array([16383, 16384, 16385, 20000, 24575, 28000, 32767], dtype=np.int64)
+    _check_topk(idx.cpu().numpy(), cnt.cpu().numpy(), sc[0][rows].astype(np.float64), None, S,
+                k, rows)
+
+
 def test_topk_golden_fixtures_on_gpu():
     from test_oracle_pins import _parse_golden
     dsa = _dsa()
