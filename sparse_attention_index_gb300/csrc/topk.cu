@@ -68,7 +68,8 @@ struct TopkSmem {
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
   if (u == 0x80000000u) u = 0u;
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  // negative: all bits flipped; otherwise the sign bit set
+  return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
 }
 
 // Inclusive block scan of one int per thread; returns the inclusive value and
@@ -681,6 +682,11 @@ struct RowKeys {
     }
     return make_uint4(kq[0], kq[1], kq[2], kq[3]);
   }
+  // a group of four keys of the row with no segment ids (4c + 3 < len)
+  __device__ __forceinline__ uint4 load4_full(int c) const {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(srow) + c);
+    return make_uint4(order_key(f.x), order_key(f.y), order_key(f.z), order_key(f.w));
+  }
   __device__ __forceinline__ uint32_t key(int s) const { return order_key(__ldg(srow + s)); }
 };
 
@@ -1008,12 +1014,18 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
         uint32_t* segk = sm->ckey + wid * kSeg;
         int wc = 0;
         const uint32_t lt = (1u << lane) - 1u;
+        // invalid keys map to 0, every valid one to at least 1
+        const uint32_t Lv = L > 0u ? L : 1u;
+        // groups that lie wholly inside the row need no per-key validity when there are
+        // no segment ids
+        const int nfull = rk.seg_row ? 0 : len >> 2;
         for (int c0 = 0; c0 < nq; c0 += 4 * NT) {
           uint4 kv[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int c = c0 + u * NT + tid;
-            kv[u] = c < nq ? rk.load4(c) : make_uint4(0u, 0u, 0u, 0u);
+            kv[u] = c < nfull ? rk.load4_full(c)
+                              : (c < nq ? rk.load4(c) : make_uint4(0u, 0u, 0u, 0u));
           }
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -1021,7 +1033,7 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
             const int c = c0 + u * NT + tid;
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const bool cd = kk[e] != 0u && kk[e] >= L;
+              const bool cd = kk[e] >= Lv;
               const uint32_t bal = __ballot_sync(0xffffffffu, cd);
               const int r = wc + __popc(bal & lt);
               if (cd && r < kSeg) {
