@@ -105,3 +105,19 @@ def test_index_topk_validation(dsa):
     assert f(P, P, P, 1, None, 1, 1024, 48, 128, 8, 256, P, P, P, need, None) == 2     # Hi not 2^n
     assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need - 16, None) == 3  # small ws
     assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, None, need, None) == 3   # no ws
+
+
+def test_index_topk_fp8_validation(dsa):
+    """The e4m3 form of the fused indexer + top-k refuses the same bad arguments, plus a
+    misaligned key scale and an index head dim that is not a multiple of 16."""
+    f = dsa.lib.dsa_index_topk_fp8
+    need = dsa.lib.dsa_index_topk_workspace_size(1, 1024, 256)
+    # q_idx, k_idx, k_scale, w, w_dtype, seg, B, S, Hi, Di, k, block_rows, idx, count, ws,
+    # ws_bytes, stream
+    assert f(None, P, None, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need, None) == 1
+    odd = ctypes.c_void_p((1 << 20) + 4)   # k_scale not on a 16-byte boundary
+    assert f(P, P, odd, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need, None) == 1
+    assert f(P, P, None, P, 1, None, 1, 1024, 64, 40, 8, 256, P, P, P, need, None) == 1
+    assert f(P, P, None, P, 1, None, 1, 1024, 64, 128, 8, 100, P, P, P, need, None) == 1
+    assert f(P, P, None, P, 1, None, 1, 1024, 48, 128, 8, 256, P, P, P, need, None) == 2
+    assert f(P, P, None, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need - 16, None) == 3
