@@ -79,6 +79,12 @@ def stage_work(wl: synth.Workload):
     }
 
 
+def step_flop(wl: synth.Workload, stages) -> float:
+    """Whole-step FLOP: the contractions of the stages that ran, each counted once."""
+    work = stage_work(wl)
+    return sum(work[s]["flop"] for s in stages if "flop" in work[s])
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -528,7 +534,7 @@ def main(argv=None):
     peaks = load_peaks()
     work = stage_work(wl)
     tokens = wl.B * wl.S
-    total_flop = sum(work[s]["flop"] for s in r["stages"] if "flop" in work[s])
+    total_flop = step_flop(wl, r["stages"])
     stages_out = {}
     for s in r["stages"]:
         ms = r["stage_ms"][s]

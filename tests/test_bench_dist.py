@@ -83,3 +83,19 @@ def test_reference_arm_under_two_ranks():
     assert line["n_gpus"] == 2
     assert line["unit"] == "tokens/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_step_flop_counts_each_stage_that_ran_once():
+    """The whole-step TFLOP/s of the bench line: the fused indexer + top-k counts the indexer's
+    contraction once, and the loss stages count only when they run."""
+    import bench
+    import synth
+    wl = synth.WORKLOADS["v32_671b_s16k"]
+    causal, sel = bench.pair_counts(wl)
+    unfused = bench.step_flop(wl, ["indexer", "topk", "attn_fwd", "attn_bwd"])
+    assert unfused == (2.0 * wl.Hi * wl.Di * causal + 2.0 * wl.H * (wl.Dqk + wl.Dv) * sel
+                       + 2.0 * wl.H * (3 * wl.Dqk + 2 * wl.Dv) * sel)
+    assert bench.step_flop(wl, ["indexer_topk", "attn_fwd", "attn_bwd"]) == unfused
+    with_loss = bench.step_flop(wl, ["indexer", "topk", "attn_fwd", "attn_bwd", "loss_fwd",
+                                     "loss_bwd"])
+    assert with_loss == unfused + 2.0 * wl.H * wl.Dqk * sel + 3 * 2.0 * wl.Hi * wl.Di * sel
