@@ -248,6 +248,8 @@ def run_ours(args, wl, rank, world, local_rank):
     count = torch.empty((B, S), dtype=torch.int32, device=device)
     O = torch.empty((B, S, wl.H, wl.Dv), dtype=torch.bfloat16, device=device)
     lse = torch.empty((B, S, wl.H), dtype=torch.float32, device=device)
+    fwd_ws = torch.empty((max(dsa.fwd_workspace_bytes(B, S, wl.H, wl.Hkv, wl.Dqk, wl.Dv), 16),),
+                         dtype=torch.uint8, device=device)
     if wl.backward:
         dQ = torch.empty_like(Q)
         dK = torch.empty_like(K)
@@ -297,7 +299,7 @@ def run_ours(args, wl, rank, world, local_rank):
             dsa.dsa_topk(scores, k, seg, idx=idx, count=count, stream=stream)
         ev[e].record(stream)
         e += 1
-        dsa.dsa_sparse_attn_fwd(Q, K, V, idx, wl.scale, O=O, lse=lse, stream=stream)
+        dsa.dsa_sparse_attn_fwd(Q, K, V, idx, wl.scale, O=O, lse=lse, ws=fwd_ws, stream=stream)
         ev[e].record(stream)
         e += 1
         if wl.backward:
@@ -344,13 +346,10 @@ def run_ours(args, wl, rank, world, local_rank):
 
     # ---- end to end through the public API: pinned host in, host out
     e2e = None
-    if fp8 and not args.no_e2e:
-        e2e = {"unavailable": "the host pipeline takes bf16 indexer inputs"}
-    if fused and not args.no_e2e:
-        e2e = {"unavailable": "the host pipeline runs the unfused indexer and top-k"}
-    if not args.no_e2e and not fp8 and not fused:
+    if not args.no_e2e:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
-        h_in = {"q_idx": pin(ind["q_idx"]), "k_idx": pin(ind["k_idx"]), "w": pin(ind["w"]),
+        src = ind8 if fp8 else ind   # e4m3 bytes of the same dyadic values
+        h_in = {"q_idx": pin(src["q_idx"]), "k_idx": pin(src["k_idx"]), "w": pin(ind["w"]),
                 "Q": pin(att["Q"]), "K": pin(att["K"]), "V": pin(att["V"])}
         if seg is not None:
             h_in["seg"] = pin(ind["seg"])
@@ -360,7 +359,9 @@ def run_ours(args, wl, rank, world, local_rank):
         # three streams, overlapped (sparse_attention_index_gb300.HostPipeline)
         pipe = dsa.HostPipeline(B, S, wl.Hi, wl.Di, wl.H, wl.Dqk, wl.Dv, k, wl.scale,
                                 backward=wl.backward, segments=seg is not None, device=device,
-                                Hkv=wl.Hkv, indexer_loss=loss)
+                                Hkv=wl.Hkv, indexer_loss=loss,
+                                indexer_dtype="e4m3" if fp8 else "bf16",
+                                fused_block_rows=args.fused_topk if fused else 0)
         h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in pipe.out.items()}
         h2d = sum(t.numel() * t.element_size() for t in h_in.values())
         d2h = sum(t.numel() * t.element_size() for t in h_out.values())

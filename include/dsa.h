@@ -176,12 +176,20 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* seg, int B, 
  * rows and puts the heads on the 128 lanes of a tile. The other evaluates dense
  * 128 x 128 (query, key) tiles of one head under a bitmap of the selection and
  * skips tiles without a selected key (see dsa_sparse_attn_fwd_dense). The call
- * takes the one with fewer tile products for the shape. The dense-tile kernel
- * allocates its bitmap (B*S*ceil(S/128)*16 bytes) stream-ordered on `stream`.
+ * takes the one with fewer tile products for the shape.
+ *
+ *   ws  workspace of dsa_sparse_attn_fwd_workspace_size() bytes, 16-byte aligned:
+ *       the dense-tile kernel's selection bitmap and tile flags (overwritten). It
+ *       is reserved whenever that kernel can take the shape, whichever kernel
+ *       the call then picks; where the size is 0, ws may be NULL.
+ *
+ * DSA_ERR_WORKSPACE if ws is NULL, misaligned or smaller than the size (when the
+ * size is not 0).
  */
+size_t dsa_sparse_attn_fwd_workspace_size(int B, int S, int H, int Hkv, int Dqk, int Dv);
 int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
                         int S, int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O,
-                        float* lse, void* stream);
+                        float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * dsa_sparse_attn_fwd_kernel - which kernel dsa_sparse_attn_fwd runs for a shape:
@@ -201,13 +209,14 @@ int dsa_sparse_attn_fwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, in
  * dsa_sparse_attn_fwd_dense - the same result from the dense-tile kernel only
  * (the pages' own design evaluates the masked logits as dense blocks with
  * partial mask blocks: "Support Ring Attention with DeepSeek DSA Sparse
- * Indexer", Forward Flow). Arguments as for dsa_sparse_attn_fwd. Supported:
- * any Hkv dividing H, 1 <= H <= 128, (Dqk, Dv) in {(128, 128), (192, 128)},
- * S <= 65536, a positive scale; DSA_ERR_UNSUPPORTED otherwise.
+ * Indexer", Forward Flow). Arguments, workspace included, as for
+ * dsa_sparse_attn_fwd. Supported: any Hkv dividing H, 1 <= H <= 128, (Dqk, Dv)
+ * in {(128, 128), (192, 128)}, S <= 65536, a positive scale; DSA_ERR_UNSUPPORTED
+ * otherwise.
  */
 int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
                               int B, int S, int H, int Hkv, int Dqk, int Dv, int k, float scale,
-                              void* O, float* lse, void* stream);
+                              void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * dsa_sparse_attn_bwd - gradients of the sparse attention ("Support Ring
@@ -221,8 +230,10 @@ int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const
  *   Q, K, V, idx as for the forward; O, lse the forward's outputs;
  *   dO bf16 [B, S, H, Dv];  dQ bf16 [B, S, H, Dqk] out;
  *   dK bf16 [B, S, Hkv, Dqk] out;  dV bf16 [B, S, Hkv, Dv] out;
- *   ws  workspace of dsa_sparse_attn_bwd_workspace_size() bytes (fp32 dK/dV
- *       accumulators; overwritten).
+ *   ws  workspace of dsa_sparse_attn_bwd_workspace_size() bytes, 16-byte aligned
+ *       (overwritten): the fp32 dK/dV accumulators [B*S*Hkv, Dqk + Dv] rounded up
+ *       to 256 bytes, then, whenever the dense-tile kernels can take the shape,
+ *       their selection bitmap, tile flags and Delta (fp32 [B, S, H]).
  *
  * Supported shapes as for the forward. dK/dV are summed with fp32 atomics, so
  * their rounding order is not fixed from run to run.
@@ -239,8 +250,7 @@ int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32
  * (batch, key tile, group of heads) items, both under the bitmap of the selection
  * (the pages' design: dense blocks with partial mask blocks and a key-major pass
  * for dK / dV, "Support Ring Attention with DeepSeek DSA Sparse Indexer",
- * Backward Flow). Arguments as for dsa_sparse_attn_bwd; the bitmap and Delta
- * (B*S*ceil(S/128)*16 + B*S*H*4 bytes) are allocated stream-ordered on `stream`.
+ * Backward Flow). Arguments, workspace included, as for dsa_sparse_attn_bwd.
  * Supported: any Hkv dividing H, 1 <= H <= 128, (Dqk, Dv) in {(128, 128),
  * (192, 128)}, S <= 65536, a positive scale; DSA_ERR_UNSUPPORTED otherwise.
  * dsa_sparse_attn_bwd takes these kernels when they have fewer tile products for
@@ -289,7 +299,8 @@ int dsa_sparse_attn_bwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, in
  *    accumulating, so calls whose work overlaps on the GPU (two streams, or
  *    two host threads) race and corrupt each other's dK/dV. Serialise them.
  *  - Arguments, supported shapes and results are those of dsa_sparse_attn_bwd
- *    with Hkv = 1 (per-head K/V needs the dense-tile kernels, which allocate).
+ *    with Hkv = 1 (per-head K/V needs the dense-tile kernels, whose scratch is
+ *    part of dsa_sparse_attn_bwd's workspace).
  */
 #define DSA_NOALLOC_BWD_MAX_FLOATS 8388608
 int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const void* V, const int32_t* idx,

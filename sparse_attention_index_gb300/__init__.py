@@ -37,7 +37,8 @@ STATUS = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "D
 # every symbol include/dsa.h declares
 EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa_index_scores",
            "dsa_index_scores_fp8",
-           "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense",
+           "dsa_topk_workspace_size", "dsa_topk", "dsa_sparse_attn_fwd_workspace_size",
+           "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense",
            "dsa_sparse_attn_fwd_kernel", "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_kernel",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
            "dsa_sparse_attn_bwd_noalloc", "dsa_indexer_loss", "dsa_indexer_loss_bwd",
@@ -66,7 +67,10 @@ def _load() -> ctypes.CDLL:
     lib.dsa_topk_workspace_size.argtypes = [ci, ci, ci]
     lib.dsa_topk_workspace_size.restype = sz
     lib.dsa_topk.argtypes = [vp, i64, vp, ci, ci, ci, vp, vp, vp, sz, vp]
-    lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp]
+    lib.dsa_sparse_attn_fwd_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
+    lib.dsa_sparse_attn_fwd_workspace_size.restype = sz
+    lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp,
+                                        sz, vp]
     lib.dsa_sparse_attn_fwd_dense.argtypes = lib.dsa_sparse_attn_fwd.argtypes
     lib.dsa_sparse_attn_fwd_kernel.argtypes = [ci, ci, ci, ci, ci, ci, ci, cf]
     lib.dsa_sparse_attn_fwd_kernel.restype = ci
@@ -199,9 +203,16 @@ def dsa_topk(scores, k: int, seg=None, S: int | None = None, idx=None, count=Non
     return idx, count
 
 
-def dsa_sparse_attn_fwd(Q, K, V, idx, scale: float, O=None, lse=None, stream=None,
+def fwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv) -> int:
+    return int(lib.dsa_sparse_attn_fwd_workspace_size(B, S, H, Hkv, Dqk, Dv))
+
+
+def dsa_sparse_attn_fwd(Q, K, V, idx, scale: float, O=None, lse=None, ws=None, stream=None,
                         _entry: str = "dsa_sparse_attn_fwd"):
-    """Q [B,S,H,Dqk], K [B,S,Hkv,Dqk], V [B,S,Hkv,Dv] bf16, idx [B,S,k] -> (O bf16, lse fp32)."""
+    """Q [B,S,H,Dqk], K [B,S,Hkv,Dqk], V [B,S,Hkv,Dv] bf16, idx [B,S,k] -> (O bf16, lse fp32).
+
+    ws: a device byte buffer of at least fwd_workspace_bytes(...) (allocated here if None).
+    """
     B, S, H, Dqk = Q.shape
     Hkv, Dv = V.shape[2], V.shape[3]
     k = idx.shape[2]
@@ -209,10 +220,15 @@ def dsa_sparse_attn_fwd(Q, K, V, idx, scale: float, O=None, lse=None, stream=Non
         O = torch.empty((B, S, H, Dv), dtype=torch.bfloat16, device=Q.device)
     if lse is None:
         lse = torch.empty((B, S, H), dtype=torch.float32, device=Q.device)
+    need = fwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv)
+    if ws is None and need > 0:
+        ws = torch.empty((need,), dtype=torch.uint8, device=Q.device)
     rc = getattr(lib, _entry)(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
                               _dev(V, "V", torch.bfloat16), _dev(idx, "idx", torch.int32),
                               B, S, H, Hkv, Dqk, Dv, k, float(scale),
                               _dev(O, "O", torch.bfloat16), _dev(lse, "lse", torch.float32),
+                              None if ws is None else _dev(ws, "ws"),
+                              0 if ws is None else ws.numel() * ws.element_size(),
                               _stream(stream))
     _check(rc, _entry)
     return O, lse
@@ -229,9 +245,10 @@ def dsa_sparse_attn_fwd_kernel(B, S, H, Hkv, Dqk, Dv, k, scale: float) -> int:
     return r
 
 
-def dsa_sparse_attn_fwd_dense(Q, K, V, idx, scale: float, O=None, lse=None, stream=None):
+def dsa_sparse_attn_fwd_dense(Q, K, V, idx, scale: float, O=None, lse=None, ws=None,
+                              stream=None):
     """dsa_sparse_attn_fwd through the dense-tile kernel only (same arguments and result)."""
-    return dsa_sparse_attn_fwd(Q, K, V, idx, scale, O=O, lse=lse, stream=stream,
+    return dsa_sparse_attn_fwd(Q, K, V, idx, scale, O=O, lse=lse, ws=ws, stream=stream,
                                _entry="dsa_sparse_attn_fwd_dense")
 
 
@@ -253,7 +270,7 @@ def dsa_sparse_attn_bwd(Q, K, V, idx, O, lse, dO, scale: float, dQ=None, dK=None
     if dV is None:
         dV = torch.empty((B, S, Hkv, Dv), dtype=torch.bfloat16, device=dev)
     need = bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv)
-    if ws is None:
+    if ws is None:   # the fp32 dK / dV accumulators and the dense-tile kernels' scratch
         ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
     rc = getattr(lib, _entry)(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
                               _dev(V, "V", torch.bfloat16), _dev(idx, "idx", torch.int32),
@@ -322,16 +339,27 @@ class HostPipeline:
     """
 
     def __init__(self, B, S, Hi, Di, H, Dqk, Dv, topk, scale, backward=True, segments=False,
-                 device=None, Hkv=1, indexer_loss=False, grad_scale=None):
+                 device=None, Hkv=1, indexer_loss=False, grad_scale=None, indexer_dtype="bf16",
+                 fused_block_rows=0):
         """indexer_loss: also run the indexer loss (objective grad_scale * sum of the
         per-query losses, default 1/(B*S)) and its gradient each step, returning kl,
-        dq_idx, dk_idx and dw."""
+        dq_idx, dk_idx and dw. indexer_dtype "e4m3": q_idx / k_idx are e4m3 bytes and the
+        fp8 indexer runs. fused_block_rows > 0: the indexer and the top-k run fused through
+        blocks of that many query rows (dsa_index_topk), with no [B, S, S] score matrix."""
+        if indexer_dtype not in ("bf16", "e4m3"):
+            raise ValueError("indexer_dtype is 'bf16' or 'e4m3'")
+        if indexer_loss and (indexer_dtype != "bf16" or fused_block_rows):
+            raise ValueError("the indexer loss reads the bf16 indexer inputs and the score matrix")
         dev = torch.device("cuda") if device is None else torch.device(device)
         self.dev, self.topk, self.scale, self.backward = dev, topk, scale, backward
         self.loss = indexer_loss
+        self.fp8 = indexer_dtype == "e4m3"
+        self.block_rows = fused_block_rows
         self.grad_scale = 1.0 / (B * S) if grad_scale is None else grad_scale
         e = lambda *shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
-        self.d = {"q_idx": e(B, S, Hi, Di), "k_idx": e(B, S, Di), "w": e(B, S, Hi, dt=torch.float32)}
+        idt = torch.uint8 if self.fp8 else torch.bfloat16
+        self.d = {"q_idx": e(B, S, Hi, Di, dt=idt), "k_idx": e(B, S, Di, dt=idt),
+                  "w": e(B, S, Hi, dt=torch.float32)}
         if segments:
             self.d["seg"] = e(B, S, dt=torch.int32)
         self.big = []
@@ -342,7 +370,13 @@ class HostPipeline:
             self.big.append(sets)
         self.n = 0
         ld = (S + 3) // 4 * 4
-        self.scores = e(B, S, ld, dt=torch.float32)
+        if fused_block_rows:   # one block of query rows of scores
+            self.scores = None
+            self.topk_ws = e(max(index_topk_workspace_bytes(B, S, fused_block_rows), 16),
+                             dt=torch.uint8)
+        else:
+            self.scores = e(B, S, ld, dt=torch.float32)
+        self.fwd_ws = e(max(fwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv), 16), dt=torch.uint8)
         self.out = {"idx": e(B, S, topk, dt=torch.int32), "count": e(B, S, dt=torch.int32),
                     "O": e(B, S, H, Dv), "lse": e(B, S, H, dt=torch.float32)}
         if backward:
@@ -398,17 +432,27 @@ class HostPipeline:
         sc = self.s_c
         sc.wait_event(in1)
         self._wait(sc, self.ev_out1)
-        dsa_index_scores(d["q_idx"], d["k_idx"], d["w"], d.get("seg"), scores=self.scores,
-                         stream=sc)
+        if self.block_rows:
+            dsa_index_topk(d["q_idx"], d["k_idx"], d["w"], self.topk, d.get("seg"),
+                           block_rows=self.block_rows, idx=o["idx"], count=o["count"],
+                           ws=self.topk_ws, stream=sc)
+        elif self.fp8:
+            dsa_index_scores_fp8(d["q_idx"], d["k_idx"], d["w"], d.get("seg"),
+                                 scores=self.scores, stream=sc)
+        else:
+            dsa_index_scores(d["q_idx"], d["k_idx"], d["w"], d.get("seg"), scores=self.scores,
+                             stream=sc)
         idx_read = ev()
         idx_read.record(sc)
-        dsa_topk(self.scores, self.topk, d.get("seg"), idx=o["idx"], count=o["count"], stream=sc)
+        if not self.block_rows:
+            dsa_topk(self.scores, self.topk, d.get("seg"), idx=o["idx"], count=o["count"],
+                     stream=sc)
         topk_done = ev()
         topk_done.record(sc)
         sc.wait_event(in2)
         self._wait(sc, self.ev_out2)
         dsa_sparse_attn_fwd(bd["Q"], bd["K"], bd["V"], o["idx"], self.scale, O=o["O"],
-                            lse=o["lse"], stream=sc)
+                            lse=o["lse"], ws=self.fwd_ws, stream=sc)
         fwd_done = ev()
         fwd_done.record(sc)
         bwd_done = fwd_done

@@ -312,7 +312,7 @@ int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scal
 int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                     const void* O, const float* lse, const void* dO, int B, int S, int H, int Dqk,
                     int Dv, int k, float scale, void* dQ, void* dK, void* dV, float* ws_dkv,
-                    cudaStream_t stream, int path, int Hkv) {
+                    cudaStream_t stream, int path, int Hkv, void* scratch) {
   AttnParams p = make_attn_params(Q, K, V, idx, B, S, H, k, scale);
   p.Hkv = Hkv;
   p.O_in = static_cast<const uint16_t*>(O);
@@ -320,10 +320,12 @@ int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* 
   p.dO = static_cast<const uint16_t*>(dO);
   p.dQ = static_cast<uint16_t*>(dQ);
   p.ws = ws_dkv;
+  p.scratch = static_cast<uint8_t*>(scratch);
   const long long rows = static_cast<long long>(B) * S;
   if (rows * H > 0x7fffffffLL || H > 128 || Hkv < 1 || H % Hkv != 0) return DSA_ERR_UNSUPPORTED;
   const bool dense_ok = attn_bwd_dense_supported(B, S, H, Dqk, Dv, scale);
-  // per-head or grouped K / V: the dense-tile kernels only (they allocate their bitmap)
+  // per-head or grouped K / V: the dense-tile kernels only, whose scratch the no-allocation
+  // path does not have
   if (Hkv > 1 && (!dense_ok || path == kBwdPathNoAlloc)) return DSA_ERR_UNSUPPORTED;
   if (path == kBwdPathDense && !dense_ok) return DSA_ERR_UNSUPPORTED;
   if (cudaMemsetAsync(ws_dkv, 0, static_cast<size_t>(rows) * Hkv * (Dqk + Dv) * sizeof(float),

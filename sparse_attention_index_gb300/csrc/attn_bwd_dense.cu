@@ -969,50 +969,42 @@ int launch_bwd_dense_dims(const AttnParams& p, cudaStream_t stream) {
   const int QT = (p.S + kT - 1) / kT;
   const int W4 = QT * 4;
   const long long rows = static_cast<long long>(p.B) * p.S;
-  const size_t bits_bytes = static_cast<size_t>(rows) * W4 * sizeof(uint32_t);
-  const size_t any_off = (bits_bytes + 255) / 256 * 256;
+  // the bitmap, the tile flags and Delta live in the caller's workspace
+  if (p.scratch == nullptr) return DSA_ERR_WORKSPACE;
+  const DenseScratch ly = dense_scratch_layout(p.B, p.S, p.H, p.Hkv, DQK, DV, true);
   const size_t any_bytes = static_cast<size_t>(p.B) * QT * QT;
-  const size_t delta_off = (any_off + any_bytes + 255) / 256 * 256;
-  const size_t delta_bytes = static_cast<size_t>(rows) * p.H * sizeof(float);
-  void* ws = nullptr;
-  if (cudaMallocAsync(&ws, delta_off + delta_bytes, stream) != cudaSuccess) return DSA_ERR_CUDA;
   DenseBwdParams dp;
   dp.a = p;
-  dp.bits = static_cast<uint32_t*>(ws);
-  dp.any = static_cast<uint8_t*>(ws) + any_off;
-  dp.delta = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + delta_off);
+  dp.bits = reinterpret_cast<uint32_t*>(p.scratch + ly.bits_off);
+  dp.any = p.scratch + ly.any_off;
+  dp.delta = reinterpret_cast<float*>(p.scratch + ly.delta_off);
   dp.W4 = W4;
   dp.QT = QT;
-  int rc = DSA_OK;
   CUtensorMap mk, mv, mq, mdo;
   const size_t smem_a = LA::kTailOff + sizeof(DqTail), smem_b = LB::kTailOff + sizeof(DkvTail);
   auto ka = attn_bwd_dense_dq_kernel<DQK, DV>;
   auto kb = attn_bwd_dense_dkv_kernel<DQK, DV>;
-  if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + any_off, 0, any_bytes, stream) != cudaSuccess ||
+  if (cudaMemsetAsync(p.scratch + ly.any_off, 0, any_bytes, stream) != cudaSuccess ||
       !make_kv_map(&mk, p.K, rows, p.Hkv, DQK) || !make_kv_map(&mv, p.V, rows, p.Hkv, DV) ||
       !make_head_rows_map(&mq, p.Q, rows, p.H, DQK) ||
       !make_head_rows_map(&mdo, p.dO, rows, p.H, DV) ||
       cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_a)) != cudaSuccess ||
       cudaFuncSetAttribute(kb, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem_b)) != cudaSuccess) {
-    rc = DSA_ERR_CUDA;
-  } else {
-    launch_dense_mask(p.idx, p.B, p.S, p.k, W4, QT, const_cast<uint32_t*>(dp.bits),
-                      const_cast<uint8_t*>(dp.any), p.err, stream);
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long items_a = static_cast<long long>(QT) * p.B * p.H;
-    const long long items_b =
-        static_cast<long long>(QT) * p.B * ((p.H + kGroupHeads - 1) / kGroupHeads);
-    ka<<<static_cast<int>(items_a < sms ? items_a : sms), kThreadsB, smem_a, stream>>>(mk, mv, dp);
-    kb<<<static_cast<int>(items_b < sms ? items_b : sms), kThreadsB, smem_b, stream>>>(mk, mv, mq,
-                                                                                      mdo, dp);
-    if (cudaGetLastError() != cudaSuccess) rc = DSA_ERR_CUDA;
-  }
-  if (cudaFreeAsync(ws, stream) != cudaSuccess) rc = DSA_ERR_CUDA;
-  return rc;
+                           static_cast<int>(smem_b)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  launch_dense_mask(p.idx, p.B, p.S, p.k, W4, QT, const_cast<uint32_t*>(dp.bits),
+                    const_cast<uint8_t*>(dp.any), p.err, stream);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const long long items_a = static_cast<long long>(QT) * p.B * p.H;
+  const long long items_b =
+      static_cast<long long>(QT) * p.B * ((p.H + kGroupHeads - 1) / kGroupHeads);
+  ka<<<static_cast<int>(items_a < sms ? items_a : sms), kThreadsB, smem_a, stream>>>(mk, mv, dp);
+  kb<<<static_cast<int>(items_b < sms ? items_b : sms), kThreadsB, smem_b, stream>>>(mk, mv, mq,
+                                                                                    mdo, dp);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace

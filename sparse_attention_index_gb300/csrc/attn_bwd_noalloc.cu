@@ -51,8 +51,6 @@ float* scratch_for_current_device() {
   return g_scratch_addr[dev];
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const void* V,
@@ -60,15 +58,12 @@ extern "C" int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const v
                                            const void* dO, int B, int S, int H, int Hkv, int Dqk,
                                            int Dv, int k, float scale, void* dQ, void* dK,
                                            void* dV, void* stream) {
-  if (!Q || !K || !V || !idx || !O || !lse || !dO || !dQ || !dK || !dV)
-    return DSA_ERR_INVALID_ARG;
-  if (B < 1 || S < 1 || H < 1 || Hkv < 1 || k < 1 || Dqk < 1 || Dv < 1)
-    return DSA_ERR_INVALID_ARG;
-  if (Dqk % 16 != 0 || Dv % 16 != 0 || H % Hkv != 0) return DSA_ERR_INVALID_ARG;
-  const void* ptrs[] = {Q, K, V, idx, O, lse, dO, dQ, dK, dV};
-  for (const void* p : ptrs)
-    if (!aligned16(p)) return DSA_ERR_INVALID_ARG;
-  if (Hkv != 1 || H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  // the same argument checks as dsa_sparse_attn_bwd
+  const int rc = dsa::attn_bwd_args_status(Q, K, V, idx, O, lse, dO, B, S, H, Hkv, Dqk, Dv, k,
+                                           dQ, dK, dV);
+  if (rc != DSA_OK) return rc;
+  // per-head K/V runs on the dense-tile kernels, whose scratch this entry point lacks
+  if (Hkv != 1) return DSA_ERR_UNSUPPORTED;
   // the accumulator needs one fp32 row of Dqk + Dv per key
   const unsigned long long need =
       static_cast<unsigned long long>(B) * S * Hkv * (static_cast<unsigned>(Dqk) + Dv);
@@ -77,5 +72,6 @@ extern "C" int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const v
   if (ws == nullptr) return DSA_ERR_CUDA;
   // launch_attn_bwd zeroes the rows it uses (cudaMemsetAsync) before accumulating
   return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
-                              ws, static_cast<cudaStream_t>(stream), dsa::kBwdPathNoAlloc);
+                              ws, static_cast<cudaStream_t>(stream), dsa::kBwdPathNoAlloc, 1,
+                              nullptr);
 }

@@ -185,11 +185,12 @@ int launch_fwd_dims(const AttnParams& p, long long rows, cudaStream_t stream) {
 
 int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
                     int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
-                    cudaStream_t stream, int path, int Hkv) {
+                    cudaStream_t stream, int path, int Hkv, void* scratch) {
   AttnParams p = make_attn_params(Q, K, V, idx, B, S, H, k, scale);
   p.O = static_cast<uint16_t*>(O);
   p.lse = lse;
   p.Hkv = Hkv;
+  p.scratch = static_cast<uint8_t*>(scratch);
   const long long rows = static_cast<long long>(B) * S;
   if (rows * H > 0x7fffffffLL || H > 128 || Hkv < 1 || H % Hkv != 0) return DSA_ERR_UNSUPPORTED;
   if (Hkv > 1 || path == kFwdPathDense)

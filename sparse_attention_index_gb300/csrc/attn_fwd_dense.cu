@@ -577,15 +577,12 @@ int launch_dense(const AttnParams& p, cudaStream_t stream) {
   using L = DenseLayout<DQK, DV>;
   const int QT = (p.S + kTile - 1) / kTile;
   const int W4 = QT * 4;
-  const size_t bits_bytes = static_cast<size_t>(p.B) * p.S * W4 * sizeof(uint32_t);
+  // the bitmap and the tile flags live in the caller's workspace (dense_scratch_layout)
+  if (p.scratch == nullptr) return DSA_ERR_WORKSPACE;
+  const DenseScratch ly = dense_scratch_layout(p.B, p.S, p.H, p.Hkv, DQK, DV, false);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(p.scratch + ly.bits_off);
+  uint8_t* any = p.scratch + ly.any_off;
   const size_t any_bytes = static_cast<size_t>(p.B) * QT * QT;
-  const size_t any_off = (bits_bytes + 255) / 256 * 256;
-  void* ws = nullptr;
-  // stream-ordered scratch: allocated, used and freed in the caller's stream order
-  if (cudaMallocAsync(&ws, any_off + any_bytes, stream) != cudaSuccess) return DSA_ERR_CUDA;
-  int rc = DSA_OK;
-  uint32_t* bits = static_cast<uint32_t*>(ws);
-  uint8_t* any = static_cast<uint8_t*>(ws) + any_off;
   CUtensorMap mk, mv;
   const long long krows = static_cast<long long>(p.B) * p.S;
   const size_t smem = L::kTailOff + sizeof(DenseTail);
@@ -593,26 +590,22 @@ int launch_dense(const AttnParams& p, cudaStream_t stream) {
   if (cudaMemsetAsync(any, 0, any_bytes, stream) != cudaSuccess ||
       !make_tile_map(&mk, p.K, krows, p.Hkv, DQK) || !make_tile_map(&mv, p.V, krows, p.Hkv, DV) ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess) {
-    rc = DSA_ERR_CUDA;
-  } else {
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    launch_dense_mask(p.idx, p.B, p.S, p.k, W4, QT, bits, any, p.err, stream);
-    const long long items = static_cast<long long>(QT) * p.B * p.H;
-    const int grid = static_cast<int>(items < sms ? items : sms);
-    DenseParams dp;
-    dp.a = p;
-    dp.bits = bits;
-    dp.any = any;
-    dp.W4 = W4;
-    dp.QT = QT;
-    kern<<<grid, kThreads, smem, stream>>>(mk, mv, dp);
-    if (cudaGetLastError() != cudaSuccess) rc = DSA_ERR_CUDA;
-  }
-  if (cudaFreeAsync(ws, stream) != cudaSuccess) rc = DSA_ERR_CUDA;
-  return rc;
+                           static_cast<int>(smem)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  launch_dense_mask(p.idx, p.B, p.S, p.k, W4, QT, bits, any, p.err, stream);
+  const long long items = static_cast<long long>(QT) * p.B * p.H;
+  const int grid = static_cast<int>(items < sms ? items : sms);
+  DenseParams dp;
+  dp.a = p;
+  dp.bits = bits;
+  dp.any = any;
+  dp.W4 = W4;
+  dp.QT = QT;
+  kern<<<grid, kThreads, smem, stream>>>(mk, mv, dp);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace

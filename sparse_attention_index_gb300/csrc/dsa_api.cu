@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/dsa.h"
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
@@ -16,8 +18,11 @@ __device__ int g_device_error = 0;
 int* device_error_word() {
   constexpr int kMaxDevices = 64;
   static int* addr[kMaxDevices] = {};
+  static std::mutex lock;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  // host threads making their first call on a device at the same time fill one entry
+  std::lock_guard<std::mutex> guard(lock);
   if (addr[dev] == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
@@ -34,17 +39,63 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
 
-bool attn_common_ok(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
-                    int H, int Hkv, int Dqk, int Dv, int k) {
-  if (!Q || !K || !V || !idx) return false;
-  if (B < 1 || S < 1 || H < 1 || Hkv < 1 || k < 1 || Dqk < 1 || Dv < 1) return false;
-  if (Dqk % 16 != 0 || Dv % 16 != 0) return false;
-  if (H % Hkv != 0) return false;
-  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(idx)) return false;
-  return true;
+}  // namespace
+
+namespace dsa {
+
+int attn_fwd_args_status(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
+                         int S, int H, int Hkv, int Dqk, int Dv, int k, const void* O,
+                         const void* lse) {
+  if (!Q || !K || !V || !idx || !O || !lse) return DSA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || H < 1 || Hkv < 1 || k < 1 || Dqk < 1 || Dv < 1)
+    return DSA_ERR_INVALID_ARG;
+  if (Dqk % 16 != 0 || Dv % 16 != 0 || H % Hkv != 0) return DSA_ERR_INVALID_ARG;
+  const void* ptrs[] = {Q, K, V, idx, O, lse};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return DSA_ERR_INVALID_ARG;
+  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
+  if (H > 128 || !attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
+  return DSA_OK;
 }
 
+int attn_bwd_args_status(const void* Q, const void* K, const void* V, const int32_t* idx,
+                         const void* O, const void* lse, const void* dO, int B, int S, int H,
+                         int Hkv, int Dqk, int Dv, int k, const void* dQ, const void* dK,
+                         const void* dV) {
+  if (!dO || !dQ || !dK || !dV) return DSA_ERR_INVALID_ARG;
+  const void* ptrs[] = {dO, dQ, dK, dV};
+  for (const void* ptr : ptrs)
+    if (!aligned16(ptr)) return DSA_ERR_INVALID_ARG;
+  return attn_fwd_args_status(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k, O, lse);
+}
+
+bool dense_tiles_fit(int S, int H, int Hkv, int Dqk, int Dv) {
+  return S >= 1 && S <= 65536 && H >= 1 && H <= 128 && Hkv >= 1 && H % Hkv == 0 &&
+         ((Dqk == 192 && Dv == 128) || (Dqk == 128 && Dv == 128));
+}
+
+namespace {
+size_t round256(size_t n) { return (n + 255) / 256 * 256; }
 }  // namespace
+
+DenseScratch dense_scratch_layout(int B, int S, int H, int Hkv, int Dqk, int Dv, bool delta) {
+  DenseScratch ly = {0, 0, 0, 0};
+  if (B < 1 || !dense_tiles_fit(S, H, Hkv, Dqk, Dv)) return ly;
+  const size_t QT = (static_cast<size_t>(S) + 127) / 128;
+  const size_t rows = static_cast<size_t>(B) * S;
+  ly.bits_off = 0;
+  ly.any_off = round256(rows * QT * 4 * sizeof(uint32_t));
+  ly.delta_off = round256(ly.any_off + static_cast<size_t>(B) * QT * QT);
+  ly.bytes = delta ? round256(ly.delta_off + rows * H * sizeof(float)) : ly.delta_off;
+  return ly;
+}
+
+size_t bwd_accumulator_bytes(int B, int S, int Hkv, int Dqk, int Dv) {
+  if (B < 1 || S < 1 || Hkv < 1 || Dqk < 1 || Dv < 1) return 0;
+  return round256(static_cast<size_t>(B) * S * Hkv * (Dqk + Dv) * sizeof(float));
+}
+
+}  // namespace dsa
 
 extern "C" {
 
@@ -134,15 +185,50 @@ int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* seg, int B, 
   return dsa::launch_topk(scores, ld_scores, seg, B, S, k, idx, count, as_stream(stream));
 }
 
+size_t dsa_sparse_attn_fwd_workspace_size(int B, int S, int H, int Hkv, int Dqk, int Dv) {
+  return dsa::dense_scratch_layout(B, S, H, Hkv, Dqk, Dv, false).bytes;
+}
+
+}  // extern "C"
+
+namespace {
+
+int attn_fwd_impl(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
+                  int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O, float* lse,
+                  void* ws, size_t ws_bytes, void* stream, int path) {
+  const int rc = dsa::attn_fwd_args_status(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k, O, lse);
+  if (rc != DSA_OK) return rc;
+  const size_t need = dsa_sparse_attn_fwd_workspace_size(B, S, H, Hkv, Dqk, Dv);
+  if (need > 0 && (!ws || ws_bytes < need || !aligned16(ws))) return DSA_ERR_WORKSPACE;
+  return dsa::launch_attn_fwd(Q, K, V, idx, B, S, H, Dqk, Dv, k, scale, O, lse,
+                              as_stream(stream), path, Hkv, need > 0 ? ws : nullptr);
+}
+
+int attn_bwd_impl(const void* Q, const void* K, const void* V, const int32_t* idx, const void* O,
+                  const float* lse, const void* dO, int B, int S, int H, int Hkv, int Dqk, int Dv,
+                  int k, float scale, void* dQ, void* dK, void* dV, void* ws, size_t ws_bytes,
+                  void* stream, int path) {
+  const int rc = dsa::attn_bwd_args_status(Q, K, V, idx, O, lse, dO, B, S, H, Hkv, Dqk, Dv, k,
+                                           dQ, dK, dV);
+  if (rc != DSA_OK) return rc;
+  const size_t need = dsa_sparse_attn_bwd_workspace_size(B, S, H, Hkv, Dqk, Dv);
+  if (!ws || ws_bytes < need || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+  const size_t acc = dsa::bwd_accumulator_bytes(B, S, Hkv, Dqk, Dv);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
+                              reinterpret_cast<float*>(base), as_stream(stream), path, Hkv,
+                              need > acc ? base + acc : nullptr);
+}
+
+}  // namespace
+
+extern "C" {
+
 int dsa_sparse_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
                         int S, int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O,
-                        float* lse, void* stream) {
-  if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
-  if (!O || !lse || !aligned16(O) || !aligned16(lse)) return DSA_ERR_INVALID_ARG;
-  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
-  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
-  return dsa::launch_attn_fwd(Q, K, V, idx, B, S, H, Dqk, Dv, k, scale, O, lse,
-                              as_stream(stream), dsa::kFwdPathAuto, Hkv);
+                        float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return attn_fwd_impl(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k, scale, O, lse, ws, ws_bytes,
+                       stream, dsa::kFwdPathAuto);
 }
 
 int dsa_sparse_attn_fwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, int k,
@@ -153,55 +239,33 @@ int dsa_sparse_attn_fwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, in
   return dsa::attn_fwd_kernel_kind(B, S, H, Dqk, Dv, k, scale, Hkv);
 }
 
-int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
-                        int S, int H, int Hkv, int Dqk, int Dv, int k, float scale, void* O,
-                        float* lse, void* stream) {
-  if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
-  if (!O || !lse || !aligned16(O) || !aligned16(lse)) return DSA_ERR_INVALID_ARG;
-  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
-  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
-  return dsa::launch_attn_fwd(Q, K, V, idx, B, S, H, Dqk, Dv, k, scale, O, lse,
-                              as_stream(stream), dsa::kFwdPathDense, Hkv);
+int dsa_sparse_attn_fwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
+                              int B, int S, int H, int Hkv, int Dqk, int Dv, int k, float scale,
+                              void* O, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  return attn_fwd_impl(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k, scale, O, lse, ws, ws_bytes,
+                       stream, dsa::kFwdPathDense);
 }
 
 size_t dsa_sparse_attn_bwd_workspace_size(int B, int S, int H, int Hkv, int Dqk, int Dv) {
-  (void)H;
-  if (B < 1 || S < 1 || Hkv < 1 || Dqk < 1 || Dv < 1) return 0;
-  return static_cast<size_t>(B) * S * Hkv * (Dqk + Dv) * sizeof(float);
+  const size_t acc = dsa::bwd_accumulator_bytes(B, S, Hkv, Dqk, Dv);
+  if (acc == 0) return 0;
+  return acc + dsa::dense_scratch_layout(B, S, H, Hkv, Dqk, Dv, true).bytes;
 }
 
 int dsa_sparse_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                         const void* O, const float* lse, const void* dO, int B, int S, int H,
                         int Hkv, int Dqk, int Dv, int k, float scale, void* dQ, void* dK, void* dV,
                         void* ws, size_t ws_bytes, void* stream) {
-  if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
-  if (!O || !lse || !dO || !dQ || !dK || !dV) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(O) || !aligned16(lse) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
-      !aligned16(dV))
-    return DSA_ERR_INVALID_ARG;
-  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
-  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
-  const size_t need = dsa_sparse_attn_bwd_workspace_size(B, S, H, Hkv, Dqk, Dv);
-  if (!ws || ws_bytes < need || !aligned16(ws)) return DSA_ERR_WORKSPACE;
-  return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
-                              static_cast<float*>(ws), as_stream(stream), dsa::kBwdPathAuto, Hkv);
+  return attn_bwd_impl(Q, K, V, idx, O, lse, dO, B, S, H, Hkv, Dqk, Dv, k, scale, dQ, dK, dV, ws,
+                       ws_bytes, stream, dsa::kBwdPathAuto);
 }
 
 int dsa_sparse_attn_bwd_dense(const void* Q, const void* K, const void* V, const int32_t* idx,
-                        const void* O, const float* lse, const void* dO, int B, int S, int H,
-                        int Hkv, int Dqk, int Dv, int k, float scale, void* dQ, void* dK, void* dV,
-                        void* ws, size_t ws_bytes, void* stream) {
-  if (!attn_common_ok(Q, K, V, idx, B, S, H, Hkv, Dqk, Dv, k)) return DSA_ERR_INVALID_ARG;
-  if (!O || !lse || !dO || !dQ || !dK || !dV) return DSA_ERR_INVALID_ARG;
-  if (!aligned16(O) || !aligned16(lse) || !aligned16(dO) || !aligned16(dQ) || !aligned16(dK) ||
-      !aligned16(dV))
-    return DSA_ERR_INVALID_ARG;
-  // Hkv > 1 runs on the dense-tile kernels only; the launchers refuse it elsewhere
-  if (H > 128 || !dsa::attn_dims_supported(Dqk, Dv)) return DSA_ERR_UNSUPPORTED;
-  const size_t need = dsa_sparse_attn_bwd_workspace_size(B, S, H, Hkv, Dqk, Dv);
-  if (!ws || ws_bytes < need || !aligned16(ws)) return DSA_ERR_WORKSPACE;
-  return dsa::launch_attn_bwd(Q, K, V, idx, O, lse, dO, B, S, H, Dqk, Dv, k, scale, dQ, dK, dV,
-                              static_cast<float*>(ws), as_stream(stream), dsa::kBwdPathDense, Hkv);
+                              const void* O, const float* lse, const void* dO, int B, int S,
+                              int H, int Hkv, int Dqk, int Dv, int k, float scale, void* dQ,
+                              void* dK, void* dV, void* ws, size_t ws_bytes, void* stream) {
+  return attn_bwd_impl(Q, K, V, idx, O, lse, dO, B, S, H, Hkv, Dqk, Dv, k, scale, dQ, dK, dV, ws,
+                       ws_bytes, stream, dsa::kBwdPathDense);
 }
 
 int dsa_sparse_attn_bwd_kernel(int B, int S, int H, int Hkv, int Dqk, int Dv, int k,

@@ -18,6 +18,7 @@ struct AttnParams {
   float* lse;
   uint16_t* dQ;
   float* ws;   // fp32 [B*S, Dqk + Dv] dK / dV accumulators
+  uint8_t* scratch;   // the dense-tile kernels' part of the caller's workspace (or null)
   int* err;    // device error word
   int test_drop_arrive;   // failure-detection test only: see attn_fwd_tc.cu
 };

@@ -40,24 +40,54 @@ constexpr int kFwdGatherTc = 0, kFwdDenseTc = 1, kFwdMmaSync = 2;
 // Hkv > 1 (per-head or grouped K / V) runs on the dense-tile kernels only: the others
 // share one K / V row between all heads. Returns -DSA_ERR_UNSUPPORTED where no kernel applies.
 int attn_fwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale, int Hkv = 1);
+// scratch: the dense-tile kernels' scratch (dense_scratch_layout without Delta) or nullptr
+// when the caller guarantees the dense-tile kernel is not taken
 int launch_attn_fwd(const void* Q, const void* K, const void* V, const int32_t* idx, int B, int S,
                     int H, int Dqk, int Dv, int k, float scale, void* O, float* lse,
-                    cudaStream_t stream, int path = kFwdPathAuto, int Hkv = 1);
+                    cudaStream_t stream, int path, int Hkv, void* scratch);
 
 // path: kBwdPathAuto (the cheaper of the gathered-key and dense-tile kernels),
-// kBwdPathNoAlloc (never the dense-tile kernels, which allocate their bitmap) or
-// kBwdPathDense (the dense-tile kernels, DSA_ERR_UNSUPPORTED where they do not apply)
+// kBwdPathNoAlloc (never the dense-tile kernels, whose scratch lives in the caller's
+// workspace) or kBwdPathDense (the dense-tile kernels, DSA_ERR_UNSUPPORTED where they
+// do not apply)
 constexpr int kBwdPathAuto = 0, kBwdPathNoAlloc = 1, kBwdPathDense = 2;
 // the kernels the automatic path runs: gathered-key tcgen05 (+ finalize: 2 launches),
 // dense-tile tcgen05 (bitmap, dq, dk/dv, finalize: 4) or mma.sync (+ finalize: 2)
 constexpr int kBwdGatherTc = 0, kBwdDenseTc = 1, kBwdMmaSync = 2;
 int attn_bwd_kernel_kind(int B, int S, int H, int Dqk, int Dv, int k, float scale, int Hkv = 1);
+// ws_dkv: the fp32 dK / dV accumulators; scratch: the dense-tile kernels' scratch
+// (dense_scratch_layout with Delta) or nullptr on kBwdPathNoAlloc
 int launch_attn_bwd(const void* Q, const void* K, const void* V, const int32_t* idx,
                     const void* O, const float* lse, const void* dO, int B, int S, int H, int Dqk,
                     int Dv, int k, float scale, void* dQ, void* dK, void* dV, float* ws_dkv,
-                    cudaStream_t stream, int path = kBwdPathAuto, int Hkv = 1);
+                    cudaStream_t stream, int path, int Hkv, void* scratch);
 
 bool attn_dims_supported(int Dqk, int Dv);
+
+// Host validation shared by the attention entry points (dsa_api.cu, attn_bwd_noalloc.cu):
+// DSA_OK, DSA_ERR_INVALID_ARG (null or misaligned pointer, bad size) or DSA_ERR_UNSUPPORTED
+// (H > 128, head dims without a kernel), in that order of precedence.
+int attn_fwd_args_status(const void* Q, const void* K, const void* V, const int32_t* idx, int B,
+                         int S, int H, int Hkv, int Dqk, int Dv, int k, const void* O,
+                         const void* lse);
+int attn_bwd_args_status(const void* Q, const void* K, const void* V, const int32_t* idx,
+                         const void* O, const void* lse, const void* dO, int B, int S, int H,
+                         int Hkv, int Dqk, int Dv, int k, const void* dQ, const void* dK,
+                         const void* dV);
+
+// Scratch of the dense-tile attention kernels, carved from the caller's workspace: the
+// selection bitmap [B*S, 4*QT] uint32 (QT = ceil(S / 128) query tiles of 128 rows), the
+// tile flags [B, QT, QT] bytes and, for the backward, Delta fp32 [B*S, H]; each part
+// starts on a 256-byte boundary. bytes = 0 when the dense-tile kernels cannot take the
+// shape (dense_tiles_fit false), so nothing is reserved for it.
+struct DenseScratch {
+  size_t bits_off, any_off, delta_off, bytes;
+};
+bool dense_tiles_fit(int S, int H, int Hkv, int Dqk, int Dv);
+DenseScratch dense_scratch_layout(int B, int S, int H, int Hkv, int Dqk, int Dv, bool delta);
+// the backward's workspace: fp32 dK / dV accumulators [B*S*Hkv, Dqk + Dv], then (from
+// this offset, a multiple of 256) the dense-tile scratch
+size_t bwd_accumulator_bytes(int B, int S, int Hkv, int Dqk, int Dv);
 
 // indexer auxiliary loss: target, KL and dI (kl zeroed here), then the gradient into
 // q_idx, k_idx and w (dk zeroed here)

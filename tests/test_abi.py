@@ -37,9 +37,29 @@ def test_status_strings_and_version(dsa):
     assert dsa.lib.dsa_version() == 100
 
 
+def _r256(n):
+    return (n + 255) // 256 * 256
+
+
 def test_workspace_sizes(dsa):
-    assert dsa.lib.dsa_sparse_attn_bwd_workspace_size(1, 16384, 128, 1, 192, 128) == \
-        16384 * 320 * 4
+    """The attention workspaces hold the fp32 dK / dV accumulators and, wherever the
+    dense-tile kernels can take the shape, their bitmap [B*S, 4*QT] uint32, tile flags
+    [B, QT, QT] bytes and (backward) Delta [B*S, H] fp32, each on a 256-byte boundary."""
+    B, S, H = 1, 16384, 128
+    QT = S // 128
+    bits, flags, delta = B * S * QT * 16, B * QT * QT, B * S * H * 4
+    dense_fwd = _r256(bits) + _r256(flags)
+    dense_bwd = dense_fwd + _r256(delta)
+    acc = B * S * 320 * 4
+    assert dsa.lib.dsa_sparse_attn_fwd_workspace_size(B, S, H, 1, 192, 128) == dense_fwd
+    assert dsa.lib.dsa_sparse_attn_bwd_workspace_size(B, S, H, 1, 192, 128) == acc + dense_bwd
+    # per-head K / V: accumulators per K / V head
+    assert dsa.lib.dsa_sparse_attn_bwd_workspace_size(1, 4096, 128, 128, 192, 128) == \
+        4096 * 128 * 320 * 4 + _r256(4096 * 32 * 16) + _r256(32 * 32) + _r256(4096 * 128 * 4)
+    # no dense-tile kernel for these shapes: nothing reserved for it
+    assert dsa.lib.dsa_sparse_attn_fwd_workspace_size(1, 131072, 128, 1, 192, 128) == 0
+    assert dsa.lib.dsa_sparse_attn_fwd_workspace_size(1, 128, 2, 1, 32, 32) == 0
+    assert dsa.lib.dsa_sparse_attn_bwd_workspace_size(1, 128, 2, 1, 32, 32) == _r256(128 * 64 * 4)
     assert dsa.lib.dsa_sparse_attn_bwd_workspace_size(0, 1, 1, 1, 1, 1) == 0
     assert dsa.lib.dsa_topk_workspace_size(1, 16384, 2048) == 0
 
@@ -73,21 +93,40 @@ def test_topk_validation(dsa):
 
 def test_attention_validation(dsa):
     fwd = dsa.lib.dsa_sparse_attn_fwd
+    fneed = dsa.lib.dsa_sparse_attn_fwd_workspace_size(1, 64, 16, 1, 192, 128)
+    assert fneed > 0
+    W = (P, fneed)
     # B, S, H, Hkv, Dqk, Dv, k
-    assert fwd(P, P, P, P, 1, 64, 16, 1, 192, 128, 8, 0.1, None, P, None) == 1   # null O
-    assert fwd(P, P, P, P, 1, 64, 16, 3, 192, 128, 8, 0.1, P, P, None) == 1      # H % Hkv
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 192, 128, 8, 0.1, None, P, *W, None) == 1   # null O
+    assert fwd(P, P, P, P, 1, 64, 16, 3, 192, 128, 8, 0.1, P, P, *W, None) == 1      # H % Hkv
     # per-head K / V runs on the dense-tile kernels only, which take (192, 128) / (128, 128)
-    assert fwd(P, P, P, P, 1, 64, 16, 16, 64, 64, 8, 0.1, P, P, None) == 2       # Hkv = H, 64
-    assert fwd(P, P, P, P, 1, 70000, 16, 16, 192, 128, 8, 0.1, P, P, None) == 2  # Hkv = H, S
-    assert fwd(P, P, P, P, 1, 64, 256, 1, 192, 128, 8, 0.1, P, P, None) == 2     # H > 128
-    assert fwd(P, P, P, P, 1, 64, 16, 1, 96, 128, 8, 0.1, P, P, None) == 2       # dims
-    assert fwd(P, P, P, P, 1, 64, 16, 1, 100, 128, 8, 0.1, P, P, None) == 1      # Dqk % 16
+    assert fwd(P, P, P, P, 1, 64, 16, 16, 64, 64, 8, 0.1, P, P, *W, None) == 2       # Hkv = H, 64
+    assert fwd(P, P, P, P, 1, 70000, 16, 16, 192, 128, 8, 0.1, P, P, *W, None) == 2  # Hkv = H, S
+    assert fwd(P, P, P, P, 1, 64, 256, 1, 192, 128, 8, 0.1, P, P, *W, None) == 2     # H > 128
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 96, 128, 8, 0.1, P, P, *W, None) == 2       # dims
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 100, 128, 8, 0.1, P, P, *W, None) == 1      # Dqk % 16
+    # the dense-tile kernel's bitmap is the caller's: refused without it, whichever kernel
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 192, 128, 8, 0.1, P, P, None, fneed, None) == 3
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 192, 128, 8, 0.1, P, P, P, fneed - 1, None) == 3
+    assert fwd(P, P, P, P, 1, 64, 16, 1, 192, 128, 8, 0.1, P, P, MIS, fneed, None) == 3
+    assert dsa.lib.dsa_sparse_attn_fwd_dense(P, P, P, P, 1, 64, 16, 4, 192, 128, 8, 0.1, P, P,
+                                             None, 0, None) == 3
     bwd = dsa.lib.dsa_sparse_attn_bwd
     need = dsa.lib.dsa_sparse_attn_bwd_workspace_size(1, 64, 16, 1, 192, 128)
+    assert need == _r256(64 * 320 * 4) + fneed + _r256(64 * 16 * 4)
     args = [P] * 7 + [1, 64, 16, 1, 192, 128, 8, 0.1] + [P, P, P]
     assert bwd(*args, None, need, None) == 3                                      # no ws
     assert bwd(*args, P, need - 4, None) == 3                                     # small ws
+    assert bwd(*args, MIS, need, None) == 3                                       # misaligned
     assert bwd(*([P] * 6 + [None] + args[7:]), P, need, None) == 1                # null dO
+    assert dsa.lib.dsa_sparse_attn_bwd_dense(*args, P, need - 256, None) == 3
+    # the no-allocation backward: the same argument checks, then its own limits
+    na = dsa.lib.dsa_sparse_attn_bwd_noalloc
+    assert na(*([P] * 6 + [None] + args[7:]), None) == 1                          # null dO
+    assert na(*([P] * 7 + [1, 64, 16, 1, 100, 128, 8, 0.1] + [P, P, P]), None) == 1  # Dqk % 16
+    assert na(*([P] * 7 + [1, 64, 256, 1, 192, 128, 8, 0.1] + [P, P, P]), None) == 2  # H > 128
+    assert na(*([P] * 7 + [1, 64, 16, 16, 192, 128, 8, 0.1] + [P, P, P]), None) == 2  # Hkv > 1
+    assert na(*([P] * 7 + [1, 40000, 16, 1, 192, 128, 8, 0.1] + [P, P, P]), None) == 3  # limit
 
 
 def test_index_topk_validation(dsa):

@@ -81,3 +81,36 @@ def test_host_pipeline_with_indexer_loss():
     assert torch.equal(h_out["dq_idx"], dq.cpu())
     assert rel_err(host_f64(h_out["dw"]), host_f64(dw)) <= 1e-6
     assert rel_err(host_f64(h_out["dk_idx"]), host_f64(dk)) <= 1e-5
+
+
+@pytest.mark.parametrize("form", [("e4m3", 0), ("bf16", 256), ("e4m3", 512)])
+def test_host_pipeline_fp8_and_fused_indexer(form):
+    """The pipeline with e4m3 indexer inputs and / or the indexer and top-k fused through
+    blocks of query rows: on the dyadic inputs (exact in e4m3) its index lists, O and dQ equal
+    the bf16, unfused device-resident path bit for bit."""
+    import sparse_attention_index_gb300 as dsa
+    dtype, block = form
+    wl = synth.WORKLOADS["packed_s489"]
+    ind = synth.indexer_inputs(wl)
+    ind8 = synth.indexer_inputs_fp8(wl, "none")
+    att = synth.attention_inputs(wl)
+    seg = dev(ind["seg"])
+    ref = dsa.dsa_layer(bf16_dev(ind["q_idx"]), bf16_dev(ind["k_idx"]), dev(ind["w"]),
+                        bf16_dev(att["Q"]), bf16_dev(att["K"]), bf16_dev(att["V"]), wl.topk,
+                        wl.scale, seg=seg, dO=bf16_dev(att["dO"]))
+    torch.cuda.synchronize()
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    src = ind8 if dtype == "e4m3" else ind
+    h_in = {"q_idx": pin(src["q_idx"]), "k_idx": pin(src["k_idx"]), "w": pin(ind["w"]),
+            "seg": pin(ind["seg"])}
+    h_in.update({n: pin(att[n]) for n in ("Q", "K", "V", "dO")})
+    pipe = dsa.HostPipeline(wl.B, wl.S, wl.Hi, wl.Di, wl.H, wl.Dqk, wl.Dv, wl.topk, wl.scale,
+                            backward=True, segments=True, indexer_dtype=dtype,
+                            fused_block_rows=block)
+    h_out = {n: torch.zeros(t.shape, dtype=t.dtype).pin_memory() for n, t in pipe.out.items()}
+    for _ in range(3):
+        pipe.step(h_in, h_out)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_last_device_error() == 0
+    for n in ("idx", "count", "O", "lse", "dQ"):
+        assert torch.equal(h_out[n], ref[n].cpu()), n
