@@ -257,20 +257,26 @@ def test_topk_long_rows_k2048():
 
 def test_topk_long_rows_with_segments():
     """Rows longer than the shared stage with packed documents: the long-row kernel with its
-    per-key segment test (its whole-group fast path applies only without segment ids), and a
-    row whose document is shorter than k."""
+    per-key segment test (its whole-group fast path applies only without segment ids), and
+    rows whose document is shorter than k."""
     dsa = _dsa()
     S, k = 20000, 300
     rng = np.random.default_rng(12)
     sc = rng.standard_normal((1, S, S), dtype=np.float32)
-    seg = synth.segments(1, S, 2, seed=12)
+    # documents [0, 9000), [9000, 19800), [19800, 20000): the last one holds 200 < k keys and
+    # its rows lie beyond the staged kernel's 16384 keys
+    seg = np.zeros((1, S), dtype=np.int32)
+    seg[0, 9000:] = 1
+    seg[0, 19800:] = 2
     idx, cnt = dsa.dsa_topk(dev(sc), k, dev(seg))
     assert dsa.dsa_get_last_device_error() == 0
-    start = int(np.argmax(seg[0] == seg[0, S - 1]))   # first row of the last document
-    extra = [start + 50] if start + 50 >= 16384 else []
-    rows = np.array(sorted({16383, 16384, 16385, 18000, S - 1, *extra}), dtype=np.int64)
+    rows = np.array([16383, 16384, 16385, 18000, 19799, 19800, 19850, S - 1], dtype=np.int64)
+    short = [r for r in rows if r - 19800 + 1 < k and r >= 19800]
+    assert len(short) == 3 and min(short) >= 16384
     _check_topk(idx.cpu().numpy(), cnt.cpu().numpy(), sc[0][rows].astype(np.float64), seg, S,
                 k, rows)
+    got = cnt.cpu().numpy()[0]
+    assert [int(got[r]) for r in short] == [r - 19800 + 1 for r in short]
 
 
 def test_topk_golden_fixtures_on_gpu():

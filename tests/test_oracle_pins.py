@@ -127,6 +127,41 @@ def test_indexer_weight_homogeneity_and_linearity():
         np.testing.assert_array_equal(ab[t, : t + 1], a[t, : t + 1] + b2[t, : t + 1])
 
 
+def test_indexer_integer_inputs_match_exact_int64_arithmetic():
+    """Integer q, k and w: every score is an integer, computed here in numpy int64 with
+    no floating point at all (per head, per key: a dot product, a max with 0, a weight)."""
+    B, S, Hi, Di = 2, 45, 5, 24
+    q = synth.dyadic_bf16((B, S, Hi, Di), 41, 1, -4, 4, 0)
+    k = synth.dyadic_bf16((B, S, Di), 41, 2, -4, 4, 0)
+    w = synth.dyadic_f32((B, S, Hi), 41, 3, -3, 3, 0)
+    got = oracle.index_scores(q, k, w, None)
+    qi = bf16_bits_to_f64(q).astype(np.int64)
+    ki = bf16_bits_to_f64(k).astype(np.int64)
+    wi = w.astype(np.int64)
+    assert np.array_equal(qi, bf16_bits_to_f64(q)) and np.array_equal(wi, w)
+    for b in range(B):
+        z = np.einsum("thd,sd->ths", qi[b], ki[b])                 # int64 [S, Hi, S]
+        ref = np.einsum("th,ths->ts", wi[b], np.maximum(z, 0))     # int64 [S, S]
+        for t in range(S):
+            np.testing.assert_array_equal(got[b * S + t, : t + 1], ref[t, : t + 1])
+
+
+def test_indexer_matches_fp64_torch_matmul_of_the_dense_product():
+    """One fp64 torch.matmul of [S*Hi, Di] x [Di, S], then ReLU, the head weights and the
+    sum over heads: the scores of every causal pair, on the dyadic tiny workload."""
+    wl = synth.WORKLOADS["tiny_s128"]
+    inp = synth.indexer_inputs(wl)
+    got = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], None)
+    S, Hi, Di = wl.S, wl.Hi, wl.Di
+    q = torch.from_numpy(bf16_bits_to_f64(inp["q_idx"])[0].reshape(S * Hi, Di))
+    k = torch.from_numpy(bf16_bits_to_f64(inp["k_idx"])[0])
+    z = torch.matmul(q, k.T).reshape(S, Hi, S)
+    w = torch.from_numpy(inp["w"][0].astype(np.float64))
+    ref = (w[:, :, None] * torch.relu(z)).sum(1).numpy()
+    tri = np.tril(np.ones((S, S), dtype=bool))
+    np.testing.assert_array_equal(got[:, :S][tri], ref[tri])
+
+
 # ------------------------------------------------------- fp8 index scores
 
 # OCP 8-bit floating point specification, E4M3 (bias 7, exponent 0 subnormal,
@@ -493,6 +528,23 @@ def test_attn_bwd_closed_form_sums():
     _, dKb, dVb = oracle.attn_bwd(Q, K, V, idx, dO, scale, rows=rows_b)
     np.testing.assert_allclose(dKa + dKb, dK, rtol=1e-12, atol=1e-13)
     np.testing.assert_allclose(dVa + dVb, dV, rtol=1e-12, atol=1e-13)
+
+
+def test_attn_bwd_unselected_keys_get_no_gradient():
+    """A key that no query lists receives no gradient: dK = dV = 0 there, exactly. The
+    selection keeps only even keys, and key S - 1 (odd) is listed by nobody else either."""
+    B, S, H, Dqk, Dv = 1, 24, 3, 16, 8
+    Q, K, V, dO, _, _ = _attn_case(B, S, H, 1, Dqk, Dv, seed=34, k=4)
+    idx = np.full((B, S, 6), -1, dtype=np.int32)
+    for t in range(S):
+        evens = [s for s in range(0, t + 1, 2)][-6:]
+        idx[0, t, : len(evens)] = evens
+    dQ, dK, dV = oracle.attn_bwd(Q, K, V, idx, dO, 0.25)
+    odd = np.arange(1, S, 2)
+    assert np.all(dK[0, odd] == 0.0) and np.all(dV[0, odd] == 0.0)
+    # the listed keys do get some gradient (the test is not vacuous)
+    listed = np.unique(idx[idx >= 0])
+    assert np.all(np.abs(dV[0, listed]).sum(-1).sum(-1) > 0)
 
 
 # ------------------------------------------------------------- indexer loss
