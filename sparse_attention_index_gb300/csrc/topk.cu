@@ -4,27 +4,18 @@
 // per query turns the index scores into the index mask. Equal scores go to the
 // lower key index, -0.0 equals +0.0.)
 //
-// One CTA per query row (b, t). The valid keys are s in [0, t] with, when
-// segment ids are given, seg[s] == seg[t]; n = their number.
-//   n <= k : every valid key is selected (ordered compaction, no score read).
-//   n >  k : the scores are mapped to order-preserving 32-bit keys (-0 -> +0)
-//            and the k-th largest key T is found digit by digit with
-//            shared-memory histograms. Rows that fit in shared memory are staged
-//            there (16-byte asynchronous copies). The first level bins key >> 17
-//            (64 bins per octave) over 32 octaves of the sign where a 512-score
-//            sample puts the k-th largest score, with one bin each for the keys
-//            below and above that window; it is built while the keys are
-//            converted. When at most kCandCap keys share the threshold bin, one
-//            sweep writes the bitmap of the keys above it and the list of the keys
-//            in it; the remaining digits are resolved on the list, whose selected
-//            keys join the bitmaps, and one bitmap word per thread emits the
-//            selection in ascending order (through a shared staging row for
-//            coalesced stores). Otherwise 11 + 11 + 10 bit levels run over all
-//            staged keys and an ordered sweep per warp segment writes the result.
-//            Longer rows take 4 x 8-bit passes over global memory (L2) with
-//            warp-aggregated (__match_any_sync) histograms. Every selection takes
-//            the keys > T and the lowest-index `need` keys == T. Slots m..k-1
-//            get -1.
+// The valid keys of query row (b, t) are s in [0, t] with, when segment ids are
+// given, seg[s] == seg[t]; n = their number. Scores are mapped to order-preserving
+// 32-bit keys (-0 -> +0; 0 marks an invalid key).
+//   n <= k : every valid key is selected (an ordered compaction).
+//   n >  k : the k-th largest key T is found, and the keys > T and the lowest-index
+//            `need` keys == T are emitted in ascending order from two bitmaps.
+// Rows of at most kStageMax keys (sr::topk_short_kernel, one 256-thread CTA per row):
+// a 2048-key sample places a window [L, U) around T; one sweep over the row sets the
+// bitmap of the keys >= U and lists the keys in [L, U); T's digits are resolved on the
+// list (a generic radix select over the row when the window misses). Longer rows
+// (topk_long_kernel, one persistent 1024-thread CTA per SM) run the same selection with
+// passes over the row in L2.
 
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
@@ -32,11 +23,7 @@
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
-constexpr int kStageMax = 16384;   // keys staged in shared memory per row
-constexpr int kCandCap = 1024;     // threshold-bin keys resolved as a list
-static_assert(kStageMax <= 32 * kThreads, "one bitmap word per thread");
+constexpr int kStageMax = 16384;   // rows of at most this many keys: the short-row kernel
 
 struct TopkParams {
   const float* scores;
@@ -45,7 +32,6 @@ struct TopkParams {
   int B, S, k;
   int32_t* idx;
   int32_t* count;
-  int stage_cap;
   int t_lo, t_hi;        // the query rows of this launch (all of them, or one block)
   long long rows_blk;    // rows per batch of the score buffer: row t is its row t - t_lo
 };
@@ -55,14 +41,6 @@ __device__ __forceinline__ const float* score_row(const TopkParams& p, int b, in
   return p.scores + (static_cast<long long>(b) * p.rows_blk + (t - p.t_lo)) * p.ld;
 }
 
-struct TopkSmem {
-  uint32_t hist[2048];
-  int warp_tot[kWarps];
-  int wgt[kWarps], weq[kWarps];
-  int bcast[4];
-  uint32_t ubc[4];
-};
-
 // Larger float -> larger key; -0.0 and +0.0 map to the same key; key 0 is never
 // produced by a non-NaN score and marks an invalid (masked) key.
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -70,189 +48,6 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   if (u == 0x80000000u) u = 0u;
   // negative: all bits flipped; otherwise the sign bit set
   return u ^ (static_cast<uint32_t>(static_cast<int32_t>(u) >> 31) | 0x80000000u);
-}
-
-// Inclusive block scan of one int per thread; returns the inclusive value and
-// the block total.
-__device__ __forceinline__ int block_scan(int v, int& total, TopkSmem* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) sm->warp_tot[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int w = lane < kWarps ? sm->warp_tot[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    if (lane < kWarps) sm->warp_tot[lane] = w;   // inclusive prefix of warp totals
-  }
-  __syncthreads();
-  const int before = warp > 0 ? sm->warp_tot[warp - 1] : 0;
-  total = sm->warp_tot[kWarps - 1];
-  __syncthreads();   // warp_tot is reused by the next call
-  return x + before;
-}
-
-// Ordered selection: for s in [0, len), flags(s) gives (gt, eq). Every gt element
-// and the first `need` eq elements (in s order) are written to out[] in ascending s;
-// an element's slot is (#gt before it) + min(#eq before it, need). Each warp owns one
-// contiguous, 32-aligned segment; one block barrier orders the warps.
-template <class Flags>
-__device__ __forceinline__ void ordered_select(int len, Flags flags, int need, int32_t* out,
-                                               int kmax, TopkSmem* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int seg_len = ((len + kThreads - 1) / kThreads) * 32;
-  const int s_begin = warp * seg_len, s_end = min(len, s_begin + seg_len);
-  int cg = 0, ce = 0;
-  for (int s = s_begin + lane; s < s_end; s += 32) {
-    const int2 f = flags(s);
-    cg += f.x;
-    ce += f.y;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    cg += __shfl_xor_sync(0xffffffffu, cg, o);
-    ce += __shfl_xor_sync(0xffffffffu, ce, o);
-  }
-  if (lane == 0) {
-    sm->wgt[warp] = cg;
-    sm->weq[warp] = ce;
-  }
-  __syncthreads();
-  int gt_base = 0, eq_base = 0;
-  for (int w = 0; w < warp; ++w) {
-    gt_base += sm->wgt[w];
-    eq_base += sm->weq[w];
-  }
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int s0 = s_begin; s0 < s_end; s0 += 32) {
-    const int s = s0 + lane;
-    const int2 f = s < s_end ? flags(s) : make_int2(0, 0);
-    const uint32_t bg = __ballot_sync(0xffffffffu, f.x), be = __ballot_sync(0xffffffffu, f.y);
-    const int eq_before = eq_base + __popc(be & lt);
-    const int pos = gt_base + __popc(bg & lt) + min(eq_before, need);
-    if ((f.x || (f.y && eq_before < need)) && pos < kmax) out[pos] = s;
-    gt_base += __popc(bg);
-    eq_base += __popc(be);
-  }
-}
-
-// Over nb histogram bins taken from the top: the bin holding the `need`-th largest
-// key, the number of keys in higher bins and in that bin (broadcast through sm).
-__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, TopkSmem* sm,
-                                         int& bin, int& above, int& in_bin) {
-  // up to 4 bins per thread (nb <= 4 * kThreads), the highest bins to thread 0
-  const int per = nb > kThreads ? nb / kThreads : 1;
-  const int tid = threadIdx.x;
-  int c[4] = {0, 0, 0, 0};
-  int sum = 0;
-  for (int i = 0; i < per; ++i) {
-    const int j = tid * per + i;
-    c[i] = j < nb ? static_cast<int>(hist[nb - 1 - j]) : 0;
-    sum += c[i];
-  }
-  int tot;
-  const int incl = block_scan(sum, tot, sm);
-  int run = incl - sum;
-  for (int i = 0; i < per; ++i) {
-    if (run < need && run + c[i] >= need) {
-      sm->bcast[0] = nb - 1 - (tid * per + i);
-      sm->bcast[1] = run;
-      sm->bcast[2] = c[i];
-    }
-    run += c[i];
-  }
-  __syncthreads();
-  bin = sm->bcast[0];
-  above = sm->bcast[1];
-  in_bin = sm->bcast[2];
-  __syncthreads();
-}
-
-// Final ordered selection over the staged keys (uint4 groups of four consecutive
-// keys): every key with (key & mask) > prefix and the first `need` keys with
-// (key & mask) == prefix, written to out[] in ascending key index. Each warp owns
-// a contiguous segment of groups; a count sweep gives the segment offsets, a
-// write sweep places each key at (#gt before it) + min(#eq before it, need).
-__device__ __forceinline__ void select_staged(const uint4* keys4, int nq, uint32_t mask,
-                                              uint32_t prefix, int need, int32_t* out,
-                                              int kmax, TopkSmem* sm) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int segq = ((nq + kWarps * 32 - 1) / (kWarps * 32)) * 32;
-  const int q_begin = warp * segq, q_end = min(nq, q_begin + segq);
-  int cg = 0, ce = 0;
-  for (int q = q_begin + lane; q < q_end; q += 32) {
-    const uint4 kv = keys4[q];
-    const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t km = kk[e] & mask;
-      cg += (kk[e] != 0u && km > prefix);
-      ce += (kk[e] != 0u && km == prefix);
-    }
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    cg += __shfl_xor_sync(0xffffffffu, cg, o);
-    ce += __shfl_xor_sync(0xffffffffu, ce, o);
-  }
-  if (lane == 0) {
-    sm->wgt[warp] = cg;
-    sm->weq[warp] = ce;
-  }
-  __syncthreads();
-  int gt_base = 0, eq_base = 0;
-  for (int w = 0; w < warp; ++w) {
-    gt_base += sm->wgt[w];
-    eq_base += sm->weq[w];
-  }
-  for (int q0 = q_begin; q0 < q_end; q0 += 32) {
-    const int q = q0 + lane;
-    uint32_t kk[4] = {0u, 0u, 0u, 0u};
-    if (q < q_end) {
-      const uint4 kv = keys4[q];
-      kk[0] = kv.x;
-      kk[1] = kv.y;
-      kk[2] = kv.z;
-      kk[3] = kv.w;
-    }
-    int fg[4], fe[4], ng = 0, ne = 0;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t km = kk[e] & mask;
-      fg[e] = kk[e] != 0u && km > prefix;
-      fe[e] = kk[e] != 0u && km == prefix;
-      ng += fg[e];
-      ne += fe[e];
-    }
-    // warp inclusive scan of (gt count | eq count << 16)
-    const int own = ng | (ne << 16);
-    int incl = own;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += y;
-    }
-    const int excl = incl - own;
-    int g_before = gt_base + (excl & 0xFFFF), e_before = eq_base + (excl >> 16);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int pos = g_before + min(e_before, need);
-      if ((fg[e] || (fe[e] && e_before < need)) && pos < kmax) out[pos] = 4 * q + e;
-      g_before += fg[e];
-      e_before += fe[e];
-    }
-    const int tot = __shfl_sync(0xffffffffu, incl, 31);
-    gt_base += tot & 0xFFFF;
-    eq_base += tot >> 16;
-  }
 }
 
 // First-level bins: h = key >> 17 (sign, exponent and six mantissa bits) over a
@@ -289,175 +84,391 @@ struct LevelOne {
   }
 };
 
-// Selection when the first level leaves at most kCandCap keys in the threshold bin
-// ((key & 0xFFFE0000) == prefix): one sweep over the staged keys writes the
-// bitmap of the keys above the bin and the list of the keys in it; the remaining
-// digits are resolved on that list alone; the selected list keys are added to the
-// bitmaps (above T / equal to T) and one word per thread emits the selection in
-// ascending order, the first `need` keys equal to T included. The histogram area
-// holds the bitmaps, the list and the small histogram, and then the output row.
-__device__ __forceinline__ void select_candidates(const uint32_t* keys, const uint4* keys4,
-                                                  int len, int nq, const LevelOne& w1,
-                                                  uint32_t bin1, int need, int in_bin,
-                                                  int32_t* out, int kmax, TopkSmem* sm) {
-  const int tid = threadIdx.x, lane = tid & 31;
-  uint32_t* gtw = sm->hist;                                     // [512] above T
-  uint32_t* eqw = sm->hist + 512;                               // [512] equal to T
-  uint16_t* cand = reinterpret_cast<uint16_t*>(sm->hist + 1024);   // [kCandCap]
-  uint32_t* h2 = sm->hist + 1536;                               // [512]
-  const bool inner = w1.interior(bin1);
-  uint32_t mask = inner ? 0xFFFE0000u : 0u;
-  uint32_t prefix = inner ? w1.prefix(bin1) : 0u;
-  const int nwords = (len + 31) >> 5;
-  const int ncand = in_bin;
-  for (int i = tid; i < 512; i += kThreads) eqw[i] = 0u;
-  if (tid == 0) sm->ubc[3] = 0u;
-  __syncthreads();
-  const uint32_t lt = (1u << lane) - 1u;
-  for (int c0 = 0; c0 < nq; c0 += kThreads) {
-    const int c = c0 + tid;
-    uint32_t kk[4] = {0u, 0u, 0u, 0u};
-    if (c < nq) {
-      const uint4 kv = keys4[c];
-      kk[0] = kv.x;
-      kk[1] = kv.y;
-      kk[2] = kv.z;
-      kk[3] = kv.w;
-    }
-    uint32_t nib = 0u;
-    bool cd[4];
+// ------------------------------------------------------------------ short rows
+// Rows of at most kStageMax keys: one CTA of 256 threads per row, the row read from
+// global memory (no staging), so that six or more rows are in flight per SM.
+//   n <= k : an ordered compaction of the valid keys.
+//   n >  k : a sample of 2048 keys (eight per thread, spread over the row) gives, by
+//            its order statistics, two keys L < U with the k-th largest key T most
+//            likely in [L, U): the sample rank of T, k * ns / n, plus / minus kZ
+//            binomial standard deviations, placed by a coarse histogram of the sample
+//            over the whole key range and a fine one inside the two coarse bins. One
+//            coalesced sweep over the row sets the bitmap of the keys >= U, counts
+//            them (A) and lists the keys in [L, U) with their indices. When
+//            A <= k <= A + (listed keys) and the list fits, T lies in the list and
+//            its remaining digits are resolved there; otherwise (a miss: rare) a
+//            generic radix select over the row finds T. Either way the keys > T and
+//            the lowest-index `need` keys == T are emitted in ascending order from
+//            two bitmaps, through a shared staging row.
+namespace sr {
+
+constexpr int NT = 256;
+constexpr int NW = NT / 32;
+constexpr int kWords = kStageMax / 32;   // bitmap words of the longest row
+constexpr int kWpt = kWords / NT;        // bitmap words per thread
+static_assert(kWpt == 2, "two bitmap words per thread");
+constexpr int kCand = 2048;              // window keys held in shared memory
+constexpr int kSampleGroups = 2;         // uint4 sample groups per thread
+constexpr float kZ = 3.5f;               // window half-width in standard deviations
+constexpr int kSweepDepth = 4;           // groups of four keys per thread in flight
+
+struct Smem {
+  uint32_t hist[2048];   // sample and level histograms, then the output row
+  uint32_t gtw[kWords];  // keys above T
+  uint32_t eqw[kWords];  // keys equal to T
+  uint32_t cw[kWords];   // window keys (in [L, U))
+  uint32_t ckey[kCand];  // window keys: the order key
+  uint16_t cidx[kCand];  //   and the key index
+  int warp_tot[NW];
+  int bcast[4];
+  uint32_t ubc[8];
+};
+
+__device__ __forceinline__ int block_scan(int v, int& total, Smem* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t b1 = w1.bucket(kk[e]);
-      nib |= static_cast<uint32_t>(kk[e] != 0u && b1 > bin1) << e;
-      cd[e] = kk[e] != 0u && b1 == bin1;
-    }
-    // lanes 8j..8j+7 hold the 32 keys of one bitmap word
-    uint32_t wv = nib << (4 * (lane & 7));
-    wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
-    wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
-    wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
-    if ((lane & 7) == 0 && c < nq) gtw[c >> 3] = wv;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sm->warp_tot[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < NW ? sm->warp_tot[lane] : 0;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t bal = __ballot_sync(0xffffffffu, cd[e]);
-      if (bal) {
-        const int leader = __ffs(bal) - 1;
-        uint32_t base = 0u;
-        if (lane == leader) base = atomicAdd(&sm->ubc[3], static_cast<uint32_t>(__popc(bal)));
-        base = __shfl_sync(0xffffffffu, base, leader);
-        const uint32_t r = base + __popc(bal & lt);
-        if (cd[e] && r < kCandCap) cand[r] = static_cast<uint16_t>(4 * c + e);
-      }
+    for (int o = 1; o < NW; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
     }
+    if (lane < NW) sm->warp_tot[lane] = w;
   }
   __syncthreads();
-  // remaining digits on the list: bits 16..8 and 7..0 of an interior bin,
-  // four bytes otherwise
-  const int nlev = inner ? 2 : 4;
-  int cur = in_bin;
-#pragma unroll 1
-  for (int lvl = 0; lvl < nlev && cur != need; ++lvl) {
-    const int shift = inner ? 8 - 8 * lvl : 24 - 8 * lvl;
-    const int nb = inner && lvl == 0 ? 512 : 256;
-    const uint32_t low = (1u << shift) - 1u;
-    for (int i = tid; i < nb; i += kThreads) h2[i] = 0u;
-    if (tid == 0) {
-      sm->ubc[1] = 0u;
-      sm->ubc[2] = 0xFFFFFFFFu;
-    }
-    __syncthreads();
-    uint32_t lo_or = 0u, lo_and = 0xFFFFFFFFu;
-    for (int j = tid; j < ncand; j += kThreads) {
-      const uint32_t key = keys[cand[j]];
-      if ((key & mask) == prefix) {
-        atomicAdd(&h2[(key >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
-        lo_or |= key & low;
-        lo_and &= key & low;
-      }
-    }
-    lo_or = __reduce_or_sync(0xffffffffu, lo_or);
-    lo_and = __reduce_and_sync(0xffffffffu, lo_and);
-    if (lane == 0) {
-      atomicOr(&sm->ubc[1], lo_or);
-      atomicAnd(&sm->ubc[2], lo_and);
-    }
-    __syncthreads();
-    const uint32_t all_or = sm->ubc[1], all_and = sm->ubc[2];
-    int bin, above;
-    find_bin(h2, nb, need, sm, bin, above, cur);
-    prefix |= static_cast<uint32_t>(bin) << shift;
-    mask |= static_cast<uint32_t>(nb - 1) << shift;
-    need -= above;
-    if (all_or == (all_and & low)) {
-      prefix |= all_or;
-      mask |= low;
-      break;
-    }
+  const int before = warp > 0 ? sm->warp_tot[warp - 1] : 0;
+  total = sm->warp_tot[NW - 1];
+  __syncthreads();   // warp_tot is reused by the next call
+  return x + before;
+}
+
+// Over nb <= 2048 bins taken from the top: the bin holding the need-th largest key
+// (need >= 1), the number of keys in higher bins and in that bin.
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, Smem* sm,
+                                         int& bin, int& above, int& in_bin) {
+  const int per = nb > NT ? nb / NT : 1;
+  const int tid = threadIdx.x;
+  int c[8];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int j = tid * per + i;
+    c[i] = i < per && j < nb ? static_cast<int>(hist[nb - 1 - j]) : 0;
+    sum += c[i];
   }
-  // list keys above T / equal to T into the bitmaps
-  for (int j = tid; j < ncand; j += kThreads) {
-    const int sj = cand[j];
-    const uint32_t km = keys[sj] & mask;
-    if (km > prefix) atomicOr(&gtw[sj >> 5], 1u << (sj & 31));
-    else if (km == prefix) atomicOr(&eqw[sj >> 5], 1u << (sj & 31));
+  int tot;
+  const int incl = block_scan(sum, tot, sm);
+  int run = incl - sum;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i < per && run < need && run + c[i] >= need) {
+      sm->bcast[0] = nb - 1 - (tid * per + i);
+      sm->bcast[1] = run;
+      sm->bcast[2] = c[i];
+    }
+    run += c[i];
   }
   __syncthreads();
-  // one word per thread: offsets by a block scan of (above count | equal count << 16)
-  uint32_t g = 0u, q = 0u;
-  if (tid < nwords) {
-    g = gtw[tid];
-    q = eqw[tid];
+  bin = sm->bcast[0];
+  above = sm->bcast[1];
+  in_bin = sm->bcast[2];
+  __syncthreads();
+}
+
+// the row's keys: order keys of the valid scores, 0 elsewhere (the row stride is a
+// multiple of 4 and at least S, so every group of four inside the row can be read)
+struct Row {
+  const float* srow;
+  const int32_t* seg_row;
+  int len, seg_t;
+  bool seg16;   // seg_row is 16-byte aligned: whole groups of four ids in one load
+  // bit e: key 4c + e is valid
+  __device__ __forceinline__ uint32_t valid4(int c) const {
+    const int s0 = 4 * c;
+    const uint32_t in_row = s0 + 3 < len ? 0xFu : (len > s0 ? (1u << (len - s0)) - 1u : 0u);
+    if (!seg_row) return in_row;
+    if (seg16 && s0 + 3 < len) {
+      const int4 g = __ldg(reinterpret_cast<const int4*>(seg_row + s0));
+      return static_cast<uint32_t>(g.x == seg_t) | static_cast<uint32_t>(g.y == seg_t) << 1 |
+             static_cast<uint32_t>(g.z == seg_t) << 2 | static_cast<uint32_t>(g.w == seg_t) << 3;
+    }
+    uint32_t m = 0u;
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (((in_row >> e) & 1u) && __ldg(seg_row + s0 + e) == seg_t) m |= 1u << e;
+    return m;
   }
-  const int own = __popc(g) | (__popc(q) << 16);
+  // the raw scores of group c, NaN for the invalid keys
+  __device__ __forceinline__ void load4f(int c, float (&f)[4]) const {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(srow) + c);
+    f[0] = v.x;
+    f[1] = v.y;
+    f[2] = v.z;
+    f[3] = v.w;
+    if (seg_row || 4 * c + 3 >= len) {
+      const uint32_t m = valid4(c);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (!((m >> e) & 1u)) f[e] = __int_as_float(0x7fc00000);
+    }
+  }
+  __device__ __forceinline__ void load4(int c, uint32_t (&kq)[4]) const {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(srow) + c);
+    const float fv[4] = {f.x, f.y, f.z, f.w};
+    const uint32_t m = valid4(c);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) kq[e] = ((m >> e) & 1u) ? order_key(fv[e]) : 0u;
+  }
+};
+
+// lanes 8j..8j+7 of a warp hold the 32 keys of one bitmap word (four each): the word
+__device__ __forceinline__ uint32_t gather_word(uint32_t nib, int lane) {
+  uint32_t wv = nib << (4 * (lane & 7));
+  wv |= __shfl_xor_sync(0xffffffffu, wv, 1);
+  wv |= __shfl_xor_sync(0xffffffffu, wv, 2);
+  wv |= __shfl_xor_sync(0xffffffffu, wv, 4);
+  return wv;
+}
+
+// the keys > T (gtw) and the lowest-index `need` keys == T (eqw), `total` keys in all,
+// into out[0, total) in ascending key index, and -1 into out[total, kmax); each thread
+// owns words 2 * tid and 2 * tid + 1
+__device__ __forceinline__ void emit(int nwords, int need, int total, int32_t* out, int kmax,
+                                     Smem* sm) {
+  const int tid = threadIdx.x;
+  uint32_t g[kWpt], q[kWpt];
+  int cg = 0, ce = 0;
+#pragma unroll
+  for (int i = 0; i < kWpt; ++i) {
+    const int w = kWpt * tid + i;
+    g[i] = w < nwords ? sm->gtw[w] : 0u;
+    q[i] = w < nwords ? sm->eqw[w] : 0u;
+    cg += __popc(g[i]);
+    ce += __popc(q[i]);
+  }
+  const int own = cg | (ce << 16);
   int tot;
   const int excl = block_scan(own, tot, sm) - own;   // every word is read before this returns
-  int gb = excl & 0xFFFF, eb = excl >> 16;
+  int eb = excl >> 16;
+  // a selected key's slot = the selected keys before it: keys above T, and of the keys
+  // equal to T the first `need` only
+  int pos = (excl & 0xFFFF) + min(eb, need);
   int32_t* ost = kmax <= 2048 ? reinterpret_cast<int32_t*>(sm->hist) : out;
-  uint32_t bits = g | q;
-  while (bits) {
-    const int b = __ffs(bits) - 1;
-    bits &= bits - 1u;
-    const int sj = tid * 32 + b;
-    if ((g >> b) & 1u) {
-      const int pos = gb + min(eb, need);
-      if (pos < kmax) ost[pos] = sj;
-      ++gb;
-    } else {
-      if (eb < need && gb + eb < kmax) ost[gb + eb] = sj;
-      ++eb;
+#pragma unroll
+  for (int i = 0; i < kWpt; ++i) {
+    uint32_t qk = 0u, m = q[i];
+    for (int room = need - eb; m != 0u && room > 0; --room) {
+      const uint32_t low = m & (0u - m);
+      qk |= low;
+      m ^= low;
+    }
+    eb += __popc(q[i]);
+    uint32_t sel = g[i] | qk;
+    while (sel) {
+      const int bpos = __ffs(sel) - 1;
+      sel &= sel - 1u;
+      if (pos < kmax) ost[pos] = (kWpt * tid + i) * 32 + bpos;
+      ++pos;
     }
   }
   if (ost != out) {
     __syncthreads();
-    for (int j = tid; j < kmax; j += kThreads) out[j] = ost[j];
+    for (int j = tid; j < kmax; j += NT) out[j] = j < total ? ost[j] : -1;
+  } else {
+    for (int j = total + tid; j < kmax; j += NT) out[j] = -1;
   }
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  TopkSmem* sm = reinterpret_cast<TopkSmem*>(smem_raw);
-  uint32_t* keys = reinterpret_cast<uint32_t*>(smem_raw + sizeof(TopkSmem));
+// a float x_t with  order_key(x) >= key  <=>  x >= x_t  for every non-NaN x: the float of
+// that order key; NaN (nothing passes) above the key of +inf, -inf (everything passes) at
+// or below the key of -inf
+__device__ __forceinline__ float key_to_float(uint32_t key) {
+  if (key > 0xFF800000u) return __int_as_float(0x7fc00000);
+  if (key <= 0x007FFFFFu) return -INFINITY;
+  return __uint_as_float(key >= 0x80000000u ? key ^ 0x80000000u : ~key);
+}
 
-  // rows t_lo <= t < min(t_hi, stage_cap) of every batch row, long rows first
-  const int sc = min(p.t_hi, p.stage_cap) - p.t_lo;
-  const long long i = static_cast<long long>(gridDim.x) - 1 - blockIdx.x;
-  const int b = static_cast<int>(i / sc);
-  const int t = p.t_lo + static_cast<int>(i - static_cast<long long>(b) * sc);
-  const long long row = static_cast<long long>(b) * p.S + t;
-  const int len = t + 1;
+// Remaining digits of T below the known bits `mask` (prefix) over the keys visit(fn)
+// presents, in levels of up to 11 bits from bit hb down: per level a histogram of the
+// keys still in play, the bin of the need-th largest, and an early stop when that
+// bin holds exactly the keys needed or every key in play has the same lower bits.
+template <class Visit>
+__device__ __forceinline__ void resolve(Visit visit, int hb, uint32_t& prefix, uint32_t& mask,
+                                        int& need, int cur, Smem* sm) {
+  const int tid = threadIdx.x, lane = tid & 31;
+#pragma unroll 1
+  while (hb >= 0 && cur != need) {
+    const int nbits = hb + 1 < 11 ? hb + 1 : 11;
+    const int shift = hb + 1 - nbits, nb = 1 << nbits;
+    const uint32_t low = (1u << shift) - 1u;
+    for (int i = tid; i < nb; i += NT) sm->hist[i] = 0u;
+    if (tid == 0) {
+      sm->ubc[4] = 0u;            // OR of the bits below this level
+      sm->ubc[5] = 0xFFFFFFFFu;   // AND of the bits below this level
+    }
+    __syncthreads();
+    uint32_t lo_or = 0u, lo_and = 0xFFFFFFFFu;
+    visit([&](uint32_t key) {
+      if (key != 0u && (key & mask) == prefix) {
+        atomicAdd(&sm->hist[(key >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
+        lo_or |= key & low;
+        lo_and &= key & low;
+      }
+    });
+    lo_or = __reduce_or_sync(0xffffffffu, lo_or);
+    lo_and = __reduce_and_sync(0xffffffffu, lo_and);
+    if (lane == 0) {
+      atomicOr(&sm->ubc[4], lo_or);
+      atomicAnd(&sm->ubc[5], lo_and);
+    }
+    __syncthreads();
+    const uint32_t all_or = sm->ubc[4], all_and = sm->ubc[5];
+    int bin, above;
+    find_bin(sm->hist, nb, need, sm, bin, above, cur);
+    prefix |= static_cast<uint32_t>(bin) << shift;
+    mask |= static_cast<uint32_t>(nb - 1) << shift;
+    need -= above;
+    if (all_or == (all_and & low)) {
+      // every key still in play has the same lower bits: T is resolved
+      prefix |= all_or;
+      mask |= low;
+      break;
+    }
+    hb = shift - 1;
+  }
+}
+
+// Over the coarse sample histogram hist[b] (b = key >> 21): cbU = the smallest bin with
+// cum(b) <= rU (2048: none; cum(b) = sample keys in bins >= b), cumU = cum(cbU); cbL = the
+// largest bin with cum(b) >= rL (-1: none), cumL1 = cum(cbL + 1).
+__device__ __forceinline__ void coarse_window(int rU, int rL, int& cbU, int& cbL, int& cumU,
+                                              int& cumL1, Smem* sm) {
   const int tid = threadIdx.x;
-  const int lane = tid & 31;
+  if (tid == 0) {
+    sm->bcast[0] = 2048;
+    sm->bcast[1] = 0;
+    sm->bcast[2] = -1;
+    sm->bcast[3] = 0;
+  }
+  int c[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = static_cast<int>(sm->hist[2047 - (8 * tid + j)]);
+    sum += c[j];
+  }
+  int tot;
+  int run = block_scan(sum, tot, sm) - sum;   // cum of the bins above this thread's
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int bb = 2047 - (8 * tid + j);
+    const int cum = run + c[j];
+    // cum(bb) <= rU < cum(bb - 1): bb is the smallest such bin
+    if (cum <= rU) {
+      const int next = bb > 0 ? static_cast<int>(sm->hist[bb - 1]) : 0;
+      if (bb == 0 || cum + next > rU) {
+        sm->bcast[0] = bb;
+        sm->bcast[1] = cum;
+      }
+    }
+    if (run < rL && cum >= rL) {
+      sm->bcast[2] = bb;
+      sm->bcast[3] = run;
+    }
+    run = cum;
+  }
+  __syncthreads();
+  cbU = sm->bcast[0];
+  cumU = sm->bcast[1];
+  cbL = sm->bcast[2];
+  cumL1 = sm->bcast[3];
+  __syncthreads();
+}
+
+// From the fine histograms (hist[0,1024): bits 20..11 of the keys in coarse bin cbU - 1;
+// hist[1024,2048): of those in coarse bin cbL): U = the lowest fine edge in bin cbU - 1
+// with at most rU sample keys at or above it (else the coarse edge of cbU), L = the
+// highest fine edge in bin cbL with at least rL (0 when there is no such bin).
+__device__ __forceinline__ void fine_window(int rU, int rL, int cbU, int cbL, int cumU, int cumL1,
+                                            uint32_t& U, uint32_t& L, Smem* sm) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const bool lhalf = tid >= NT / 2;   // threads of the L half
+  const int h0 = lhalf ? 1024 : 0;
+  const int t8 = (tid & (NT / 2 - 1)) * 8;   // 8 fine bins per thread, from the top
+  if (tid == 0) {
+    sm->bcast[0] = -1;
+    sm->bcast[1] = -1;
+  }
+  int c[8], sum = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    c[j] = static_cast<int>(sm->hist[h0 + 1023 - (t8 + j)]);
+    sum += c[j];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm->warp_tot[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = lhalf ? NW / 2 : 0; w < warp; ++w) before += sm->warp_tot[w];
+  int run = before + incl - sum + (lhalf ? cumL1 : cumU);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int fb = 1023 - (t8 + j);
+    const int cum = run + c[j];
+    if (!lhalf) {
+      // the smallest fine bin of coarse bin cbU - 1 with cum <= rU
+      if (cbU >= 1 && cum <= rU) {
+        const int next = fb > 0 ? static_cast<int>(sm->hist[fb - 1]) : rU + 1;
+        if (cum + next > rU) sm->bcast[0] = fb;
+      }
+    } else if (cbL >= 0 && run < rL && cum >= rL) {
+      sm->bcast[1] = fb;
+    }
+    run = cum;
+  }
+  __syncthreads();
+  const int fu = sm->bcast[0], fl = sm->bcast[1];
+  U = cbU >= 2048 ? 0xFFFFFFFFu : static_cast<uint32_t>(cbU) << 21;
+  if (fu >= 0) U = (static_cast<uint32_t>(cbU - 1) << 21) | (static_cast<uint32_t>(fu) << 11);
+  L = cbL < 0 ? 0u : static_cast<uint32_t>(cbL) << 21;
+  if (fl >= 0) L |= static_cast<uint32_t>(fl) << 11;
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  Smem* sm = reinterpret_cast<Smem*>(smem_raw);
+  // rows t_lo <= t < min(t_hi, kStageMax) of every batch row, longest first
+  const int nsc = min(p.t_hi, kStageMax) - p.t_lo;
+  const long long i = static_cast<long long>(gridDim.x) - 1 - blockIdx.x;
+  const int b = static_cast<int>(i / nsc);
+  const int t = p.t_lo + static_cast<int>(i - static_cast<long long>(b) * nsc);
+  const long long row = static_cast<long long>(b) * p.S + t;
+  const int len = t + 1, nq = (len + 3) >> 2, nwords = (len + 31) >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int32_t* seg_row = p.seg ? p.seg + static_cast<long long>(b) * p.S : nullptr;
   const int seg_t = seg_row ? seg_row[t] : 0;
-  const float* srow = score_row(p, b, t);
+  const Row rk{score_row(p, b, t), seg_row, len, seg_t,
+               (reinterpret_cast<uintptr_t>(seg_row) & 15u) == 0};
   int32_t* out = p.idx + row * p.k;
 
   // number of valid keys
   int n = len;
   if (seg_row) {
     int c = 0;
-    for (int s = tid; s < len; s += kThreads) c += (seg_row[s] == seg_t);
+    for (int q = tid; q < nq; q += NT) c += __popc(rk.valid4(q));
     int tot;
     block_scan(c, tot, sm);
     n = tot;
@@ -465,171 +476,212 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(const TopkParams p) {
 
   if (n <= p.k) {
     // every valid key is selected, in ascending order
-    ordered_select(
-        len, [&](int s) { return make_int2(!seg_row || seg_row[s] == seg_t, 0); }, 0, out, p.k,
-        sm);
-    for (int j = n + tid; j < p.k; j += kThreads) out[j] = -1;
+    if (!seg_row) {
+      for (int j = tid; j < p.k; j += NT) out[j] = j < len ? j : -1;
+    } else {
+      for (int c0 = 0; c0 < nq; c0 += NT) {
+        const int c = c0 + tid;
+        const uint32_t wv = gather_word(c < nq ? rk.valid4(c) : 0u, lane);
+        if ((lane & 7) == 0 && c < nq) {
+          sm->gtw[c >> 3] = wv;
+          sm->eqw[c >> 3] = 0u;
+        }
+      }
+      __syncthreads();
+      emit(nwords, 0, n, out, p.k, sm);
+    }
     if (p.count && tid == 0) p.count[row] = n;
     return;
   }
 
-  {
-    // ---- rows held in shared memory: 11 + 11 + 10 bit radix select, the first
-    // histogram built while the row is loaded
-    // raw scores -> shared memory with 16-byte asynchronous copies (rows are
-    // 16-byte aligned: ld is a multiple of 4)
-    const int nvec = len >> 2;
-    for (int c = tid; c < nvec; c += kThreads)
-      cp_async_16(smem_u32(keys + 4 * c), srow + 4 * c, 16u);
-    cp_async_commit();
-    for (int s = 4 * nvec + tid; s < len; s += kThreads)
-      keys[s] = __float_as_uint(__ldg(srow + s));
-    for (int i = tid; i < 2048; i += kThreads) sm->hist[i] = 0u;
-    if (tid == 0) {
-      sm->ubc[0] = 0u;
-      sm->ubc[1] = 0u;
-      sm->ubc[2] = 0u;
-      sm->ubc[3] = 0u;
+  // ---- sample: eight keys per thread (two groups of four), spread over the row, or
+  // every group once when the row has at most 2 * NT of them
+  uint32_t sk[kSampleGroups][4];
+  const bool full = nq <= kSampleGroups * NT;
+#pragma unroll
+  for (int j = 0; j < kSampleGroups; ++j) {
+    const int c = full ? tid + NT * j
+                       : static_cast<int>((static_cast<long long>(tid + NT * j) * nq) /
+                                          (kSampleGroups * NT));
+    if (c < nq) {
+      rk.load4(c, sk[j]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sk[j][e] = 0u;
     }
-    cp_async_wait<0>();
-    __syncthreads();
-    const int nq = (len + 3) >> 2;
-    uint4* keys4 = reinterpret_cast<uint4*>(keys);
-    // first-level window from up to 512 evenly spread valid scores (from the
-    // whole row when none of them is valid): the largest positive score, the
-    // largest negative magnitude and the share of scores >= 0
-    uint32_t npos, nval;
-    {
-      const int si = static_cast<int>((static_cast<long long>(tid) * len) / kThreads);
-      const bool v = !seg_row || seg_row[si] == seg_t;
-      const uint32_t u = keys[si];
-      const bool pos = v && ((u & 0x80000000u) == 0u || u == 0x80000000u);
-      const uint32_t ap = __reduce_max_sync(0xffffffffu, pos ? (u & 0x7FFFFFFFu) : 0u);
-      const uint32_t an = __reduce_max_sync(0xffffffffu, v && !pos ? (u & 0x7FFFFFFFu) : 0u);
-      if (lane == 0) {
-        atomicMax(&sm->ubc[0], ap);
-        atomicMax(&sm->ubc[1], an);
+  }
+  for (int j = tid; j < 2048; j += NT) sm->hist[j] = 0u;
+  if (tid == 0) {
+    for (int j = 0; j < 8; ++j) sm->ubc[j] = 0u;
+  }
+  __syncthreads();
+  // coarse level: 2048 bins of key >> 21 (sign, exponent, two mantissa bits) over the
+  // whole key range, so the window may hold T on either side of zero
+  int nvalid = 0;
+#pragma unroll
+  for (int j = 0; j < kSampleGroups; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (sk[j][e] != 0u) {
+        atomicAdd(&sm->hist[sk[j][e] >> 21], 1u);
+        ++nvalid;
       }
-      npos = static_cast<uint32_t>(__syncthreads_count(pos));
-      nval = static_cast<uint32_t>(__syncthreads_count(v));
+  nvalid = __reduce_add_sync(0xffffffffu, nvalid);
+  if (lane == 0) atomicAdd(&sm->ubc[3], static_cast<uint32_t>(nvalid));
+  __syncthreads();
+  const uint32_t ns = sm->ubc[3];
+  // sample ranks bracketing T: rank r = k * ns / n from the top, +- kZ sigma (binomial,
+  // with the finite-population factor: a full sample gives the exact rank)
+  const float pk = static_cast<float>(p.k) / static_cast<float>(n);
+  const float fr = static_cast<float>(ns) / static_cast<float>(n);
+  const float r = pk * static_cast<float>(ns);
+  const float sd = sqrtf(fmaxf(static_cast<float>(ns) * pk * (1.f - pk) * (1.f - fr), 0.f));
+  const int rU = static_cast<int>(floorf(r - kZ * sd));   // keys >= U: likely all selected
+  const int rL = static_cast<int>(ceilf(r + kZ * sd));    // keys >= L: likely at least k
+  int cbU, cbL, cumU, cumL1;
+  coarse_window(rU, rL, cbU, cbL, cumU, cumL1, sm);
+  // fine level: 1024 bins of bits 20..11 inside the coarse bin just below U (hist[0,1024))
+  // and inside the coarse bin of L (hist[1024,2048)), to place U and L 2^11 keys apart
+  for (int j = tid; j < 2048; j += NT) sm->hist[j] = 0u;
+  __syncthreads();
+  const int cu = cbU - 1;   // the coarse bin below U (-1: none)
+#pragma unroll
+  for (int j = 0; j < kSampleGroups; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t kk = sk[j][e];
+      if (kk == 0u) continue;
+      const int cb = static_cast<int>(kk >> 21);
+      const uint32_t fb = (kk >> 11) & 1023u;
+      if (cb == cu) atomicAdd(&sm->hist[fb], 1u);
+      if (cb == cbL) atomicAdd(&sm->hist[1024 + fb], 1u);
     }
-    if (nval == 0u) {
-      uint32_t ap = 0u, an = 0u, cp = 0u, cv = 0u;
-      for (int si = tid; si < len; si += kThreads) {
-        if (seg_row[si] != seg_t) continue;
-        const uint32_t u = keys[si];
-        const bool pos = (u & 0x80000000u) == 0u || u == 0x80000000u;
-        if (pos) ap = max(ap, u & 0x7FFFFFFFu);
-        else an = max(an, u & 0x7FFFFFFFu);
-        cp += pos;
-        ++cv;
-      }
-      ap = __reduce_max_sync(0xffffffffu, ap);
-      an = __reduce_max_sync(0xffffffffu, an);
-      cp = __reduce_add_sync(0xffffffffu, cp);
-      cv = __reduce_add_sync(0xffffffffu, cv);
-      if (lane == 0) {
-        atomicMax(&sm->ubc[0], ap);
-        atomicMax(&sm->ubc[1], an);
-        atomicAdd(&sm->ubc[2], cp);
-        atomicAdd(&sm->ubc[3], cv);
-      }
-      __syncthreads();
-      npos = sm->ubc[2];
-      nval = sm->ubc[3];
+  __syncthreads();
+  uint32_t U, L;
+  fine_window(rU, rL, cbU, cbL, cumU, cumL1, U, L, sm);
+  for (int w = tid; w < nwords; w += NT) sm->eqw[w] = 0u;
+
+  // ---- one sweep: keys >= U into gtw (counted), keys in [L, U) into the list. The tests
+  // run on the raw scores against L and U as floats (the order map is monotone, and an
+  // invalid key is read as NaN, which fails every comparison); only listed keys are
+  // mapped to order keys.
+  const float fU = key_to_float(U), fL = key_to_float(L);
+  int cnt_above = 0;
+  // kSweepDepth groups of four per thread in flight per step (one DRAM latency per step)
+  for (int c0 = 0; c0 < nq; c0 += kSweepDepth * NT) {
+    float f[kSweepDepth][4];
+#pragma unroll
+    for (int u = 0; u < kSweepDepth; ++u) {
+      const int c = c0 + u * NT + tid;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) f[u][e] = __int_as_float(0x7fc00000);
+      if (c < nq) rk.load4f(c, f[u]);
     }
-    // the k-th largest score is expected >= 0 when at least k of the n valid
-    // scores are expected >= 0
-    const bool positive_side =
-        static_cast<unsigned long long>(npos) * n >= static_cast<unsigned long long>(nval) * p.k;
-    const LevelOne w1 = LevelOne::make(sm->ubc[0], sm->ubc[1], positive_side);
-    // order keys in place (invalid -> 0; the tail of the last uint4 -> 0) and the
-    // first-level histogram, four consecutive keys per thread
-    for (int c = tid; c < nq; c += kThreads) {
-      const uint4 raw = keys4[c];
-      const uint32_t rv[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t kq[4];
+#pragma unroll
+    for (int u = 0; u < kSweepDepth; ++u) {
+      const int c = c0 + u * NT + tid;
+      uint32_t nib = 0u, cm = 0u;
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int si = 4 * c + e;
-        const bool v = si < len && (!seg_row || seg_row[si] == seg_t);
-        kq[e] = v ? order_key(__uint_as_float(rv[e])) : 0u;
+        nib |= static_cast<uint32_t>(f[u][e] >= fU) << e;
+        cm |= static_cast<uint32_t>(f[u][e] >= fL && !(f[u][e] >= fU)) << e;
       }
-      keys4[c] = make_uint4(kq[0], kq[1], kq[2], kq[3]);
+      cnt_above += __popc(nib);
+      const uint32_t wv = gather_word(nib, lane), wc = gather_word(cm, lane);
+      if ((lane & 7) == 0 && c < nq) {
+        sm->gtw[c >> 3] = wv;
+        sm->cw[c >> 3] = wc;
+      }
+    }
+  }
+  cnt_above = __reduce_add_sync(0xffffffffu, cnt_above);
+  if (lane == 0) atomicAdd(&sm->ubc[7], static_cast<uint32_t>(cnt_above));
+  __syncthreads();   // gtw, cw and the count are complete
+  // the window keys, from their bitmap, into the list in ascending index (keys re-read)
+  uint32_t cwv[kWpt];
+  int cc = 0;
 #pragma unroll
-      for (int e = 0; e < 4; ++e)
-        if (kq[e] != 0u) atomicAdd(&sm->hist[w1.bucket(kq[e])], 1u);
+  for (int i = 0; i < kWpt; ++i) {
+    const int w = kWpt * tid + i;
+    cwv[i] = w < nwords ? sm->cw[w] : 0u;
+    cc += __popc(cwv[i]);
+  }
+  int ncand;
+  int slot = block_scan(cc, ncand, sm) - cc;
+  const int A = static_cast<int>(sm->ubc[7]);
+  if (ncand <= kCand) {
+#pragma unroll
+    for (int i = 0; i < kWpt; ++i) {
+      uint32_t m = cwv[i];
+      while (m) {
+        const int bpos = __ffs(m) - 1;
+        m &= m - 1u;
+        const int sidx = (kWpt * tid + i) * 32 + bpos;
+        sm->ckey[slot] = order_key(__ldg(rk.srow + sidx));
+        sm->cidx[slot] = static_cast<uint16_t>(sidx);
+        ++slot;
+      }
+    }
+  }
+  __syncthreads();
+
+  uint32_t prefix = 0u, mask = 0u;
+  int need = p.k;
+  if (A <= p.k && A + ncand >= p.k && ncand <= kCand) {
+    // T is in the list: its digits below the common prefix of L and U - 1
+    need = p.k - A;
+    if (need > 0) {
+      const uint32_t d = L ^ (U - 1u);
+      const int hb = d == 0u ? -1 : 31 - __clz(d);
+      mask = hb < 0 ? 0xFFFFFFFFu : (hb >= 31 ? 0u : ~((2u << hb) - 1u));
+      prefix = L & mask;
+      resolve([&](auto fn) {
+        for (int j = tid; j < ncand; j += NT) fn(sm->ckey[j]);
+      }, hb, prefix, mask, need, ncand, sm);
+      // list keys above T / equal to T into the bitmaps
+      for (int j = tid; j < ncand; j += NT) {
+        const uint32_t km = sm->ckey[j] & mask;
+        const int s = sm->cidx[j];
+        if (km > prefix) atomicOr(&sm->gtw[s >> 5], 1u << (s & 31));
+        else if (km == prefix) atomicOr(&sm->eqw[s >> 5], 1u << (s & 31));
+      }
+      __syncthreads();
+    }
+  } else {
+    // the window missed (or its list overflowed): radix select over the whole row,
+    // then both bitmaps from one more sweep
+    resolve([&](auto fn) {
+      for (int c = tid; c < nq; c += NT) {
+        uint32_t kq[4];
+        rk.load4(c, kq);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) fn(kq[e]);
+      }
+    }, 31, prefix, mask, need, n, sm);
+    for (int c0 = 0; c0 < nq; c0 += NT) {
+      const int c = c0 + tid;
+      uint32_t kq[4] = {0u, 0u, 0u, 0u};
+      if (c < nq) rk.load4(c, kq);
+      uint32_t ng = 0u, ne = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const uint32_t km = kq[e] & mask;
+        ng |= static_cast<uint32_t>(kq[e] != 0u && km > prefix) << e;
+        ne |= static_cast<uint32_t>(kq[e] != 0u && km == prefix) << e;
+      }
+      const uint32_t wg = gather_word(ng, lane), we = gather_word(ne, lane);
+      if ((lane & 7) == 0 && c < nq) {
+        sm->gtw[c >> 3] = wg;
+        sm->eqw[c >> 3] = we;
+      }
     }
     __syncthreads();
-    int bin, above, in_bin;
-    find_bin(sm->hist, 2048, p.k, sm, bin, above, in_bin);
-    if (in_bin <= kCandCap) {
-      select_candidates(keys, keys4, len, nq, w1, static_cast<uint32_t>(bin), p.k - above,
-                        in_bin, out, p.k, sm);
-      if (p.count && tid == 0) p.count[row] = p.k;
-      return;
-    }
-    // many keys share the threshold bin: 11 + 11 + 10 bit levels over all staged
-    // keys
-    uint32_t prefix = 0u, mask = 0u;
-    int need = p.k;
-    in_bin = -1;
-    const int shifts[3] = {21, 10, 0};
-    const int nbins[3] = {2048, 2048, 1024};
-    const int nlev = 3;
-#pragma unroll 1
-    for (int lvl = 0; lvl < nlev && in_bin != need; ++lvl) {
-      const int shift = shifts[lvl], nb = nbins[lvl];
-      const uint32_t low = (1u << shift) - 1u;
-      for (int i = tid; i < nb; i += kThreads) sm->hist[i] = 0u;
-      if (tid == 0) {
-        sm->ubc[1] = 0u;            // OR of the bits below this level
-        sm->ubc[2] = 0xFFFFFFFFu;   // AND of the bits below this level
-      }
-      __syncthreads();
-      uint32_t lo_or = 0u, lo_and = 0xFFFFFFFFu;
-      for (int c = tid; c < nq; c += kThreads) {
-        const uint4 kv = keys4[c];
-        const uint32_t kk[4] = {kv.x, kv.y, kv.z, kv.w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (kk[e] != 0u && (kk[e] & mask) == prefix) {
-            atomicAdd(&sm->hist[(kk[e] >> shift) & static_cast<uint32_t>(nb - 1)], 1u);
-            lo_or |= kk[e] & low;
-            lo_and &= kk[e] & low;
-          }
-      }
-      lo_or = __reduce_or_sync(0xffffffffu, lo_or);
-      lo_and = __reduce_and_sync(0xffffffffu, lo_and);
-      if (lane == 0) {
-        atomicOr(&sm->ubc[1], lo_or);
-        atomicAnd(&sm->ubc[2], lo_and);
-      }
-      __syncthreads();
-      const uint32_t all_or = sm->ubc[1], all_and = sm->ubc[2];
-      find_bin(sm->hist, nb, need, sm, bin, above, in_bin);
-      prefix |= static_cast<uint32_t>(bin) << shift;
-      mask |= static_cast<uint32_t>(nb - 1) << shift;
-      need -= above;
-      if (all_or == (all_and & low)) {
-        // every key still in play has the same lower bits: the key is resolved
-        prefix |= all_or;
-        mask |= low;
-        break;
-      }
-    }
-    // output row staged in the (now free) histogram when it fits
-    int32_t* ostage = p.k <= 2048 ? reinterpret_cast<int32_t*>(sm->hist) : out;
-    select_staged(keys4, nq, mask, prefix, need, ostage, p.k, sm);
-    if (ostage != out) {
-      __syncthreads();
-      for (int j = tid; j < p.k; j += kThreads) out[j] = ostage[j];
-    }
-    if (p.count && tid == 0) p.count[row] = p.k;
-    return;
   }
-  // rows longer than the shared stage are handled by topk_long_kernel
+  emit(nwords, need, p.k, out, p.k, sm);
+  if (p.count && tid == 0) p.count[row] = p.k;
 }
+
+}  // namespace sr
 
 // ------------------------------------------------------------------ long rows
 // Rows longer than the shared stage (t >= kStageMax): one persistent CTA of 1024
@@ -1273,19 +1325,17 @@ int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B,
   p.t_lo = t_lo;
   p.t_hi = t_hi;
   p.rows_blk = rows_blk;
-  p.stage_cap = S < kStageMax ? S : kStageMax;
-  p.stage_cap = (p.stage_cap + 3) & ~3;   // whole uint4 groups
-  const size_t smem = sizeof(TopkSmem) + static_cast<size_t>(p.stage_cap) * 4;
-  if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return DSA_ERR_CUDA;
   const long long rows = static_cast<long long>(B) * S;
   if (rows > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
-  // rows t < stage_cap: one CTA per row with the row staged in shared memory
-  const int short_hi = t_hi < p.stage_cap ? t_hi : p.stage_cap;
+  // rows t < kStageMax: one CTA of sr::NT threads per row
+  const int short_hi = t_hi < kStageMax ? t_hi : kStageMax;
   if (short_hi > t_lo) {
+    const size_t smem = sizeof(sr::Smem);
+    if (cudaFuncSetAttribute(sr::topk_short_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return DSA_ERR_CUDA;
     const long long nshort = static_cast<long long>(B) * (short_hi - t_lo);
-    topk_kernel<<<static_cast<unsigned>(nshort), kThreads, smem, stream>>>(p);
+    sr::topk_short_kernel<<<static_cast<unsigned>(nshort), sr::NT, smem, stream>>>(p);
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   }
   const int long_lo = t_lo > kStageMax ? t_lo : kStageMax;
