@@ -236,11 +236,13 @@ def run_ours(args, wl, rank, world, local_rank):
     dO = to_dev(att["dO"], True) if wl.backward else None
     B, S, k = wl.B, wl.S, wl.topk
     ld = (S + 3) // 4 * 4
-    fused = args.fused_topk > 0
-    if fused:   # one block of query rows of scores instead of the [B, S, S] matrix
-        R = args.fused_topk
-        topk_ws = torch.empty((dsa.index_topk_workspace_bytes(B, S, R),), dtype=torch.uint8,
-                              device=device)
+    fused = args.fused_topk > 0 or args.stream_topk > 0
+    stream_form = args.stream_topk > 0
+    if fused:   # one block of query rows of scores (or none) instead of the [B, S, S] matrix
+        R = args.stream_topk if stream_form else args.fused_topk
+        wsb = (dsa.index_topk_stream_workspace_bytes(B, S, R) if stream_form
+               else dsa.index_topk_workspace_bytes(B, S, R))
+        topk_ws = torch.empty((wsb,), dtype=torch.uint8, device=device)
         scores = None
     else:
         scores = torch.empty((B, S, ld), dtype=torch.float32, device=device)
@@ -276,7 +278,9 @@ def run_ours(args, wl, rank, world, local_rank):
         == dsa.DSA_FWD_DENSE_TC else 1
     bwd_launches = (4 if dsa.dsa_sparse_attn_bwd_kernel(B, S, wl.H, wl.Hkv, wl.Dqk, wl.Dv, k, wl.scale)
                     == dsa.DSA_BWD_DENSE_TC else 2) if wl.backward else 0
-    if fused:   # per block of query rows: the indexer, the staged and / or the long-row top-k
+    if stream_form:   # sample, window, emit, finish; then per block two gated launches
+        idx_launches = 4 + 2 * ((S + R - 1) // R)
+    elif fused:   # per block of query rows: the indexer, the staged and / or the long-row top-k
         idx_launches = sum(1 + (t_lo < 16384) + (min(t_lo + R, S) > 16384)
                            for t_lo in range(0, S, R))
     else:
@@ -286,7 +290,10 @@ def run_ours(args, wl, rank, world, local_rank):
     def step(ev):
         ev[0].record(stream)
         e = 1
-        if fused:
+        if stream_form:
+            dsa.dsa_index_topk_stream(q_idx, k_idx, w, k, seg, block_rows=R, idx=idx,
+                                      count=count, ws=topk_ws, stream=stream)
+        elif fused:
             dsa.dsa_index_topk(q_idx, k_idx, w, k, seg, block_rows=R, idx=idx, count=count,
                                ws=topk_ws, stream=stream)   # e4m3 inputs: the fp8 indexer
         else:
@@ -361,7 +368,7 @@ def run_ours(args, wl, rank, world, local_rank):
                                 backward=wl.backward, segments=seg is not None, device=device,
                                 Hkv=wl.Hkv, indexer_loss=loss,
                                 indexer_dtype="e4m3" if fp8 else "bf16",
-                                fused_block_rows=args.fused_topk if fused else 0)
+                                fused_block_rows=R if fused else 0, stream_form=stream_form)
         h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory() for n, t in pipe.out.items()}
         h2d = sum(t.numel() * t.element_size() for t in h_in.values())
         d2h = sum(t.numel() * t.element_size() for t in h_out.values())
@@ -473,6 +480,8 @@ def workload_config(wl, args=None):
         cfg["indexer_loss"] = True
     if args is not None and getattr(args, "fused_topk", 0):
         cfg["fused_topk_block_rows"] = args.fused_topk
+    if args is not None and getattr(args, "stream_topk", 0):
+        cfg["stream_topk_block_rows"] = args.stream_topk
     return cfg
 
 
@@ -489,6 +498,9 @@ def main(argv=None):
     ap.add_argument("--fused-topk", type=int, default=0, metavar="BLOCK_ROWS",
                     help="run the indexer and the top-k fused through blocks of this many query "
                          "rows (a multiple of 256): no [B, S, S] score matrix")
+    ap.add_argument("--stream-topk", type=int, default=0, metavar="BLOCK_ROWS",
+                    help="run the indexer and the top-k in the streaming form (no score rows; "
+                         "blocks of this many query rows, a multiple of 256, for rows it leaves)")
     ap.add_argument("--indexer-loss", action="store_true",
                     help="add the indexer auxiliary loss and its gradient to every step")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -497,9 +509,12 @@ def main(argv=None):
     ap.add_argument("--cpu-rows-per-step", type=int, default=0,
                     help="rows per reference-arm step (default: 4 per host core)")
     args = ap.parse_args(argv)
-    if args.fused_topk and (args.fused_topk % 256 or args.indexer_loss):
-        ap.error("--fused-topk takes a multiple of 256 and no --indexer-loss "
-                 "(the loss reads the score matrix)")
+    for opt, val in (("--fused-topk", args.fused_topk), ("--stream-topk", args.stream_topk)):
+        if val and (val % 256 or args.indexer_loss):
+            ap.error(f"{opt} takes a multiple of 256 and no --indexer-loss "
+                     "(the loss reads the score matrix)")
+    if args.fused_topk and args.stream_topk:
+        ap.error("--fused-topk and --stream-topk are two forms of the same stage: pick one")
     if args.indexer_loss:
         if args.indexer_dtype != "bf16":
             ap.error("--indexer-loss takes the bf16 indexer (its backward reads bf16 inputs)")

@@ -344,6 +344,51 @@ int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scal
                        void* stream);
 
 /*
+ * dsa_index_topk_stream - dsa_index_scores followed by dsa_topk, with no score row in
+ * memory (the streaming form of the fused indexer + top-k; "Implement QK attention head
+ * chunking for CSA", Description: the dense score products do not fit at long context).
+ * Results are those of dsa_index_topk, bit for bit.
+ *
+ *  1. A sampled indexer pass scores evenly spaced 128-key tiles of each query group's
+ *     causal range: a 16th of its tiles, at least 8 and at most 32 (all of them when
+ *     there are fewer).
+ *  2. From each row's sample, a window [L, U) around its k-th largest score: the sample's
+ *     order statistics at rank k * (sampled) / (valid keys), +- 5 standard deviations.
+ *  3. The full indexer pass keeps, per row, the keys scoring >= U (their indices, in the
+ *     row's idx slots) and the keys in [L, U) (index and score, up to 4096), and stores
+ *     no other score.
+ *  4. Each row is settled from these two lists: when at most k keys score >= U and the
+ *     two lists together hold at least min(k, valid keys), the k-th largest score lies in
+ *     the window and is found there; ties go to the lower key index as in dsa_topk.
+ *  5. A row the lists cannot settle (the sample misplaced its window, or a list
+ *     overflowed) marks its block of block_rows query rows; such blocks are redone by
+ *     dsa_index_topk's memory form (indexer and top-k of the block's scores in `ws`),
+ *     launches that a flag on the device switches on. On typical score distributions few
+ *     or no blocks are redone.
+ *
+ *   q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di, k, idx, count: as for dsa_index_topk;
+ *   block_rows  rows per redone block: a positive multiple of 256;
+ *   ws          at least dsa_index_topk_stream_workspace_size(B, S, block_rows) bytes:
+ *               the samples (16 KB per query row), the window lists (32 KB per query row)
+ *               and one block of fp32 scores (B * block_rows * S * 4 bytes).
+ *
+ * Supported as for dsa_index_scores, with S <= 131072; DSA_ERR_UNSUPPORTED otherwise.
+ */
+size_t dsa_index_topk_stream_workspace_size(int B, int S, int block_rows);
+int dsa_index_topk_stream(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
+                          const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
+                          int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dsa_index_topk_stream_fp8 - dsa_index_topk_stream on e4m3 q_idx / k_idx with an optional
+ * per-key scale of k (as dsa_index_scores_fp8; Di a multiple of 16).
+ */
+int dsa_index_topk_stream_fp8(const void* q_idx, const void* k_idx, const float* k_scale,
+                              const void* w, int w_dtype, const int32_t* seg, int B, int S, int Hi,
+                              int Di, int k, int block_rows, int32_t* idx, int32_t* count,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/*
  * dsa_indexer_loss - the indexer's auxiliary loss and its gradient with respect
  * to the index scores.
  *

@@ -42,7 +42,9 @@ EXPORTS = ("dsa_status_string", "dsa_version", "dsa_get_last_device_error", "dsa
            "dsa_sparse_attn_fwd_kernel", "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_kernel",
            "dsa_sparse_attn_bwd_workspace_size", "dsa_sparse_attn_bwd",
            "dsa_sparse_attn_bwd_noalloc", "dsa_indexer_loss", "dsa_indexer_loss_bwd",
-           "dsa_index_topk_workspace_size", "dsa_index_topk", "dsa_index_topk_fp8")
+           "dsa_index_topk_workspace_size", "dsa_index_topk", "dsa_index_topk_fp8",
+           "dsa_index_topk_stream_workspace_size", "dsa_index_topk_stream",
+           "dsa_index_topk_stream_fp8")
 
 
 class DsaError(RuntimeError):
@@ -91,9 +93,13 @@ def _load() -> ctypes.CDLL:
     lib.dsa_index_topk.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, sz, vp]
     lib.dsa_index_topk_fp8.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp,
                                        sz, vp]
+    lib.dsa_index_topk_stream_workspace_size.argtypes = [ci, ci, ci]
+    lib.dsa_index_topk_stream_workspace_size.restype = sz
+    lib.dsa_index_topk_stream.argtypes = lib.dsa_index_topk.argtypes
+    lib.dsa_index_topk_stream_fp8.argtypes = lib.dsa_index_topk_fp8.argtypes
     for name in ("dsa_get_last_device_error", "dsa_index_scores", "dsa_index_scores_fp8", "dsa_topk",
                  "dsa_indexer_loss", "dsa_indexer_loss_bwd", "dsa_index_topk",
-                 "dsa_index_topk_fp8",
+                 "dsa_index_topk_fp8", "dsa_index_topk_stream", "dsa_index_topk_stream_fp8",
                  "dsa_sparse_attn_fwd", "dsa_sparse_attn_fwd_dense", "dsa_sparse_attn_bwd",
                  "dsa_sparse_attn_bwd_dense", "dsa_sparse_attn_bwd_noalloc"):
         getattr(lib, name).restype = ci
@@ -340,12 +346,14 @@ class HostPipeline:
 
     def __init__(self, B, S, Hi, Di, H, Dqk, Dv, topk, scale, backward=True, segments=False,
                  device=None, Hkv=1, indexer_loss=False, grad_scale=None, indexer_dtype="bf16",
-                 fused_block_rows=0):
+                 fused_block_rows=0, stream_form=False):
         """indexer_loss: also run the indexer loss (objective grad_scale * sum of the
         per-query losses, default 1/(B*S)) and its gradient each step, returning kl,
         dq_idx, dk_idx and dw. indexer_dtype "e4m3": q_idx / k_idx are e4m3 bytes and the
         fp8 indexer runs. fused_block_rows > 0: the indexer and the top-k run fused through
-        blocks of that many query rows (dsa_index_topk), with no [B, S, S] score matrix."""
+        blocks of that many query rows (dsa_index_topk), with no [B, S, S] score matrix;
+        with stream_form, in the streaming form (dsa_index_topk_stream: no score rows; the
+        blocks are those its fallback redoes)."""
         if indexer_dtype not in ("bf16", "e4m3"):
             raise ValueError("indexer_dtype is 'bf16' or 'e4m3'")
         if indexer_loss and (indexer_dtype != "bf16" or fused_block_rows):
@@ -355,6 +363,7 @@ class HostPipeline:
         self.loss = indexer_loss
         self.fp8 = indexer_dtype == "e4m3"
         self.block_rows = fused_block_rows
+        self.stream_form = bool(stream_form and fused_block_rows)
         self.grad_scale = 1.0 / (B * S) if grad_scale is None else grad_scale
         e = lambda *shape, dt=torch.bfloat16: torch.empty(shape, dtype=dt, device=dev)  # noqa: E731
         idt = torch.uint8 if self.fp8 else torch.bfloat16
@@ -372,8 +381,9 @@ class HostPipeline:
         ld = (S + 3) // 4 * 4
         if fused_block_rows:   # one block of query rows of scores
             self.scores = None
-            self.topk_ws = e(max(index_topk_workspace_bytes(B, S, fused_block_rows), 16),
-                             dt=torch.uint8)
+            wsb = (index_topk_stream_workspace_bytes(B, S, fused_block_rows) if self.stream_form
+                   else index_topk_workspace_bytes(B, S, fused_block_rows))
+            self.topk_ws = e(max(wsb, 16), dt=torch.uint8)
         else:
             self.scores = e(B, S, ld, dt=torch.float32)
         self.fwd_ws = e(max(fwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv), 16), dt=torch.uint8)
@@ -433,9 +443,10 @@ class HostPipeline:
         sc.wait_event(in1)
         self._wait(sc, self.ev_out1)
         if self.block_rows:
-            dsa_index_topk(d["q_idx"], d["k_idx"], d["w"], self.topk, d.get("seg"),
-                           block_rows=self.block_rows, idx=o["idx"], count=o["count"],
-                           ws=self.topk_ws, stream=sc)
+            fuse = dsa_index_topk_stream if self.stream_form else dsa_index_topk
+            fuse(d["q_idx"], d["k_idx"], d["w"], self.topk, d.get("seg"),
+                 block_rows=self.block_rows, idx=o["idx"], count=o["count"], ws=self.topk_ws,
+                 stream=sc)
         elif self.fp8:
             dsa_index_scores_fp8(d["q_idx"], d["k_idx"], d["w"], d.get("seg"),
                                  scores=self.scores, stream=sc)
@@ -510,6 +521,47 @@ class HostPipeline:
 
 def index_topk_workspace_bytes(B, S, block_rows) -> int:
     return int(lib.dsa_index_topk_workspace_size(B, S, block_rows))
+
+
+def index_topk_stream_workspace_bytes(B, S, block_rows) -> int:
+    return int(lib.dsa_index_topk_stream_workspace_size(B, S, block_rows))
+
+
+def dsa_index_topk_stream(q_idx, k_idx, w, k: int, seg=None, block_rows: int | None = None,
+                          idx=None, count=None, ws=None, stream=None, k_scale=None):
+    """Indexer scores and top-k with no score rows in memory (the streaming form).
+
+    Same arguments and results as dsa_index_topk; `block_rows` (a multiple of 256, default
+    S / 8 rounded up) sizes the blocks that the memory form redoes for rows the sampled
+    window does not settle.
+    """
+    B, S, Hi, Di = q_idx.shape
+    dev = q_idx.device
+    if block_rows is None:
+        block_rows = max(256, (S // 8 + 255) // 256 * 256)
+    if idx is None:
+        idx = torch.empty((B, S, k), dtype=torch.int32, device=dev)
+    if count is None:
+        count = torch.empty((B, S), dtype=torch.int32, device=dev)
+    need = index_topk_stream_workspace_bytes(B, S, block_rows)
+    if ws is None:
+        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    w_dtype = DSA_F32 if w.dtype == torch.float32 else DSA_BF16
+    tail = (None if seg is None else _dev(seg, "seg", torch.int32), B, S, Hi, Di, k, block_rows,
+            _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32), _dev(ws, "ws"),
+            ws.numel() * ws.element_size(), _stream(stream))
+    if q_idx.dtype in _FP8_DTYPES:
+        rc = lib.dsa_index_topk_stream_fp8(_dev8(q_idx, "q_idx"), _dev8(k_idx, "k_idx"),
+                                           None if k_scale is None else _dev(k_scale, "k_scale",
+                                                                             torch.float32),
+                                           _dev(w, "w"), w_dtype, *tail)
+        _check(rc, "dsa_index_topk_stream_fp8")
+    else:
+        rc = lib.dsa_index_topk_stream(_dev(q_idx, "q_idx", torch.bfloat16),
+                                       _dev(k_idx, "k_idx", torch.bfloat16), _dev(w, "w"),
+                                       w_dtype, *tail)
+        _check(rc, "dsa_index_topk_stream")
+    return idx, count
 
 
 def dsa_index_topk(q_idx, k_idx, w, k: int, seg=None, block_rows: int = 2048, idx=None,

@@ -341,6 +341,115 @@ int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scal
                          idx, count, ws, ws_bytes, stream, 1);
 }
 
+}  // extern "C"
+
+namespace {
+
+// the streaming form's workspace: sample scores, window thresholds, list counts, window
+// lists, block flags and one block of rows of scores for the rows the lists do not settle
+struct StreamLayout {
+  size_t sample, thr, cnt, win, flags, buf, bytes;
+};
+
+size_t r256(size_t n) { return (n + 255) / 256 * 256; }
+
+StreamLayout stream_layout(int B, int S, int block_rows) {
+  StreamLayout ly = {0, 0, 0, 0, 0, 0, 0};
+  if (B < 1 || S < 1 || block_rows < 1) return ly;
+  const size_t rows = static_cast<size_t>(B) * S;
+  const size_t ld = (static_cast<size_t>(S) + 3) / 4 * 4;
+  const size_t R = block_rows < S ? block_rows : S;
+  const size_t nblk = (static_cast<size_t>(S) + R - 1) / R;
+  ly.sample = 0;
+  ly.thr = r256(rows * dsa::kSampleKeys * sizeof(float));
+  ly.cnt = ly.thr + r256(rows * 2 * sizeof(float));
+  ly.win = ly.cnt + r256(rows * 4 * sizeof(int));
+  ly.flags = ly.win + r256(rows * dsa::kStreamWindowCap * sizeof(int2));
+  ly.buf = ly.flags + r256(nblk * sizeof(int));
+  ly.bytes = ly.buf + r256(static_cast<size_t>(B) * R * ld * sizeof(float));
+  return ly;
+}
+
+int index_topk_stream_impl(const void* q_idx, const void* k_idx, const float* k_scale,
+                           const void* w, int w_dtype, const int32_t* seg, int B, int S, int Hi,
+                           int Di, int k, int block_rows, int32_t* idx, int32_t* count, void* ws,
+                           size_t ws_bytes, void* stream, int fp8) {
+  if (!q_idx || !k_idx || !w || !idx) return DSA_ERR_INVALID_ARG;
+  if (k_scale && !aligned16(k_scale)) return DSA_ERR_INVALID_ARG;
+  if (fp8 && Di % 16 != 0) return DSA_ERR_INVALID_ARG;
+  if (B < 1 || S < 1 || Hi < 1 || Di < 1 || k < 1) return DSA_ERR_INVALID_ARG;
+  if (block_rows < 256 || block_rows % 256 != 0) return DSA_ERR_INVALID_ARG;
+  if (w_dtype != DSA_F32 && w_dtype != DSA_BF16) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(idx) ||
+      (count && !aligned16(count)) || (seg && !aligned16(seg)))
+    return DSA_ERR_INVALID_ARG;
+  if (Di % 8 != 0) return DSA_ERR_INVALID_ARG;
+  if (!dsa::indexer_dims_supported(Hi, Di)) return DSA_ERR_UNSUPPORTED;
+  if (S > dsa::kStreamMaxS || static_cast<long long>(B) * S * Hi >= (1LL << 31))
+    return DSA_ERR_UNSUPPORTED;
+  const StreamLayout ly = stream_layout(B, S, block_rows);
+  if (!ws || ws_bytes < ly.bytes || !aligned16(ws)) return DSA_ERR_WORKSPACE;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* sample = reinterpret_cast<float*>(base + ly.sample);
+  float* thr = reinterpret_cast<float*>(base + ly.thr);
+  int* cnt = reinterpret_cast<int*>(base + ly.cnt);
+  int2* win = reinterpret_cast<int2*>(base + ly.win);
+  int* flags = reinterpret_cast<int*>(base + ly.flags);
+  float* buf = reinterpret_cast<float*>(base + ly.buf);
+  const cudaStream_t st = as_stream(stream);
+  const long long rows = static_cast<long long>(B) * S;
+  const int R = block_rows < S ? block_rows : S;
+  const int nblk = (S + R - 1) / R;
+  const int wb = w_dtype == DSA_BF16;
+  if (cudaMemsetAsync(cnt, 0, static_cast<size_t>(rows) * 4 * sizeof(int), st) != cudaSuccess ||
+      cudaMemsetAsync(flags, 0, static_cast<size_t>(nblk) * sizeof(int), st) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  int rc = dsa::launch_index_sample(q_idx, k_idx, w, wb, seg, B, S, Hi, Di, st, fp8, k_scale,
+                                    sample);
+  if (rc == DSA_OK) rc = dsa::launch_stream_window(sample, seg, B, S, 256 / Hi, k, thr, st);
+  if (rc == DSA_OK)
+    rc = dsa::launch_index_emit(q_idx, k_idx, w, wb, seg, B, S, Hi, Di, st, fp8, k_scale, thr,
+                                cnt, idx, k, win, dsa::kStreamWindowCap);
+  if (rc == DSA_OK)
+    rc = dsa::launch_stream_finish(seg, B, S, k, cnt, win, dsa::kStreamWindowCap, idx, count,
+                                   flags, R, st);
+  // the rows the lists did not settle: their blocks again through the memory form, each
+  // launch gated on its block's flag on the device
+  const long long ld = (static_cast<long long>(S) + 3) / 4 * 4;
+  for (int bi = 0; rc == DSA_OK && bi < nblk; ++bi) {
+    const int t_lo = bi * R, t_hi = t_lo + R < S ? t_lo + R : S;
+    rc = dsa::launch_index_scores_rows(q_idx, k_idx, w, wb, seg, B, S, Hi, Di, buf, ld, st, fp8,
+                                       k_scale, t_lo, t_hi, R, flags + bi);
+    if (rc == DSA_OK)
+      rc = dsa::launch_topk_rows(buf, ld, seg, B, S, k, idx, count, st, t_lo, t_hi, R,
+                                 flags + bi);
+  }
+  return rc;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t dsa_index_topk_stream_workspace_size(int B, int S, int block_rows) {
+  return stream_layout(B, S, block_rows).bytes;
+}
+
+int dsa_index_topk_stream(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
+                          const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
+                          int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream) {
+  return index_topk_stream_impl(q_idx, k_idx, nullptr, w, w_dtype, seg, B, S, Hi, Di, k,
+                                block_rows, idx, count, ws, ws_bytes, stream, 0);
+}
+
+int dsa_index_topk_stream_fp8(const void* q_idx, const void* k_idx, const float* k_scale,
+                              const void* w, int w_dtype, const int32_t* seg, int B, int S, int Hi,
+                              int Di, int k, int block_rows, int32_t* idx, int32_t* count,
+                              void* ws, size_t ws_bytes, void* stream) {
+  return index_topk_stream_impl(q_idx, k_idx, k_scale, w, w_dtype, seg, B, S, Hi, Di, k,
+                                block_rows, idx, count, ws, ws_bytes, stream, 1);
+}
+
 int dsa_indexer_loss(const void* Q, const void* K, const int32_t* idx, const float* lse,
                      const float* scores, int64_t ld_scores, int B, int S, int H, int Hkv,
                      int Dqk, int k, float scale, float grad_scale, float* kl, float* dI,

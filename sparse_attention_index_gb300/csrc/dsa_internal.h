@@ -11,6 +11,24 @@ namespace dsa {
 // Device address of the library's error word on the current device.
 int* device_error_word();
 
+// The streaming form of the fused indexer + top-k (dsa_index_topk_stream): a sampled
+// indexer pass scores sample_tiles(nkb) evenly spaced 128-key tiles of the nkb tiles of each
+// query group's causal range (a 16th of them, at least 8 and at most kSampleTiles; all of
+// them when there are fewer), kSampleKeys slots per row.
+constexpr int kSampleTiles = 32;
+constexpr int kSampleKeys = kSampleTiles * 128;
+__host__ __device__ inline int sample_tiles(int nkb) {
+  int nt = nkb / 16;
+  nt = nt < 8 ? 8 : (nt > kSampleTiles ? kSampleTiles : nt);
+  return nkb < nt ? nkb : nt;
+}
+constexpr int kStreamMaxS = 131072;     // keys per row the finishing kernel's bitmaps hold
+constexpr int kStreamWindowCap = 4096;  // window keys listed per row
+// the m-th of the nt tiles sampled out of nkb (increasing in m; every tile when nt == nkb)
+__host__ __device__ inline int sample_tile(int m, int nt, int nkb) {
+  return nt == nkb ? m : static_cast<int>((static_cast<long long>(m) * nkb) / nt);
+}
+
 // fp8 != 0: q_idx / k_idx are e4m3 bytes and k_scale (fp32 [B, S] or nullptr) scales
 // each key's score.
 int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
@@ -23,13 +41,33 @@ int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int
 int launch_index_scores_rows(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
                              const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
                              int64_t ld, cudaStream_t stream, int fp8, const float* k_scale,
-                             int t_lo, int t_hi, long long rows_blk);
+                             int t_lo, int t_hi, long long rows_blk, const int* gate = nullptr);
 
 int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
                 int32_t* idx, int32_t* count, cudaStream_t stream);
+// gate non-null: the kernels do nothing unless *gate != 0 (read on the device)
 int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
                      int32_t* idx, int32_t* count, cudaStream_t stream, int t_lo, int t_hi,
-                     long long rows_blk);
+                     long long rows_blk, const int* gate = nullptr);
+
+// Streaming form passes. sample: [B*S, kSampleKeys] scores (NaN: not a valid key) of the
+// sampled tiles. thr: [B*S, 2] (U, L) per row; cnt: [B*S, 4] zeroed before the emit pass;
+// above: [B*S, k]; win: [B*S, cw] (key index, score bits).
+int launch_index_sample(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                        const int32_t* seg, int B, int S, int Hi, int Di, cudaStream_t stream,
+                        int fp8, const float* k_scale, float* sample);
+int launch_index_emit(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                      const int32_t* seg, int B, int S, int Hi, int Di, cudaStream_t stream,
+                      int fp8, const float* k_scale, const float* thr, int* cnt, int32_t* above,
+                      int k, int2* win, int cw);
+// per row: (U, L) from the sample (rows with t < k: none needed, NaN)
+int launch_stream_window(const float* sample, const int32_t* seg, int B, int S, int G, int k,
+                         float* thr, cudaStream_t stream);
+// per row: the selection from the above / window lists into idx (in place) and count; a
+// row the lists cannot settle sets flags[t / block_rows] = 1 and writes nothing
+int launch_stream_finish(const int32_t* seg, int B, int S, int k, const int* cnt,
+                         const int2* win, int cw, int32_t* idx, int32_t* count, int* flags,
+                         int block_rows, cudaStream_t stream);
 
 // path: kFwdPathAuto (the cheaper of the gathered-key and dense-tile kernels) or
 // kFwdPathDense (the dense-tile kernel, DSA_ERR_UNSUPPORTED where it does not apply)

@@ -46,6 +46,10 @@ constexpr int kAccBufs = 2;
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + kEpiWarps * 32;
 constexpr int kErr = DSA_STAGE_INDEXER | DSA_DEVERR_TIMEOUT;
+constexpr int kModeStore = 0, kModeSample = 1, kModeEmit = 2;
+// emit mode: items of at most this many queries (Hi >= 16) count their lists in shared
+// memory and store the counts once per item; others add into global memory per warp
+constexpr int kEmitSmemQueries = 16;
 
 struct IndexerParams {
   int B, S, Di;
@@ -68,6 +72,16 @@ struct IndexerParams {
   float* scores;
   long long ld;
   int* err;
+  int mode;               // kModeStore, kModeSample or kModeEmit
+  const int* gate;        // non-null: the launch does nothing unless *gate != 0
+  // kModeSample: the scores of up to kSampleTiles evenly spaced key tiles of each row
+  float* sample;          // [B * S, kSampleKeys], NaN where the key is not valid
+  // kModeEmit: per row, keys scoring >= U into `above` and keys in [L, U) into `win`
+  const float* thr;       // [B * S, 2]: U, L (NaN: none)
+  int* cnt;               // [B * S, 4]: keys >= U, keys in [L, U), valid keys (with seg)
+  int32_t* above;         // [B * S, k]
+  int2* win;              // [B * S, cw]: (key index, score bits)
+  int k, cw;
 };
 
 struct SmemTail {
@@ -79,6 +93,7 @@ struct SmemTail {
   uint64_t drain;
   uint32_t tmem_base;
   int abort_flag;
+  int ecnt[kQSlots][kEmitSmemQueries][4];   // emit mode: list counters per item slot and query
 };
 
 __device__ __forceinline__ void item_coords(const IndexerParams& p, int item, int& b, int& t0,
@@ -91,6 +106,48 @@ __device__ __forceinline__ void item_coords(const IndexerParams& p, int item, in
   int t_last = t0 + p.G - 1;
   if (t_last > p.S - 1) t_last = p.S - 1;
   nkb = t_last / kKeysPerTile + 1;
+}
+
+// Key tiles an item runs: all nkb of them, or (sample mode) sample_tiles(nkb) evenly spaced
+// ones; tile_at(m) is the m-th (sample_tile), increasing in m.
+template <int MODE>
+__device__ __forceinline__ int item_tiles(int nkb) {
+  return MODE == kModeSample ? sample_tiles(nkb) : nkb;
+}
+template <int MODE>
+__device__ __forceinline__ int tile_at(int m, int nt, int nkb) {
+  return MODE == kModeSample ? sample_tile(m, nt, nkb) : m;
+}
+
+// Emit mode, for one query row and the 32 keys of a warp (lane = key): keys scoring >= U
+// join the row's `above` list, keys in [L, U) its window list, one atomic per list and
+// warp; with segment ids the valid keys are counted too. Warp-collective.
+__device__ __forceinline__ void emit_keys(const IndexerParams& p, long long row, int* cnt, int s,
+                                          float val, bool valid, int lane) {
+  const float U = __ldg(p.thr + 2 * row), L = __ldg(p.thr + 2 * row + 1);
+  const bool above = valid && val >= U;
+  const bool win = valid && val >= L && !(val >= U);
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t bal = __ballot_sync(0xffffffffu, above);
+  if (bal) {
+    int base = 0;
+    if (lane == 0) base = atomicAdd(cnt, __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(bal & lt);
+    if (above && pos < p.k) p.above[row * p.k + pos] = s;
+  }
+  bal = __ballot_sync(0xffffffffu, win);
+  if (bal) {
+    int base = 0;
+    if (lane == 0) base = atomicAdd(cnt + 1, __popc(bal));
+    base = __shfl_sync(0xffffffffu, base, 0);
+    const int pos = base + __popc(bal & lt);
+    if (win && pos < p.cw) p.win[row * p.cw + pos] = make_int2(s, __float_as_int(val));
+  }
+  if (p.seg != nullptr) {
+    bal = __ballot_sync(0xffffffffu, valid);
+    if (lane == 0 && bal) atomicAdd(cnt + 2, __popc(bal));
+  }
 }
 
 // Drain wait used only at exit: ignores the abort flag, still bounded.
@@ -115,11 +172,12 @@ __device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(d));
 }
 
-template <int HI, bool F8>
+template <int HI, bool F8, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap tm_q,
                    const __grid_constant__ CUtensorMap tm_k, const IndexerParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
+  if (p.gate != nullptr && *reinterpret_cast<const volatile int*>(p.gate) == 0) return;
   // The swizzled tiles need 1024-byte alignment. The dynamic window starts
   // 1024-aligned when the kernel has no static shared memory; refuse to run
   // (and say so) rather than feed misaligned tiles to TMA / UMMA.
@@ -152,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(&tail->drain, 1);
     tail->abort_flag = 0;
+    for (int i = 0; i < kQSlots * kEmitSmemQueries * 4; ++i) (&tail->ecnt[0][0][0])[i] = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
@@ -167,6 +226,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t atom_bytes = p.atom_bytes;
   const uint32_t sbo = 8u * atom_bytes;
+  // emit mode with few queries per item: the list counters live in shared memory, per item
+  // slot; the producer stores an item's counts and zeroes them once every epilogue warp has
+  // released the slot (w_empty), before the slot's next item
+  constexpr bool kSmemCnt = MODE == kModeEmit && kColsPerTile / HI <= kEmitSmemQueries;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -175,6 +238,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t k_par = 1, q_par = 1;
     uint32_t k_issued[kKStages] = {0, 0, 0}, q_issued[kQSlots] = {0, 0};
     uint32_t k_last_par[kKStages] = {0, 0, 0}, q_last_par[kQSlots] = {0, 0};
+    int slot_b[kQSlots] = {-1, -1}, slot_t0[kQSlots] = {0, 0};   // the item of each slot
+    auto flush_counts = [&](int sl) {
+      if constexpr (kSmemCnt) {
+        if (slot_b[sl] < 0) return;
+        for (int i = lane; i < (kColsPerTile / HI) * 3; i += 32) {
+          const int q = i / 3, c = i - 3 * q, t = slot_t0[sl] + q;
+          if (t < p.t_end)
+            p.cnt[4 * (static_cast<long long>(slot_b[sl]) * p.S + t) + c] = tail->ecnt[sl][q][c];
+          tail->ecnt[sl][q][c] = 0;
+        }
+        slot_b[sl] = -1;
+      }
+    };
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
       int b, t0, nkb;
@@ -182,6 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       int okw = 1;
       if (lane == 0) okw = mbar_wait(&tail->w_empty[qs], q_par, abort_flag, p.err, kErr) ? 1 : 0;
       if (__shfl_sync(0xffffffffu, okw, 0) == 0) break;
+      flush_counts(qs);   // the slot's previous item is finished
+      slot_b[qs] = b;
+      slot_t0[qs] = t0;
       for (int c = lane; c < kColsPerTile; c += 32) {
         const int tq = t0 + c / HI;
         float wv = 0.f;
@@ -204,7 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           q_issued[qs] = 1;
           q_last_par[qs] = q_par ^ 1u;
         }
-        for (int j = 0; ok && j < nkb; ++j) {
+        const int nt = item_tiles<MODE>(nkb);
+        for (int m = 0; ok && m < nt; ++m) {
+          const int j = tile_at<MODE>(m, nt, nkb);
           if (!mbar_wait(&tail->k_empty[ks], k_par, abort_flag, p.err, kErr)) { ok = false; break; }
           mbar_arrive_expect_tx(&tail->k_full[ks], p.k_stage_bytes);
           const int krow = b * p.S + j * kKeysPerTile;
@@ -217,6 +298,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (++qs == kQSlots) { qs = 0; q_par ^= 1u; }
+    }
+    // the counts of the items still in flight, once their slots are released
+    for (int i = 0; kSmemCnt && ok && i < kQSlots; ++i) {
+      if (slot_b[qs] >= 0) {
+        int okw = 1;
+        if (lane == 0) okw = mbar_wait(&tail->w_empty[qs], q_par, abort_flag, p.err, kErr) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, okw, 0) == 0) break;
+        flush_counts(qs);
+      }
       if (++qs == kQSlots) { qs = 0; q_par ^= 1u; }
     }
     // Let every copy this warp started land before the CTA exits.
@@ -240,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         item_coords(p, item, b, t0, nkb);
         if (!mbar_wait(&tail->q_full[qs], q_par, abort_flag, p.err, kErr)) { ok = false; break; }
         const uint32_t q_addr = smem_u32(q_smem + qs * p.q_slot_bytes);
-        for (int j = 0; j < nkb; ++j) {
+        const int nt = item_tiles<MODE>(nkb);
+        for (int m = 0; m < nt; ++m) {
           if (!mbar_wait(&tail->k_full[ks], k_par, abort_flag, p.err, kErr)) { ok = false; break; }
           if (!mbar_wait(&tail->acc_empty[as], a_par, abort_flag, p.err, kErr)) { ok = false; break; }
           tc_fence_after();
@@ -289,7 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!__all_sync(0xffffffffu, mbar_wait(&tail->w_full[ws], w_par, abort_flag, p.err, kErr))) break;
       const float* w_item = tail->w_s[ws];
 
-      for (int j = 0; j < nkb; ++j) {
+      const int nt = item_tiles<MODE>(nkb);
+      for (int m = 0; m < nt; ++m) {
+        const int j = tile_at<MODE>(m, nt, nkb);
         if (!__all_sync(0xffffffffu, mbar_wait(&tail->acc_full[as], a_par, abort_flag, p.err, kErr))) {
           ok = false;
           break;
@@ -331,12 +425,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < QPC; ++i) {
               const int qi = (half * 128 + cq * 32) / HI + i;
               const int t = t0 + qi;
-              if (t < p.t_end && s <= t) {
-                float val = acc2[i].x + acc2[i].y;
-                if (F8 && p.k_scale != nullptr) val *= ks;
-                if (p.seg != nullptr && seg_s != __ldg(p.seg + b * p.S + t)) val = -INFINITY;
-                p.scores[(static_cast<long long>(b) * p.rows_blk + (t - p.t_base)) * p.ld + s] =
-                    val;
+              if (MODE == kModeStore) {
+                if (t < p.t_end && s <= t) {
+                  float val = acc2[i].x + acc2[i].y;
+                  if (F8 && p.k_scale != nullptr) val *= ks;
+                  if (p.seg != nullptr && seg_s != __ldg(p.seg + b * p.S + t)) val = -INFINITY;
+                  p.scores[(static_cast<long long>(b) * p.rows_blk + (t - p.t_base)) * p.ld + s] =
+                      val;
+                }
+                acc2[i] = make_float2(0.f, 0.f);
+                continue;
+              }
+              const bool in_t = t < p.t_end;   // the same for every lane of the warp
+              float val = acc2[i].x + acc2[i].y;
+              if (F8 && p.k_scale != nullptr) val *= ks;
+              const bool same_doc = p.seg == nullptr || !in_t || s > t ||
+                                    seg_s == __ldg(p.seg + b * p.S + t);
+              if (MODE == kModeSample) {
+                if (in_t)
+                  p.sample[(static_cast<long long>(b) * p.S + t) * kSampleKeys + m * kKeysPerTile +
+                           quarter * 32 + lane] =
+                      s <= t && same_doc ? val : __int_as_float(0x7fc00000);
+              } else if (in_t) {
+                const long long row = static_cast<long long>(b) * p.S + t;
+                int* c = kSmemCnt ? &tail->ecnt[ws][qi][0] : p.cnt + 4 * row;
+                emit_keys(p, row, c, s, val, s <= t && same_doc, lane);
               }
               acc2[i] = make_float2(0.f, 0.f);
             }
@@ -403,10 +516,10 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t rows, int cols, int b
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int HI, bool F8>
+template <int HI, bool F8, int MODE>
 int launch_hi(const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& p,
               size_t smem_bytes, cudaStream_t stream) {
-  auto kern = indexer_kernel<HI, F8>;
+  auto kern = indexer_kernel<HI, F8, MODE>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem_bytes)) != cudaSuccess)
     return DSA_ERR_CUDA;
@@ -427,20 +540,29 @@ bool indexer_dims_supported(int Hi, int Di) {
   return hi_ok && di_ok;
 }
 
-template <bool F8>
+template <bool F8, int MODE>
 int launch_hi_any(int Hi, const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& p,
                   size_t smem_bytes, cudaStream_t stream) {
   switch (Hi) {
-    case 1: return launch_hi<1, F8>(mq, mk, p, smem_bytes, stream);
-    case 2: return launch_hi<2, F8>(mq, mk, p, smem_bytes, stream);
-    case 4: return launch_hi<4, F8>(mq, mk, p, smem_bytes, stream);
-    case 8: return launch_hi<8, F8>(mq, mk, p, smem_bytes, stream);
-    case 16: return launch_hi<16, F8>(mq, mk, p, smem_bytes, stream);
-    case 32: return launch_hi<32, F8>(mq, mk, p, smem_bytes, stream);
-    case 64: return launch_hi<64, F8>(mq, mk, p, smem_bytes, stream);
-    case 128: return launch_hi<128, F8>(mq, mk, p, smem_bytes, stream);
+    case 1: return launch_hi<1, F8, MODE>(mq, mk, p, smem_bytes, stream);
+    case 2: return launch_hi<2, F8, MODE>(mq, mk, p, smem_bytes, stream);
+    case 4: return launch_hi<4, F8, MODE>(mq, mk, p, smem_bytes, stream);
+    case 8: return launch_hi<8, F8, MODE>(mq, mk, p, smem_bytes, stream);
+    case 16: return launch_hi<16, F8, MODE>(mq, mk, p, smem_bytes, stream);
+    case 32: return launch_hi<32, F8, MODE>(mq, mk, p, smem_bytes, stream);
+    case 64: return launch_hi<64, F8, MODE>(mq, mk, p, smem_bytes, stream);
+    case 128: return launch_hi<128, F8, MODE>(mq, mk, p, smem_bytes, stream);
     default: return DSA_ERR_UNSUPPORTED;
   }
+}
+
+template <bool F8>
+int launch_mode(int Hi, const CUtensorMap& mq, const CUtensorMap& mk, const IndexerParams& p,
+                size_t smem_bytes, cudaStream_t stream) {
+  if (p.mode == kModeSample)
+    return launch_hi_any<F8, kModeSample>(Hi, mq, mk, p, smem_bytes, stream);
+  if (p.mode == kModeEmit) return launch_hi_any<F8, kModeEmit>(Hi, mq, mk, p, smem_bytes, stream);
+  return launch_hi_any<F8, kModeStore>(Hi, mq, mk, p, smem_bytes, stream);
 }
 
 int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
@@ -450,11 +572,14 @@ int launch_index_scores(const void* q_idx, const void* k_idx, const void* w, int
                                   stream, fp8, k_scale, 0, S, S);
 }
 
-int launch_index_scores_rows(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
-                             const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
-                             int64_t ld, cudaStream_t stream, int fp8, const float* k_scale,
-                             int t_lo, int t_hi, long long rows_blk) {
-  IndexerParams p;
+namespace {
+
+// the launch of one indexer pass; `extra` carries the mode and its buffers
+int launch_pass(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                const int32_t* seg, int B, int S, int Hi, int Di, float* scores, int64_t ld,
+                cudaStream_t stream, int fp8, const float* k_scale, int t_lo, int t_hi,
+                long long rows_blk, const IndexerParams& extra) {
+  IndexerParams p = extra;
   p.B = B;
   p.S = S;
   p.Di = Di;
@@ -503,8 +628,52 @@ int launch_index_scores_rows(const void* q_idx, const void* k_idx, const void* w
 
   const size_t smem_bytes = kQSlots * static_cast<size_t>(p.q_slot_bytes) +
                             kKStages * static_cast<size_t>(p.k_stage_bytes) + sizeof(SmemTail);
-  return fp8 ? launch_hi_any<true>(Hi, mq, mk, p, smem_bytes, stream)
-             : launch_hi_any<false>(Hi, mq, mk, p, smem_bytes, stream);
+  return fp8 ? launch_mode<true>(Hi, mq, mk, p, smem_bytes, stream)
+             : launch_mode<false>(Hi, mq, mk, p, smem_bytes, stream);
+}
+
+IndexerParams no_extra() {
+  IndexerParams e = {};
+  e.mode = kModeStore;
+  return e;
+}
+
+}  // namespace
+
+int launch_index_scores_rows(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                             const int32_t* seg, int B, int S, int Hi, int Di, float* scores,
+                             int64_t ld, cudaStream_t stream, int fp8, const float* k_scale,
+                             int t_lo, int t_hi, long long rows_blk, const int* gate) {
+  IndexerParams e = no_extra();
+  e.gate = gate;
+  return launch_pass(q_idx, k_idx, w, w_is_bf16, seg, B, S, Hi, Di, scores, ld, stream, fp8,
+                     k_scale, t_lo, t_hi, rows_blk, e);
+}
+
+int launch_index_sample(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                        const int32_t* seg, int B, int S, int Hi, int Di, cudaStream_t stream,
+                        int fp8, const float* k_scale, float* sample) {
+  IndexerParams e = no_extra();
+  e.mode = kModeSample;
+  e.sample = sample;
+  return launch_pass(q_idx, k_idx, w, w_is_bf16, seg, B, S, Hi, Di, nullptr, 0, stream, fp8,
+                     k_scale, 0, S, S, e);
+}
+
+int launch_index_emit(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
+                      const int32_t* seg, int B, int S, int Hi, int Di, cudaStream_t stream,
+                      int fp8, const float* k_scale, const float* thr, int* cnt, int32_t* above,
+                      int k, int2* win, int cw) {
+  IndexerParams e = no_extra();
+  e.mode = kModeEmit;
+  e.thr = thr;
+  e.cnt = cnt;
+  e.above = above;
+  e.k = k;
+  e.win = win;
+  e.cw = cw;
+  return launch_pass(q_idx, k_idx, w, w_is_bf16, seg, B, S, Hi, Di, nullptr, 0, stream, fp8,
+                     k_scale, 0, S, S, e);
 }
 
 }  // namespace dsa

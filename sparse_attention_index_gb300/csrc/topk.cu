@@ -34,7 +34,12 @@ struct TopkParams {
   int32_t* count;
   int t_lo, t_hi;        // the query rows of this launch (all of them, or one block)
   long long rows_blk;    // rows per batch of the score buffer: row t is its row t - t_lo
+  const int* gate;       // non-null: the launch does nothing unless *gate != 0
 };
+
+__device__ __forceinline__ bool gated_off(const TopkParams& p) {
+  return p.gate != nullptr && *reinterpret_cast<const volatile int*>(p.gate) == 0;
+}
 
 // the scores of query row t of batch row b
 __device__ __forceinline__ const float* score_row(const TopkParams& p, int b, int t) {
@@ -124,7 +129,8 @@ struct Smem {
   uint32_t ubc[8];
 };
 
-__device__ __forceinline__ int block_scan(int v, int& total, Smem* sm) {
+template <class SM>
+__device__ __forceinline__ int block_scan(int v, int& total, SM* sm) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
 #pragma unroll
@@ -152,7 +158,8 @@ __device__ __forceinline__ int block_scan(int v, int& total, Smem* sm) {
 
 // Over nb <= 2048 bins taken from the top: the bin holding the need-th largest key
 // (need >= 1), the number of keys in higher bins and in that bin.
-__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, Smem* sm,
+template <class SM>
+__device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, SM* sm,
                                          int& bin, int& above, int& in_bin) {
   const int per = nb > NT ? nb / NT : 1;
   const int tid = threadIdx.x;
@@ -300,9 +307,9 @@ __device__ __forceinline__ float key_to_float(uint32_t key) {
 // presents, in levels of up to 11 bits from bit hb down: per level a histogram of the
 // keys still in play, the bin of the need-th largest, and an early stop when that
 // bin holds exactly the keys needed or every key in play has the same lower bits.
-template <class Visit>
+template <class Visit, class SM>
 __device__ __forceinline__ void resolve(Visit visit, int hb, uint32_t& prefix, uint32_t& mask,
-                                        int& need, int cur, Smem* sm) {
+                                        int& need, int cur, SM* sm) {
   const int tid = threadIdx.x, lane = tid & 31;
 #pragma unroll 1
   while (hb >= 0 && cur != need) {
@@ -349,8 +356,9 @@ __device__ __forceinline__ void resolve(Visit visit, int hb, uint32_t& prefix, u
 // Over the coarse sample histogram hist[b] (b = key >> 21): cbU = the smallest bin with
 // cum(b) <= rU (2048: none; cum(b) = sample keys in bins >= b), cumU = cum(cbU); cbL = the
 // largest bin with cum(b) >= rL (-1: none), cumL1 = cum(cbL + 1).
+template <class SM>
 __device__ __forceinline__ void coarse_window(int rU, int rL, int& cbU, int& cbL, int& cumU,
-                                              int& cumL1, Smem* sm) {
+                                              int& cumL1, SM* sm) {
   const int tid = threadIdx.x;
   if (tid == 0) {
     sm->bcast[0] = 2048;
@@ -396,8 +404,9 @@ __device__ __forceinline__ void coarse_window(int rU, int rL, int& cbU, int& cbL
 // hist[1024,2048): of those in coarse bin cbL): U = the lowest fine edge in bin cbU - 1
 // with at most rU sample keys at or above it (else the coarse edge of cbU), L = the
 // highest fine edge in bin cbL with at least rL (0 when there is no such bin).
+template <class SM>
 __device__ __forceinline__ void fine_window(int rU, int rL, int cbU, int cbL, int cumU, int cumL1,
-                                            uint32_t& U, uint32_t& L, Smem* sm) {
+                                            uint32_t& U, uint32_t& L, SM* sm) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const bool lhalf = tid >= NT / 2;   // threads of the L half
   const int h0 = lhalf ? 1024 : 0;
@@ -449,6 +458,7 @@ __device__ __forceinline__ void fine_window(int rU, int rL, int cbU, int cbL, in
 
 __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  if (gated_off(p)) return;
   Smem* sm = reinterpret_cast<Smem*>(smem_raw);
   // rows t_lo <= t < min(t_hi, kStageMax) of every batch row, longest first
   const int nsc = min(p.t_hi, kStageMax) - p.t_lo;
@@ -683,6 +693,253 @@ __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
 
 }  // namespace sr
 
+// ------------------------------------------------------- streaming form (no score rows)
+// The indexer's sample pass leaves, per query row, the scores of sample_tiles(nkb) evenly
+// spaced 128-key tiles of its query group's causal range (NaN where a key is not valid).
+// stream_window_kernel turns them into the row's window [L, U) as floats, exactly as the
+// short-row kernel does with its own sample. The indexer's emit pass then lists every
+// valid key scoring >= U (into the row's idx slots, unordered) and every key in [L, U)
+// (index and score) without storing any other score. stream_finish_kernel settles the row
+// from the two lists, or flags its block of rows for the memory form.
+namespace st {
+
+constexpr int NT = 256;
+constexpr int NW = NT / 32;
+constexpr int kMaxS = kStreamMaxS;       // keys per row (bitmaps of kMaxS bits)
+constexpr int kWords = kMaxS / 32;
+constexpr int kCw = kStreamWindowCap;    // window keys per row
+// window half-width in standard deviations: a row the window misses costs its whole
+// block of rows, so the odds of a miss are kept near 1e-6 per row
+constexpr float kZ = 5.f;
+
+struct WinSmem {
+  uint32_t hist[2048];
+  int warp_tot[NW];
+  int bcast[4];
+  uint32_t ubc[8];
+};
+
+struct FinSmem {
+  uint32_t hist[2048];       // level histograms, then the output row
+  uint32_t gtw[kWords];      // keys above T
+  uint32_t eqw[kWords];      // keys equal to T
+  uint32_t ckey[kCw];        // window keys: order key
+  int32_t cidx[kCw];         //   and index
+  int warp_tot[NW];
+  int bcast[4];
+  uint32_t ubc[8];
+};
+
+// one CTA per row: (U, L) as floats from the row's sample, NaN for rows that need none
+__global__ void __launch_bounds__(NT) stream_window_kernel(const float* sample, int B, int S,
+                                                           int G, int k, float* thr) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  WinSmem* sm = reinterpret_cast<WinSmem*>(smem_raw);
+  const long long row = blockIdx.x;
+  const int t = static_cast<int>(row % S);
+  const int tid = threadIdx.x, lane = tid & 31;
+  if (t + 1 <= k) {   // at most k valid keys: all of them are selected
+    if (tid == 0) {
+      thr[2 * row] = __int_as_float(0x7fc00000);
+      thr[2 * row + 1] = __int_as_float(0x7fc00000);
+    }
+    return;
+  }
+  // the sampled tiles of the row's query group (as the indexer's sample pass chose them)
+  const int t0 = (t / G) * G, t_last = min(t0 + G - 1, S - 1);
+  const int nkb = t_last / 128 + 1, nt = sample_tiles(nkb);
+  const float* srow = sample + row * kSampleKeys;
+  uint32_t sk[kSampleKeys / NT];
+  int causal = 0;   // sampled slots with key <= t
+#pragma unroll
+  for (int j = 0; j < kSampleKeys / NT; ++j) {
+    const int slot = tid + NT * j, m = slot >> 7;
+    sk[j] = 0u;
+    if (m < nt) {
+      const int key = sample_tile(m, nt, nkb) * 128 + (slot & 127);
+      causal += key <= t;
+      const float v = srow[slot];
+      if (v == v) sk[j] = order_key(v);   // NaN: not a valid key
+    }
+  }
+  for (int j = tid; j < 2048; j += NT) sm->hist[j] = 0u;
+  if (tid == 0)
+    for (int j = 0; j < 8; ++j) sm->ubc[j] = 0u;
+  __syncthreads();
+  int nvalid = 0;
+#pragma unroll
+  for (int j = 0; j < kSampleKeys / NT; ++j)
+    if (sk[j] != 0u) {
+      atomicAdd(&sm->hist[sk[j] >> 21], 1u);
+      ++nvalid;
+    }
+  nvalid = __reduce_add_sync(0xffffffffu, nvalid);
+  causal = __reduce_add_sync(0xffffffffu, causal);
+  if (lane == 0) {
+    atomicAdd(&sm->ubc[3], static_cast<uint32_t>(nvalid));
+    atomicAdd(&sm->ubc[4], static_cast<uint32_t>(causal));
+  }
+  __syncthreads();
+  const uint32_t ns = sm->ubc[3], nc = sm->ubc[4];
+  // valid keys of the row: t + 1 without documents; with documents estimated from the
+  // sample's share of valid keys among its causal ones (only the window depends on it)
+  const float n = nc > 0 ? static_cast<float>(t + 1) * static_cast<float>(ns) / static_cast<float>(nc)
+                         : static_cast<float>(t + 1);
+  const float pk = fminf(static_cast<float>(k) / fmaxf(n, 1.f), 1.f);
+  const float fr = fminf(static_cast<float>(ns) / fmaxf(n, 1.f), 1.f);
+  const float r = pk * static_cast<float>(ns);
+  const float sd = sqrtf(fmaxf(static_cast<float>(ns) * pk * (1.f - pk) * (1.f - fr), 0.f));
+  const int rU = static_cast<int>(floorf(r - kZ * sd));
+  const int rL = static_cast<int>(ceilf(r + kZ * sd));
+  int cbU, cbL, cumU, cumL1;
+  sr::coarse_window(rU, rL, cbU, cbL, cumU, cumL1, sm);
+  for (int j = tid; j < 2048; j += NT) sm->hist[j] = 0u;
+  __syncthreads();
+  const int cu = cbU - 1;
+#pragma unroll
+  for (int j = 0; j < kSampleKeys / NT; ++j) {
+    const uint32_t kk = sk[j];
+    if (kk == 0u) continue;
+    const int cb = static_cast<int>(kk >> 21);
+    const uint32_t fb = (kk >> 11) & 1023u;
+    if (cb == cu) atomicAdd(&sm->hist[fb], 1u);
+    if (cb == cbL) atomicAdd(&sm->hist[1024 + fb], 1u);
+  }
+  __syncthreads();
+  uint32_t U, L;
+  sr::fine_window(rU, rL, cbU, cbL, cumU, cumL1, U, L, sm);
+  if (tid == 0) {
+    thr[2 * row] = sr::key_to_float(U);
+    thr[2 * row + 1] = sr::key_to_float(L);
+  }
+}
+
+// the keys > T (gtw) and the lowest-index `need` keys == T (eqw), `total` in all, into
+// out[0, total) ascending and -1 into out[total, kmax); each thread owns a contiguous run
+// of `per` bitmap words
+__device__ __forceinline__ void emit_words(int nwords, int need, int total, int32_t* out,
+                                           int kmax, FinSmem* sm) {
+  const int tid = threadIdx.x;
+  const int per = (nwords + NT - 1) / NT;
+  const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
+  int cg = 0, ce = 0;
+  for (int w = w0; w < w1; ++w) {
+    cg += __popc(sm->gtw[w]);
+    ce += __popc(sm->eqw[w]);
+  }
+  const int own = cg | (ce << 16);
+  int tot;
+  const int excl = sr::block_scan(own, tot, sm) - own;
+  int eb = excl >> 16;
+  int pos = (excl & 0xFFFF) + min(eb, need);
+  int32_t* ost = kmax <= 2048 ? reinterpret_cast<int32_t*>(sm->hist) : out;
+  for (int w = w0; w < w1; ++w) {
+    const uint32_t q = sm->eqw[w];
+    uint32_t qk = 0u, m = q;
+    for (int room = need - eb; m != 0u && room > 0; --room) {
+      const uint32_t low = m & (0u - m);
+      qk |= low;
+      m ^= low;
+    }
+    eb += __popc(q);
+    uint32_t sel = sm->gtw[w] | qk;
+    while (sel) {
+      const int bpos = __ffs(sel) - 1;
+      sel &= sel - 1u;
+      if (pos < kmax) ost[pos] = w * 32 + bpos;
+      ++pos;
+    }
+  }
+  if (ost != out) {
+    __syncthreads();
+    for (int j = tid; j < kmax; j += NT) out[j] = j < total ? ost[j] : -1;
+  } else {
+    for (int j = total + tid; j < kmax; j += NT) out[j] = -1;
+  }
+}
+
+// one CTA per row, longest rows first
+__global__ void __launch_bounds__(NT) stream_finish_kernel(const int32_t* seg, int B, int S, int k,
+                                                           const int* cnt, const int2* win, int cw,
+                                                           int32_t* idx, int32_t* count,
+                                                           int* flags, int block_rows) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  FinSmem* sm = reinterpret_cast<FinSmem*>(smem_raw);
+  const long long i = static_cast<long long>(gridDim.x) - 1 - blockIdx.x;
+  const int b = static_cast<int>(i / S), t = static_cast<int>(i % S);
+  const long long row = i;
+  const int len = t + 1, nwords = (len + 31) >> 5;
+  const int tid = threadIdx.x;
+  const int32_t* seg_row = seg ? seg + static_cast<long long>(b) * S : nullptr;
+  const int seg_t = seg_row ? seg_row[t] : 0;
+  int32_t* out = idx + row * k;
+  for (int w = tid; w < nwords; w += NT) {
+    sm->gtw[w] = 0u;
+    sm->eqw[w] = 0u;
+  }
+  __syncthreads();
+  if (len <= k) {
+    // every valid key is selected
+    int n = 0;
+    for (int s = tid; s < len; s += NT)
+      if (!seg_row || __ldg(seg_row + s) == seg_t) {
+        atomicOr(&sm->gtw[s >> 5], 1u << (s & 31));
+        ++n;
+      }
+    int tot;
+    sr::block_scan(n, tot, sm);
+    emit_words(nwords, 0, tot, out, k, sm);
+    if (count && tid == 0) count[row] = tot;
+    return;
+  }
+  const int A = cnt[4 * row], W = cnt[4 * row + 1];
+  const int n = seg_row ? cnt[4 * row + 2] : len;
+  const int m = n < k ? n : k;   // keys to select
+  const bool settled = A <= m && W <= cw && (n <= k ? A + W == n : A + W >= k);
+  if (!settled) {
+    // the sampled window missed this row: the memory form redoes its block of rows
+    if (tid == 0) flags[t / block_rows] = 1;
+    return;
+  }
+  // the keys >= U (written unordered into the row's own idx slots by the emit pass)
+  const int above_n = A;
+  for (int j = tid; j < above_n; j += NT) {
+    const int s = out[j];
+    atomicOr(&sm->gtw[s >> 5], 1u << (s & 31));
+  }
+  for (int j = tid; j < W; j += NT) {
+    const int2 e = win[row * cw + j];
+    sm->cidx[j] = e.x;
+    sm->ckey[j] = order_key(__int_as_float(e.y));
+  }
+  if (tid == 0)
+    for (int j = 0; j < 8; ++j) sm->ubc[j] = 0u;
+  __syncthreads();
+  int need = m - A;
+  if (need > 0 && W == need) {
+    for (int j = tid; j < W; j += NT) atomicOr(&sm->gtw[sm->cidx[j] >> 5], 1u << (sm->cidx[j] & 31));
+    need = 0;
+    __syncthreads();
+  } else if (need > 0) {
+    // T among the window keys: every listed key lies in [L, U), so radix over all 32 bits
+    uint32_t prefix = 0u, mask = 0u;
+    sr::resolve([&](auto fn) {
+      for (int j = tid; j < W; j += NT) fn(sm->ckey[j]);
+    }, 31, prefix, mask, need, W, sm);
+    for (int j = tid; j < W; j += NT) {
+      const uint32_t km = sm->ckey[j] & mask;
+      const int s = sm->cidx[j];
+      if (km > prefix) atomicOr(&sm->gtw[s >> 5], 1u << (s & 31));
+      else if (km == prefix) atomicOr(&sm->eqw[s >> 5], 1u << (s & 31));
+    }
+    __syncthreads();
+  }
+  emit_words(nwords, need, m, out, k, sm);
+  if (count && tid == 0) count[row] = m;
+}
+
+}  // namespace st
+
 // ------------------------------------------------------------------ long rows
 // Rows longer than the shared stage (t >= kStageMax): one persistent CTA of 1024
 // threads per SM, so that the rows in flight (152 x at most 512 KB at S = 131072)
@@ -804,15 +1061,26 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need,
 // digits below a known prefix over the keys visit(fn) presents (see the staged
 // path: histogram levels, early stop when the bin holds exactly the keys needed
 // or every key in play has the same lower bits)
+// Up to four digit levels (shift, number of bins) held in registers: selected by constant
+// index, so that no table lands in local memory, where streaming rows would evict it to DRAM.
+struct Levels {
+  int n, s0, s1, s2, s3, b0, b1, b2, b3;
+  __device__ __forceinline__ int shift(int l) const {
+    return l == 0 ? s0 : (l == 1 ? s1 : (l == 2 ? s2 : s3));
+  }
+  __device__ __forceinline__ int bins(int l) const {
+    return l == 0 ? b0 : (l == 1 ? b1 : (l == 2 ? b2 : b3));
+  }
+};
+
 template <class Visit>
-__device__ __forceinline__ void resolve_levels(Visit visit, uint32_t* hist, int nlev,
-                                               const int* shifts, const int* nbins,
+__device__ __forceinline__ void resolve_levels(Visit visit, uint32_t* hist, const Levels lv,
                                                uint32_t& prefix, uint32_t& mask, int& need,
                                                int in_bin, Smem* sm) {
   const int tid = threadIdx.x, lane = tid & 31;
 #pragma unroll 1
-  for (int lvl = 0; lvl < nlev && in_bin != need; ++lvl) {
-    const int shift = shifts[lvl], nb = nbins[lvl];
+  for (int lvl = 0; lvl < lv.n && in_bin != need; ++lvl) {
+    const int shift = lv.shift(lvl), nb = lv.bins(lvl);
     const uint32_t low = (1u << shift) - 1u;
     for (int i = tid; i < nb; i += NT) hist[i] = 0u;
     if (tid == 0) {
@@ -934,14 +1202,13 @@ __device__ __forceinline__ void finish_candidates(const RowKeys& rk, bool inner,
                                                   const TopkParams& p, int32_t* out, Smem* sm) {
   const int tid = threadIdx.x;
   const int ncand = min(in_bin, kLongCand);
-  const int shifts_in[2] = {8, 0}, nbins_in[2] = {512, 256};
-  const int shifts_out[4] = {24, 16, 8, 0}, nbins_out[4] = {256, 256, 256, 256};
+  const Levels lv_in = {2, 8, 0, 0, 0, 512, 256, 0, 0};
+  const Levels lv_out = {4, 24, 16, 8, 0, 256, 256, 256, 256};
   resolve_levels(
       [&](auto fn) {
         for (int j = tid; j < ncand; j += NT) fn(rk.key(static_cast<int>(sm->cand[j])));
       },
-      sm->hist, inner ? 2 : 4, inner ? shifts_in : shifts_out, inner ? nbins_in : nbins_out,
-      prefix, mask, need, in_bin, sm);
+      sm->hist, inner ? lv_in : lv_out, prefix, mask, need, in_bin, sm);
   for (int j = tid; j < ncand; j += NT) {
     const int sj = static_cast<int>(sm->cand[j]);
     const uint32_t km = rk.key(sj) & mask;
@@ -1257,8 +1524,8 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
     } else {
       in_bin = -1;
     }
-    const int shifts_in[2] = {6, 0}, nbins_in[2] = {2048, 64};
-    const int shifts_out[3] = {21, 10, 0}, nbins_out[3] = {2048, 2048, 1024};
+    const Levels lv_in = {2, 6, 0, 0, 0, 2048, 64, 0, 0};
+    const Levels lv_out = {3, 21, 10, 0, 0, 2048, 2048, 1024, 0};
     resolve_levels(
         [&](auto fn) {
           for (int c = tid; c < nq; c += NT) {
@@ -1269,8 +1536,7 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
             fn(kv.w);
           }
         },
-        sm->hist, inner ? 2 : 3, inner ? shifts_in : shifts_out, inner ? nbins_in : nbins_out,
-        prefix, mask, need, in_bin, sm);
+        sm->hist, inner ? lv_in : lv_out, prefix, mask, need, in_bin, sm);
     select_sweep(rk, nq, mask, prefix, need, out, p.k, sm);
   }
   if (p.count && tid == 0) p.count[row] = p.k;
@@ -1282,6 +1548,7 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
 // rows t0 <= t < t_hi of every batch row; persistent, longest rows first
 __global__ void __launch_bounds__(lr::NT, 1) topk_long_kernel(const TopkParams p, int t0) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  if (gated_off(p)) return;
   lr::Smem* sm = reinterpret_cast<lr::Smem*>(smem_raw);
   const int tid = threadIdx.x;
   const long long nlong = static_cast<long long>(p.B) * (p.t_hi - t0);
@@ -1312,8 +1579,9 @@ int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int 
 
 int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
                      int32_t* idx, int32_t* count, cudaStream_t stream, int t_lo, int t_hi,
-                     long long rows_blk) {
+                     long long rows_blk, const int* gate) {
   TopkParams p;
+  p.gate = gate;
   p.scores = scores;
   p.ld = ld;
   p.seg = seg;
@@ -1354,6 +1622,31 @@ int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B,
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   }
   return DSA_OK;
+}
+
+int launch_stream_window(const float* sample, const int32_t* seg, int B, int S, int G, int k,
+                         float* thr, cudaStream_t stream) {
+  (void)seg;
+  const long long rows = static_cast<long long>(B) * S;
+  if (rows > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+  st::stream_window_kernel<<<static_cast<unsigned>(rows), st::NT, sizeof(st::WinSmem), stream>>>(
+      sample, B, S, G, k, thr);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int launch_stream_finish(const int32_t* seg, int B, int S, int k, const int* cnt,
+                         const int2* win, int cw, int32_t* idx, int32_t* count, int* flags,
+                         int block_rows, cudaStream_t stream) {
+  if (S > st::kMaxS || cw > st::kCw) return DSA_ERR_UNSUPPORTED;
+  const long long rows = static_cast<long long>(B) * S;
+  if (rows > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(st::FinSmem);
+  if (cudaFuncSetAttribute(st::stream_finish_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  st::stream_finish_kernel<<<static_cast<unsigned>(rows), st::NT, smem, stream>>>(
+      seg, B, S, k, cnt, win, cw, idx, count, flags, block_rows);
+  return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 }  // namespace dsa

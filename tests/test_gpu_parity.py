@@ -707,3 +707,76 @@ def test_index_topk_fp8_matches_oracle(case):
     ref_idx, ref_cnt = oracle.topk(sc, inp["seg"], S, k, B=B)
     assert np.array_equal(idx.cpu().numpy().reshape(-1, k), ref_idx)
     assert np.array_equal(cnt.cpu().numpy().reshape(-1), ref_cnt)
+
+
+# ------------------------------- fused indexer + top-k, streaming form (no score rows)
+
+@pytest.mark.parametrize("case", [
+    # B, S, Hi, Di, k, ndocs, block_rows
+    (1, 128, 4, 32, 4, 0, 256),        # the tiny workload's shape: every tile sampled
+    (2, 3000, 64, 128, 300, 0, 512),   # rows past 16 tiles: a sampled window per row
+    (1, 2500, 64, 128, 2048, 0, 256),  # k near the row length
+    (2, 2000, 16, 64, 100, 3, 512),    # packed documents: windows from an estimated count
+    (1, 489, 64, 128, 512, 3, 256),    # every row has at most k keys
+    (1, 4100, 4, 32, 64, 0, 1024),     # 64 queries per indexer tile
+])
+def test_index_topk_stream_matches_oracle(case):
+    """The streaming form (sampled window, candidate lists, no score row) against the oracle's
+    top-k of the oracle's scores, every row, bit for bit."""
+    dsa = _dsa()
+    B, S, Hi, Di, k, ndocs, R = case
+    inp = _indexer_case(B, S, Hi, Di, seed=820 + S + Hi, ndocs=ndocs)
+    seg = None if inp["seg"] is None else dev(inp["seg"])
+    idx, cnt = dsa.dsa_index_topk_stream(bf16_dev(inp["q_idx"]), bf16_dev(inp["k_idx"]),
+                                         dev(inp["w"]), k, seg, block_rows=R)
+    assert dsa.dsa_get_last_device_error() == 0
+    sc = oracle.index_scores(inp["q_idx"], inp["k_idx"], inp["w"], inp["seg"])
+    ref_idx, ref_cnt = oracle.topk(sc, inp["seg"], S, k, B=B)
+    assert np.array_equal(idx.cpu().numpy().reshape(-1, k), ref_idx)
+    assert np.array_equal(cnt.cpu().numpy().reshape(-1), ref_cnt)
+
+
+def test_index_topk_stream_matches_unfused_path_at_v32_shape():
+    """The V3.2 indexer shape at S = 6000 with top-2048 (the bench's distribution of scores):
+    the streaming form equals the unfused indexer + top-k on every row."""
+    dsa = _dsa()
+    wl = synth.WORKLOADS["v32_671b_s16k"].replace(S=6000)
+    ind = synth.indexer_inputs(wl)
+    q, kk, w = bf16_dev(ind["q_idx"]), bf16_dev(ind["k_idx"]), dev(ind["w"])
+    idx_s, cnt_s = dsa.dsa_index_topk_stream(q, kk, w, wl.topk)
+    idx_u, cnt_u = dsa.dsa_topk(dsa.dsa_index_scores(q, kk, w), wl.topk)
+    assert dsa.dsa_get_last_device_error() == 0
+    assert torch.equal(idx_s, idx_u) and torch.equal(cnt_s, cnt_u)
+
+
+@pytest.mark.parametrize("S", [6000, 20000])
+def test_index_topk_stream_rows_left_to_the_memory_form(S):
+    """Every score equal: each row's window holds all its keys, so every row with more than
+    4096 keys overflows the window list and is left unsettled; its block is redone by the
+    memory form (gated on the device), across the 16384-key boundary for S = 20000. The
+    selection is then the k lowest indices."""
+    dsa = _dsa()
+    B, Hi, Di, k = 1, 64, 128, 100
+    one = torch.full((B, S, Hi, Di), 0.125, dtype=torch.bfloat16, device="cuda")
+    kk = torch.full((B, S, Di), 0.125, dtype=torch.bfloat16, device="cuda")
+    w = torch.full((B, S, Hi), 0.0625, dtype=torch.float32, device="cuda")
+    idx, cnt = dsa.dsa_index_topk_stream(one, kk, w, k, block_rows=2048)
+    assert dsa.dsa_get_last_device_error() == 0
+    t = np.arange(S)
+    ref = np.where(np.arange(k)[None, :] <= t[:, None], np.arange(k)[None, :], -1)
+    assert np.array_equal(idx.cpu().numpy().reshape(S, k), ref)
+    assert np.array_equal(cnt.cpu().numpy().reshape(S), np.minimum(t + 1, k))
+
+
+def test_index_topk_stream_fp8_matches_oracle():
+    dsa = _dsa()
+    B, S, Hi, Di, k, ndocs = 1, 2600, 64, 128, 256, 2
+    _, inp = _fp8_inputs(B, S, Hi, Di, ndocs, "pow2", seed=870)
+    seg = dev(inp["seg"])
+    idx, cnt = dsa.dsa_index_topk_stream(dev(inp["q_idx"]), dev(inp["k_idx"]), dev(inp["w"]), k,
+                                         seg, block_rows=512, k_scale=dev(inp["k_scale"]))
+    assert dsa.dsa_get_last_device_error() == 0
+    sc = oracle.index_scores_fp8(inp["q_idx"], inp["k_idx"], inp["w"], inp["seg"], inp["k_scale"])
+    ref_idx, ref_cnt = oracle.topk(sc, inp["seg"], S, k, B=B)
+    assert np.array_equal(idx.cpu().numpy().reshape(-1, k), ref_idx)
+    assert np.array_equal(cnt.cpu().numpy().reshape(-1), ref_cnt)

@@ -149,3 +149,28 @@ def test_indexer_loss_full_size():
     assert abs(via_dw - rhs) <= 1e-4 * abs(rhs)
     assert abs(via_dk - rhs) <= 2e-3 * abs(rhs)      # G in bf16 (2^-9) in the dk, dq products
     assert abs(via_dq - rhs) <= 2e-3 * abs(rhs)
+
+
+@pytest.mark.slow
+def test_index_topk_stream_long_context():
+    """The streaming form (no score rows) at the long-context shape S = 131072: every row equal
+    to the memory form's (block-fused indexer + top-k), and sampled rows (t = 0, k-1, k, S-1
+    and uniform draws) equal to the oracle's top-k of the oracle's scores."""
+    import sparse_attention_index_gb300 as dsa
+    wl = synth.WORKLOADS["long_s128k"]
+    ind = synth.indexer_inputs(wl)
+    qd, kd, wd = bf16_dev(ind["q_idx"]), bf16_dev(ind["k_idx"]), dev(ind["w"])
+    S, k = wl.S, wl.topk
+    idx_s, cnt_s = dsa.dsa_index_topk_stream(qd, kd, wd, k)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_last_device_error() == 0
+    idx_m, cnt_m = dsa.dsa_index_topk(qd, kd, wd, k, block_rows=8192)
+    torch.cuda.synchronize()
+    assert dsa.dsa_get_last_device_error() == 0
+    assert torch.equal(idx_s, idx_m) and torch.equal(cnt_s, cnt_m)
+    del idx_m, cnt_m
+    rows = synth.sample_rows(wl, 6)
+    sc = oracle.index_scores(ind["q_idx"], ind["k_idx"], ind["w"], None, rows=rows)
+    ref_idx, ref_cnt = oracle.topk(sc, None, S, k, rows=rows, B=wl.B)
+    assert np.array_equal(idx_s.cpu().numpy().reshape(-1, k)[rows], ref_idx)
+    assert np.array_equal(cnt_s.cpu().numpy().reshape(-1)[rows], ref_cnt)
