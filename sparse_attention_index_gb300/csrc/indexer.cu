@@ -330,25 +330,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b, t0, nkb;
         item_coords(p, item, b, t0, nkb);
         if (!mbar_wait(&tail->q_full[qs], q_par, abort_flag, p.err, kErr)) { ok = false; break; }
-        const uint32_t q_addr = smem_u32(q_smem + qs * p.q_slot_bytes);
+        // base descriptors of the item's Q slot and (below) of each key stage, advanced by
+        // constants per MMA: issue blocks at the pipe's pace, so scalar work per MMA would
+        // leave the tensor pipe idle between instructions
+        const uint64_t bdesc0 = umma_sdesc(smem_u32(q_smem + qs * p.q_slot_bytes), sbo, p.layout);
         const int nt = item_tiles<MODE>(nkb);
         for (int m = 0; m < nt; ++m) {
           if (!mbar_wait(&tail->k_full[ks], k_par, abort_flag, p.err, kErr)) { ok = false; break; }
           if (!mbar_wait(&tail->acc_empty[as], a_par, abort_flag, p.err, kErr)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t k_addr = smem_u32(k_smem + ks * p.k_stage_bytes);
+          const uint64_t adesc0 = umma_sdesc(smem_u32(k_smem + ks * p.k_stage_bytes), sbo, p.layout);
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(as * kColsPerTile);
+          auto mma = [&](uint64_t ad, uint64_t bd, uint32_t acc) {
+            if (F8)
+              umma_f8(d_tmem, ad, bd, idesc, acc);
+            else
+              umma_bf16(d_tmem, ad, bd, idesc, acc);
+          };
           for (int a = 0; a < p.n_atoms; ++a) {
-            for (int kk = 0; kk < ksteps_per_atom; ++kk) {
-              const uint32_t off = static_cast<uint32_t>(kk) * 32u;
-              const uint64_t adesc =
-                  umma_sdesc(k_addr + a * kKeysPerTile * atom_bytes + off, sbo, p.layout);
-              const uint64_t bdesc =
-                  umma_sdesc(q_addr + a * kColsPerTile * atom_bytes + off, sbo, p.layout);
-              if (F8)
-                umma_f8(d_tmem, adesc, bdesc, idesc, (a | kk) != 0 ? 1u : 0u);
-              else
-                umma_bf16(d_tmem, adesc, bdesc, idesc, (a | kk) != 0 ? 1u : 0u);
+            const uint64_t ad = umma_desc_adv(adesc0, a * kKeysPerTile * atom_bytes);
+            const uint64_t bd = umma_desc_adv(bdesc0, a * kColsPerTile * atom_bytes);
+            if (ksteps_per_atom == 4) {   // 128-byte rows: four MMAs of 32 bytes of K each
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma(umma_desc_adv(ad, kk * 32u), umma_desc_adv(bd, kk * 32u), (a | kk) != 0 ? 1u : 0u);
+            } else {
+              for (int kk = 0; kk < ksteps_per_atom; ++kk)
+                mma(umma_desc_adv(ad, kk * 32u), umma_desc_adv(bd, kk * 32u), (a | kk) != 0 ? 1u : 0u);
             }
           }
           umma_commit(&tail->k_empty[ks]);
