@@ -61,17 +61,19 @@ def pair_counts(wl: synth.Workload):
     return causal, sel
 
 
-def stage_work(wl: synth.Workload):
-    """Algorithmic work per step: FLOP for the contractions, bytes for top-k.
+def stage_work(wl: synth.Workload, indexer_loss: bool = False):
+    """Algorithmic work per step: FLOP for the contractions, bytes for top-k (the causal
+    scores read, idx written, and with the indexer loss the selected scores written too).
 
     The indexer loss: its forward is the target's logit product (H x Dqk per selected
     pair); its backward the three products Z, dq and dk (Hi x Di each per selected pair).
     """
     causal, sel = pair_counts(wl)
+    slots = wl.topk * wl.B * wl.S
     return {
         "indexer": {"flop": 2.0 * wl.Hi * wl.Di * causal},
         "indexer_topk": {"flop": 2.0 * wl.Hi * wl.Di * causal},
-        "topk": {"bytes": 4.0 * causal + 4.0 * wl.topk * wl.B * wl.S},
+        "topk": {"bytes": 4.0 * causal + 4.0 * slots * (2 if indexer_loss else 1)},
         "attn_fwd": {"flop": 2.0 * wl.H * (wl.Dqk + wl.Dv) * sel},
         "attn_bwd": {"flop": 2.0 * wl.H * (3 * wl.Dqk + 2 * wl.Dv) * sel} if wl.backward else None,
         "loss_fwd": {"flop": 2.0 * wl.H * wl.Dqk * sel},
@@ -271,6 +273,10 @@ def run_ours(args, wl, rank, world, local_rank):
         dq_idx = torch.empty((B, S, wl.Hi, wl.Di), dtype=torch.float32, device=device)
         dk_idx = torch.empty((B, S, wl.Di), dtype=torch.float32, device=device)
         dw = torch.empty((B, S, wl.Hi), dtype=torch.float32, device=device)
+        # the top-k hands the loss the selected scores slot by slot (read contiguously)
+        sel = torch.empty((B, S, k), dtype=torch.float32, device=device)
+    else:
+        sel = None
     # indexer, top-k, the forward (two launches on the dense-tile kernel: bitmap build +
     # attention), the backward and its finalize (four on the dense-tile kernels: bitmap,
     # dQ pass, dK / dV pass, finalize)
@@ -292,10 +298,10 @@ def run_ours(args, wl, rank, world, local_rank):
         e = 1
         if stream_form:
             dsa.dsa_index_topk_stream(q_idx, k_idx, w, k, seg, block_rows=R, idx=idx,
-                                      count=count, ws=topk_ws, stream=stream)
+                                      count=count, ws=topk_ws, stream=stream, vals=sel)
         elif fused:
             dsa.dsa_index_topk(q_idx, k_idx, w, k, seg, block_rows=R, idx=idx, count=count,
-                               ws=topk_ws, stream=stream)   # e4m3 inputs: the fp8 indexer
+                               ws=topk_ws, stream=stream, vals=sel)   # e4m3: the fp8 indexer
         else:
             if fp8:
                 dsa.dsa_index_scores_fp8(q_idx, k_idx, w, seg, scores=scores, stream=stream)
@@ -303,7 +309,7 @@ def run_ours(args, wl, rank, world, local_rank):
                 dsa.dsa_index_scores(q_idx, k_idx, w, seg, scores=scores, stream=stream)
             ev[e].record(stream)
             e += 1
-            dsa.dsa_topk(scores, k, seg, idx=idx, count=count, stream=stream)
+            dsa.dsa_topk(scores, k, seg, idx=idx, count=count, vals=sel, stream=stream)
         ev[e].record(stream)
         e += 1
         dsa.dsa_sparse_attn_fwd(Q, K, V, idx, wl.scale, O=O, lse=lse, ws=fwd_ws, stream=stream)
@@ -315,8 +321,8 @@ def run_ours(args, wl, rank, world, local_rank):
             ev[e].record(stream)
             e += 1
         if loss:
-            dsa.dsa_indexer_loss(Q, K, idx, lse, scores, wl.scale, 1.0 / (B * S), kl=kl, dI=dI,
-                                 stream=stream)
+            dsa.dsa_indexer_loss(Q, K, idx, lse, None, wl.scale, 1.0 / (B * S), kl=kl, dI=dI,
+                                 stream=stream, sel_scores=sel)
             ev[e].record(stream)
             dsa.dsa_indexer_loss_bwd(q_idx, k_idx, w, idx, dI, dq_idx=dq_idx, dk_idx=dk_idx,
                                      dw=dw, stream=stream)
@@ -510,9 +516,8 @@ def main(argv=None):
                     help="rows per reference-arm step (default: 4 per host core)")
     args = ap.parse_args(argv)
     for opt, val in (("--fused-topk", args.fused_topk), ("--stream-topk", args.stream_topk)):
-        if val and (val % 256 or args.indexer_loss):
-            ap.error(f"{opt} takes a multiple of 256 and no --indexer-loss "
-                     "(the loss reads the score matrix)")
+        if val and val % 256:
+            ap.error(f"{opt} takes a multiple of 256")
     if args.fused_topk and args.stream_topk:
         ap.error("--fused-topk and --stream-topk are two forms of the same stage: pick one")
     if args.indexer_loss:
@@ -548,7 +553,7 @@ def main(argv=None):
         return 0
 
     peaks = load_peaks()
-    work = stage_work(wl)
+    work = stage_work(wl, args.indexer_loss)
     tokens = wl.B * wl.S
     total_flop = step_flop(wl, r["stages"])
     stages_out = {}

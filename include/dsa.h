@@ -143,11 +143,17 @@ int dsa_index_scores_fp8(const void* q_idx, const void* k_idx, const float* k_sc
  *   idx     int32 [B, S, k] out: the selected keys in ascending order,
  *           slots m(t)..k-1 set to -1
  *   count   int32 [B, S] out, or NULL: m(t)
+ *   vals    fp32 [B, S, k] out, or NULL: the score of the key in each slot of idx,
+ *           -inf at slots holding -1. It is read back from the score row just after
+ *           the row's selection (while the row is in L2), so that a consumer of the
+ *           selected scores (dsa_indexer_loss with ld_scores = 0) reads k contiguous
+ *           floats per row instead of gathering them from the row.
  *   ws      workspace of dsa_topk_workspace_size() bytes (may be NULL if 0)
  */
 size_t dsa_topk_workspace_size(int B, int S, int k);
 int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* seg, int B, int S, int k,
-             int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream);
+             int32_t* idx, int32_t* count, float* vals, void* ws, size_t ws_bytes,
+             void* stream);
 
 /*
  * dsa_sparse_attn_fwd - attention over the selected keys ("Support Ring
@@ -321,7 +327,8 @@ int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
  * long context).
  *
  *   q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di as for dsa_index_scores;
- *   k, idx [B, S, k], count [B, S] (or NULL) as for dsa_topk (identical results);
+ *   k, idx [B, S, k], count [B, S] (or NULL), vals [B, S, k] (or NULL) as for dsa_topk
+ *               (identical results);
  *   block_rows  query rows per block: a positive multiple of 256;
  *   ws          at least dsa_index_topk_workspace_size(B, S, block_rows) bytes.
  *
@@ -330,7 +337,8 @@ int dsa_sparse_attn_bwd_noalloc(const void* Q, const void* K, const void* V, con
 size_t dsa_index_topk_workspace_size(int B, int S, int block_rows);
 int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
                    const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
-                   int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream);
+                   int32_t* idx, int32_t* count, float* vals, void* ws, size_t ws_bytes,
+                   void* stream);
 
 /*
  * dsa_index_topk_fp8 - dsa_index_topk on e4m3 q_idx / k_idx with an optional
@@ -340,8 +348,8 @@ int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dt
  */
 int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scale, const void* w,
                        int w_dtype, const int32_t* seg, int B, int S, int Hi, int Di, int k,
-                       int block_rows, int32_t* idx, int32_t* count, void* ws, size_t ws_bytes,
-                       void* stream);
+                       int block_rows, int32_t* idx, int32_t* count, float* vals, void* ws,
+                       size_t ws_bytes, void* stream);
 
 /*
  * dsa_index_topk_stream - dsa_index_scores followed by dsa_topk, with no score row in
@@ -355,8 +363,9 @@ int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scal
  *  2. From each row's sample, a window [L, U) around its k-th largest score: the sample's
  *     order statistics at rank k * (sampled) / (valid keys), +- 5 standard deviations.
  *  3. The full indexer pass keeps, per row, the keys scoring >= U (their indices, in the
- *     row's idx slots) and the keys in [L, U) (index and score, up to 4096), and stores
- *     no other score.
+ *     row's idx slots, and with vals their scores in the row's vals slots) and the keys in
+ *     [L, U) (index and score, up to 4096), and stores no other score. Rows with at most
+ *     k keys take every valid key this way (U = L = -inf).
  *  4. Each row is settled from these two lists: when at most k keys score >= U and the
  *     two lists together hold at least min(k, valid keys), the k-th largest score lies in
  *     the window and is found there; ties go to the lower key index as in dsa_topk.
@@ -366,7 +375,9 @@ int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scal
  *     launches that a flag on the device switches on. On typical score distributions few
  *     or no blocks are redone.
  *
- *   q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di, k, idx, count: as for dsa_index_topk;
+ *   q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di, k, idx, count, vals: as for
+ *               dsa_index_topk; vals needs k <= 2048 (the scores of a row are staged by
+ *               slot in shared memory), DSA_ERR_UNSUPPORTED otherwise;
  *   block_rows  rows per redone block: a positive multiple of 256;
  *   ws          at least dsa_index_topk_stream_workspace_size(B, S, block_rows) bytes:
  *               the samples (16 KB per query row), the window lists (32 KB per query row)
@@ -377,7 +388,8 @@ int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scal
 size_t dsa_index_topk_stream_workspace_size(int B, int S, int block_rows);
 int dsa_index_topk_stream(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
                           const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
-                          int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream);
+                          int32_t* idx, int32_t* count, float* vals, void* ws, size_t ws_bytes,
+                          void* stream);
 
 /*
  * dsa_index_topk_stream_fp8 - dsa_index_topk_stream on e4m3 q_idx / k_idx with an optional
@@ -386,7 +398,7 @@ int dsa_index_topk_stream(const void* q_idx, const void* k_idx, const void* w, i
 int dsa_index_topk_stream_fp8(const void* q_idx, const void* k_idx, const float* k_scale,
                               const void* w, int w_dtype, const int32_t* seg, int B, int S, int Hi,
                               int Di, int k, int block_rows, int32_t* idx, int32_t* count,
-                              void* ws, size_t ws_bytes, void* stream);
+                              float* vals, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * dsa_indexer_loss - the indexer's auxiliary loss and its gradient with respect
@@ -411,7 +423,9 @@ int dsa_index_topk_stream_fp8(const void* q_idx, const void* k_idx, const float*
  *
  *   Q      bf16 [B, S, H, Dqk]     K    bf16 [B, S, Hkv, Dqk]
  *   idx    int32 [B, S, k]          lse  fp32 [B, S, H] (from dsa_sparse_attn_fwd)
- *   scores fp32 [B, S, ld_scores]   only the selected entries are read
+ *   scores fp32 [B, S, ld_scores]   only the selected entries are read; or, with
+ *          ld_scores = 0, fp32 [B, S, k]: the selected keys' scores slot by slot (the
+ *          `vals` of dsa_topk / dsa_index_topk / dsa_index_topk_stream), read contiguously
  *   kl     fp32 [B, S] out          dI   fp32 [B, S, k] out
  *
  * Hkv divides H (head h reads K head h / (H / Hkv)). The tensor-core kernel takes

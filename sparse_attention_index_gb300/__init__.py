@@ -68,7 +68,7 @@ def _load() -> ctypes.CDLL:
     lib.dsa_index_scores_fp8.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, vp, i64, vp]
     lib.dsa_topk_workspace_size.argtypes = [ci, ci, ci]
     lib.dsa_topk_workspace_size.restype = sz
-    lib.dsa_topk.argtypes = [vp, i64, vp, ci, ci, ci, vp, vp, vp, sz, vp]
+    lib.dsa_topk.argtypes = [vp, i64, vp, ci, ci, ci, vp, vp, vp, vp, sz, vp]
     lib.dsa_sparse_attn_fwd_workspace_size.argtypes = [ci, ci, ci, ci, ci, ci]
     lib.dsa_sparse_attn_fwd_workspace_size.restype = sz
     lib.dsa_sparse_attn_fwd.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, ci, cf, vp, vp, vp,
@@ -90,9 +90,10 @@ def _load() -> ctypes.CDLL:
     lib.dsa_indexer_loss_bwd.argtypes = [vp, vp, vp, vp, vp, ci, ci, ci, ci, ci, vp, vp, vp, vp]
     lib.dsa_index_topk_workspace_size.argtypes = [ci, ci, ci]
     lib.dsa_index_topk_workspace_size.restype = sz
-    lib.dsa_index_topk.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, sz, vp]
+    lib.dsa_index_topk.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp, sz,
+                                   vp]
     lib.dsa_index_topk_fp8.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp, vp, vp,
-                                       sz, vp]
+                                       vp, sz, vp]
     lib.dsa_index_topk_stream_workspace_size.argtypes = [ci, ci, ci]
     lib.dsa_index_topk_stream_workspace_size.restype = sz
     lib.dsa_index_topk_stream.argtypes = lib.dsa_index_topk.argtypes
@@ -193,20 +194,36 @@ def dsa_index_scores_fp8(q_idx, k_idx, w, seg=None, k_scale=None, scores=None,
     return scores
 
 
-def dsa_topk(scores, k: int, seg=None, S: int | None = None, idx=None, count=None, stream=None):
-    """scores fp32 [B,S,ld] -> (idx int32 [B,S,k] ascending / -1 padded, count int32 [B,S])."""
+def _vals_out(vals, B, S, k, dev):
+    """vals: None (not wanted), True (allocate) or an fp32 [B, S, k] tensor."""
+    if vals is None or vals is False:
+        return None
+    if vals is True:
+        return torch.empty((B, S, k), dtype=torch.float32, device=dev)
+    return vals
+
+
+def dsa_topk(scores, k: int, seg=None, S: int | None = None, idx=None, count=None, vals=None,
+             stream=None):
+    """scores fp32 [B,S,ld] -> (idx int32 [B,S,k] ascending / -1 padded, count int32 [B,S]).
+
+    vals: True or an fp32 [B,S,k] tensor to have each slot's score as well (-inf at empty
+    slots); the result is then (idx, count, vals).
+    """
     B, S_, ld = scores.shape
     S = S_ if S is None else S
     if idx is None:
         idx = torch.empty((B, S, k), dtype=torch.int32, device=scores.device)
     if count is None:
         count = torch.empty((B, S), dtype=torch.int32, device=scores.device)
+    vals = _vals_out(vals, B, S, k, scores.device)
     rc = lib.dsa_topk(_dev(scores, "scores", torch.float32), ld,
                       None if seg is None else _dev(seg, "seg", torch.int32), B, S, k,
-                      _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32), None, 0,
+                      _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32),
+                      None if vals is None else _dev(vals, "vals", torch.float32), None, 0,
                       _stream(stream))
     _check(rc, "dsa_topk")
-    return idx, count
+    return (idx, count) if vals is None else (idx, count, vals)
 
 
 def fwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv) -> int:
@@ -349,15 +366,16 @@ class HostPipeline:
                  fused_block_rows=0, stream_form=False):
         """indexer_loss: also run the indexer loss (objective grad_scale * sum of the
         per-query losses, default 1/(B*S)) and its gradient each step, returning kl,
-        dq_idx, dk_idx and dw. indexer_dtype "e4m3": q_idx / k_idx are e4m3 bytes and the
-        fp8 indexer runs. fused_block_rows > 0: the indexer and the top-k run fused through
-        blocks of that many query rows (dsa_index_topk), with no [B, S, S] score matrix;
-        with stream_form, in the streaming form (dsa_index_topk_stream: no score rows; the
-        blocks are those its fallback redoes)."""
+        dq_idx, dk_idx and dw; the top-k hands the loss its selected scores slot by slot, so
+        it runs with every form of the top-k. indexer_dtype "e4m3": q_idx / k_idx are e4m3
+        bytes and the fp8 indexer runs. fused_block_rows > 0: the indexer and the top-k run
+        fused through blocks of that many query rows (dsa_index_topk), with no [B, S, S]
+        score matrix; with stream_form, in the streaming form (dsa_index_topk_stream: no
+        score rows; the blocks are those its fallback redoes)."""
         if indexer_dtype not in ("bf16", "e4m3"):
             raise ValueError("indexer_dtype is 'bf16' or 'e4m3'")
-        if indexer_loss and (indexer_dtype != "bf16" or fused_block_rows):
-            raise ValueError("the indexer loss reads the bf16 indexer inputs and the score matrix")
+        if indexer_loss and indexer_dtype != "bf16":
+            raise ValueError("the indexer loss's backward reads the bf16 indexer inputs")
         dev = torch.device("cuda") if device is None else torch.device(device)
         self.dev, self.topk, self.scale, self.backward = dev, topk, scale, backward
         self.loss = indexer_loss
@@ -393,9 +411,11 @@ class HostPipeline:
             self.out.update({"dQ": e(B, S, H, Dqk), "dK": e(B, S, Hkv, Dqk),
                              "dV": e(B, S, Hkv, Dv)})
             self.ws = e(bwd_workspace_bytes(B, S, H, Hkv, Dqk, Dv), dt=torch.uint8)
+        self.sel = None
         if indexer_loss:
             f32 = torch.float32
             self.dI = e(B, S, topk, dt=f32)
+            self.sel = e(B, S, topk, dt=f32)   # the selected scores, by slot
             self.out.update({"kl": e(B, S, dt=f32), "dq_idx": e(B, S, Hi, Di, dt=f32),
                              "dk_idx": e(B, S, Di, dt=f32), "dw": e(B, S, Hi, dt=f32)})
         self.s_in, self.s_c, self.s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
@@ -446,7 +466,7 @@ class HostPipeline:
             fuse = dsa_index_topk_stream if self.stream_form else dsa_index_topk
             fuse(d["q_idx"], d["k_idx"], d["w"], self.topk, d.get("seg"),
                  block_rows=self.block_rows, idx=o["idx"], count=o["count"], ws=self.topk_ws,
-                 stream=sc)
+                 stream=sc, vals=self.sel)
         elif self.fp8:
             dsa_index_scores_fp8(d["q_idx"], d["k_idx"], d["w"], d.get("seg"),
                                  scores=self.scores, stream=sc)
@@ -457,7 +477,7 @@ class HostPipeline:
         idx_read.record(sc)
         if not self.block_rows:
             dsa_topk(self.scores, self.topk, d.get("seg"), idx=o["idx"], count=o["count"],
-                     stream=sc)
+                     vals=self.sel, stream=sc)
         topk_done = ev()
         topk_done.record(sc)
         sc.wait_event(in2)
@@ -476,11 +496,12 @@ class HostPipeline:
             bwd_done.record(sc)
         attn_read = bwd_done
         if self.loss:
-            # reads Q, K, the scores and the indexer inputs: the next step's copies into
-            # them wait for it (idx_read, attn_read)
+            # reads Q, K, the selected scores and the indexer inputs: the next step's copies
+            # into them wait for it (idx_read, attn_read)
             self._wait(sc, self.ev_out4)
-            dsa_indexer_loss(bd["Q"], bd["K"], o["idx"], o["lse"], self.scores, self.scale,
-                             self.grad_scale, kl=o["kl"], dI=self.dI, stream=sc)
+            dsa_indexer_loss(bd["Q"], bd["K"], o["idx"], o["lse"], None, self.scale,
+                             self.grad_scale, kl=o["kl"], dI=self.dI, stream=sc,
+                             sel_scores=self.sel)
             dsa_indexer_loss_bwd(d["q_idx"], d["k_idx"], d["w"], o["idx"], self.dI,
                                  dq_idx=o["dq_idx"], dk_idx=o["dk_idx"], dw=o["dw"], stream=sc)
             loss_done = ev()
@@ -528,12 +549,12 @@ def index_topk_stream_workspace_bytes(B, S, block_rows) -> int:
 
 
 def dsa_index_topk_stream(q_idx, k_idx, w, k: int, seg=None, block_rows: int | None = None,
-                          idx=None, count=None, ws=None, stream=None, k_scale=None):
+                          idx=None, count=None, ws=None, stream=None, k_scale=None, vals=None):
     """Indexer scores and top-k with no score rows in memory (the streaming form).
 
-    Same arguments and results as dsa_index_topk; `block_rows` (a multiple of 256, default
-    S / 8 rounded up) sizes the blocks that the memory form redoes for rows the sampled
-    window does not settle.
+    Same arguments and results as dsa_index_topk (vals needs k <= 2048); `block_rows` (a
+    multiple of 256, default S / 8 rounded up) sizes the blocks that the memory form redoes
+    for rows the sampled window does not settle.
     """
     B, S, Hi, Di = q_idx.shape
     dev = q_idx.device
@@ -547,8 +568,10 @@ def dsa_index_topk_stream(q_idx, k_idx, w, k: int, seg=None, block_rows: int | N
     if ws is None:
         ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
     w_dtype = DSA_F32 if w.dtype == torch.float32 else DSA_BF16
+    vals = _vals_out(vals, B, S, k, dev)
     tail = (None if seg is None else _dev(seg, "seg", torch.int32), B, S, Hi, Di, k, block_rows,
-            _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32), _dev(ws, "ws"),
+            _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32),
+            None if vals is None else _dev(vals, "vals", torch.float32), _dev(ws, "ws"),
             ws.numel() * ws.element_size(), _stream(stream))
     if q_idx.dtype in _FP8_DTYPES:
         rc = lib.dsa_index_topk_stream_fp8(_dev8(q_idx, "q_idx"), _dev8(k_idx, "k_idx"),
@@ -561,16 +584,16 @@ def dsa_index_topk_stream(q_idx, k_idx, w, k: int, seg=None, block_rows: int | N
                                        _dev(k_idx, "k_idx", torch.bfloat16), _dev(w, "w"),
                                        w_dtype, *tail)
         _check(rc, "dsa_index_topk_stream")
-    return idx, count
+    return (idx, count) if vals is None else (idx, count, vals)
 
 
 def dsa_index_topk(q_idx, k_idx, w, k: int, seg=None, block_rows: int = 2048, idx=None,
-                   count=None, ws=None, stream=None, k_scale=None):
+                   count=None, ws=None, stream=None, k_scale=None, vals=None):
     """Indexer scores and top-k fused through blocks of query rows (no [B,S,S] scores).
 
     Same arguments and results as dsa_index_scores (or dsa_index_scores_fp8, for e4m3
-    q_idx / k_idx, with k_scale) followed by dsa_topk; the scores of one block of
-    block_rows query rows (a multiple of 256) live in `ws`.
+    q_idx / k_idx, with k_scale) followed by dsa_topk (vals as there); the scores of one
+    block of block_rows query rows (a multiple of 256) live in `ws`.
     """
     B, S, Hi, Di = q_idx.shape
     dev = q_idx.device
@@ -582,8 +605,10 @@ def dsa_index_topk(q_idx, k_idx, w, k: int, seg=None, block_rows: int = 2048, id
     if ws is None:
         ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
     w_dtype = DSA_F32 if w.dtype == torch.float32 else DSA_BF16
+    vals = _vals_out(vals, B, S, k, dev)
     tail = (None if seg is None else _dev(seg, "seg", torch.int32), B, S, Hi, Di, k, block_rows,
-            _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32), _dev(ws, "ws"),
+            _dev(idx, "idx", torch.int32), _dev(count, "count", torch.int32),
+            None if vals is None else _dev(vals, "vals", torch.float32), _dev(ws, "ws"),
             ws.numel() * ws.element_size(), _stream(stream))
     if q_idx.dtype in _FP8_DTYPES:
         rc = lib.dsa_index_topk_fp8(_dev8(q_idx, "q_idx"), _dev8(k_idx, "k_idx"),
@@ -596,16 +621,17 @@ def dsa_index_topk(q_idx, k_idx, w, k: int, seg=None, block_rows: int = 2048, id
                                 _dev(k_idx, "k_idx", torch.bfloat16), _dev(w, "w"), w_dtype,
                                 *tail)
         _check(rc, "dsa_index_topk")
-    return idx, count
+    return (idx, count) if vals is None else (idx, count, vals)
 
 
 def dsa_indexer_loss(Q, K, idx, lse, scores, scale: float, grad_scale: float = 1.0, kl=None,
-                     dI=None, stream=None):
+                     dI=None, stream=None, sel_scores=None):
     """Indexer auxiliary loss -> (kl fp32 [B,S], dI fp32 [B,S,k]).
 
     Q [B,S,H,Dqk] bf16, K [B,S,1,Dqk] bf16, idx [B,S,k] int32, lse [B,S,H] fp32 (the
-    attention forward's), scores [B,S,ld] fp32 (the index scores). dI is the gradient of
-    grad_scale * kl.sum() with respect to the score at each slot of idx.
+    attention forward's), scores [B,S,ld] fp32 (the index scores), or scores=None and
+    sel_scores [B,S,k] fp32: the selected keys' scores by slot (the top-k's vals). dI is
+    the gradient of grad_scale * kl.sum() with respect to the score at each slot of idx.
     """
     B, S, H, Dqk = Q.shape
     Hkv = K.shape[2]
@@ -616,7 +642,9 @@ def dsa_indexer_loss(Q, K, idx, lse, scores, scale: float, grad_scale: float = 1
         dI = torch.empty((B, S, k), dtype=torch.float32, device=Q.device)
     rc = lib.dsa_indexer_loss(_dev(Q, "Q", torch.bfloat16), _dev(K, "K", torch.bfloat16),
                               _dev(idx, "idx", torch.int32), _dev(lse, "lse", torch.float32),
-                              _dev(scores, "scores", torch.float32), scores.shape[-1], B, S, H,
+                              _dev(scores if scores is not None else sel_scores, "scores",
+                                   torch.float32),
+                              scores.shape[-1] if scores is not None else 0, B, S, H,
                               Hkv, Dqk, k, float(scale), float(grad_scale),
                               _dev(kl, "kl", torch.float32), _dev(dI, "dI", torch.float32),
                               _stream(stream))

@@ -172,17 +172,18 @@ size_t dsa_topk_workspace_size(int B, int S, int k) {
 }
 
 int dsa_topk(const float* scores, int64_t ld_scores, const int32_t* seg, int B, int S, int k,
-             int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream) {
+             int32_t* idx, int32_t* count, float* vals, void* ws, size_t ws_bytes,
+             void* stream) {
   (void)ws;
   (void)ws_bytes;
   if (!scores || !idx) return DSA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || k < 1) return DSA_ERR_INVALID_ARG;
   if (ld_scores < S || ld_scores % 4 != 0) return DSA_ERR_INVALID_ARG;
   if (!aligned16(scores) || !aligned16(idx) || (seg && !aligned16(seg)) ||
-      (count && !aligned16(count)))
+      (count && !aligned16(count)) || (vals && !aligned16(vals)))
     return DSA_ERR_INVALID_ARG;
   if (static_cast<long long>(B) * S >= (1LL << 31)) return DSA_ERR_UNSUPPORTED;
-  return dsa::launch_topk(scores, ld_scores, seg, B, S, k, idx, count, as_stream(stream));
+  return dsa::launch_topk(scores, ld_scores, seg, B, S, k, idx, count, vals, as_stream(stream));
 }
 
 size_t dsa_sparse_attn_fwd_workspace_size(int B, int S, int H, int Hkv, int Dqk, int Dv) {
@@ -290,9 +291,10 @@ namespace {
 
 int index_topk_impl(const void* q_idx, const void* k_idx, const float* k_scale, const void* w,
                     int w_dtype, const int32_t* seg, int B, int S, int Hi, int Di, int k,
-                    int block_rows, int32_t* idx, int32_t* count, void* ws, size_t ws_bytes,
-                    void* stream, int fp8) {
+                    int block_rows, int32_t* idx, int32_t* count, float* vals, void* ws,
+                    size_t ws_bytes, void* stream, int fp8) {
   if (!q_idx || !k_idx || !w || !idx) return DSA_ERR_INVALID_ARG;
+  if (vals && !aligned16(vals)) return DSA_ERR_INVALID_ARG;
   if (k_scale && !aligned16(k_scale)) return DSA_ERR_INVALID_ARG;
   if (fp8 && Di % 16 != 0) return DSA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || Hi < 1 || Di < 1 || k < 1) return DSA_ERR_INVALID_ARG;
@@ -315,8 +317,8 @@ int index_topk_impl(const void* q_idx, const void* k_idx, const float* k_scale, 
                                            Di, buf, ld, as_stream(stream), fp8, k_scale, t_lo,
                                            t_hi, R);
     if (rc != DSA_OK) return rc;
-    rc = dsa::launch_topk_rows(buf, ld, seg, B, S, k, idx, count, as_stream(stream), t_lo, t_hi,
-                               R);
+    rc = dsa::launch_topk_rows(buf, ld, seg, B, S, k, idx, count, vals, as_stream(stream), t_lo,
+                               t_hi, R);
     if (rc != DSA_OK) return rc;
   }
   return DSA_OK;
@@ -328,17 +330,18 @@ extern "C" {
 
 int dsa_index_topk(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
                    const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
-                   int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream) {
+                   int32_t* idx, int32_t* count, float* vals, void* ws, size_t ws_bytes,
+                   void* stream) {
   return index_topk_impl(q_idx, k_idx, nullptr, w, w_dtype, seg, B, S, Hi, Di, k, block_rows,
-                         idx, count, ws, ws_bytes, stream, 0);
+                         idx, count, vals, ws, ws_bytes, stream, 0);
 }
 
 int dsa_index_topk_fp8(const void* q_idx, const void* k_idx, const float* k_scale, const void* w,
                        int w_dtype, const int32_t* seg, int B, int S, int Hi, int Di, int k,
-                       int block_rows, int32_t* idx, int32_t* count, void* ws, size_t ws_bytes,
-                       void* stream) {
+                       int block_rows, int32_t* idx, int32_t* count, float* vals, void* ws,
+                       size_t ws_bytes, void* stream) {
   return index_topk_impl(q_idx, k_idx, k_scale, w, w_dtype, seg, B, S, Hi, Di, k, block_rows,
-                         idx, count, ws, ws_bytes, stream, 1);
+                         idx, count, vals, ws, ws_bytes, stream, 1);
 }
 
 }  // extern "C"
@@ -372,9 +375,10 @@ StreamLayout stream_layout(int B, int S, int block_rows) {
 
 int index_topk_stream_impl(const void* q_idx, const void* k_idx, const float* k_scale,
                            const void* w, int w_dtype, const int32_t* seg, int B, int S, int Hi,
-                           int Di, int k, int block_rows, int32_t* idx, int32_t* count, void* ws,
-                           size_t ws_bytes, void* stream, int fp8) {
+                           int Di, int k, int block_rows, int32_t* idx, int32_t* count,
+                           float* vals, void* ws, size_t ws_bytes, void* stream, int fp8) {
   if (!q_idx || !k_idx || !w || !idx) return DSA_ERR_INVALID_ARG;
+  if (vals && !aligned16(vals)) return DSA_ERR_INVALID_ARG;
   if (k_scale && !aligned16(k_scale)) return DSA_ERR_INVALID_ARG;
   if (fp8 && Di % 16 != 0) return DSA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || Hi < 1 || Di < 1 || k < 1) return DSA_ERR_INVALID_ARG;
@@ -387,6 +391,7 @@ int index_topk_stream_impl(const void* q_idx, const void* k_idx, const float* k_
   if (!dsa::indexer_dims_supported(Hi, Di)) return DSA_ERR_UNSUPPORTED;
   if (S > dsa::kStreamMaxS || static_cast<long long>(B) * S * Hi >= (1LL << 31))
     return DSA_ERR_UNSUPPORTED;
+  if (vals && k > 2048) return DSA_ERR_UNSUPPORTED;   // the finish stages scores by slot
   const StreamLayout ly = stream_layout(B, S, block_rows);
   if (!ws || ws_bytes < ly.bytes || !aligned16(ws)) return DSA_ERR_WORKSPACE;
   uint8_t* base = static_cast<uint8_t*>(ws);
@@ -409,10 +414,10 @@ int index_topk_stream_impl(const void* q_idx, const void* k_idx, const float* k_
   if (rc == DSA_OK) rc = dsa::launch_stream_window(sample, seg, B, S, 256 / Hi, k, thr, st);
   if (rc == DSA_OK)
     rc = dsa::launch_index_emit(q_idx, k_idx, w, wb, seg, B, S, Hi, Di, st, fp8, k_scale, thr,
-                                cnt, idx, k, win, dsa::kStreamWindowCap);
+                                cnt, idx, vals, k, win, dsa::kStreamWindowCap);
   if (rc == DSA_OK)
     rc = dsa::launch_stream_finish(seg, B, S, k, cnt, win, dsa::kStreamWindowCap, idx, count,
-                                   flags, R, st);
+                                   vals, flags, R, st);
   // the rows the lists did not settle: their blocks again through the memory form, each
   // launch gated on its block's flag on the device
   const long long ld = (static_cast<long long>(S) + 3) / 4 * 4;
@@ -421,7 +426,7 @@ int index_topk_stream_impl(const void* q_idx, const void* k_idx, const float* k_
     rc = dsa::launch_index_scores_rows(q_idx, k_idx, w, wb, seg, B, S, Hi, Di, buf, ld, st, fp8,
                                        k_scale, t_lo, t_hi, R, flags + bi);
     if (rc == DSA_OK)
-      rc = dsa::launch_topk_rows(buf, ld, seg, B, S, k, idx, count, st, t_lo, t_hi, R,
+      rc = dsa::launch_topk_rows(buf, ld, seg, B, S, k, idx, count, vals, st, t_lo, t_hi, R,
                                  flags + bi);
   }
   return rc;
@@ -437,17 +442,18 @@ size_t dsa_index_topk_stream_workspace_size(int B, int S, int block_rows) {
 
 int dsa_index_topk_stream(const void* q_idx, const void* k_idx, const void* w, int w_dtype,
                           const int32_t* seg, int B, int S, int Hi, int Di, int k, int block_rows,
-                          int32_t* idx, int32_t* count, void* ws, size_t ws_bytes, void* stream) {
+                          int32_t* idx, int32_t* count, float* vals, void* ws, size_t ws_bytes,
+                          void* stream) {
   return index_topk_stream_impl(q_idx, k_idx, nullptr, w, w_dtype, seg, B, S, Hi, Di, k,
-                                block_rows, idx, count, ws, ws_bytes, stream, 0);
+                                block_rows, idx, count, vals, ws, ws_bytes, stream, 0);
 }
 
 int dsa_index_topk_stream_fp8(const void* q_idx, const void* k_idx, const float* k_scale,
                               const void* w, int w_dtype, const int32_t* seg, int B, int S, int Hi,
                               int Di, int k, int block_rows, int32_t* idx, int32_t* count,
-                              void* ws, size_t ws_bytes, void* stream) {
+                              float* vals, void* ws, size_t ws_bytes, void* stream) {
   return index_topk_stream_impl(q_idx, k_idx, k_scale, w, w_dtype, seg, B, S, Hi, Di, k,
-                                block_rows, idx, count, ws, ws_bytes, stream, 1);
+                                block_rows, idx, count, vals, ws, ws_bytes, stream, 1);
 }
 
 int dsa_indexer_loss(const void* Q, const void* K, const int32_t* idx, const float* lse,
@@ -456,7 +462,9 @@ int dsa_indexer_loss(const void* Q, const void* K, const int32_t* idx, const flo
                      void* stream) {
   if (!Q || !K || !idx || !lse || !scores || !kl || !dI) return DSA_ERR_INVALID_ARG;
   if (B < 1 || S < 1 || H < 1 || Hkv < 1 || Dqk < 1 || k < 1) return DSA_ERR_INVALID_ARG;
-  if (H % Hkv != 0 || ld_scores < S) return DSA_ERR_INVALID_ARG;
+  // ld_scores = 0: scores holds the selected keys' scores slot by slot ([B, S, k])
+  if (H % Hkv != 0 || ld_scores < 0 || (ld_scores > 0 && ld_scores < S))
+    return DSA_ERR_INVALID_ARG;
   if (!aligned16(Q) || !aligned16(K) || !aligned16(idx) || !aligned16(lse) ||
       !aligned16(scores) || !aligned16(kl) || !aligned16(dI))
     return DSA_ERR_INVALID_ARG;

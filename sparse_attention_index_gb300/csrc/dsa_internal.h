@@ -43,12 +43,13 @@ int launch_index_scores_rows(const void* q_idx, const void* k_idx, const void* w
                              int64_t ld, cudaStream_t stream, int fp8, const float* k_scale,
                              int t_lo, int t_hi, long long rows_blk, const int* gate = nullptr);
 
+// vals non-null: each slot's score as well ([B, S, k], -inf at slots without a key)
 int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
-                int32_t* idx, int32_t* count, cudaStream_t stream);
+                int32_t* idx, int32_t* count, float* vals, cudaStream_t stream);
 // gate non-null: the kernels do nothing unless *gate != 0 (read on the device)
 int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
-                     int32_t* idx, int32_t* count, cudaStream_t stream, int t_lo, int t_hi,
-                     long long rows_blk, const int* gate = nullptr);
+                     int32_t* idx, int32_t* count, float* vals, cudaStream_t stream, int t_lo,
+                     int t_hi, long long rows_blk, const int* gate = nullptr);
 
 // Streaming form passes. sample: [B*S, kSampleKeys] scores (NaN: not a valid key) of the
 // sampled tiles. thr: [B*S, 2] (U, L) per row; cnt: [B*S, 4] zeroed before the emit pass;
@@ -59,15 +60,17 @@ int launch_index_sample(const void* q_idx, const void* k_idx, const void* w, int
 int launch_index_emit(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
                       const int32_t* seg, int B, int S, int Hi, int Di, cudaStream_t stream,
                       int fp8, const float* k_scale, const float* thr, int* cnt, int32_t* above,
-                      int k, int2* win, int cw);
-// per row: (U, L) from the sample (rows with t < k: none needed, NaN)
+                      float* above_vals, int k, int2* win, int cw);
+// per row: (U, L) from the sample (rows with t < k: every valid key selected, -inf)
 int launch_stream_window(const float* sample, const int32_t* seg, int B, int S, int G, int k,
                          float* thr, cudaStream_t stream);
 // per row: the selection from the above / window lists into idx (in place) and count; a
 // row the lists cannot settle sets flags[t / block_rows] = 1 and writes nothing
+// vals (k <= 2048): the selected scores by slot; the emit pass wrote those of the keys
+// >= U beside their list entries (above_vals)
 int launch_stream_finish(const int32_t* seg, int B, int S, int k, const int* cnt,
-                         const int2* win, int cw, int32_t* idx, int32_t* count, int* flags,
-                         int block_rows, cudaStream_t stream);
+                         const int2* win, int cw, int32_t* idx, int32_t* count, float* vals,
+                         int* flags, int block_rows, cudaStream_t stream);
 
 // path: kFwdPathAuto (the cheaper of the gathered-key and dense-tile kernels) or
 // kFwdPathDense (the dense-tile kernel, DSA_ERR_UNSUPPORTED where it does not apply)

@@ -368,7 +368,8 @@ __global__ void __launch_bounds__(kFwdThreads, 1) loss_fwd_kernel(const LossFwdP
       const int t = static_cast<int>(row % p.S);
       const int par = ri & 1;
       const int32_t* irow = p.idx + row * p.k;
-      const float* srow = p.scores + row * p.ld;
+      // the row's scores by key (ld > 0), or the selected keys' scores by slot (ld == 0)
+      const float* srow = p.scores + row * (p.ld > 0 ? p.ld : p.k);
       // the row's LSE (log2 units) and the log-sum-exp of its selected index scores:
       // the 256 epilogue threads read slots j = e + 256 u (sixteen loads in flight per
       // thread) and keep the scores of the first kFwdKeepChunks chunks in sv[par]
@@ -395,7 +396,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) loss_fwd_kernel(const LossFwdP
           } else if (s > t) {
             sk[u] = -1;
           }
-          vv[u] = sk[u] >= 0 ? __ldg(srow + sk[u]) * kLog2e : 0.f;
+          vv[u] = sk[u] >= 0 ? __ldg(srow + (p.ld > 0 ? sk[u] : j0 + u * 256)) * kLog2e : 0.f;
         }
 #pragma unroll
         for (int u = 0; u < 16; ++u) {
@@ -510,7 +511,7 @@ __global__ void __launch_bounds__(kFwdThreads, 1) loss_fwd_kernel(const LossFwdP
         } else {
           const int s = slot_key(irow, j, kend, t, p.S);
           valid = s >= 0;
-          if (valid) v2 = __ldg(srow + s) * kLog2e;
+          if (valid) v2 = __ldg(srow + (p.ld > 0 ? s : j)) * kLog2e;
         }
         if (j < p.k) {
           float d = 0.f;

@@ -62,14 +62,16 @@ __global__ void __launch_bounds__(kSimtThreads) loss_fwd_simt_kernel(const SimtL
   const long long b = row / p.S;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int32_t* irow = p.idx + row * p.k;
-  const float* srow = p.scores + row * p.ld;
+  // the row's scores by key (ld > 0), or the selected keys' scores by slot (ld == 0)
+  const float* srow = p.scores + row * (p.ld > 0 ? p.ld : p.k);
+  auto score = [&](int s, int j) { return p.ld > 0 ? srow[s] : srow[j]; };
   const int code = DSA_STAGE_LOSS | DSA_DEVERR_BAD_INDEX;
   // log-sum-exp of the selected scores (the student's normaliser)
   float m = -INFINITY, l = 0.f;
   for (int j = tid; j < p.k; j += kSimtThreads) {
     const int s = sel_key(irow, j, t, p.S, p.err, code);
     if (s < 0) continue;
-    const float v = srow[s];
+    const float v = score(s, j);
     if (v > m) {
       l = l * expf(m - v) + 1.f;
       m = v;
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(kSimtThreads) loss_fwd_simt_kernel(const SimtL
     e = warp_sum(e);
     if (lane == 0) {
       const float pbar = e / static_cast<float>(p.H);
-      const float lq = srow[s] - logz;
+      const float lq = score(s, j) - logz;
       p.dI[row * p.k + j] = p.grad_scale * (expf(lq) - pbar);
       if (pbar > 0.f) kl_acc += pbar * (logf(pbar) - lq);
     }

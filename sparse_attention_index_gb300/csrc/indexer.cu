@@ -80,6 +80,7 @@ struct IndexerParams {
   const float* thr;       // [B * S, 2]: U, L (NaN: none)
   int* cnt;               // [B * S, 4]: keys >= U, keys in [L, U), valid keys (with seg)
   int32_t* above;         // [B * S, k]
+  float* above_vals;      // null, or [B * S, k]: the scores beside the `above` entries
   int2* win;              // [B * S, cw]: (key index, score bits)
   int k, cw;
 };
@@ -134,7 +135,10 @@ __device__ __forceinline__ void emit_keys(const IndexerParams& p, long long row,
     if (lane == 0) base = atomicAdd(cnt, __popc(bal));
     base = __shfl_sync(0xffffffffu, base, 0);
     const int pos = base + __popc(bal & lt);
-    if (above && pos < p.k) p.above[row * p.k + pos] = s;
+    if (above && pos < p.k) {
+      p.above[row * p.k + pos] = s;
+      if (p.above_vals) p.above_vals[row * p.k + pos] = val;
+    }
   }
   bal = __ballot_sync(0xffffffffu, win);
   if (bal) {
@@ -671,12 +675,13 @@ int launch_index_sample(const void* q_idx, const void* k_idx, const void* w, int
 int launch_index_emit(const void* q_idx, const void* k_idx, const void* w, int w_is_bf16,
                       const int32_t* seg, int B, int S, int Hi, int Di, cudaStream_t stream,
                       int fp8, const float* k_scale, const float* thr, int* cnt, int32_t* above,
-                      int k, int2* win, int cw) {
+                      float* above_vals, int k, int2* win, int cw) {
   IndexerParams e = no_extra();
   e.mode = kModeEmit;
   e.thr = thr;
   e.cnt = cnt;
   e.above = above;
+  e.above_vals = above_vals;
   e.k = k;
   e.win = win;
   e.cw = cw;

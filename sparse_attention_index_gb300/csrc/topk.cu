@@ -16,6 +16,11 @@
 // list (a generic radix select over the row when the window misses). Longer rows
 // (topk_long_kernel, one persistent 1024-thread CTA per SM) run the same selection with
 // passes over the row in L2.
+//
+// Optionally each slot's score goes out too (vals, -inf at slots without a key): it is
+// read back from the row while the row is still in L2, right after its selection, so
+// that a consumer of the selected scores (the indexer loss) reads k contiguous floats
+// per row instead of gathering them from the whole score row.
 
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
@@ -32,6 +37,7 @@ struct TopkParams {
   int B, S, k;
   int32_t* idx;
   int32_t* count;
+  float* vals;           // non-null: [B, S, k] scores of the selected keys, -inf past them
   int t_lo, t_hi;        // the query rows of this launch (all of them, or one block)
   long long rows_blk;    // rows per batch of the score buffer: row t is its row t - t_lo
   const int* gate;       // non-null: the launch does nothing unless *gate != 0
@@ -247,9 +253,11 @@ __device__ __forceinline__ uint32_t gather_word(uint32_t nib, int lane) {
 
 // the keys > T (gtw) and the lowest-index `need` keys == T (eqw), `total` keys in all,
 // into out[0, total) in ascending key index, and -1 into out[total, kmax); each thread
-// owns words 2 * tid and 2 * tid + 1
+// owns words 2 * tid and 2 * tid + 1. With VALS, each slot's score from srow into vals as
+// well (-inf past total).
+template <bool VALS>
 __device__ __forceinline__ void emit(int nwords, int need, int total, int32_t* out, int kmax,
-                                     Smem* sm) {
+                                     Smem* sm, const float* srow, float* vals) {
   const int tid = threadIdx.x;
   uint32_t g[kWpt], q[kWpt];
   int cg = 0, ce = 0;
@@ -282,15 +290,31 @@ __device__ __forceinline__ void emit(int nwords, int need, int total, int32_t* o
     while (sel) {
       const int bpos = __ffs(sel) - 1;
       sel &= sel - 1u;
-      if (pos < kmax) ost[pos] = (kWpt * tid + i) * 32 + bpos;
+      const int key = (kWpt * tid + i) * 32 + bpos;
+      if (pos < kmax) {
+        ost[pos] = key;
+        if (VALS && ost == out) vals[pos] = __ldg(srow + key);
+      }
       ++pos;
     }
   }
   if (ost != out) {
     __syncthreads();
-    for (int j = tid; j < kmax; j += NT) out[j] = j < total ? ost[j] : -1;
+    if (VALS) {
+#pragma unroll 4
+      for (int j = tid; j < kmax; j += NT) {
+        const int key = j < total ? ost[j] : -1;
+        out[j] = key;
+        vals[j] = key >= 0 ? __ldg(srow + key) : -INFINITY;
+      }
+    } else {
+      for (int j = tid; j < kmax; j += NT) out[j] = j < total ? ost[j] : -1;
+    }
   } else {
-    for (int j = total + tid; j < kmax; j += NT) out[j] = -1;
+    for (int j = total + tid; j < kmax; j += NT) {
+      out[j] = -1;
+      if (VALS) vals[j] = -INFINITY;
+    }
   }
 }
 
@@ -473,6 +497,7 @@ __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
   const Row rk{score_row(p, b, t), seg_row, len, seg_t,
                (reinterpret_cast<uintptr_t>(seg_row) & 15u) == 0};
   int32_t* out = p.idx + row * p.k;
+  float* vout = p.vals ? p.vals + row * p.k : nullptr;
 
   // number of valid keys
   int n = len;
@@ -487,7 +512,10 @@ __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
   if (n <= p.k) {
     // every valid key is selected, in ascending order
     if (!seg_row) {
-      for (int j = tid; j < p.k; j += NT) out[j] = j < len ? j : -1;
+      for (int j = tid; j < p.k; j += NT) {
+        out[j] = j < len ? j : -1;
+        if (vout) vout[j] = j < len ? __ldg(rk.srow + j) : -INFINITY;
+      }
     } else {
       for (int c0 = 0; c0 < nq; c0 += NT) {
         const int c = c0 + tid;
@@ -498,7 +526,10 @@ __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
         }
       }
       __syncthreads();
-      emit(nwords, 0, n, out, p.k, sm);
+      if (vout)
+        emit<true>(nwords, 0, n, out, p.k, sm, rk.srow, vout);
+      else
+        emit<false>(nwords, 0, n, out, p.k, sm, rk.srow, vout);
     }
     if (p.count && tid == 0) p.count[row] = n;
     return;
@@ -687,7 +718,10 @@ __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
     }
     __syncthreads();
   }
-  emit(nwords, need, p.k, out, p.k, sm);
+  if (vout)
+    emit<true>(nwords, need, p.k, out, p.k, sm, rk.srow, vout);
+  else
+    emit<false>(nwords, need, p.k, out, p.k, sm, rk.srow, vout);
   if (p.count && tid == 0) p.count[row] = p.k;
 }
 
@@ -721,10 +755,12 @@ struct WinSmem {
 
 struct FinSmem {
   uint32_t hist[2048];       // level histograms, then the output row
-  uint32_t gtw[kWords];      // keys above T
+  uint32_t gtw[kWords];      // keys above T (with vals: then the selected keys of each word)
   uint32_t eqw[kWords];      // keys equal to T
   uint32_t ckey[kCw];        // window keys: order key
   int32_t cidx[kCw];         //   and index
+  int wbase[kWords];         // with vals: the first slot of each word's selected keys
+  float vst[2048];           // with vals: the row's selected scores by slot
   int warp_tot[NW];
   int bcast[4];
   uint32_t ubc[8];
@@ -738,10 +774,10 @@ __global__ void __launch_bounds__(NT) stream_window_kernel(const float* sample, 
   const long long row = blockIdx.x;
   const int t = static_cast<int>(row % S);
   const int tid = threadIdx.x, lane = tid & 31;
-  if (t + 1 <= k) {   // at most k valid keys: all of them are selected
+  if (t + 1 <= k) {   // at most k valid keys: all of them are selected (U = L = -inf)
     if (tid == 0) {
-      thr[2 * row] = __int_as_float(0x7fc00000);
-      thr[2 * row + 1] = __int_as_float(0x7fc00000);
+      thr[2 * row] = -INFINITY;
+      thr[2 * row + 1] = -INFINITY;
     }
     return;
   }
@@ -816,9 +852,12 @@ __global__ void __launch_bounds__(NT) stream_window_kernel(const float* sample, 
 
 // the keys > T (gtw) and the lowest-index `need` keys == T (eqw), `total` in all, into
 // out[0, total) ascending and -1 into out[total, kmax); each thread owns a contiguous run
-// of `per` bitmap words
+// of `per` bitmap words. With vals (kmax <= 2048) each slot's score as well: the keys
+// >= U have theirs beside the unordered list in out[0, A) / vals[0, A) (the emit pass
+// wrote them there), the window keys in wrow[0, W); each goes to its key's slot.
 __device__ __forceinline__ void emit_words(int nwords, int need, int total, int32_t* out,
-                                           int kmax, FinSmem* sm) {
+                                           int kmax, FinSmem* sm, float* vals, int A,
+                                           const int2* wrow, int W) {
   const int tid = threadIdx.x;
   const int per = (nwords + NT - 1) / NT;
   const int w0 = min(tid * per, nwords), w1 = min(w0 + per, nwords);
@@ -843,6 +882,10 @@ __device__ __forceinline__ void emit_words(int nwords, int need, int total, int3
     }
     eb += __popc(q);
     uint32_t sel = sm->gtw[w] | qk;
+    if (vals) {   // only this thread reads its words from here on
+      sm->wbase[w] = pos;
+      sm->gtw[w] = sel;
+    }
     while (sel) {
       const int bpos = __ffs(sel) - 1;
       sel &= sel - 1u;
@@ -852,8 +895,28 @@ __device__ __forceinline__ void emit_words(int nwords, int need, int total, int3
   }
   if (ost != out) {
     __syncthreads();
-    for (int j = tid; j < kmax; j += NT) out[j] = j < total ? ost[j] : -1;
-  } else {
+    if (vals) {
+      // a selected key's slot: its word's first slot plus the selected keys below it
+      auto slot = [&](int key) {
+        const uint32_t m = sm->gtw[key >> 5], bit = 1u << (key & 31);
+        return (m & bit) ? sm->wbase[key >> 5] + __popc(m & (bit - 1u)) : -1;
+      };
+      for (int j = tid; j < A; j += NT) {
+        const int q = slot(out[j]);
+        if (q >= 0 && q < kmax) sm->vst[q] = vals[j];
+      }
+      for (int j = tid; j < W; j += NT) {
+        const int2 e = wrow[j];
+        const int q = slot(e.x);
+        if (q >= 0 && q < kmax) sm->vst[q] = __int_as_float(e.y);
+      }
+      __syncthreads();   // every old entry of out / vals is read before they are rewritten
+    }
+    for (int j = tid; j < kmax; j += NT) {
+      out[j] = j < total ? ost[j] : -1;
+      if (vals) vals[j] = j < total ? sm->vst[j] : -INFINITY;
+    }
+  } else {   // (kmax > 2048: never with vals)
     for (int j = total + tid; j < kmax; j += NT) out[j] = -1;
   }
 }
@@ -861,7 +924,7 @@ __device__ __forceinline__ void emit_words(int nwords, int need, int total, int3
 // one CTA per row, longest rows first
 __global__ void __launch_bounds__(NT) stream_finish_kernel(const int32_t* seg, int B, int S, int k,
                                                            const int* cnt, const int2* win, int cw,
-                                                           int32_t* idx, int32_t* count,
+                                                           int32_t* idx, int32_t* count, float* vals,
                                                            int* flags, int block_rows) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   FinSmem* sm = reinterpret_cast<FinSmem*>(smem_raw);
@@ -873,25 +936,14 @@ __global__ void __launch_bounds__(NT) stream_finish_kernel(const int32_t* seg, i
   const int32_t* seg_row = seg ? seg + static_cast<long long>(b) * S : nullptr;
   const int seg_t = seg_row ? seg_row[t] : 0;
   int32_t* out = idx + row * k;
+  float* vout = vals ? vals + row * k : nullptr;
+  (void)seg_t;
   for (int w = tid; w < nwords; w += NT) {
     sm->gtw[w] = 0u;
     sm->eqw[w] = 0u;
   }
   __syncthreads();
-  if (len <= k) {
-    // every valid key is selected
-    int n = 0;
-    for (int s = tid; s < len; s += NT)
-      if (!seg_row || __ldg(seg_row + s) == seg_t) {
-        atomicOr(&sm->gtw[s >> 5], 1u << (s & 31));
-        ++n;
-      }
-    int tot;
-    sr::block_scan(n, tot, sm);
-    emit_words(nwords, 0, tot, out, k, sm);
-    if (count && tid == 0) count[row] = tot;
-    return;
-  }
+  // (rows of at most k keys have U = -inf: their every valid key is in the list >= U)
   const int A = cnt[4 * row], W = cnt[4 * row + 1];
   const int n = seg_row ? cnt[4 * row + 2] : len;
   const int m = n < k ? n : k;   // keys to select
@@ -934,7 +986,7 @@ __global__ void __launch_bounds__(NT) stream_finish_kernel(const int32_t* seg, i
     }
     __syncthreads();
   }
-  emit_words(nwords, need, m, out, k, sm);
+  emit_words(nwords, need, m, out, k, sm, vout, A, win + row * cw, W);
   if (count && tid == 0) count[row] = m;
 }
 
@@ -1568,20 +1620,32 @@ __global__ void __launch_bounds__(lr::NT, 1) topk_long_kernel(const TopkParams p
     }
     const lr::RowKeys rk{score_row(p, b, t), seg_row, t + 1, seg_t};
     lr::select_row(rk, t, n, p, p.idx + row * p.k, row, sm);
+    if (p.vals) {
+      // the row's slots are written (by every thread, in whichever path selected them):
+      // their scores, while the row is in L2
+      __syncthreads();
+      const int32_t* o = p.idx + row * p.k;
+      float* v = p.vals + row * p.k;
+      for (int j = tid; j < p.k; j += lr::NT) {
+        const int s = __ldcg(o + j);
+        v[j] = s >= 0 ? __ldg(rk.srow + s) : -INFINITY;
+      }
+    }
   }
 }
 }  // namespace
 
 int launch_topk(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
-                int32_t* idx, int32_t* count, cudaStream_t stream) {
-  return launch_topk_rows(scores, ld, seg, B, S, k, idx, count, stream, 0, S, S);
+                int32_t* idx, int32_t* count, float* vals, cudaStream_t stream) {
+  return launch_topk_rows(scores, ld, seg, B, S, k, idx, count, vals, stream, 0, S, S);
 }
 
 int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B, int S, int k,
-                     int32_t* idx, int32_t* count, cudaStream_t stream, int t_lo, int t_hi,
-                     long long rows_blk, const int* gate) {
+                     int32_t* idx, int32_t* count, float* vals, cudaStream_t stream, int t_lo,
+                     int t_hi, long long rows_blk, const int* gate) {
   TopkParams p;
   p.gate = gate;
+  p.vals = vals;
   p.scores = scores;
   p.ld = ld;
   p.seg = seg;
@@ -1635,9 +1699,10 @@ int launch_stream_window(const float* sample, const int32_t* seg, int B, int S, 
 }
 
 int launch_stream_finish(const int32_t* seg, int B, int S, int k, const int* cnt,
-                         const int2* win, int cw, int32_t* idx, int32_t* count, int* flags,
-                         int block_rows, cudaStream_t stream) {
+                         const int2* win, int cw, int32_t* idx, int32_t* count, float* vals,
+                         int* flags, int block_rows, cudaStream_t stream) {
   if (S > st::kMaxS || cw > st::kCw) return DSA_ERR_UNSUPPORTED;
+  if (vals && k > 2048) return DSA_ERR_UNSUPPORTED;   // the scores are staged by slot
   const long long rows = static_cast<long long>(B) * S;
   if (rows > 0x7fffffffLL) return DSA_ERR_UNSUPPORTED;
   const size_t smem = sizeof(st::FinSmem);
@@ -1645,7 +1710,7 @@ int launch_stream_finish(const int32_t* seg, int B, int S, int k, const int* cnt
                            static_cast<int>(smem)) != cudaSuccess)
     return DSA_ERR_CUDA;
   st::stream_finish_kernel<<<static_cast<unsigned>(rows), st::NT, smem, stream>>>(
-      seg, B, S, k, cnt, win, cw, idx, count, flags, block_rows);
+      seg, B, S, k, cnt, win, cw, idx, count, vals, flags, block_rows);
   return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

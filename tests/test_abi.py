@@ -85,10 +85,12 @@ def test_index_scores_validation(dsa):
 
 def test_topk_validation(dsa):
     f = dsa.lib.dsa_topk
-    assert f(None, 128, None, 1, 128, 4, P, None, None, 0, None) == 1
-    assert f(P, 127, None, 1, 128, 4, P, None, None, 0, None) == 1
-    assert f(P, 128, None, 1, 128, 0, P, None, None, 0, None) == 1
-    assert f(P, 128, MIS, 1, 128, 4, P, None, None, 0, None) == 1
+    # scores, ld, seg, B, S, k, idx, count, vals, ws, ws_bytes, stream
+    assert f(None, 128, None, 1, 128, 4, P, None, None, None, 0, None) == 1
+    assert f(P, 127, None, 1, 128, 4, P, None, None, None, 0, None) == 1
+    assert f(P, 128, None, 1, 128, 0, P, None, None, None, 0, None) == 1
+    assert f(P, 128, MIS, 1, 128, 4, P, None, None, None, 0, None) == 1
+    assert f(P, 128, None, 1, 128, 4, P, None, MIS, None, 0, None) == 1        # vals misaligned
 
 
 def test_attention_validation(dsa):
@@ -137,13 +139,16 @@ def test_index_topk_validation(dsa):
     assert dsa.lib.dsa_index_topk_workspace_size(0, 128, 256) == 0
     f = dsa.lib.dsa_index_topk
     need = dsa.lib.dsa_index_topk_workspace_size(1, 1024, 256)
-    # q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di, k, block_rows, idx, count, ws, ws_bytes, stream
-    assert f(None, P, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need, None) == 1   # null q_idx
-    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 100, P, P, P, need, None) == 1     # block % 256
-    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 0, 256, P, P, P, need, None) == 1     # k = 0
-    assert f(P, P, P, 1, None, 1, 1024, 48, 128, 8, 256, P, P, P, need, None) == 2     # Hi not 2^n
-    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need - 16, None) == 3  # small ws
-    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, None, need, None) == 3   # no ws
+    # q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di, k, block_rows, idx, count, vals, ws,
+    # ws_bytes, stream
+    A = (1, None, 1, 1024, 64, 128, 8, 256, P, P)
+    assert f(None, P, P, *A, None, P, need, None) == 1                                # null q_idx
+    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 8, 100, P, P, None, P, need, None) == 1  # block
+    assert f(P, P, P, 1, None, 1, 1024, 64, 128, 0, 256, P, P, None, P, need, None) == 1  # k = 0
+    assert f(P, P, P, 1, None, 1, 1024, 48, 128, 8, 256, P, P, None, P, need, None) == 2  # Hi
+    assert f(P, P, P, *A, MIS, P, need, None) == 1                                    # vals
+    assert f(P, P, P, *A, None, P, need - 16, None) == 3                              # small ws
+    assert f(P, P, P, *A, None, None, need, None) == 3                                # no ws
 
 
 def test_index_topk_fp8_validation(dsa):
@@ -151,12 +156,39 @@ def test_index_topk_fp8_validation(dsa):
     misaligned key scale and an index head dim that is not a multiple of 16."""
     f = dsa.lib.dsa_index_topk_fp8
     need = dsa.lib.dsa_index_topk_workspace_size(1, 1024, 256)
-    # q_idx, k_idx, k_scale, w, w_dtype, seg, B, S, Hi, Di, k, block_rows, idx, count, ws,
-    # ws_bytes, stream
-    assert f(None, P, None, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need, None) == 1
+    # q_idx, k_idx, k_scale, w, w_dtype, seg, B, S, Hi, Di, k, block_rows, idx, count, vals,
+    # ws, ws_bytes, stream
+    assert f(None, P, None, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, None, P, need, None) == 1
     odd = ctypes.c_void_p((1 << 20) + 4)   # k_scale not on a 16-byte boundary
-    assert f(P, P, odd, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need, None) == 1
-    assert f(P, P, None, P, 1, None, 1, 1024, 64, 40, 8, 256, P, P, P, need, None) == 1
-    assert f(P, P, None, P, 1, None, 1, 1024, 64, 128, 8, 100, P, P, P, need, None) == 1
-    assert f(P, P, None, P, 1, None, 1, 1024, 48, 128, 8, 256, P, P, P, need, None) == 2
-    assert f(P, P, None, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, P, need - 16, None) == 3
+    assert f(P, P, odd, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, None, P, need, None) == 1
+    assert f(P, P, None, P, 1, None, 1, 1024, 64, 40, 8, 256, P, P, None, P, need, None) == 1
+    assert f(P, P, None, P, 1, None, 1, 1024, 64, 128, 8, 100, P, P, None, P, need, None) == 1
+    assert f(P, P, None, P, 1, None, 1, 1024, 48, 128, 8, 256, P, P, None, P, need, None) == 2
+    assert f(P, P, None, P, 1, None, 1, 1024, 64, 128, 8, 256, P, P, None, P, need - 16,
+             None) == 3
+
+
+def test_index_topk_stream_validation(dsa):
+    """The streaming form refuses bad arguments before any launch: its selected scores
+    (vals) are staged by slot, so they need k <= 2048."""
+    f = dsa.lib.dsa_index_topk_stream
+    need = dsa.lib.dsa_index_topk_stream_workspace_size(1, 8192, 1024)
+    assert need > 0
+    # q_idx, k_idx, w, w_dtype, seg, B, S, Hi, Di, k, block_rows, idx, count, vals, ws,
+    # ws_bytes, stream
+    assert f(P, P, P, 1, None, 1, 8192, 64, 128, 4096, 1024, P, P, P, P, need, None) == 2
+    assert f(P, P, P, 1, None, 1, 8192, 64, 128, 2048, 1024, P, P, MIS, P, need, None) == 1
+    assert f(P, P, P, 1, None, 1, 200000, 64, 128, 2048, 1024, P, P, None, P, need, None) == 2
+    assert f(P, P, P, 1, None, 1, 8192, 64, 128, 2048, 1024, P, P, P, P, need - 16, None) == 3
+    assert dsa.lib.dsa_index_topk_stream_fp8(P, P, None, P, 1, None, 1, 8192, 64, 128, 4096,
+                                             1024, P, P, P, P, need, None) == 2
+
+
+def test_indexer_loss_validation(dsa):
+    """The loss reads the scores by key (ld_scores >= S) or the top-k's selected scores by
+    slot (ld_scores = 0); other strides are refused before any launch."""
+    f = dsa.lib.dsa_indexer_loss
+    # Q, K, idx, lse, scores, ld, B, S, H, Hkv, Dqk, k, scale, grad_scale, kl, dI, stream
+    assert f(P, P, P, P, P, -4, 1, 128, 16, 1, 128, 8, 0.1, 1.0, P, P, None) == 1
+    assert f(P, P, P, P, P, 64, 1, 128, 16, 1, 128, 8, 0.1, 1.0, P, P, None) == 1
+    assert f(P, P, P, P, None, 0, 1, 128, 16, 1, 128, 8, 0.1, 1.0, P, P, None) == 1
