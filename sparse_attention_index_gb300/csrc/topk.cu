@@ -328,16 +328,18 @@ __device__ __forceinline__ float key_to_float(uint32_t key) {
 }
 
 // Remaining digits of T below the known bits `mask` (prefix) over the keys visit(fn)
-// presents, in levels of up to 11 bits from bit hb down: per level a histogram of the
-// keys still in play, the bin of the need-th largest, and an early stop when that
-// bin holds exactly the keys needed or every key in play has the same lower bits.
+// presents, in levels of up to max_bits (<= 11) bits from bit hb down: per level a
+// histogram of the keys still in play, the bin of the need-th largest, and an early stop
+// when that bin holds exactly the keys needed or every key in play has the same lower
+// bits. A few hundred listed keys take 8-bit levels (one bin per thread to clear and
+// scan); a whole row takes 11-bit ones.
 template <class Visit, class SM>
 __device__ __forceinline__ void resolve(Visit visit, int hb, uint32_t& prefix, uint32_t& mask,
-                                        int& need, int cur, SM* sm) {
+                                        int& need, int cur, SM* sm, int max_bits = 11) {
   const int tid = threadIdx.x, lane = tid & 31;
 #pragma unroll 1
   while (hb >= 0 && cur != need) {
-    const int nbits = hb + 1 < 11 ? hb + 1 : 11;
+    const int nbits = hb + 1 < max_bits ? hb + 1 : max_bits;
     const int shift = hb + 1 - nbits, nb = 1 << nbits;
     const uint32_t low = (1u << shift) - 1u;
     for (int i = tid; i < nb; i += NT) sm->hist[i] = 0u;
@@ -678,7 +680,7 @@ __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
       prefix = L & mask;
       resolve([&](auto fn) {
         for (int j = tid; j < ncand; j += NT) fn(sm->ckey[j]);
-      }, hb, prefix, mask, need, ncand, sm);
+      }, hb, prefix, mask, need, ncand, sm, 8);
       // list keys above T / equal to T into the bitmaps
       for (int j = tid; j < ncand; j += NT) {
         const uint32_t km = sm->ckey[j] & mask;
@@ -977,7 +979,7 @@ __global__ void __launch_bounds__(NT) stream_finish_kernel(const int32_t* seg, i
     uint32_t prefix = 0u, mask = 0u;
     sr::resolve([&](auto fn) {
       for (int j = tid; j < W; j += NT) fn(sm->ckey[j]);
-    }, 31, prefix, mask, need, W, sm);
+    }, 31, prefix, mask, need, W, sm, 8);
     for (int j = tid; j < W; j += NT) {
       const uint32_t km = sm->ckey[j] & mask;
       const int s = sm->cidx[j];
