@@ -640,7 +640,9 @@ __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
   cnt_above = __reduce_add_sync(0xffffffffu, cnt_above);
   if (lane == 0) atomicAdd(&sm->ubc[7], static_cast<uint32_t>(cnt_above));
   __syncthreads();   // gtw, cw and the count are complete
-  // the window keys, from their bitmap, into the list in ascending index (keys re-read)
+  // the window keys, from their bitmap, into the list in ascending index: the indices
+  // first, then their order keys from scores the sweep left in L2, read by every thread
+  // in turn so that the loads overlap instead of following each thread's bits
   uint32_t cwv[kWpt];
   int cc = 0;
 #pragma unroll
@@ -659,12 +661,12 @@ __global__ void __launch_bounds__(NT, 6) topk_short_kernel(const TopkParams p) {
       while (m) {
         const int bpos = __ffs(m) - 1;
         m &= m - 1u;
-        const int sidx = (kWpt * tid + i) * 32 + bpos;
-        sm->ckey[slot] = order_key(__ldg(rk.srow + sidx));
-        sm->cidx[slot] = static_cast<uint16_t>(sidx);
-        ++slot;
+        sm->cidx[slot++] = static_cast<uint16_t>((kWpt * tid + i) * 32 + bpos);
       }
     }
+    __syncthreads();
+#pragma unroll 4
+    for (int j = tid; j < ncand; j += NT) sm->ckey[j] = order_key(__ldg(rk.srow + sm->cidx[j]));
   }
   __syncthreads();
 
