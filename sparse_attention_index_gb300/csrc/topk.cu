@@ -997,22 +997,22 @@ __global__ void __launch_bounds__(NT) stream_finish_kernel(const int32_t* seg, i
 }  // namespace st
 
 // ------------------------------------------------------------------ long rows
-// Rows longer than the shared stage (t >= kStageMax): one persistent CTA of 1024
-// threads per SM, so that the rows in flight (152 x at most 512 KB at S = 131072)
-// stay in L2 between passes. Every pass reads the row from global memory in
-// 16-byte groups of four keys: the first from DRAM (first-level histogram), the
-// following ones from L2. The selection is the same as for staged rows: a window
+// Rows longer than the shared stage (t >= kStageMax): two persistent CTAs of 512
+// threads per SM, each on its own row, so that one row's barrier-bound phases (the
+// sample, the bins, the list and the emission) overlap the other's pass over its
+// keys; each row is prefetched whole into L2 (304 rows in flight, at most 512 KB
+// each at S = 131072). Every pass reads the row from global memory in 16-byte
+// groups of four keys. The selection is the same as for staged rows: a window
 // histogram, then either a candidate list with bitmaps (rows of at most
 // kLongWords * 32 keys and at most kLongCand keys in the threshold bin) or further
 // levels over the row with an ordered sweep.
 namespace lr {
 
-constexpr int NT = 1024;
+constexpr int NT = 512;
 constexpr int NW = NT / 32;
 constexpr int kLongWords = 4096;   // bitmap words: rows up to 131072 keys
-// candidates of the one-pass path: each warp appends to its own segment of 256; at
-// S = 131072 a row leaves about 3.3K candidates, ~105 per warp, and segments of 128
-// overflowed on about half of the rows beyond t = 90K
+// candidates of the one-pass path: each warp appends to its own segment of 512; at
+// S = 131072 the 2048-key sample leaves a row about 4K candidates, ~250 per warp
 constexpr int kLongCand = 8192;
 constexpr int kWpt = kLongWords / NT;   // bitmap words per thread
 
@@ -1081,16 +1081,17 @@ __device__ __forceinline__ int block_scan(int v, int& total, Smem* sm) {
   return x + before;
 }
 
-// the bin of the need-th largest key among nb bins (nb <= 2 * NT), keys above it
+// the bin of the need-th largest key among nb bins (nb <= 2048), keys above it
 // and in it
 __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need, Smem* sm,
                                          int& bin, int& above, int& in_bin) {
   const int per = nb > NT ? nb / NT : 1;
   const int tid = threadIdx.x;
-  int c[2];
+  constexpr int kPer = (2048 + NT - 1) / NT;
+  int c[kPer];
   int sum = 0;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kPer; ++i) {
     const int j = tid * per + i;
     c[i] = i < per && j < nb ? static_cast<int>(hist[nb - 1 - j]) : 0;
     sum += c[i];
@@ -1099,7 +1100,7 @@ __device__ __forceinline__ void find_bin(const uint32_t* hist, int nb, int need,
   const int incl = block_scan(sum, tot, sm);
   int run = incl - sum;
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
+  for (int i = 0; i < kPer; ++i) {
     if (i < per && run < need && run + c[i] >= need) {
       sm->bcast[0] = nb - 1 - (tid * per + i);
       sm->bcast[1] = run;
@@ -1468,7 +1469,7 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
   }
   for (int i = tid; i < 2048; i += NT) sm->hist[i] = 0u;
   if (tid < 4) sm->ubc[tid] = 0u;
-  // the first group of each thread (the row's first 4096 keys) places the window
+  // the first group of each thread (the row's first 4 * NT keys) places the window
   const uint4 first = tid < nq ? rk.load4(tid) : make_uint4(0u, 0u, 0u, 0u);
   {
     const uint32_t fk[4] = {first.x, first.y, first.z, first.w};
@@ -1601,8 +1602,8 @@ __device__ __forceinline__ void select_row(const RowKeys& rk, int t, int n, cons
 
 }  // namespace lr
 
-// rows t0 <= t < t_hi of every batch row; persistent, longest rows first
-__global__ void __launch_bounds__(lr::NT, 1) topk_long_kernel(const TopkParams p, int t0) {
+// rows t0 <= t < t_hi of every batch row; persistent, longest rows first, two CTAs per SM
+__global__ void __launch_bounds__(lr::NT, 2) topk_long_kernel(const TopkParams p, int t0) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   if (gated_off(p)) return;
   lr::Smem* sm = reinterpret_cast<lr::Smem*>(smem_raw);
@@ -1623,6 +1624,19 @@ __global__ void __launch_bounds__(lr::NT, 1) topk_long_kernel(const TopkParams p
       n = tot;
     }
     const lr::RowKeys rk{score_row(p, b, t), seg_row, t + 1, seg_t};
+    {
+      // the whole row into L2 ahead of its passes (16 KB per bulk prefetch, one per
+      // thread): the sample's round trip and the later passes then overlap its transfer
+      const long long bytes = static_cast<long long>((t + 4) >> 2) * 16;
+      const long long c0 = static_cast<long long>(tid) * 16384;
+      if (c0 < bytes) {
+        const long long sz = bytes - c0 < 16384 ? bytes - c0 : 16384;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                         reinterpret_cast<const char*>(rk.srow) + c0),
+                     "r"(static_cast<uint32_t>(sz))
+                     : "memory");
+      }
+    }
     lr::select_row(rk, t, n, p, p.idx + row * p.k, row, sm);
     if (p.vals) {
       // the row's slots are written (by every thread, in whichever path selected them):
@@ -1676,7 +1690,7 @@ int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B,
   }
   const int long_lo = t_lo > kStageMax ? t_lo : kStageMax;
   if (S > kStageMax && t_hi > long_lo) {
-    // longer rows: persistent CTAs, one per SM
+    // longer rows: persistent CTAs, two per SM
     const size_t lsmem = sizeof(lr::Smem);
     if (cudaFuncSetAttribute(topk_long_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(lsmem)) != cudaSuccess)
@@ -1685,7 +1699,7 @@ int launch_topk_rows(const float* scores, int64_t ld, const int32_t* seg, int B,
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const long long nlong = static_cast<long long>(B) * (t_hi - long_lo);
-    const int grid = static_cast<int>(nlong < sms ? nlong : sms);
+    const int grid = static_cast<int>(nlong < 2 * sms ? nlong : 2 * sms);
     topk_long_kernel<<<grid, lr::NT, lsmem, stream>>>(p, long_lo);
     if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
   }

@@ -279,6 +279,28 @@ def test_topk_long_rows_with_segments():
     assert [int(got[r]) for r in short] == [r - 19800 + 1 for r in short]
 
 
+def test_topk_long_rows_ties_two_pass():
+    """Long rows whose candidate list cannot settle them in one pass: a row of equal scores
+    (every key a candidate), a row with 4 distinct values (about 5000 keys tied at the
+    threshold), a row of +0 and -0 only, and a row with half its keys tied at 1.0 above
+    normal noise. The long-row kernel takes its two-pass path for these; neighbouring rows
+    of plain noise take the one-pass path in the same launch."""
+    dsa = _dsa()
+    S, k = 20000, 2048
+    rng = np.random.default_rng(21)
+    sc = rng.standard_normal((1, S, S), dtype=np.float32)
+    sc[0, 17000, :] = 0.25
+    sc[0, 18000, :] = rng.integers(0, 4, S).astype(np.float32)
+    sc[0, 19000, :] = np.where(rng.random(S) < 0.5, np.float32(0.0), np.float32(-0.0))
+    sc[0, 19999, :] = np.where(rng.random(S) < 0.5, np.float32(1.0),
+                               np.minimum(rng.standard_normal(S).astype(np.float32), 0.9))
+    idx, cnt = dsa.dsa_topk(dev(sc), k)
+    assert dsa.dsa_get_last_device_error() == 0
+    rows = np.array([16999, 17000, 17001, 18000, 19000, 19998, 19999], dtype=np.int64)
+    _check_topk(idx.cpu().numpy(), cnt.cpu().numpy(), sc[0][rows].astype(np.float64), None, S,
+                k, rows)
+
+
 def test_topk_golden_fixtures_on_gpu():
     from test_oracle_pins import _parse_golden
     dsa = _dsa()
