@@ -154,6 +154,56 @@ __device__ __forceinline__ void emit_keys(const IndexerParams& p, long long row,
   }
 }
 
+// Emit mode for the NQ queries of one epilogue warp and the 32 keys of its lanes (key s
+// of this lane), after a tile: every list of every query reserves its slots at once
+// (lane q for the keys >= U of query q, lane 8 + q for its window keys, lane 16 + q
+// for its valid keys when there are segment ids), then each lane writes its entries.
+// cnt[q][*] are the item's shared-memory counters of item query q0 + q. Warp-collective.
+template <int NQ>
+__device__ __forceinline__ void emit_tile(const IndexerParams& p, const float (&val)[NQ],
+                                          int (*cnt)[4], int q0, int b, int t0, int s,
+                                          int seg_s, int lane) {
+  static_assert(NQ <= 8, "one lane per query and list");
+  const uint32_t lt = (1u << lane) - 1u;
+  bool fa[NQ], fw[NQ];
+  uint32_t ba[NQ], bw[NQ];
+  uint32_t mine = 0u;
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const int t = t0 + q0 + q;
+    const bool in_t = t < p.t_end;   // the same for every lane of the warp
+    const long long row = static_cast<long long>(b) * p.S + t;
+    bool valid = false;
+    float U = INFINITY, L = INFINITY;
+    if (in_t) {
+      valid = s <= t && (p.seg == nullptr || seg_s == __ldg(p.seg + b * p.S + t));
+      U = __ldg(p.thr + 2 * row);
+      L = __ldg(p.thr + 2 * row + 1);
+    }
+    fa[q] = valid && val[q] >= U;
+    fw[q] = valid && val[q] >= L && !(val[q] >= U);
+    ba[q] = __ballot_sync(0xffffffffu, fa[q]);
+    bw[q] = __ballot_sync(0xffffffffu, fw[q]);
+    const uint32_t bv = p.seg != nullptr ? __ballot_sync(0xffffffffu, valid) : 0u;
+    if (lane == q) mine = ba[q];
+    if (lane == 8 + q) mine = bw[q];
+    if (lane == 16 + q) mine = bv;
+  }
+  int base = 0;
+  if (mine != 0u) base = atomicAdd(&cnt[q0 + (lane & 7)][lane >> 3], __popc(mine));
+#pragma unroll
+  for (int q = 0; q < NQ; ++q) {
+    const long long row = static_cast<long long>(b) * p.S + t0 + q0 + q;
+    const int pa = __shfl_sync(0xffffffffu, base, q) + __popc(ba[q] & lt);
+    const int pw = __shfl_sync(0xffffffffu, base, 8 + q) + __popc(bw[q] & lt);
+    if (fa[q] && pa < p.k) {
+      p.above[row * p.k + pa] = s;
+      if (p.above_vals) p.above_vals[row * p.k + pa] = val[q];
+    }
+    if (fw[q] && pw < p.cw) p.win[row * p.cw + pw] = make_int2(s, __float_as_int(val[q]));
+  }
+}
+
 // Drain wait used only at exit: ignores the abort flag, still bounded.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* err) {
   const uint32_t a = smem_u32(bar);
@@ -234,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // slot; the producer stores an item's counts and zeroes them once every epilogue warp has
   // released the slot (w_empty), before the slot's next item
   constexpr bool kSmemCnt = MODE == kModeEmit && kColsPerTile / HI <= kEmitSmemQueries;
+  constexpr int kEmitNqw = kSmemCnt ? 128 / HI : 1;   // queries of one epilogue warp's columns
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -412,6 +463,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         float2 acc2[QPC];
 #pragma unroll
         for (int i = 0; i < QPC; ++i) acc2[i] = make_float2(0.f, 0.f);
+        // emit mode with shared-memory counters: this warp's scores of the tile, one per
+        // query, listed together after the tile (one atomic instruction for every list)
+        float ev[kEmitNqw];
         auto chunk = [&](int ch, const uint32_t (&v)[32]) {
           const float* wrow = w_item + half * 128 + ch * 32;
 #pragma unroll
@@ -458,10 +512,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                   p.sample[(static_cast<long long>(b) * p.S + t) * kSampleKeys + m * kKeysPerTile +
                            quarter * 32 + lane] =
                       s <= t && same_doc ? val : __int_as_float(0x7fc00000);
+              } else if constexpr (kSmemCnt) {
+                (void)same_doc;
+                ev[(cq * 32) / HI + i] = val;
               } else if (in_t) {
                 const long long row = static_cast<long long>(b) * p.S + t;
-                int* c = kSmemCnt ? &tail->ecnt[ws][qi][0] : p.cnt + 4 * row;
-                emit_keys(p, row, c, s, val, s <= t && same_doc, lane);
+                emit_keys(p, row, p.cnt + 4 * row, s, val, s <= t && same_doc, lane);
               }
               acc2[i] = make_float2(0.f, 0.f);
             }
@@ -480,6 +536,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&tail->acc_empty[as]);
         if (++as == kAccBufs) { as = 0; a_par ^= 1u; }
+        if constexpr (kSmemCnt) emit_tile<kEmitNqw>(p, ev, tail->ecnt[ws], (half * 128) / HI, b,
+                                                    t0, s, seg_s, lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&tail->w_empty[ws]);
