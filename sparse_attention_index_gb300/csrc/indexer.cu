@@ -125,7 +125,8 @@ __device__ __forceinline__ int tile_at(int m, int nt, int nkb) {
 // warp; with segment ids the valid keys are counted too. Warp-collective.
 __device__ __forceinline__ void emit_keys(const IndexerParams& p, long long row, int* cnt, int s,
                                           float val, bool valid, int lane) {
-  const float U = __ldg(p.thr + 2 * row), L = __ldg(p.thr + 2 * row + 1);
+  const float2 ul = __ldg(reinterpret_cast<const float2*>(p.thr) + row);   // (U, L)
+  const float U = ul.x, L = ul.y;
   const bool above = valid && val >= U;
   const bool win = valid && val >= L && !(val >= U);
   const uint32_t lt = (1u << lane) - 1u;
@@ -177,8 +178,9 @@ __device__ __forceinline__ void emit_tile(const IndexerParams& p, const float (&
     float U = INFINITY, L = INFINITY;
     if (in_t) {
       valid = s <= t && (p.seg == nullptr || seg_s == __ldg(p.seg + b * p.S + t));
-      U = __ldg(p.thr + 2 * row);
-      L = __ldg(p.thr + 2 * row + 1);
+      const float2 ul = __ldg(reinterpret_cast<const float2*>(p.thr) + row);   // (U, L)
+      U = ul.x;
+      L = ul.y;
     }
     fa[q] = valid && val[q] >= U;
     fw[q] = valid && val[q] >= L && !(val[q] >= U);

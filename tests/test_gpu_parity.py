@@ -741,6 +741,10 @@ def test_index_topk_fp8_matches_oracle(case):
     (2, 2000, 16, 64, 100, 3, 512),    # packed documents: windows from an estimated count
     (1, 489, 64, 128, 512, 3, 256),    # every row has at most k keys
     (1, 4100, 4, 32, 64, 0, 1024),     # 64 queries per indexer tile
+    (1, 2300, 32, 32, 200, 0, 512),    # 4 queries per epilogue warp, listed per tile
+    (1, 1500, 128, 128, 100, 2, 512),  # one query per epilogue warp, packed documents
+    (1, 1800, 8, 64, 150, 0, 512),     # 32 queries per tile: list counters in global memory
+    (1, 1200, 1, 64, 50, 0, 256),      # one head: 256 queries per tile
 ])
 def test_index_topk_stream_matches_oracle(case):
     """The streaming form (sampled window, candidate lists, no score row) against the oracle's
