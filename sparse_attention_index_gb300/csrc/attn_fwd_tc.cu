@@ -465,23 +465,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
         const uint32_t vm0 = h.valid[0], vm1 = h.valid[1], vm2 = h.valid[2];
         const bool all_valid = (vm0 & vm1 & vm2) == 0xffffffffu;
         const uint32_t sbase = tmem + lane_off + L::kColS + sb * kNK;
-        uint32_t s0[32], s1[32], s2[32];
-        tmem_ld_x32(sbase, s0);
-        tmem_ld_x32(sbase + 32, s1);
-        tmem_ld_x32(sbase + 64, s2);
-        tmem_ld_wait();
+        // the chunk's maximum over its valid keys, 32 columns at a time; S is read from TMEM
+        // again for the exponentials, so that no 96 logits are held in registers (TMEM loads
+        // are cheap, and the kernel then fits its registers without spilling)
         float mx = -INFINITY;
-        if (all_valid) {
+#pragma unroll 1
+        for (int part = 0; part < 3; ++part) {
+          uint32_t sv[32];
+          tmem_ld_x32(sbase + part * 32, sv);
+          tmem_ld_wait();
+          const uint32_t vm = part == 0 ? vm0 : (part == 1 ? vm1 : vm2);
+          if (all_valid) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            mx = fmaxf(mx, fmaxf(__uint_as_float(s0[j]),
-                                 fmaxf(__uint_as_float(s1[j]), __uint_as_float(s2[j]))));
-        } else {
+            for (int j = 0; j < 32; ++j) mx = fmaxf(mx, __uint_as_float(sv[j]));
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if ((vm0 >> j) & 1u) mx = fmaxf(mx, __uint_as_float(s0[j]));
-            if ((vm1 >> j) & 1u) mx = fmaxf(mx, __uint_as_float(s1[j]));
-            if ((vm2 >> j) & 1u) mx = fmaxf(mx, __uint_as_float(s2[j]));
+            for (int j = 0; j < 32; ++j)
+              if ((vm >> j) & 1u) mx = fmaxf(mx, __uint_as_float(sv[j]));
           }
         }
         if (first) {
@@ -518,7 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_tc_kernel(const AttnPara
         float ls = 0.f;
 #pragma unroll
         for (int part = 0; part < 3; ++part) {
-          const uint32_t* sv = part == 0 ? s0 : (part == 1 ? s1 : s2);
+          uint32_t sv[32];
+          tmem_ld_x32(sbase + part * 32, sv);
+          tmem_ld_wait();
           const uint32_t vm = part == 0 ? vm0 : (part == 1 ? vm1 : vm2);
           uint32_t pk[16];
 #pragma unroll
