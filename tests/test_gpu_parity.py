@@ -294,11 +294,17 @@ def test_topk_long_rows_ties_two_pass():
     sc[0, 19000, :] = np.where(rng.random(S) < 0.5, np.float32(0.0), np.float32(-0.0))
     sc[0, 19999, :] = np.where(rng.random(S) < 0.5, np.float32(1.0),
                                np.minimum(rng.standard_normal(S).astype(np.float32), 0.9))
-    idx, cnt = dsa.dsa_topk(dev(sc), k)
+    idx, cnt, vals = dsa.dsa_topk(dev(sc), k, vals=True)
     assert dsa.dsa_get_last_device_error() == 0
     rows = np.array([16999, 17000, 17001, 18000, 19000, 19998, 19999], dtype=np.int64)
-    _check_topk(idx.cpu().numpy(), cnt.cpu().numpy(), sc[0][rows].astype(np.float64), None, S,
-                k, rows)
+    idx_h = idx.cpu().numpy()
+    _check_topk(idx_h, cnt.cpu().numpy(), sc[0][rows].astype(np.float64), None, S, k, rows)
+    # each slot's score is the row's score at the selected key (bit for bit; -0 stays -0)
+    vals_h = vals.cpu().numpy().reshape(S, k)[rows]
+    for r, t in enumerate(rows):
+        sel = idx_h[0, t]
+        assert np.all(sel >= 0)
+        assert np.array_equal(vals_h[r].view(np.uint32), sc[0, t, sel].view(np.uint32))
 
 
 def test_topk_golden_fixtures_on_gpu():
