@@ -218,6 +218,17 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, int* 
   }
 }
 
+__device__ __forceinline__ void tmem_ld_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // acc += a * b on both halves with one paired fp32 FMA (each half rounds as fmaf)
 __device__ __forceinline__ void ffma2(float2& acc, float2 a, float2 b) {
   unsigned long long d, x, y;
@@ -434,8 +445,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int e = warp - 2;              // 0..7
     const int quarter = warp & 3;        // TMEM lane quarter this warp may access
     const int half = e >> 2;             // which 128 of the 256 columns
-    constexpr int QPC = HI >= 32 ? 1 : 32 / HI;  // queries per 32-column chunk
-    constexpr int CPQ = HI >= 32 ? HI / 32 : 1;  // chunks per query
+    // The e4m3 kernel's MMAs take half the bf16 time, so its epilogue sets its pace: at 64
+    // index heads its warps keep their 128 head weights in registers for a whole item (no
+    // shared-memory weight loads per tile) and read TMEM 16 columns at a time to make room
+    // for them. The bf16 kernel (waiting less on its epilogue) keeps the weights in shared
+    // memory, and so do fewer heads, whose many queries per chunk leave no registers.
+    constexpr bool kRegW = F8 && MODE == kModeStore && HI == 64;
+    constexpr int CW = kRegW ? 16 : 32;           // columns per chunk (one TMEM load)
+    constexpr int QPC = HI >= CW ? 1 : CW / HI;   // queries per chunk
+    constexpr int CPQ = HI >= CW ? HI / CW : 1;   // chunks per query
     int as = 0, ws = 0;
     uint32_t a_par = 0, w_par = 0;
     bool ok = true;
@@ -445,6 +463,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // head weights of this query group: column c = (query c / HI, head c % HI)
       if (!__all_sync(0xffffffffu, mbar_wait(&tail->w_full[ws], w_par, abort_flag, p.err, kErr))) break;
       const float* w_item = tail->w_s[ws];
+      float wreg[kRegW ? 128 : 1];
+      if constexpr (kRegW) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float4 w4 = *reinterpret_cast<const float4*>(w_item + half * 128 + 4 * i);
+          wreg[4 * i] = w4.x;
+          wreg[4 * i + 1] = w4.y;
+          wreg[4 * i + 2] = w4.z;
+          wreg[4 * i + 3] = w4.w;
+        }
+      }
 
       const int nt = item_tiles<MODE>(nkb);
       for (int m = 0; m < nt; ++m) {
@@ -468,11 +497,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         // emit mode with shared-memory counters: this warp's scores of the tile, one per
         // query, listed together after the tile (one atomic instruction for every list)
         float ev[kEmitNqw];
-        auto chunk = [&](int ch, const uint32_t (&v)[32]) {
-          const float* wrow = w_item + half * 128 + ch * 32;
+        auto chunk = [&](int ch, const uint32_t (&v)[CW]) {
+          const float* wrow = w_item + half * 128 + ch * CW;
 #pragma unroll
-          for (int j4 = 0; j4 < 32; j4 += 4) {
-            const float4 w4 = *reinterpret_cast<const float4*>(wrow + j4);   // 4 weights per load
+          for (int j4 = 0; j4 < CW; j4 += 4) {
+            float4 w4;
+            if constexpr (kRegW) {
+              w4 = make_float4(wreg[ch * CW + j4], wreg[ch * CW + j4 + 1], wreg[ch * CW + j4 + 2],
+                               wreg[ch * CW + j4 + 3]);
+            } else {
+              w4 = *reinterpret_cast<const float4*>(wrow + j4);   // 4 weights per load
+            }
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
               const int jj = j4 + 2 * u;
@@ -480,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float2 r2 = make_float2(fmaxf(__uint_as_float(v[jj]), 0.f),
                                             fmaxf(__uint_as_float(v[jj + 1]), 0.f));
               if (HI >= 2) {
-                ffma2(acc2[jj / (32 / QPC)], r2, w2);
+                ffma2(acc2[jj / (CW / QPC)], r2, w2);
               } else {   // one head per query: every column is its own query
                 acc2[jj].x = fmaf(w2.x, r2.x, acc2[jj].x);
                 acc2[jj + 1].x = fmaf(w2.y, r2.y, acc2[jj + 1].x);
@@ -491,7 +526,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int cq = ch + 1 - CPQ;
 #pragma unroll
             for (int i = 0; i < QPC; ++i) {
-              const int qi = (half * 128 + cq * 32) / HI + i;
+              const int qi = (half * 128 + cq * CW) / HI + i;
               const int t = t0 + qi;
               if (MODE == kModeStore) {
                 if (t < p.t_end && s <= t) {
@@ -516,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       s <= t && same_doc ? val : __int_as_float(0x7fc00000);
               } else if constexpr (kSmemCnt) {
                 (void)same_doc;
-                ev[(cq * 32) / HI + i] = val;
+                ev[(cq * CW) / HI + i] = val;
               } else if (in_t) {
                 const long long row = static_cast<long long>(b) * p.S + t;
                 emit_keys(p, row, p.cnt + 4 * row, s, val, s <= t && same_doc, lane);
@@ -525,14 +560,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         };
+        if constexpr (kRegW) {
 #pragma unroll
-        for (int pr = 0; pr < 2; ++pr) {
-          uint32_t va[32], vb[32];
-          tmem_ld_x32(t_base + (2 * pr) * 32, va);
-          tmem_ld_x32(t_base + (2 * pr + 1) * 32, vb);
-          tmem_ld_wait();
-          chunk(2 * pr, va);
-          chunk(2 * pr + 1, vb);
+          for (int ch = 0; ch < 128 / CW; ++ch) {
+            uint32_t v[CW];
+            tmem_ld_x16(t_base + ch * CW, v);
+            tmem_ld_wait();
+            chunk(ch, v);
+          }
+        } else {
+#pragma unroll
+          for (int pr = 0; pr < 2; ++pr) {
+            uint32_t va[CW], vb[CW];
+            tmem_ld_x32(t_base + (2 * pr) * 32, va);
+            tmem_ld_x32(t_base + (2 * pr + 1) * 32, vb);
+            tmem_ld_wait();
+            chunk(2 * pr, va);
+            chunk(2 * pr + 1, vb);
+          }
         }
         tc_fence_before();
         __syncwarp();

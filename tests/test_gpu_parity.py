@@ -241,6 +241,29 @@ def test_topk_rows_longer_than_the_shared_stage():
                 k, rows)
 
 
+def test_topk_long_rows_two_batches():
+    """Two batch rows past the shared stage: the persistent long-row CTAs take (batch, query)
+    rows interleaved, longest first; sampled rows of both against the oracle, with each
+    slot's selected score."""
+    dsa = _dsa()
+    B, S, k = 2, 17000, 100
+    rng = np.random.default_rng(23)
+    sc = rng.standard_normal((B, S, S), dtype=np.float32)
+    sc[1, -1, ::5] = 2.75   # ties at the top of batch row 1's last query
+    idx, cnt, vals = dsa.dsa_topk(dev(sc), k, vals=True)
+    assert dsa.dsa_get_last_device_error() == 0
+    rows = np.array([100, 16383, 16384, 16999, S + 16384, S + 16500, 2 * S - 1], dtype=np.int64)
+    idx_h = idx.cpu().numpy()
+    _check_topk(idx_h, cnt.cpu().numpy(), sc.reshape(B * S, S)[rows].astype(np.float64), None,
+                S, k, rows)
+    flat_idx = idx_h.reshape(B * S, k)
+    flat_vals = vals.cpu().numpy().reshape(B * S, k)
+    for r in rows:
+        sel = flat_idx[r]
+        want = np.where(sel >= 0, sc.reshape(B * S, S)[r, np.maximum(sel, 0)], -np.inf)
+        assert np.array_equal(flat_vals[r], want.astype(np.float32))
+
+
 def test_topk_long_rows_k2048():
     """Rows of 16384 to 32767 keys with k = 2048, the long-context regime of the long-row
     kernel's one-pass path (thousands of candidates per row): sampled rows against the oracle."""
